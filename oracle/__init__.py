@@ -1,0 +1,8 @@
+"""Float64 CPU oracle of the SSSL / GQA / QK-norm attention block.
+
+Test infrastructure only: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py``, never by the library. It shares no
+code with the CUDA path.
+"""
+from .attention import *  # noqa: F401,F403
+from .attention import __all__  # noqa: F401

@@ -1,0 +1,97 @@
+"""Seeded synthetic inputs for the attention block (shared by the tests, the
+benchmark and the oracle checks).
+
+This module holds no arithmetic of the method: it only draws random tensors
+with a fixed seed recipe and rounds them to the dtypes the library consumes,
+so that the CUDA path and the float64 oracle see identical bits.
+
+Recipe (stated once here and in the design doc):
+  * base seed 42 (the training script's fixed seed, autoresearch Administrator
+    & Developer Guide §3.4), plus ``100 * layer``; one ``torch.Generator`` per
+    tensor, seeded base + i in the order q, k, v, gq, gk, dO, VE, tok.
+  * q, k, v, dO ~ N(0, 1), rounded to bf16 (or kept fp32 for the fp32 build).
+  * gains gq, gk ~ 1 + gain_std * N(0, 1) in fp32 (None when gain_std is None).
+  * VE table [vocab, Hkv*d] ~ N(0, 0.02^2) in bf16; token ids ~ U[0, vocab) int32.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import torch
+
+BASE_SEED = 42
+VOCAB = 8192
+
+
+@dataclasses.dataclass(frozen=True)
+class Problem:
+    """Shapes and per-layer options of one attention call."""
+
+    B: int
+    T: int
+    Hq: int
+    Hkv: int
+    d: int
+    window: int = -1          # -1: no window (full causal)
+    causal: bool = True
+    gain_std: Optional[float] = None   # None: unit gains (NULL at the ABI)
+    ve: bool = False          # value-embedding mix on this layer
+    ve_scale: float = 0.5
+    vocab: int = VOCAB
+    eps: float = 1e-6
+
+    def replace(self, **kw) -> "Problem":
+        return dataclasses.replace(self, **kw)
+
+
+# The workloads of the benchmark configurations.
+TINY = Problem(B=1, T=256, Hq=2, Hkv=1, d=64, window=128)
+S_LAYER = Problem(B=16, T=2048, Hq=6, Hkv=3, d=128, window=1024, gain_std=0.1)
+L_LAYER = Problem(B=16, T=2048, Hq=6, Hkv=3, d=128, window=-1, gain_std=0.1)
+LONG_S = Problem(B=2, T=16384, Hq=16, Hkv=4, d=128, window=8192, gain_std=0.1)
+LONG_L = Problem(B=2, T=16384, Hq=16, Hkv=4, d=128, window=-1, gain_std=0.1)
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return g
+
+
+def make_inputs(p: Problem, layer: int = 0, dtype: torch.dtype = torch.bfloat16,
+                seed: int = BASE_SEED) -> dict:
+    """Draw the inputs of one layer on the CPU.
+
+    Returns a dict with q, k, v, dO (``dtype``), gq, gk (fp32 [d] or None),
+    ve ([vocab, Hkv*d] in ``dtype`` or None) and tok (int32 [B, T] or None).
+    """
+    s = seed + 100 * layer
+    B, T, Hq, Hkv, d = p.B, p.T, p.Hq, p.Hkv, p.d
+    out = {}
+    out["q"] = torch.randn(B, T, Hq, d, generator=_gen(s + 0)).to(dtype)
+    out["k"] = torch.randn(B, T, Hkv, d, generator=_gen(s + 1)).to(dtype)
+    out["v"] = torch.randn(B, T, Hkv, d, generator=_gen(s + 2)).to(dtype)
+    if p.gain_std is None:
+        out["gq"] = None
+        out["gk"] = None
+    else:
+        out["gq"] = 1.0 + p.gain_std * torch.randn(d, generator=_gen(s + 3))
+        out["gk"] = 1.0 + p.gain_std * torch.randn(d, generator=_gen(s + 4))
+    out["dO"] = torch.randn(B, T, Hq, d, generator=_gen(s + 5)).to(dtype)
+    if p.ve:
+        out["ve"] = (0.02 * torch.randn(p.vocab, Hkv * d, generator=_gen(s + 6))).to(dtype)
+        out["tok"] = torch.randint(0, p.vocab, (B, T), generator=_gen(s + 7),
+                                   dtype=torch.int64).to(torch.int32)
+    else:
+        out["ve"] = None
+        out["tok"] = None
+    return out
+
+
+def as_f64(t):
+    """The exact float64 value of a tensor (or None), as a NumPy array."""
+    if t is None:
+        return None
+    return t.detach().to("cpu").to(torch.float64).numpy()

@@ -1,0 +1,177 @@
+/*
+ * swa_attn.h - C ABI of the GB300 (sm_103a) attention-block library.
+ *
+ * The block computed here is the attention of the autoresearch GPT training
+ * script as its pages describe it:
+ *   - QK-norm: RMSNorm of queries and keys right before the attention dot
+ *     product (autoresearch train.py walkthrough post, model paragraph;
+ *     "autoresearch Administrator & Developer Guide" §8.2.1, F.rms_norm row),
+ *     here with optional learned per-channel gains gq, gk of shape [d];
+ *   - grouped-query attention, n_kv_head <= n_head (Guide §8.2.1, GQA row;
+ *     §6.3 techniques table): query head h reads kv head h / (Hq / Hkv);
+ *   - a causal sliding window or full causal mask per layer, chosen by the
+ *     "SSSL" window pattern (post, model paragraph; Guide §3.4 WINDOW_PATTERN);
+ *   - on value-embedding layers, v_eff = v + ve_scale * gate * VE[token]
+ *     (Guide §8.2.1, value-embedding row and its gate snippet).
+ *
+ * Two shared libraries export these symbols:
+ *   libswaattn.so       bf16 tensors, tcgen05 tensor-core kernels (the product path);
+ *   libswaattn_fp32.so  fp32 tensors, SIMT FFMA kernels (a debug build with
+ *                       the same band schedule, used to check the method at
+ *                       fp32 precision).
+ * "elem" below is bf16 (raw 16-bit bit patterns) in the first, float in the
+ * second. Gains, LSE, gate and all gradients of shared parameters are fp32 in
+ * both.
+ *
+ * Conventions common to every call:
+ *   - All tensor pointers are DEVICE pointers of the current CUDA device; the
+ *     caller owns every buffer, including the workspace. The library never
+ *     allocates or frees memory.
+ *   - Layouts are dense row-major:
+ *       q, o, dO, dq       [B, T, Hq,  d]   elem
+ *       k, v, dk, dv       [B, T, Hkv, d]   elem
+ *       lse                [B, Hq, T]       fp32, natural-log sum of exp of the
+ *                                           scaled, masked logits of each row
+ *       gq, gk, dgq, dgk   [d]              fp32
+ *       ve, dve            [vocab, Hkv*d]   elem (ve) / fp32 (dve)
+ *       tok                [B, T]           int32
+ *       ve_gate            [B, T, Hkv]      fp32
+ *   - Tensor pointers must be 16-byte aligned; the workspace 256-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream). A status other than SWA_OK returned by the host call means that
+ *     nothing was launched. Errors found on the device (a bounded wait that ran
+ *     out, a token id outside [0, vocab)) are OR-ed into a status word in the
+ *     workspace header and read back by swa_attn_check_status().
+ *   - B == 0 or T == 0 is a valid empty problem: nothing is computed; the
+ *     backward still zero-fills dgq, dgk and dve.
+ */
+#ifndef SWA_ATTN_H
+#define SWA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum swa_status {
+  SWA_OK = 0,
+  SWA_ERR_INVALID_ARG = 1,  /* bad shape, NULL pointer, misalignment, bad flag   */
+  SWA_ERR_UNSUPPORTED = 2,  /* valid but not built: d not in {64,128}, wrong GPU  */
+  SWA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed                  */
+  SWA_ERR_TIMEOUT = 4,      /* device: a bounded pipeline wait ran out            */
+  SWA_ERR_WORKSPACE = 5,    /* workspace too small for this problem               */
+  SWA_ERR_DEVICE_CHECK = 6  /* device: a token id outside [0, vocab) was skipped  */
+} swa_status;
+
+/* Problem description shared by every call. */
+typedef struct swa_params {
+  int B, T;         /* batch, sequence length (>= 0)                              */
+  int Hq, Hkv;      /* query heads, kv heads; Hq % Hkv == 0                       */
+  int d;            /* head dim: 64 or 128                                         */
+  int window;       /* -1: no window. Else, causal: key j visible to query i iff
+                       i - window <= j <= i; non-causal: iff |i - j| <= window.
+                       window >= T - 1 is the same as -1.                          */
+  int causal;       /* 1: causal (every layer of the SSSL stack); 0: bidirectional */
+  float softmax_scale; /* 0: 1/sqrt(d)                                             */
+  float eps;        /* RMSNorm epsilon, >= 0 (the script's F.rms_norm default is
+                       used by callers that pass 1e-6)                             */
+  float ve_scale;   /* multiplies gate * VE[tok]; ignored when ve == NULL          */
+  int vocab;        /* rows of the VE table; ignored when ve == NULL               */
+} swa_params;
+
+/* flags */
+#define SWA_REUSE_PROLOGUE 1u  /* the workspace still holds this problem's QK-norm /
+                                  VE-mix outputs from an earlier call with the same
+                                  inputs: skip recomputing them                       */
+#define SWA_BWD_STAGE_PRE 2u   /* backward stages to run; none of the three bits set */
+#define SWA_BWD_STAGE_MAIN 4u  /* means all of them. PRE: D = rowsum(dO * O), clear   */
+#define SWA_BWD_STAGE_POST 8u  /* the accumulators; MAIN: the attention backward;
+                                  POST: RMSNorm backward, gain and VE gradients.
+                                  Running them one call at a time, in this order,
+                                  gives the same result as one call with all three.  */
+
+/*
+ * Bytes of workspace a problem needs (forward only, or forward + backward).
+ * Returns 0 when the parameters are invalid. The workspace holds a 256-byte
+ * header (device status word), the QK-norm outputs qn, kn and their inverse
+ * RMS, v_eff on VE layers, and for the backward the fp32 accumulators.
+ * A fresh workspace must be initialised once with swa_attn_workspace_init().
+ */
+size_t swa_attn_workspace_size(const swa_params* p, int for_backward);
+
+/* Zeroes the workspace header (status word) on `stream`. */
+swa_status swa_attn_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Forward: o = softmax(scale * qn kn^T + mask) v_eff and lse, where
+ * qn = gq * q / sqrt(mean(q^2) + eps) (likewise kn) and v_eff = v on plain
+ * layers, v + ve_scale * gate * VE[tok] on value-embedding layers.
+ *   gq, gk   may be NULL (unit gains).
+ *   ve       NULL: no value embedding (tok, ve_gate ignored). Else tok is
+ *            required and ve_gate may be NULL (gate = 1, the pages' gate at
+ *            initialisation: 2 * sigmoid(0)).
+ *   flags    0 or SWA_REUSE_PROLOGUE.
+ * Writes o and lse, and the prologue outputs into the workspace (kept for the
+ * backward's SWA_REUSE_PROLOGUE).
+ */
+swa_status swa_attn_fwd(const swa_params* p, const void* q, const void* k, const void* v,
+                        const float* gq, const float* gk, const void* ve, const int32_t* tok,
+                        const float* ve_gate, void* o, float* lse, void* workspace,
+                        size_t ws_bytes, unsigned flags, void* stream);
+
+/*
+ * Backward of the forward for the loss <o, dO>: gradients of q, k, v, the
+ * gains and the VE table. Inputs as in swa_attn_fwd plus the forward's o and
+ * lse and the upstream gradient dO. Outputs (overwritten, not accumulated):
+ *   dq, dk, dv       required.
+ *   dgq, dgk         may be NULL (not computed); when non-NULL they receive
+ *                    the full gain gradient (summed over batch, time, heads).
+ *                    With gq (gk) NULL the gain is 1 and dgq (dgk) is still the
+ *                    gradient with respect to it.
+ *   dve              may be NULL; when non-NULL (and ve != NULL) it receives
+ *                    the gradient of the VE table, zero in rows no token used.
+ * The gradient of the VE gate is not produced (the gate is an input).
+ * flags: SWA_REUSE_PROLOGUE and the SWA_BWD_STAGE_* bits.
+ */
+swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const void* v,
+                        const float* gq, const float* gk, const void* ve, const int32_t* tok,
+                        const float* ve_gate, const void* o, const float* lse, const void* dO,
+                        void* dq, void* dk, void* dv, float* dgq, float* dgk, float* dve,
+                        void* workspace, size_t ws_bytes, unsigned flags, void* stream);
+
+/*
+ * Synchronises `stream`, reads the workspace status word, clears it, and
+ * returns SWA_OK, SWA_ERR_TIMEOUT or SWA_ERR_DEVICE_CHECK (timeout wins).
+ */
+swa_status swa_attn_check_status(void* workspace, void* stream);
+
+/*
+ * Window of layer `layer` of an `n_layer` stack under a window pattern of
+ * 'S' (sliding, window T/2) and 'L' (full) characters, e.g. "SSSL": the
+ * layer's character is pattern[layer % strlen(pattern)] and the last layer is
+ * always full (post, model paragraph; Guide §3.4). Returns T/2 or -1; -2 on
+ * invalid arguments (NULL/empty pattern, a character other than S/L, layer
+ * out of [0, n_layer)).
+ */
+int swa_sssl_window(int layer, int n_layer, const char* pattern, int T);
+
+/*
+ * 1 if layer `layer` of an `n_layer` stack mixes value embeddings into v:
+ * alternating layers, the last always included (Guide §8.2.1, has_ve); 0 if
+ * not; -1 on invalid arguments.
+ */
+int swa_has_ve(int layer, int n_layer);
+
+/* Static, human-readable text of a status code. */
+const char* swa_strerror(swa_status s);
+
+/* Static text naming the build: element type and kernel family. */
+const char* swa_build_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWA_ATTN_H */

@@ -1,0 +1,240 @@
+"""Python binding of the GB300 attention-block library (C ABI in
+``include/swa_attn.h``).
+
+The functions named ``swa_*`` mirror the C entry points one to one and only
+marshal arguments (tensor pointers, the CUDA stream, the parameter struct).
+``attention_forward`` / ``attention_backward`` allocate outputs and the
+workspace with PyTorch and call them. Every computation runs in the CUDA
+library; if the shared library is missing, loading it raises.
+
+Two libraries share the symbols: ``libswaattn.so`` (bf16 tensors, tcgen05
+kernels) and ``libswaattn_fp32.so`` (fp32 tensors, SIMT debug kernels). The
+binding picks the one matching the dtype of ``q``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "swa_params", "SwaError", "load",
+    "swa_attn_workspace_size", "swa_attn_workspace_init", "swa_attn_fwd", "swa_attn_bwd",
+    "swa_attn_check_status", "swa_sssl_window", "swa_has_ve", "swa_strerror",
+    "swa_build_info", "attention_forward", "attention_backward", "make_params",
+    "SWA_OK", "SWA_ERR_INVALID_ARG", "SWA_ERR_UNSUPPORTED", "SWA_ERR_CUDA", "SWA_ERR_TIMEOUT",
+    "SWA_ERR_WORKSPACE", "SWA_ERR_DEVICE_CHECK", "SWA_REUSE_PROLOGUE", "SWA_BWD_STAGE_PRE",
+    "SWA_BWD_STAGE_MAIN", "SWA_BWD_STAGE_POST",
+]
+
+SWA_OK = 0
+SWA_ERR_INVALID_ARG = 1
+SWA_ERR_UNSUPPORTED = 2
+SWA_ERR_CUDA = 3
+SWA_ERR_TIMEOUT = 4
+SWA_ERR_WORKSPACE = 5
+SWA_ERR_DEVICE_CHECK = 6
+
+SWA_REUSE_PROLOGUE = 1
+SWA_BWD_STAGE_PRE = 2
+SWA_BWD_STAGE_MAIN = 4
+SWA_BWD_STAGE_POST = 8
+
+
+class swa_params(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("T", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
+        ("d", ctypes.c_int), ("window", ctypes.c_int), ("causal", ctypes.c_int),
+        ("softmax_scale", ctypes.c_float), ("eps", ctypes.c_float),
+        ("ve_scale", ctypes.c_float), ("vocab", ctypes.c_int),
+    ]
+
+
+class SwaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {swa_strerror(status)} (status {status})")
+        self.status = status
+
+
+_LIBS: dict = {}
+_vp = ctypes.c_void_p
+
+
+def load(kind: str = "bf16") -> ctypes.CDLL:
+    """The ctypes handle of the bf16 or fp32 library (loaded once)."""
+    if kind in _LIBS:
+        return _LIBS[kind]
+    path = _build.lib_path(kind)
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{os.path.basename(path)} is not built; run sliding_window_gqa_qk_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(swa_params)
+    lib.swa_attn_workspace_size.argtypes = [P, ctypes.c_int]
+    lib.swa_attn_workspace_size.restype = ctypes.c_size_t
+    lib.swa_attn_workspace_init.argtypes = [_vp, ctypes.c_size_t, _vp]
+    lib.swa_attn_workspace_init.restype = ctypes.c_int
+    lib.swa_attn_fwd.argtypes = [P] + [_vp] * 11 + [ctypes.c_size_t, ctypes.c_uint, _vp]
+    lib.swa_attn_fwd.restype = ctypes.c_int
+    lib.swa_attn_bwd.argtypes = [P] + [_vp] * 18 + [ctypes.c_size_t, ctypes.c_uint, _vp]
+    lib.swa_attn_bwd.restype = ctypes.c_int
+    lib.swa_attn_check_status.argtypes = [_vp, _vp]
+    lib.swa_attn_check_status.restype = ctypes.c_int
+    lib.swa_sssl_window.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_char_p, ctypes.c_int]
+    lib.swa_sssl_window.restype = ctypes.c_int
+    lib.swa_has_ve.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.swa_has_ve.restype = ctypes.c_int
+    lib.swa_strerror.argtypes = [ctypes.c_int]
+    lib.swa_strerror.restype = ctypes.c_char_p
+    lib.swa_build_info.argtypes = []
+    lib.swa_build_info.restype = ctypes.c_char_p
+    _LIBS[kind] = lib
+    return lib
+
+
+def _kind_of(t: Optional[torch.Tensor]) -> str:
+    if t is not None and t.dtype == torch.float32:
+        return "fp32"
+    return "bf16"
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_params(B, T, Hq, Hkv, d, window=-1, causal=True, softmax_scale=0.0, eps=1e-6,
+                ve_scale=0.5, vocab=0) -> swa_params:
+    return swa_params(int(B), int(T), int(Hq), int(Hkv), int(d), int(window), int(bool(causal)),
+                      float(softmax_scale), float(eps), float(ve_scale), int(vocab))
+
+
+# ---------------------------------------------------------------------------
+# One-to-one wrappers of the C entry points
+# ---------------------------------------------------------------------------
+
+def swa_attn_workspace_size(p: swa_params, for_backward: int, kind: str = "bf16") -> int:
+    return int(load(kind).swa_attn_workspace_size(ctypes.byref(p), int(for_backward)))
+
+
+def swa_attn_workspace_init(ws, ws_bytes=None, stream=None, kind: str = "bf16") -> int:
+    n = ws.numel() if ws_bytes is None else ws_bytes
+    return int(load(kind).swa_attn_workspace_init(_ptr(ws), n, _stream(stream)))
+
+
+def swa_attn_fwd(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, ws, ws_bytes=None, flags=0,
+                 stream=None, kind=None) -> int:
+    kind = kind or _kind_of(q)
+    n = ws.numel() if ws_bytes is None else ws_bytes
+    return int(load(kind).swa_attn_fwd(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(gq), _ptr(gk), _ptr(ve), _ptr(tok),
+        _ptr(ve_gate), _ptr(o), _ptr(lse), _ptr(ws), n, int(flags), _stream(stream)))
+
+
+def swa_attn_bwd(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, dgq, dgk, dve,
+                 ws, ws_bytes=None, flags=0, stream=None, kind=None) -> int:
+    kind = kind or _kind_of(q)
+    n = ws.numel() if ws_bytes is None else ws_bytes
+    return int(load(kind).swa_attn_bwd(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(gq), _ptr(gk), _ptr(ve), _ptr(tok),
+        _ptr(ve_gate), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgq),
+        _ptr(dgk), _ptr(dve), _ptr(ws), n, int(flags), _stream(stream)))
+
+
+def swa_attn_check_status(ws, stream=None, kind: str = "bf16") -> int:
+    return int(load(kind).swa_attn_check_status(_ptr(ws), _stream(stream)))
+
+
+def swa_sssl_window(layer: int, n_layer: int, pattern: str, T: int, kind: str = "bf16") -> int:
+    return int(load(kind).swa_sssl_window(layer, n_layer, pattern.encode(), T))
+
+
+def swa_has_ve(layer: int, n_layer: int, kind: str = "bf16") -> int:
+    return int(load(kind).swa_has_ve(layer, n_layer))
+
+
+def swa_strerror(status: int, kind: str = "bf16") -> str:
+    try:
+        return load(kind).swa_strerror(int(status)).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def swa_build_info(kind: str = "bf16") -> str:
+    return load(kind).swa_build_info().decode()
+
+
+# ---------------------------------------------------------------------------
+# Convenience calls: allocate outputs / workspace, raise on error
+# ---------------------------------------------------------------------------
+
+def _check(status: int, what: str):
+    if status != SWA_OK:
+        raise SwaError(status, what)
+
+
+def new_workspace(p: swa_params, for_backward: bool, device, kind: str, stream=None):
+    n = swa_attn_workspace_size(p, int(for_backward), kind)
+    if n == 0:
+        raise SwaError(SWA_ERR_INVALID_ARG, "workspace size")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    _check(swa_attn_workspace_init(ws, n, stream, kind), "workspace init")
+    return ws
+
+
+def attention_forward(q, k, v, gq=None, gk=None, *, window: int = -1, causal: bool = True,
+                      softmax_scale: float = 0.0, eps: float = 1e-6, ve=None, tok=None,
+                      ve_gate=None, ve_scale: float = 0.5, workspace=None, stream=None):
+    """o, lse, workspace = attention_forward(q, k, v, ...). The workspace is
+    allocated for the backward too, so it can be passed on to
+    ``attention_backward`` with the prologue outputs kept."""
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    kind = _kind_of(q)
+    vocab = ve.shape[0] if ve is not None else 0
+    p = make_params(B, T, Hq, Hkv, d, window, causal, softmax_scale, eps, ve_scale, vocab)
+    ws = workspace if workspace is not None else new_workspace(p, True, q.device, kind, stream)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, T, dtype=torch.float32, device=q.device)
+    _check(swa_attn_fwd(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, ws, stream=stream),
+           "swa_attn_fwd")
+    return o, lse, ws
+
+
+def attention_backward(q, k, v, gq, gk, o, lse, dO, *, window: int = -1, causal: bool = True,
+                       softmax_scale: float = 0.0, eps: float = 1e-6, ve=None, tok=None,
+                       ve_gate=None, ve_scale: float = 0.5, workspace=None,
+                       reuse_prologue: bool = False, stream=None) -> dict:
+    """Gradients dq, dk, dv, dgq, dgk, dve (dve None without a VE table)."""
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    kind = _kind_of(q)
+    vocab = ve.shape[0] if ve is not None else 0
+    p = make_params(B, T, Hq, Hkv, d, window, causal, softmax_scale, eps, ve_scale, vocab)
+    ws = workspace if workspace is not None else new_workspace(p, True, q.device, kind, stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dgq = torch.empty(d, dtype=torch.float32, device=q.device)
+    dgk = torch.empty(d, dtype=torch.float32, device=q.device)
+    dve = torch.empty(ve.shape, dtype=torch.float32, device=q.device) if ve is not None else None
+    flags = SWA_REUSE_PROLOGUE if (reuse_prologue and workspace is not None) else 0
+    _check(swa_attn_bwd(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, dgq, dgk,
+                        dve, ws, flags=flags, stream=stream), "swa_attn_bwd")
+    return {"dq": dq, "dk": dk, "dv": dv, "dgq": dgq, "dgk": dgk, "dve": dve, "workspace": ws}

@@ -1,0 +1,376 @@
+// Host side of the C ABI declared in include/swa_attn.h: argument checks,
+// workspace layout, TMA descriptor set-up and the kernel launch sequence.
+//
+// Built twice from this file: with SWA_ELEM_FP32 (fp32 SIMT debug library)
+// and without (bf16 tcgen05 library).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/swa_attn.h"
+#include "common.cuh"
+#include "rowwise.cuh"
+
+#if defined(SWA_ELEM_FP32)
+#include "simt.cuh"
+#else
+#include "tc_fwd.cuh"
+#include "tc_bwd.cuh"
+#endif
+
+using namespace swa;
+
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+
+inline bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// Validated view of one call.
+struct Call {
+  swa_params p;
+  bool empty;
+  float scale;
+  WsLayout L;
+  uint8_t* ws;
+  cudaStream_t stream;
+};
+
+swa_status check_params(const swa_params* p) {
+  if (p == nullptr) return SWA_ERR_INVALID_ARG;
+  if (p->B < 0 || p->T < 0 || p->Hq < 1 || p->Hkv < 1 || p->d < 1) return SWA_ERR_INVALID_ARG;
+  if (p->Hq % p->Hkv != 0) return SWA_ERR_INVALID_ARG;
+  if (p->window < -1) return SWA_ERR_INVALID_ARG;
+  if (p->causal != 0 && p->causal != 1) return SWA_ERR_INVALID_ARG;
+  if (!std::isfinite(p->softmax_scale) || p->softmax_scale < 0.f) return SWA_ERR_INVALID_ARG;
+  if (!std::isfinite(p->eps) || p->eps < 0.f) return SWA_ERR_INVALID_ARG;
+  if (!std::isfinite(p->ve_scale)) return SWA_ERR_INVALID_ARG;
+  if (p->d != 64 && p->d != 128) return SWA_ERR_UNSUPPORTED;
+  // Grid and index limits: (batch, head) pairs index grid x, tiles of 128
+  // positions index grid y (< 65536), positions are 32-bit TMA coordinates.
+  if (p->Hq > 65535 || p->B > 65535 || p->T > (1 << 22) ||
+      static_cast<long long>(p->B) * p->Hq > (1ll << 30))
+    return SWA_ERR_UNSUPPORTED;
+  return SWA_OK;
+}
+
+swa_status check_device() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SWA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  if (major != 10 || minor != 3) return SWA_ERR_UNSUPPORTED;  // built for sm_103a only
+  return SWA_OK;
+}
+
+swa_status begin(Call& c, const swa_params* p, void* workspace, size_t ws_bytes, bool bwd,
+                 void* stream) {
+  swa_status s = check_params(p);
+  if (s != SWA_OK) return s;
+  c.p = *p;
+  c.empty = (p->B == 0 || p->T == 0);
+  c.scale = p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / std::sqrt(static_cast<float>(p->d));
+  c.L = ws_layout(p->B, p->T, p->Hq, p->Hkv, p->d);
+  c.ws = static_cast<uint8_t*>(workspace);
+  c.stream = static_cast<cudaStream_t>(stream);
+  if (workspace == nullptr || !aligned(workspace, 256)) return SWA_ERR_INVALID_ARG;
+  if (ws_bytes < (bwd ? c.L.bwd_end : c.L.fwd_end)) return SWA_ERR_WORKSPACE;
+  return SWA_OK;
+}
+
+bool tensor_ok(const void* ptr) { return ptr != nullptr && aligned(ptr, 16); }
+
+swa_status launched() {
+  return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
+template <typename T>
+T* at(const Call& c, size_t off) {
+  return reinterpret_cast<T*>(c.ws + off);
+}
+
+int row_grid(long long rows) {
+  long long blocks = (rows + kRowWarps * kRowsPerIter - 1) / (kRowWarps * kRowsPerIter);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  return static_cast<int>(blocks < 1 ? 1 : blocks);
+}
+
+swa_status run_prologue(const Call& c, const elem_t* q, const elem_t* k, const elem_t* v,
+                        const float* gq, const float* gk, const elem_t* ve, const int32_t* tok,
+                        const float* gate, bool copy_v) {
+  const swa_params& p = c.p;
+  ProArgs a{};
+  a.B = p.B; a.T = p.T; a.Hq = p.Hq; a.Hkv = p.Hkv; a.d = p.d; a.vocab = p.vocab;
+  a.eps = p.eps; a.ve_scale = p.ve_scale;
+  a.q = q; a.k = k; a.v = v; a.gq = gq; a.gk = gk; a.ve = ve; a.tok = tok; a.gate = gate;
+  a.qn = at<elem_t>(c, c.L.qn); a.kn = at<elem_t>(c, c.L.kn); a.veff = at<elem_t>(c, c.L.veff);
+  a.rstd_q = at<float>(c, c.L.rstd_q); a.rstd_k = at<float>(c, c.L.rstd_k);
+  a.status = at<uint32_t>(c, c.L.status);
+  const long long rows = static_cast<long long>(p.B) * p.T * p.Hq;
+  dim3 grid(row_grid(rows), (ve != nullptr || copy_v) ? 3 : 2);
+  if (p.d == 64) prologue_kernel<64><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
+  else prologue_kernel<128><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
+  return launched();
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Exported C ABI
+// ---------------------------------------------------------------------------
+extern "C" {
+
+size_t swa_attn_workspace_size(const swa_params* p, int for_backward) {
+  if (check_params(p) != SWA_OK) return 0;
+  const WsLayout L = ws_layout(p->B, p->T, p->Hq, p->Hkv, p->d);
+  return for_backward ? L.bwd_end : L.fwd_end;
+}
+
+swa_status swa_attn_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+  if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < 256) return SWA_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(workspace, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  return SWA_OK;
+}
+
+swa_status swa_attn_fwd(const swa_params* p, const void* q, const void* k, const void* v,
+                        const float* gq, const float* gk, const void* ve, const int32_t* tok,
+                        const float* ve_gate, void* o, float* lse, void* workspace,
+                        size_t ws_bytes, unsigned flags, void* stream) {
+  Call c;
+  swa_status s = begin(c, p, workspace, ws_bytes, false, stream);
+  if (s != SWA_OK) return s;
+  if ((flags & ~SWA_REUSE_PROLOGUE) != 0) return SWA_ERR_INVALID_ARG;
+  if (!tensor_ok(q) || !tensor_ok(k) || !tensor_ok(v) || !tensor_ok(o) || lse == nullptr)
+    return SWA_ERR_INVALID_ARG;
+  if (ve != nullptr && (!aligned(ve, 16) || tok == nullptr || p->vocab < 1))
+    return SWA_ERR_INVALID_ARG;
+  if (c.empty) return SWA_OK;
+  if ((s = check_device()) != SWA_OK) return s;
+  const elem_t* qe = static_cast<const elem_t*>(q);
+  const elem_t* ke = static_cast<const elem_t*>(k);
+  const elem_t* vin = static_cast<const elem_t*>(v);
+  const elem_t* vee = static_cast<const elem_t*>(ve);
+#if defined(SWA_ELEM_FP32)
+  const bool copy_v = true;
+#else
+  const bool copy_v = false;
+#endif
+  if (!(flags & SWA_REUSE_PROLOGUE)) {
+    if ((s = run_prologue(c, qe, ke, vin, gq, gk, vee, tok, ve_gate, copy_v)) != SWA_OK) return s;
+  }
+#if defined(SWA_ELEM_FP32)
+  SimtFwdArgs a{};
+  a.B = p->B; a.T = p->T; a.Hq = p->Hq; a.Hkv = p->Hkv; a.window = p->window;
+  a.causal = p->causal; a.scale = c.scale;
+  a.qn = at<float>(c, c.L.qn); a.kn = at<float>(c, c.L.kn); a.veff = at<float>(c, c.L.veff);
+  a.o = static_cast<float*>(o); a.lse = lse;
+  dim3 grid((p->T + kSimtTile - 1) / kSimtTile, p->Hq, p->B);
+  if (p->d == 64) {
+    cudaFuncSetAttribute(fwd_simt_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(simt_fwd_smem<64>()));
+    fwd_simt_kernel<64><<<grid, kSimtWarps * 32, simt_fwd_smem<64>(), c.stream>>>(a);
+  } else {
+    cudaFuncSetAttribute(fwd_simt_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(simt_fwd_smem<128>()));
+    fwd_simt_kernel<128><<<grid, kSimtWarps * 32, simt_fwd_smem<128>(), c.stream>>>(a);
+  }
+  return launched();
+#else
+  tc::FwdLaunch f{};
+  f.B = p->B; f.T = p->T; f.Hq = p->Hq; f.Hkv = p->Hkv; f.d = p->d;
+  f.window = p->window; f.causal = p->causal; f.scale = c.scale;
+  f.qn = at<elem_t>(c, c.L.qn); f.kn = at<elem_t>(c, c.L.kn);
+  f.v = (ve != nullptr) ? at<elem_t>(c, c.L.veff) : vin;
+  f.v_head_major = (ve != nullptr);
+  f.o = static_cast<elem_t*>(o); f.lse = lse;
+  f.status = at<uint32_t>(c, c.L.status);
+  f.wait_limit_ns = kWaitLimitNs;
+  return tc::launch_fwd(f, c.stream);
+#endif
+}
+
+swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const void* v,
+                        const float* gq, const float* gk, const void* ve, const int32_t* tok,
+                        const float* ve_gate, const void* o, const float* lse, const void* dO,
+                        void* dq, void* dk, void* dv, float* dgq, float* dgk, float* dve,
+                        void* workspace, size_t ws_bytes, unsigned flags, void* stream) {
+  Call c;
+  swa_status s = begin(c, p, workspace, ws_bytes, true, stream);
+  if (s != SWA_OK) return s;
+  const unsigned known = SWA_REUSE_PROLOGUE | SWA_BWD_STAGE_PRE | SWA_BWD_STAGE_MAIN | SWA_BWD_STAGE_POST;
+  if ((flags & ~known) != 0) return SWA_ERR_INVALID_ARG;
+  if (!tensor_ok(q) || !tensor_ok(k) || !tensor_ok(v) || !tensor_ok(o) || !tensor_ok(dO) ||
+      !tensor_ok(dq) || !tensor_ok(dk) || !tensor_ok(dv) || lse == nullptr)
+    return SWA_ERR_INVALID_ARG;
+  if (ve != nullptr && (!aligned(ve, 16) || tok == nullptr || p->vocab < 1))
+    return SWA_ERR_INVALID_ARG;
+  unsigned stages = flags & (SWA_BWD_STAGE_PRE | SWA_BWD_STAGE_MAIN | SWA_BWD_STAGE_POST);
+  if (stages == 0) stages = SWA_BWD_STAGE_PRE | SWA_BWD_STAGE_MAIN | SWA_BWD_STAGE_POST;
+  const swa_params& P = c.p;
+  cudaStream_t st = c.stream;
+  if (c.empty) {
+    // Nothing to differentiate: the shared-parameter gradients are zero.
+    if (stages & SWA_BWD_STAGE_POST) {
+      if (dgq && cudaMemsetAsync(dgq, 0, sizeof(float) * P.d, st) != cudaSuccess) return SWA_ERR_CUDA;
+      if (dgk && cudaMemsetAsync(dgk, 0, sizeof(float) * P.d, st) != cudaSuccess) return SWA_ERR_CUDA;
+      if (dve && ve && cudaMemsetAsync(dve, 0, sizeof(float) * P.vocab * P.Hkv * P.d, st) != cudaSuccess)
+        return SWA_ERR_CUDA;
+    }
+    return SWA_OK;
+  }
+  if ((s = check_device()) != SWA_OK) return s;
+  const elem_t* qe = static_cast<const elem_t*>(q);
+  const elem_t* ke = static_cast<const elem_t*>(k);
+  const elem_t* vin = static_cast<const elem_t*>(v);
+  const elem_t* vee = static_cast<const elem_t*>(ve);
+#if defined(SWA_ELEM_FP32)
+  const bool copy_v = true;
+  const int clear_acc = 0;
+#else
+  const bool copy_v = false;
+  const int clear_acc = 1;
+#endif
+  if ((stages & SWA_BWD_STAGE_PRE) && !(flags & SWA_REUSE_PROLOGUE)) {
+    if ((s = run_prologue(c, qe, ke, vin, gq, gk, vee, tok, ve_gate, copy_v)) != SWA_OK) return s;
+  }
+  const long long qrows = static_cast<long long>(P.B) * P.T * P.Hq;
+  if (stages & SWA_BWD_STAGE_PRE) {
+    PreArgs a{};
+    a.B = P.B; a.T = P.T; a.Tpad = t_pad(P.T); a.Hq = P.Hq; a.Hkv = P.Hkv; a.d = P.d;
+    a.o = static_cast<const elem_t*>(o); a.dO = static_cast<const elem_t*>(dO); a.lse = lse;
+    a.dvec = at<float>(c, c.L.dvec); a.lse2 = at<float>(c, c.L.lse2);
+    a.dq_acc = at<float>(c, c.L.dq_acc);
+    a.clear_acc = clear_acc;
+    if (P.d == 64) bwd_pre_kernel<64><<<row_grid(qrows), kRowWarps * 32, 0, st>>>(a);
+    else bwd_pre_kernel<128><<<row_grid(qrows), kRowWarps * 32, 0, st>>>(a);
+    if ((s = launched()) != SWA_OK) return s;
+  }
+  if (stages & SWA_BWD_STAGE_MAIN) {
+#if defined(SWA_ELEM_FP32)
+    SimtBwdArgs a{};
+    a.B = P.B; a.T = P.T; a.Tpad = t_pad(P.T); a.Hq = P.Hq; a.Hkv = P.Hkv; a.window = P.window;
+    a.causal = P.causal; a.scale = c.scale;
+    a.qn = at<float>(c, c.L.qn); a.kn = at<float>(c, c.L.kn); a.veff = at<float>(c, c.L.veff);
+    a.dO = static_cast<const float*>(dO); a.lse = lse; a.dvec = at<float>(c, c.L.dvec);
+    a.dq_acc = at<float>(c, c.L.dq_acc); a.dk_acc = at<float>(c, c.L.dk_acc);
+    a.dv_acc = at<float>(c, c.L.dv_acc);
+    const int nt = (P.T + kSimtTile - 1) / kSimtTile;
+    if (P.d == 64) {
+      cudaFuncSetAttribute(bwd_dq_simt_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(simt_dq_smem<64>()));
+      cudaFuncSetAttribute(bwd_dkv_simt_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(simt_dkv_smem<64>()));
+      bwd_dq_simt_kernel<64><<<dim3(nt, P.Hq, P.B), kSimtWarps * 32, simt_dq_smem<64>(), st>>>(a);
+      bwd_dkv_simt_kernel<64><<<dim3(nt, P.Hkv, P.B), kSimtWarps * 32, simt_dkv_smem<64>(), st>>>(a);
+    } else {
+      cudaFuncSetAttribute(bwd_dq_simt_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(simt_dq_smem<128>()));
+      cudaFuncSetAttribute(bwd_dkv_simt_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(simt_dkv_smem<128>()));
+      bwd_dq_simt_kernel<128><<<dim3(nt, P.Hq, P.B), kSimtWarps * 32, simt_dq_smem<128>(), st>>>(a);
+      bwd_dkv_simt_kernel<128><<<dim3(nt, P.Hkv, P.B), kSimtWarps * 32, simt_dkv_smem<128>(), st>>>(a);
+    }
+    if ((s = launched()) != SWA_OK) return s;
+#else
+    tc::BwdLaunch b{};
+    b.B = P.B; b.T = P.T; b.Hq = P.Hq; b.Hkv = P.Hkv; b.d = P.d;
+    b.window = P.window; b.causal = P.causal; b.scale = c.scale;
+    b.qn = at<elem_t>(c, c.L.qn); b.kn = at<elem_t>(c, c.L.kn);
+    b.v = (ve != nullptr) ? at<elem_t>(c, c.L.veff) : vin;
+    b.v_head_major = (ve != nullptr);
+    b.dO = static_cast<const elem_t*>(dO);
+    b.lse2 = at<float>(c, c.L.lse2); b.dvec = at<float>(c, c.L.dvec); b.Tpad = t_pad(P.T);
+    b.dq_acc = at<float>(c, c.L.dq_acc); b.dk_acc = at<float>(c, c.L.dk_acc);
+    b.dv_acc = at<float>(c, c.L.dv_acc);
+    b.status = at<uint32_t>(c, c.L.status);
+    b.wait_limit_ns = kWaitLimitNs;
+    if ((s = tc::launch_bwd(b, st)) != SWA_OK) return s;
+#endif
+  }
+  if (stages & SWA_BWD_STAGE_POST) {
+    if (dve && ve) {
+      if (cudaMemsetAsync(dve, 0, sizeof(float) * P.vocab * P.Hkv * P.d, st) != cudaSuccess)
+        return SWA_ERR_CUDA;
+    }
+    PostArgs a{};
+    a.B = P.B; a.T = P.T; a.Hq = P.Hq; a.Hkv = P.Hkv; a.d = P.d; a.vocab = P.vocab;
+    a.ve_scale = P.ve_scale;
+    a.q = qe; a.k = ke; a.gq = gq; a.gk = gk; a.tok = tok; a.gate = ve_gate;
+    a.rstd_q = at<float>(c, c.L.rstd_q); a.rstd_k = at<float>(c, c.L.rstd_k);
+    a.dq_acc = at<float>(c, c.L.dq_acc); a.dk_acc = at<float>(c, c.L.dk_acc);
+    a.dv_acc = at<float>(c, c.L.dv_acc);
+    a.dq = static_cast<elem_t*>(dq); a.dk = static_cast<elem_t*>(dk); a.dv = static_cast<elem_t*>(dv);
+    a.dve = (ve != nullptr) ? dve : nullptr;
+    a.gpart = at<float>(c, c.L.gpart);
+    a.status = at<uint32_t>(c, c.L.status);
+    dim3 grid(kPostBlocks, 3);
+    if (P.d == 64) bwd_post_kernel<64><<<grid, kRowWarps * 32, 0, st>>>(a);
+    else bwd_post_kernel<128><<<grid, kRowWarps * 32, 0, st>>>(a);
+    if ((s = launched()) != SWA_OK) return s;
+    if (dgq || dgk) {
+      GainArgs g{P.d, at<float>(c, c.L.gpart), dgq, dgk};
+      gain_sum_kernel<<<2, 128, 0, st>>>(g);
+      if ((s = launched()) != SWA_OK) return s;
+    }
+  }
+  return SWA_OK;
+}
+
+swa_status swa_attn_check_status(void* workspace, void* stream) {
+  if (workspace == nullptr || !aligned(workspace, 256)) return SWA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SWA_ERR_CUDA;
+  if (word != 0) {
+    if (cudaMemsetAsync(workspace, 0, sizeof(word), st) != cudaSuccess) return SWA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SWA_ERR_CUDA;
+  }
+  if (word & DEV_ERR_TIMEOUT) return SWA_ERR_TIMEOUT;
+  if (word & (DEV_ERR_TOKEN | DEV_ERR_BOUNDS)) return SWA_ERR_DEVICE_CHECK;
+  return SWA_OK;
+}
+
+int swa_sssl_window(int layer, int n_layer, const char* pattern, int T) {
+  if (pattern == nullptr || pattern[0] == '\0' || n_layer < 1 || layer < 0 || layer >= n_layer ||
+      T < 0)
+    return -2;
+  const size_t n = std::strlen(pattern);
+  for (size_t i = 0; i < n; ++i)
+    if (pattern[i] != 'S' && pattern[i] != 'L') return -2;
+  if (layer == n_layer - 1) return -1;  // the last layer is always global
+  return pattern[static_cast<size_t>(layer) % n] == 'S' ? T / 2 : -1;
+}
+
+int swa_has_ve(int layer, int n_layer) {
+  if (n_layer < 1 || layer < 0 || layer >= n_layer) return -1;
+  return (layer % 2) == ((n_layer - 1) % 2) ? 1 : 0;
+}
+
+const char* swa_strerror(swa_status s) {
+  switch (s) {
+    case SWA_OK: return "ok";
+    case SWA_ERR_INVALID_ARG: return "invalid argument";
+    case SWA_ERR_UNSUPPORTED: return "unsupported configuration (head dim, sizes or GPU)";
+    case SWA_ERR_CUDA: return "CUDA call failed";
+    case SWA_ERR_TIMEOUT: return "a device pipeline wait ran out of time";
+    case SWA_ERR_WORKSPACE: return "workspace too small";
+    case SWA_ERR_DEVICE_CHECK: return "device check failed (token id outside the table)";
+  }
+  return "unknown status";
+}
+
+const char* swa_build_info(void) {
+#if defined(SWA_ELEM_FP32)
+  return "swa_attn fp32 SIMT debug build, sm_103a";
+#else
+  return "swa_attn bf16 tcgen05 build, sm_103a";
+#endif
+}
+
+}  // extern "C"

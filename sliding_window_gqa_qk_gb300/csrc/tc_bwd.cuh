@@ -1,0 +1,477 @@
+// Backward attention core on the 5th-generation tensor cores (sm_103a).
+//
+// One CTA owns one 128-key tile of one (batch, kv head). It keeps its K and
+// V tiles in shared memory and its dK and dV accumulators in TMEM, and loops
+// over the G query heads of its GQA group and, for each, over the query tiles
+// of the band (tiles outside the band are never visited). So dK and dV are
+// reduced over the head group inside the CTA, without atomics. Per step, for
+// a query tile of BQ rows:
+//   S^T  = K Q^T          (TMEM)   P^T  = exp2(S^T c - LSE log2 e), masked on
+//   dP^T = V dO^T         (TMEM)          partial tiles           (smem, bf16)
+//   dS^T = P^T (dP^T - D)   (smem, bf16), D = rowsum(dO * O)
+//   dV  += P^T dO,  dK += dS^T Q                                   (TMEM)
+//   dQ   = dS K  (computed as dQ^T = K^T dS^T when d = 128)         (TMEM)
+// and dQ * scale is added into an fp32 accumulator with vector/coalesced
+// reductions (the only cross-CTA exchange).
+//
+// Roles: warp 4 TMA producer (K, V once; Q, dO, LSE, D per step, 2 stages),
+// warp 5 MMA issuer (one thread) and TMEM owner, warps 0-3 the element-wise
+// softmax backward (thread t owns key row t, TMEM lane t) and the dQ drain.
+//
+// Softmax backward written out from the forward of the attention block
+// (autoresearch Administrator & Developer Guide §8.2.1; train.py
+// walkthrough post, model paragraph): dS = P * (dP - rowsum(dP * P)) with
+// rowsum(dP * P) = rowsum(dO * O).
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include "../../include/swa_attn.h"
+#include "common.cuh"
+#include "tc_fwd.cuh"
+
+namespace swa {
+namespace tc {
+
+constexpr int kBK = 128;          // keys per CTA
+constexpr int kBwdThreads = 192;  // 6 warps
+
+struct BwdLaunch {
+  int B, T, Hq, Hkv, d, window, causal;
+  float scale;
+  const elem_t* qn;    // [B, Hq, T, d]
+  const elem_t* kn;    // [B, Hkv, T, d]
+  const elem_t* v;     // [B, Hkv, T, d] (v_head_major) or [B, T, Hkv, d]
+  bool v_head_major;
+  const elem_t* dO;    // [B, T, Hq, d]
+  const float* lse2;   // [B, Hq, Tpad]  LSE * log2(e)
+  const float* dvec;   // [B, Hq, Tpad]  D
+  int Tpad;
+  float* dq_acc;       // [B, Hq, T, d]
+  float* dk_acc;       // [B, Hkv, T, d]
+  float* dv_acc;       // [B, Hkv, T, d]
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+};
+
+struct BwdParams {
+  int T, Tpad, Hq, Hkv, window, causal, n_ktiles;
+  float scale, scale_log2;
+  const float* lse2;
+  const float* dvec;
+  float* dq_acc;
+  float* dk_acc;
+  float* dv_acc;
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+};
+
+template <int D>
+struct BwdCfg {
+  static constexpr int BQ = D == 128 ? 64 : 128;   // query rows per step
+  static constexpr int kKV = kBK * D * 2;          // K or V tile bytes
+  static constexpr int kQ = BQ * D * 2;            // Q or dO tile bytes
+  static constexpr int kP = kBK * BQ * 2;          // P^T or dS^T bytes
+  static constexpr int oK = 0;
+  static constexpr int oV = oK + kKV;
+  static constexpr int oQ = oV + kKV;              // 2 stages
+  static constexpr int oG = oQ + 2 * kQ;           // dO, 2 stages
+  static constexpr int oP = oG + 2 * kQ;
+  static constexpr int oS = oP + kP;
+  static constexpr int oL = oS + kP;               // LSE2, 2 stages of BQ floats
+  static constexpr int oD = oL + 2 * BQ * 4;       // D, 2 stages
+  static constexpr int kBytes = oD + 2 * BQ * 4;
+  static constexpr int kAlloc = kBytes + 1024;
+  // TMEM columns
+  static constexpr uint32_t cS = 0, cDP = BQ, cDV = 2 * BQ, cDK = 2 * BQ + D, cDQ = 2 * BQ + 2 * D;
+};
+
+enum {
+  BB_KV = 0,
+  BB_QFULL = 1,    // +stage
+  BB_QEMPTY = 3,   // +stage
+  BB_SFULL = 5,
+  BB_DPFULL = 6,
+  BB_PREADY = 7,
+  BB_DSREADY = 8,
+  BB_DQFULL = 9,
+  BB_DQFREE = 10,
+  BB_FINAL = 11,
+  BB_COUNT = 12
+};
+
+// Writes one bf16 row of 64-column swizzle regions: row r of a [rows][cols]
+// K-major SW128 tile (cols / 64 regions of rows * 128 bytes).
+__device__ __forceinline__ void st_sw128_chunk(uint32_t tile, int rows, int r, int chunk,
+                                               uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  const uint32_t region = static_cast<uint32_t>(chunk >> 3) * rows * 128;
+  const uint32_t addr = tile + region + (r >> 3) * 1024 + (r & 7) * 128 +
+                        static_cast<uint32_t>((chunk & 7) ^ (r & 7)) * 16;
+  st_shared_v4(addr, a, b, c, d);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                  const BwdParams prm) {
+  using C = BwdCfg<D>;
+  constexpr int BQ = C::BQ;
+  constexpr int KCH = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t bars[BB_COUNT];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ uint32_t abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bhk = blockIdx.x;                 // b * Hkv + hk
+  const int b = bhk / prm.Hkv, hk = bhk % prm.Hkv;
+  const int kt = blockIdx.y;                  // early key tiles (heaviest) first
+  const int k0 = kt * kBK;
+  const int G = prm.Hq / prm.Hkv;
+  const Band band{prm.T, prm.window, prm.causal};
+  int qlo = 0, qhi = -1;
+  q_tile_range(band, k0, kBK, BQ, qlo, qhi);
+  const int nq = qhi - qlo + 1;
+  const int n_it = nq > 0 ? nq * G : 0;
+  const WaitCtl ctl{&abort_flag, prm.status, prm.wait_limit_ns};
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(bar(BB_KV), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(BB_QFULL + s), 1);
+      mbar_init(bar(BB_QEMPTY + s), 1);
+    }
+    mbar_init(bar(BB_SFULL), 1);
+    mbar_init(bar(BB_DPFULL), 1);
+    mbar_init(bar(BB_PREADY), 4);
+    mbar_init(bar(BB_DSREADY), 4);
+    mbar_init(bar(BB_DQFULL), 1);
+    mbar_init(bar(BB_DQFREE), 4);
+    mbar_init(bar(BB_FINAL), 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&tmem_base_sh), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0 && n_it > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmG);
+      mbar_arrive_expect_tx(bar(BB_KV), 2 * C::kKV);
+      for (int c = 0; c < KCH; ++c) {
+        tma_load_4d(sbase + C::oK + c * kBK * 128, &tmK, bar(BB_KV), 64 * c, k0, hk, b);
+        tma_load_4d(sbase + C::oV + c * kBK * 128, &tmV, bar(BB_KV), 64 * c, k0, hk, b);
+      }
+      int last[2] = {-1, -1};
+      for (int it = 0; it < n_it; ++it) {
+        const int st = it & 1;
+        const int h = hk * G + it / nq;
+        const int q0 = (qlo + it % nq) * BQ;
+        if (it >= 2 && !mbar_wait(bar(BB_QEMPTY + st), ((it - 2) >> 1) & 1, ctl)) break;
+        last[st] = it;
+        mbar_arrive_expect_tx(bar(BB_QFULL + st), 2 * C::kQ + 2 * BQ * 4);
+        for (int c = 0; c < KCH; ++c) {
+          tma_load_4d(sbase + C::oQ + st * C::kQ + c * BQ * 128, &tmQ, bar(BB_QFULL + st), 64 * c,
+                      q0, h, b);
+          tma_load_4d(sbase + C::oG + st * C::kQ + c * BQ * 128, &tmG, bar(BB_QFULL + st), 64 * c,
+                      q0, h, b);
+        }
+        const long long row = (static_cast<long long>(b) * prm.Hq + h) * prm.Tpad + q0;
+        bulk_load(sbase + C::oL + st * BQ * 4, prm.lse2 + row, BQ * 4, bar(BB_QFULL + st));
+        bulk_load(sbase + C::oD + st * BQ * 4, prm.dvec + row, BQ * 4, bar(BB_QFULL + st));
+      }
+      // Let every copy this thread started land before the CTA can exit.
+      mbar_wait_drain(bar(BB_KV), 0, prm.wait_limit_ns);
+      for (int s = 0; s < 2; ++s)
+        if (last[s] >= 0) mbar_wait_drain(bar(BB_QFULL + s), (last[s] >> 1) & 1, prm.wait_limit_ns);
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0 && n_it > 0) {
+      constexpr uint32_t idST = idesc_bf16_f32(kBK, BQ, 0, 0);   // S^T, dP^T
+      constexpr uint32_t idKV = idesc_bf16_f32(kBK, D, 0, 1);    // dV, dK
+      constexpr uint32_t idQ = idesc_bf16_f32(128, 64, 1, 1);    // dQ^T (D=128) or dQ (D=64)
+      const uint32_t sK = sbase + C::oK, sV = sbase + C::oV;
+      const uint32_t sP = sbase + C::oP, sS = sbase + C::oS;
+      bool ok = mbar_wait(bar(BB_KV), 0, ctl);
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int st = it & 1, ph = it & 1;
+        const uint32_t sQ = sbase + C::oQ + st * C::kQ, sG = sbase + C::oG + st * C::kQ;
+        if (!(ok = mbar_wait(bar(BB_QFULL + st), (it >> 1) & 1, ctl))) break;
+        tc_fence_after();
+        // S^T = K Q^T and dP^T = V dO^T (K = D)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t offA = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
+          const uint32_t offB = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+          umma_bf16_ss(tmem + C::cS, sdesc_sw128(sK + offA, 16, 1024),
+                       sdesc_sw128(sQ + offB, 16, 1024), idST, kk > 0);
+        }
+        umma_commit(bar(BB_SFULL));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t offA = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
+          const uint32_t offB = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+          umma_bf16_ss(tmem + C::cDP, sdesc_sw128(sV + offA, 16, 1024),
+                       sdesc_sw128(sG + offB, 16, 1024), idST, kk > 0);
+        }
+        umma_commit(bar(BB_DPFULL));
+        // dV += P^T dO (K = BQ queries)
+        if (!(ok = mbar_wait(bar(BB_PREADY), ph, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          umma_bf16_ss(tmem + C::cDV, sdesc_sw128(sP + (kk >> 2) * (kBK * 128) + (kk & 3) * 32, 16, 1024),
+                       sdesc_sw128(sG + kk * 2048, BQ * 128, 1024), idKV, (it > 0 || kk > 0));
+        }
+        // dK += dS^T Q
+        if (!(ok = mbar_wait(bar(BB_DSREADY), ph, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          umma_bf16_ss(tmem + C::cDK, sdesc_sw128(sS + (kk >> 2) * (kBK * 128) + (kk & 3) * 32, 16, 1024),
+                       sdesc_sw128(sQ + kk * 2048, BQ * 128, 1024), idKV, (it > 0 || kk > 0));
+        }
+        // dQ (K = 128 keys); its TMEM columns must have been drained.
+        if (it >= 1 && !(ok = mbar_wait(bar(BB_DQFREE), (it - 1) & 1, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint32_t aa = (D == 128 ? sK : sS) + kk * 2048;
+          const uint32_t bb = (D == 128 ? sS : sK) + kk * 2048;
+          umma_bf16_ss(tmem + C::cDQ, sdesc_sw128(aa, kBK * 128, 1024),
+                       sdesc_sw128(bb, kBK * 128, 1024), idQ, kk > 0);
+        }
+        umma_commit(bar(BB_DQFULL));
+        umma_commit(bar(BB_QEMPTY + st));
+      }
+      umma_commit(bar(BB_FINAL));
+      mbar_wait_drain(bar(BB_FINAL), 0, prm.wait_limit_ns);
+    }
+  } else {
+    // ---------------- softmax-backward warpgroup (warps 0-3) ----------------
+    const int t = threadIdx.x;                       // key row / TMEM lane
+    const int j = k0 + t;                            // key position
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float c = prm.scale_log2;
+    const uint32_t sP = sbase + C::oP, sS = sbase + C::oS;
+    bool ok = true;
+    for (int it = 0; it < n_it && ok; ++it) {
+      const int st = it & 1, ph = it & 1;
+      const int h = hk * G + it / nq;
+      const int q0 = (qlo + it % nq) * BQ;
+      const float* sL = reinterpret_cast<const float*>(smem + C::oL + st * BQ * 4);
+      const float* sDv = reinterpret_cast<const float*>(smem + C::oD + st * BQ * 4);
+      // visible query columns of this key row: [clo, chi]
+      int clo = 0, chi = BQ - 1;
+      const bool full = tile_full(band, q0, BQ, k0, kBK);
+      if (!full) {
+        if (j >= prm.T) {
+          clo = 1; chi = 0;
+        } else {
+          if (prm.T - 1 - q0 < chi) chi = prm.T - 1 - q0;
+          if (prm.causal) {
+            if (j - q0 > clo) clo = j - q0;
+            if (prm.window >= 0 && j + prm.window - q0 < chi) chi = j + prm.window - q0;
+          } else if (prm.window >= 0) {
+            if (j - prm.window - q0 > clo) clo = j - prm.window - q0;
+            if (j + prm.window - q0 < chi) chi = j + prm.window - q0;
+          }
+        }
+      }
+      if (!(ok = mbar_wait(bar(BB_QFULL + st), (it >> 1) & 1, ctl))) break;
+      if (!(ok = mbar_wait(bar(BB_SFULL), ph, ctl))) break;
+      tc_fence_after();
+      uint32_t sr[BQ / 32][32];
+#pragma unroll
+      for (int cc = 0; cc < BQ / 32; ++cc) tmem_ld32(tmem + C::cS + lane_off + cc * 32, sr[cc]);
+      tmem_wait_ld(sr[0]);
+#pragma unroll
+      for (int cc = 1; cc < BQ / 32; ++cc) reg_fence(sr[cc]);
+      // P^T = exp2(S^T c - LSE2), masked; kept in fp32 registers for dS.
+#pragma unroll
+      for (int cc = 0; cc < BQ / 32; ++cc)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int col = cc * 32 + e;
+          const float p = ex2_approx(fmaf(__uint_as_float(sr[cc][e]), c, -sL[col]));
+          sr[cc][e] = __float_as_uint((col >= clo && col <= chi) ? p : 0.f);
+        }
+#pragma unroll
+      for (int ch = 0; ch < BQ / 8; ++ch) {
+        const int cc = ch >> 2, e0 = (ch & 3) * 8;
+        st_sw128_chunk(sP, kBK, t, ch,
+                       pack_bf16x2(__uint_as_float(sr[cc][e0 + 0]), __uint_as_float(sr[cc][e0 + 1])),
+                       pack_bf16x2(__uint_as_float(sr[cc][e0 + 2]), __uint_as_float(sr[cc][e0 + 3])),
+                       pack_bf16x2(__uint_as_float(sr[cc][e0 + 4]), __uint_as_float(sr[cc][e0 + 5])),
+                       pack_bf16x2(__uint_as_float(sr[cc][e0 + 6]), __uint_as_float(sr[cc][e0 + 7])));
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BB_PREADY));
+      // dS^T = P^T (dP^T - D)
+      if (!(ok = mbar_wait(bar(BB_DPFULL), ph, ctl))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < BQ / 32; ++cc) {
+        uint32_t dp[32];
+        tmem_ld32(tmem + C::cDP + lane_off + cc * 32, dp);
+        tmem_wait_ld(dp);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int col = cc * 32 + e;
+          const float p = __uint_as_float(sr[cc][e]);
+          const float ds = p * (__uint_as_float(dp[e]) - sDv[col]);
+          sr[cc][e] = __float_as_uint((col >= clo && col <= chi) ? ds : 0.f);
+        }
+      }
+#pragma unroll
+      for (int ch = 0; ch < BQ / 8; ++ch) {
+        const int cc = ch >> 2, e0 = (ch & 3) * 8;
+        st_sw128_chunk(sS, kBK, t, ch,
+                       pack_bf16x2(__uint_as_float(sr[cc][e0 + 0]), __uint_as_float(sr[cc][e0 + 1])),
+                       pack_bf16x2(__uint_as_float(sr[cc][e0 + 2]), __uint_as_float(sr[cc][e0 + 3])),
+                       pack_bf16x2(__uint_as_float(sr[cc][e0 + 4]), __uint_as_float(sr[cc][e0 + 5])),
+                       pack_bf16x2(__uint_as_float(sr[cc][e0 + 6]), __uint_as_float(sr[cc][e0 + 7])));
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BB_DSREADY));
+      // dQ drain: scale and add into the fp32 accumulator.
+      if (!(ok = mbar_wait(bar(BB_DQFULL), ph, ctl))) break;
+      tc_fence_after();
+      const long long qrow0 = (static_cast<long long>(b) * prm.Hq + h) * prm.T + q0;
+      if constexpr (D == 128) {
+        // dQ^T: lane = head-dim index t, columns = BQ queries.
+#pragma unroll
+        for (int cc = 0; cc < BQ / 32; ++cc) {
+          uint32_t dq[32];
+          tmem_ld32(tmem + C::cDQ + lane_off + cc * 32, dq);
+          tmem_wait_ld(dq);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int qq = cc * 32 + e;
+            if (q0 + qq < prm.T)
+              atomicAdd(prm.dq_acc + (qrow0 + qq) * D + t, __uint_as_float(dq[e]) * prm.scale);
+          }
+        }
+      } else {
+        // dQ: lane = query row t, columns = D.
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t dq[32];
+          tmem_ld32(tmem + C::cDQ + lane_off + cc * 32, dq);
+          tmem_wait_ld(dq);
+          if (q0 + t < prm.T) {
+            float* dst = prm.dq_acc + (qrow0 + t) * D + cc * 32;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              red_add_v4_f32(dst + e, __uint_as_float(dq[e]) * prm.scale,
+                             __uint_as_float(dq[e + 1]) * prm.scale,
+                             __uint_as_float(dq[e + 2]) * prm.scale,
+                             __uint_as_float(dq[e + 3]) * prm.scale);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BB_DQFREE));
+    }
+    // ---- epilogue: dK (scaled) and dV rows of this key tile ----
+    if (ok && j < prm.T) {
+      const long long krow = (static_cast<long long>(b) * prm.Hkv + hk) * prm.T + j;
+      float* dkd = prm.dk_acc + krow * D;
+      float* dvd = prm.dv_acc + krow * D;
+      if (n_it == 0) {
+        for (int e = 0; e < D; e += 4) {
+          *reinterpret_cast<float4*>(dkd + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(dvd + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    }
+    if (ok && n_it > 0) {
+      tc_fence_after();
+      const long long krow = (static_cast<long long>(b) * prm.Hkv + hk) * prm.T + j;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t vk[32], vv[32];
+        tmem_ld32(tmem + C::cDK + lane_off + cc * 32, vk);
+        tmem_ld32(tmem + C::cDV + lane_off + cc * 32, vv);
+        tmem_wait_ld(vk);
+        reg_fence(vv);
+        if (j < prm.T) {
+          float* dkd = prm.dk_acc + krow * D + cc * 32;
+          float* dvd = prm.dv_acc + krow * D + cc * 32;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            *reinterpret_cast<float4*>(dkd + e) =
+                make_float4(__uint_as_float(vk[e]) * prm.scale, __uint_as_float(vk[e + 1]) * prm.scale,
+                            __uint_as_float(vk[e + 2]) * prm.scale, __uint_as_float(vk[e + 3]) * prm.scale);
+            *reinterpret_cast<float4*>(dvd + e) =
+                make_float4(__uint_as_float(vv[e]), __uint_as_float(vv[e + 1]),
+                            __uint_as_float(vv[e + 2]), __uint_as_float(vv[e + 3]));
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+inline swa_status launch_bwd_d(const BwdLaunch& f, cudaStream_t st) {
+  using C = BwdCfg<D>;
+  CUtensorMap mq, mk, mv, mg;
+  if (!make_map_4d(&mq, f.qn, D, f.T, f.Hq, f.B, D, static_cast<long long>(f.T) * D,
+                   static_cast<long long>(f.Hq) * f.T * D, C::BQ) ||
+      !make_map_4d(&mg, f.dO, D, f.T, f.Hq, f.B, static_cast<long long>(f.Hq) * D, D,
+                   static_cast<long long>(f.T) * f.Hq * D, C::BQ) ||
+      !map_head_major(&mk, f.kn, f.B, f.Hkv, f.T, D))
+    return SWA_ERR_CUDA;
+  const bool okv = f.v_head_major ? map_head_major(&mv, f.v, f.B, f.Hkv, f.T, D)
+                                  : map_token_major(&mv, f.v, f.B, f.Hkv, f.T, D);
+  if (!okv) return SWA_ERR_CUDA;
+  BwdParams p{};
+  p.T = f.T; p.Tpad = f.Tpad; p.Hq = f.Hq; p.Hkv = f.Hkv; p.window = f.window; p.causal = f.causal;
+  p.n_ktiles = (f.T + kBK - 1) / kBK;
+  p.scale = f.scale;
+  p.scale_log2 = f.scale * 1.4426950408889634f;
+  p.lse2 = f.lse2; p.dvec = f.dvec;
+  p.dq_acc = f.dq_acc; p.dk_acc = f.dk_acc; p.dv_acc = f.dv_acc;
+  p.status = f.status; p.wait_limit_ns = f.wait_limit_ns;
+  if (cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kAlloc) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  dim3 grid(f.B * f.Hkv, p.n_ktiles);
+  bwd_tc_kernel<D><<<grid, kBwdThreads, C::kAlloc, st>>>(mq, mk, mv, mg, p);
+  return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
+inline swa_status launch_bwd(const BwdLaunch& f, cudaStream_t st) {
+  return f.d == 64 ? launch_bwd_d<64>(f, st) : launch_bwd_d<128>(f, st);
+}
+
+}  // namespace tc
+}  // namespace swa

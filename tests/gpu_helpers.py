@@ -1,0 +1,84 @@
+"""Shared helpers of the GPU parity tests: run the library through its C ABI
+and the float64 oracle on the same seeded inputs, and compare."""
+
+import numpy as np
+import torch
+
+import oracle
+import sliding_window_gqa_qk_gb300 as swa
+from sliding_window_gqa_qk_gb300.inputs import as_f64, make_inputs
+
+TOL = {"bf16": 2e-2, "fp32": 1e-5}
+DTYPE = {"bf16": torch.bfloat16, "fp32": torch.float32}
+
+
+def gate_for(p, seed=7):
+    g = torch.Generator().manual_seed(seed)
+    return 2.0 * torch.sigmoid(torch.randn(p.B, p.T, p.Hkv, generator=g))
+
+
+def inputs(p, kind, layer=0, with_gate=False):
+    x = make_inputs(p, layer=layer, dtype=DTYPE[kind])
+    x["gate"] = gate_for(p) if (with_gate and p.ve) else None
+    return x
+
+
+def run_library(p, x, reuse_prologue=True):
+    """Forward + backward through the C ABI on cuda:0. Returns CPU tensors."""
+    dev = torch.device("cuda:0")
+    g = {k: (t.to(dev).contiguous() if t is not None else None) for k, t in x.items()}
+    o, lse, ws = swa.attention_forward(
+        g["q"], g["k"], g["v"], g["gq"], g["gk"], window=p.window, causal=p.causal, eps=p.eps,
+        ve=g["ve"], tok=g["tok"], ve_gate=g["gate"], ve_scale=p.ve_scale)
+    grads = swa.attention_backward(
+        g["q"], g["k"], g["v"], g["gq"], g["gk"], o, lse, g["dO"], window=p.window,
+        causal=p.causal, eps=p.eps, ve=g["ve"], tok=g["tok"], ve_gate=g["gate"],
+        ve_scale=p.ve_scale, workspace=ws, reuse_prologue=reuse_prologue)
+    kind = "fp32" if x["q"].dtype == torch.float32 else "bf16"
+    status = swa.swa_attn_check_status(ws, kind=kind)
+    torch.cuda.synchronize()
+    out = {"o": o.cpu(), "lse": lse.cpu(), "status": status}
+    for k in ("dq", "dk", "dv", "dgq", "dgk", "dve"):
+        out[k] = grads[k].cpu() if grads[k] is not None else None
+    return out
+
+
+def run_oracle(p, x, b_slice=None):
+    f = {k: as_f64(t) for k, t in x.items()}
+    tok = x["tok"].numpy() if x["tok"] is not None else None
+    gate = f["gate"]
+    q, k, v, dO = f["q"], f["k"], f["v"], f["dO"]
+    if b_slice is not None:
+        sl = slice(b_slice, b_slice + 1)
+        q, k, v, dO = q[sl], k[sl], v[sl], dO[sl]
+        tok = tok[sl] if tok is not None else None
+        gate = gate[sl] if gate is not None else None
+    kw = dict(window=p.window, causal=p.causal, eps=p.eps, ve=f["ve"], tok=tok, gate=gate,
+              ve_scale=p.ve_scale)
+    o, lse = oracle.attention_forward(q, k, v, f["gq"], f["gk"], **kw)
+    ref = oracle.attention_backward(q, k, v, f["gq"], f["gk"], dO, **kw)
+    ref["o"], ref["lse"] = o, lse
+    return ref
+
+
+def rel_err(a, r):
+    a = as_f64(a) if isinstance(a, torch.Tensor) else np.asarray(a, dtype=np.float64)
+    r = np.asarray(r, dtype=np.float64)
+    assert a.shape == r.shape, (a.shape, r.shape)
+    assert np.all(np.isfinite(a)), "non-finite values"
+    den = np.linalg.norm(r)
+    return float(np.linalg.norm(a - r) / den) if den > 0 else float(np.linalg.norm(a))
+
+
+def compare(got, ref, tol, keys=("o", "lse", "dq", "dk", "dv", "dgq", "dgk", "dve"), sl=None):
+    errs = {}
+    for k in keys:
+        if ref.get(k) is None:
+            continue
+        a = got[k]
+        if sl is not None and k not in ("dgq", "dgk", "dve"):
+            a = a[sl]
+        errs[k] = rel_err(a, ref[k])
+    bad = {k: e for k, e in errs.items() if not e <= tol}
+    assert not bad, f"relative errors above {tol}: {bad} (all: {errs})"
+    return errs

@@ -1,0 +1,176 @@
+"""Host-side checks of the C ABI: both libraries load, export every function
+the header declares, and reject bad arguments with the documented status
+before touching the GPU. No test here launches a kernel."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import sliding_window_gqa_qk_gb300 as swa
+from sliding_window_gqa_qk_gb300 import build as swa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "swa_attn.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden", "sssl_8_layers.txt")
+
+KINDS = ["bf16", "fp32"]
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built_libraries():
+    swa_build.build()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(swa_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_library_loads_and_exports_every_declared_symbol(kind):
+    lib = swa.load(kind)
+    names = declared_functions()
+    assert "swa_attn_fwd" in names and "swa_attn_bwd" in names
+    for name in names:
+        assert hasattr(lib, name), name
+    info = swa.swa_build_info(kind)
+    assert ("bf16" in info) == (kind == "bf16")
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_layer_schedule_matches_pages_example(kind):
+    rows = [l.split() for l in open(GOLDEN) if l.strip() and not l.startswith("#")]
+    for layer, _, window, ve in rows:
+        assert swa.swa_sssl_window(int(layer), 8, "SSSL", 2048, kind) == int(window)
+        assert swa.swa_has_ve(int(layer), 8, kind) == int(ve)
+
+
+def test_layer_schedule_helpers_reject_bad_arguments():
+    assert swa.swa_sssl_window(0, 8, "SXSL", 2048) == -2
+    assert swa.swa_sssl_window(8, 8, "SSSL", 2048) == -2
+    assert swa.swa_sssl_window(-1, 8, "SSSL", 2048) == -2
+    assert swa.load("bf16").swa_sssl_window(0, 8, None, 2048) == -2
+    assert swa.swa_sssl_window(0, 8, "", 2048) == -2
+    assert swa.swa_has_ve(3, 0) == -1
+    assert swa.swa_has_ve(-1, 4) == -1
+    # last layer forced global even for an all-local pattern
+    assert swa.swa_sssl_window(5, 6, "S", 100) == -1
+    assert swa.swa_sssl_window(4, 6, "S", 101) == 50
+
+
+def test_strerror_covers_every_status():
+    texts = {swa.swa_strerror(s) for s in range(7)}
+    assert len(texts) == 7
+    assert "unknown" in swa.swa_strerror(99)
+
+
+def params(**kw):
+    base = dict(B=2, T=300, Hq=4, Hkv=2, d=128, window=150, causal=True, softmax_scale=0.0,
+                eps=1e-6, ve_scale=0.5, vocab=0)
+    base.update(kw)
+    return swa.make_params(**base)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_workspace_size(kind):
+    p = params()
+    fwd = swa.swa_attn_workspace_size(p, 0, kind)
+    bwd = swa.swa_attn_workspace_size(p, 1, kind)
+    es = 2 if kind == "bf16" else 4
+    B, T, Hq, Hkv, d = 2, 300, 4, 2, 128
+    assert fwd >= 256 + B * T * d * (Hq + 2 * Hkv) * es + 4 * B * T * (Hq + Hkv)
+    assert bwd >= fwd + 4 * B * T * d * (Hq + 2 * Hkv)
+    assert fwd % 256 == 0 and bwd % 256 == 0
+    assert swa.swa_attn_workspace_size(params(d=96), 0, kind) == 0
+    assert swa.swa_attn_workspace_size(params(Hq=3), 0, kind) == 0
+
+
+# Fake, never-dereferenced device addresses: argument checks run before any
+# CUDA call, so these are safe on a machine without a GPU.
+A = 1 << 20          # 16-byte aligned
+MIS = A + 8          # not 16-byte aligned
+
+
+def fwd_call(p, kind="bf16", ws_bytes=1 << 40, **over):
+    args = dict(q=A, k=A, v=A, gq=None, gk=None, ve=None, tok=None, gate=None, o=A, lse=A,
+                ws=A, flags=0)
+    args.update(over)
+    lib = swa.load(kind)
+    return lib.swa_attn_fwd(ctypes.byref(p), args["q"], args["k"], args["v"], args["gq"],
+                            args["gk"], args["ve"], args["tok"], args["gate"], args["o"],
+                            args["lse"], args["ws"], ws_bytes, args["flags"], None)
+
+
+def bwd_call(p, kind="bf16", ws_bytes=1 << 40, **over):
+    args = dict(q=A, k=A, v=A, gq=None, gk=None, ve=None, tok=None, gate=None, o=A, lse=A,
+                dO=A, dq=A, dk=A, dv=A, dgq=None, dgk=None, dve=None, ws=A, flags=0)
+    args.update(over)
+    lib = swa.load(kind)
+    return lib.swa_attn_bwd(ctypes.byref(p), *[args[k] for k in (
+        "q", "k", "v", "gq", "gk", "ve", "tok", "gate", "o", "lse", "dO", "dq", "dk", "dv", "dgq",
+        "dgk", "dve", "ws")], ws_bytes, args["flags"], None)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("bad,expect", [
+    (dict(Hq=3, Hkv=2), swa.SWA_ERR_INVALID_ARG),
+    (dict(Hkv=0), swa.SWA_ERR_INVALID_ARG),
+    (dict(B=-1), swa.SWA_ERR_INVALID_ARG),
+    (dict(T=-5), swa.SWA_ERR_INVALID_ARG),
+    (dict(window=-2), swa.SWA_ERR_INVALID_ARG),
+    (dict(d=96), swa.SWA_ERR_UNSUPPORTED),
+    (dict(d=256), swa.SWA_ERR_UNSUPPORTED),
+    (dict(eps=-1.0), swa.SWA_ERR_INVALID_ARG),
+    (dict(softmax_scale=-0.1), swa.SWA_ERR_INVALID_ARG),
+    (dict(softmax_scale=float("nan")), swa.SWA_ERR_INVALID_ARG),
+    (dict(ve_scale=float("inf")), swa.SWA_ERR_INVALID_ARG),
+    (dict(T=(1 << 22) + 1), swa.SWA_ERR_UNSUPPORTED),
+])
+def test_bad_params_are_rejected(kind, bad, expect):
+    p = params(**bad)
+    assert fwd_call(p, kind) == expect
+    assert bwd_call(p, kind) == expect
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_bad_pointers_flags_and_workspace_are_rejected(kind):
+    p = params()
+    lib = swa.load(kind)
+    assert lib.swa_attn_fwd(None, A, A, A, None, None, None, None, None, A, A, A, 1 << 40, 0,
+                            None) == swa.SWA_ERR_INVALID_ARG
+    for name in ("q", "k", "v", "o", "lse", "ws"):
+        assert fwd_call(p, kind, **{name: None}) == swa.SWA_ERR_INVALID_ARG, name
+    for name in ("q", "k", "v", "o"):
+        assert fwd_call(p, kind, **{name: MIS}) == swa.SWA_ERR_INVALID_ARG, name
+    assert fwd_call(p, kind, ws=A + 16) == swa.SWA_ERR_INVALID_ARG       # workspace 256-aligned
+    assert fwd_call(p, kind, flags=2) == swa.SWA_ERR_INVALID_ARG
+    need = swa.swa_attn_workspace_size(p, 0, kind)
+    assert fwd_call(p, kind, ws_bytes=need - 1) == swa.SWA_ERR_WORKSPACE
+    # value embeddings need token ids and a vocabulary size
+    assert fwd_call(params(vocab=8), kind, ve=A) == swa.SWA_ERR_INVALID_ARG
+    assert fwd_call(params(vocab=0), kind, ve=A, tok=A) == swa.SWA_ERR_INVALID_ARG
+    assert fwd_call(params(vocab=8), kind, ve=MIS, tok=A) == swa.SWA_ERR_INVALID_ARG
+    # backward
+    for name in ("q", "k", "v", "o", "lse", "dO", "dq", "dk", "dv", "ws"):
+        assert bwd_call(p, kind, **{name: None}) == swa.SWA_ERR_INVALID_ARG, name
+    for name in ("dO", "dq", "dk", "dv"):
+        assert bwd_call(p, kind, **{name: MIS}) == swa.SWA_ERR_INVALID_ARG, name
+    assert bwd_call(p, kind, flags=16) == swa.SWA_ERR_INVALID_ARG
+    need_b = swa.swa_attn_workspace_size(p, 1, kind)
+    assert bwd_call(p, kind, ws_bytes=need_b - 1) == swa.SWA_ERR_WORKSPACE
+    assert bwd_call(p, kind, ws_bytes=need) == swa.SWA_ERR_WORKSPACE  # forward-sized only
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_empty_forward_is_a_no_op(kind):
+    # B == 0 or T == 0: valid, nothing launched (so it runs without a GPU)
+    assert fwd_call(params(B=0), kind) == swa.SWA_OK
+    assert fwd_call(params(T=0), kind) == swa.SWA_OK
+
+
+def test_binding_names_mirror_the_c_abi():
+    for name in declared_functions():
+        assert hasattr(swa, name), name

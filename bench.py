@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention-block library on the 8-layer SSSL stack.
+
+Workload (one "step"): the attention blocks of an 8-layer GPT with window
+pattern "SSSL" at B=16, T=2048, Hq=6, Hkv=3, d=128: forward of layers 0..7,
+then backward of layers 7..0. Layers 0,1,2,4,5,6 use a causal window of
+T/2 = 1024, layers 3 and 7 full causal attention; layers 1,3,5,7 add
+0.5 * VE[token] to v (VE table 8192 x 384 bf16 per layer). QK-RMSNorm gains
+~ 1 + 0.1 N(0,1). Seeded synthetic inputs (no dataset).
+
+Metric: masked (in-band) TFLOP/s of fwd + bwd, counting 4 d P B Hq FLOPs for
+the forward and 10 d P B Hq for the backward (the flash-attention convention,
+S recomputed), where P = sum_i (min(i, W) + 1) is the number of visible
+(query, key) pairs of one head.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) each rank runs its own batch (weak scaling, no
+collective on the data path); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from sliding_window_gqa_qk_gb300.inputs import Problem, make_inputs  # noqa: E402
+
+N_LAYER, PATTERN = 8, "SSSL"
+B, T, HQ, HKV, D = 16, 2048, 6, 3, 128
+VOCAB, VE_SCALE = 8192, 0.5
+METRIC = "masked TFLOP/s fwd+bwd, T=2048 SSSL layers; % of GB300 bf16 tensor-core peak"
+WORKLOAD = "8-layer SSSL stack (B=16, T=2048, Hq=6, Hkv=3, d=128, W=1024 on S layers, VE on odd layers)"
+
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
+# kernel, from the ncu capture summarised in profiles/ (None until captured
+# for the current kernel).
+NCU_TRAFFIC_BYTES = None
+
+
+def layer_schedule(window_fn, ve_fn):
+    return [(window_fn(i, N_LAYER, PATTERN, T), bool(ve_fn(i, N_LAYER))) for i in range(N_LAYER)]
+
+
+def pairs(Tn: int, W: int) -> int:
+    """Visible (query, key) pairs of one head, causal, window W (-1: none)."""
+    if W < 0 or W >= Tn - 1:
+        return Tn * (Tn + 1) // 2
+    # rows i <= W see i + 1 keys, rows beyond see W + 1
+    return (W + 1) * (W + 2) // 2 + (Tn - W - 1) * (W + 1)
+
+
+def flops(Bn, Tn, Hq, d, W):
+    P = pairs(Tn, W)
+    return 4 * d * P * Bn * Hq, 10 * d * P * Bn * Hq
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Oracle leg (CPU baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(schedule, layers=None):
+    """Runs the float64 oracle on one (batch element, kv head) slice of the
+    stack's layers: 1 x T=2048 x 2 query heads. Returns (seconds, masked
+    FLOPs of the sample, description)."""
+    import numpy as np  # noqa: F401
+    import oracle
+    from sliding_window_gqa_qk_gb300.inputs import as_f64
+    layers = list(range(N_LAYER)) if layers is None else layers
+    total_t, total_f = 0.0, 0
+    for li in layers:
+        W, ve = schedule[li]
+        p = Problem(B=1, T=T, Hq=HQ // HKV, Hkv=1, d=D, window=W, gain_std=0.1, ve=ve,
+                    vocab=VOCAB)
+        x = make_inputs(p, layer=li, seed=4242)
+        f = {k: as_f64(t) for k, t in x.items()}
+        tok = x["tok"].numpy() if x["tok"] is not None else None
+        kw = dict(window=W, eps=p.eps, ve=f["ve"], tok=tok, ve_scale=VE_SCALE)
+        t0 = time.perf_counter()
+        oracle.attention_forward(f["q"], f["k"], f["v"], f["gq"], f["gk"], **kw)
+        oracle.attention_backward(f["q"], f["k"], f["v"], f["gq"], f["gk"], f["dO"], **kw)
+        total_t += time.perf_counter() - t0
+        ff, fb = flops(1, T, HQ // HKV, D, W)
+        total_f += ff + fb
+    desc = (f"float64 oracle fwd+bwd of layers {layers[0]}..{layers[-1]} of the stack on one "
+            f"(batch element, kv head) slice: B=1, T={T}, Hq={HQ // HKV}, Hkv=1, d={D}")
+    return total_t, total_f, desc
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+
+class Stack:
+    def __init__(self, swa, dev):
+        self.swa = swa
+        self.dev = dev
+        self.sched = layer_schedule(swa.swa_sssl_window, swa.swa_has_ve)
+        self.layers = []
+        for li, (W, ve) in enumerate(self.sched):
+            p = Problem(B=B, T=T, Hq=HQ, Hkv=HKV, d=D, window=W, gain_std=0.1, ve=ve, vocab=VOCAB)
+            x = make_inputs(p, layer=li)
+            g = {k: (t.to(dev) if t is not None else None) for k, t in x.items()}
+            prm = swa.make_params(B, T, HQ, HKV, D, W, True, 0.0, p.eps, VE_SCALE,
+                                  VOCAB if ve else 0)
+            ws = swa.new_workspace(prm, True, dev, "bf16")
+            L = dict(p=p, prm=prm, x=x, g=g, ws=ws)
+            L["o"] = torch.empty_like(g["q"])
+            L["lse"] = torch.empty(B, HQ, T, dtype=torch.float32, device=dev)
+            L["dq"], L["dk"], L["dv"] = (torch.empty_like(g["q"]), torch.empty_like(g["k"]),
+                                         torch.empty_like(g["v"]))
+            L["dgq"] = torch.empty(D, dtype=torch.float32, device=dev)
+            L["dgk"] = torch.empty(D, dtype=torch.float32, device=dev)
+            L["dve"] = (torch.empty(g["ve"].shape, dtype=torch.float32, device=dev) if ve else None)
+            self.layers.append(L)
+        self.flops_fwd = sum(flops(B, T, HQ, D, W)[0] for W, _ in self.sched)
+        self.flops_bwd = sum(flops(B, T, HQ, D, W)[1] for W, _ in self.sched)
+
+    def fwd(self, L):
+        g = L["g"]
+        st = self.swa.swa_attn_fwd(L["prm"], g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"],
+                                   g["tok"], None, L["o"], L["lse"], L["ws"])
+        if st != 0:
+            raise self.swa.SwaError(st, "swa_attn_fwd")
+
+    def bwd(self, L, stage):
+        g = L["g"]
+        st = self.swa.swa_attn_bwd(L["prm"], g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"],
+                                   g["tok"], None, L["o"], L["lse"], g["dO"], L["dq"], L["dk"],
+                                   L["dv"], L["dgq"], L["dgk"], L["dve"], L["ws"],
+                                   flags=self.swa.SWA_REUSE_PROLOGUE | stage)
+        if st != 0:
+            raise self.swa.SwaError(st, "swa_attn_bwd")
+
+    def step(self, ev=None):
+        """One fwd+bwd pass over the 8 layers. With ev (a list of CUDA-event
+        pairs per stage) the stages are bracketed for per-kernel timing."""
+        swa = self.swa
+        for L in self.layers:
+            if ev is not None:
+                ev["fwd"].append(_ev_pair())
+                ev["fwd"][-1][0].record()
+            self.fwd(L)
+            if ev is not None:
+                ev["fwd"][-1][1].record()
+        for L in reversed(self.layers):
+            for name, stage in (("bwd_pre", swa.SWA_BWD_STAGE_PRE),
+                                ("bwd_main", swa.SWA_BWD_STAGE_MAIN),
+                                ("bwd_post", swa.SWA_BWD_STAGE_POST)):
+                if ev is not None:
+                    ev[name].append(_ev_pair())
+                    ev[name][-1][0].record()
+                self.bwd(L, stage)
+                if ev is not None:
+                    ev[name][-1][1].record()
+
+    # launches of our kernels per step: fwd = prologue + attention; bwd =
+    # pre + main + post + gain sum
+    LAUNCHES_PER_STEP = N_LAYER * (2 + 4)
+
+
+def _ev_pair():
+    return (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+
+
+def run_ours(args, rank, world, dev):
+    import sliding_window_gqa_qk_gb300 as swa
+    swa.load("bf16")
+    stack = Stack(swa, dev)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        stack.step()
+    st = swa.swa_attn_check_status(stack.layers[0]["ws"])
+    if st != swa.SWA_OK:
+        raise swa.SwaError(st, "device status after warm-up")
+    torch.cuda.synchronize()
+    _barrier(world)
+    ev = {k: [] for k in ("fwd", "bwd_pre", "bwd_main", "bwd_post")}
+    start, stop = _ev_pair()
+    gpu_index = torch.cuda.current_device()
+    with ClockSampler(_physical_index(gpu_index)) as clocks:
+        torch.cuda.synchronize()
+        start.record()
+        for _ in range(args.steps):
+            stack.step(ev)
+        stop.record()
+        torch.cuda.synchronize()
+    _barrier(world)
+    ms_total = start.elapsed_time(stop)
+    ms = _max_over_ranks(ms_total, world) / args.steps
+    stage_ms = {k: sum(a.elapsed_time(b) for a, b in v) / args.steps for k, v in ev.items()}
+    flops_step = stack.flops_fwd + stack.flops_bwd
+    value = flops_step * world / (ms * 1e-3) / 1e12
+
+    # dominant kernel: the backward main kernel (per launch = one layer)
+    peaks, peak_kind = load_peaks()
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    bwd_main_launch_ms = stage_ms["bwd_main"] / N_LAYER
+    achieved = stack.flops_bwd / N_LAYER / (bwd_main_launch_ms * 1e-3) / 1e12
+    fwd_launch_tflops = stack.flops_fwd / (stage_ms["fwd"] * 1e-3) / 1e12
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v/dO, gains 1+0.1N, VE N(0,0.02), tokens U[0,8192))",
+        "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": T,
+                   "parallelism": f"replicas over batch x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: 8 layers x ~0.4 GB of tensors per step",
+                   "flops_per_step": flops_step,
+                   "pct_of_peak": round(100 * value / world / peak, 2),
+                   "peak_tflops": peak, "peak_source": f"{peak_kind} bf16_tflops_sustained",
+                   "stage_ms_per_step": {k: round(v, 4) for k, v in stage_ms.items()},
+                   "fwd_tflops": round(fwd_launch_tflops, 1)},
+        "roofline": {"kernel": "bwd_tc_kernel<128> (backward main)", "bound": "tensor",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": NCU_TRAFFIC_BYTES,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops_sustained)"},
+        "gpu_launches": Stack.LAUNCHES_PER_STEP * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.skip_e2e:
+        out["e2e"] = run_e2e(args, stack, world)
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        t, f, desc = oracle_sample(stack.sched, layers=[0, 3] if args.quick_cpu else None)
+        out["cpu_baseline"] = {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s",
+                               "cores": cores(), "kind": "oracle", "sample": desc,
+                               "seconds": round(t, 2)}
+    return out
+
+
+def run_e2e(args, stack, world):
+    """Same metric through the public API with host buffers: every step copies
+    the inputs of all layers from pinned host memory to the device, runs the
+    stack, and reads o and every gradient back."""
+    host_in, host_out = [], []
+    h2d = d2h = 0
+    for L in stack.layers:
+        hin = {}
+        for k in ("q", "k", "v", "dO", "gq", "gk", "ve", "tok"):
+            t = L["x"][k]
+            if t is not None:
+                hin[k] = t.pin_memory()
+                h2d += t.numel() * t.element_size()
+        host_in.append(hin)
+        hout = {}
+        for k in ("o", "dq", "dk", "dv", "dgq", "dgk", "dve"):
+            t = L[k]
+            if t is not None:
+                hout[k] = torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                d2h += t.numel() * t.element_size()
+        host_out.append(hout)
+
+    def step():
+        for L, hin in zip(stack.layers, host_in):
+            for k, t in hin.items():
+                L["g"][k].copy_(t, non_blocking=True)
+        stack.step()
+        for L, hout in zip(stack.layers, host_out):
+            for k, t in hout.items():
+                t.copy_(L[k], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    _barrier(world)
+    a, b = _ev_pair()
+    a.record()
+    for _ in range(args.steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = _max_over_ranks(a.elapsed_time(b), world) / args.steps
+    value = (stack.flops_fwd + stack.flops_bwd) * world / (ms * 1e-3) / 1e12
+    return {"value": round(value, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores, on a bounded sample of the
+    same workload per step (layers 0 and 3 of one batch/kv-head slice)."""
+    import sliding_window_gqa_qk_gb300.inputs  # noqa: F401
+    from oracle import sssl_window, has_ve
+    sched = layer_schedule(sssl_window, has_ve)
+    for _ in range(args.warmup):
+        oracle_sample(sched, layers=[0])
+    times, fl, desc = [], 0, ""
+    for _ in range(args.steps):
+        t, fl, desc = oracle_sample(sched, layers=[0, 3])
+        times.append(t)
+    sec = sum(times) / len(times)
+    value = fl / sec / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": B, "seq_len": T,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------
+# Process group plumbing (barrier and max over ranks only)
+# ---------------------------------------------------------------------------
+
+def _physical_index(i):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        parts = [x for x in vis.split(",") if x.strip()]
+        if i < len(parts) and parts[i].strip().isdigit():
+            return int(parts[i])
+    return i
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--quick-cpu", action="store_true", help="oracle sample of 2 layers only")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    out = run_ours(args, rank, world, dev)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

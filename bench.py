@@ -79,7 +79,7 @@ def load_peaks():
 class ClockSampler:
     """Samples SM clocks and throttle reasons with nvidia-smi while running."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -102,7 +102,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -112,19 +115,23 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen in samples taken
+        between t0 and t1 (wall clock; all samples when not given)."""
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for ts, line in self.lines:
+            if t0 is not None and not (t0 <= ts <= t1 + 0.25):
+                continue
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax = float(parts[2])
+                sm.append(float(parts[2]))
+                smax = float(parts[3])
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
+            for name, val in zip(names, parts[6:10]):
                 if val.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
@@ -135,10 +142,10 @@ class ClockSampler:
 # Oracle leg (CPU baseline and --impl reference)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(schedule, layers=None):
-    """Runs the float64 oracle on one (batch element, kv head) slice of the
-    stack's layers: 1 x T=2048 x 2 query heads. Returns (seconds, masked
-    FLOPs of the sample, description)."""
+def oracle_sample(schedule, layers=None, batch=1, kv_heads=1):
+    """Runs the float64 oracle on a slice of the stack's layers: `batch`
+    sequences of T=2048 and `kv_heads` kv heads (2 query heads each).
+    Returns (seconds, masked FLOPs of the sample, description)."""
     import numpy as np  # noqa: F401
     import oracle
     from sliding_window_gqa_qk_gb300.inputs import as_f64
@@ -146,8 +153,8 @@ def oracle_sample(schedule, layers=None):
     total_t, total_f = 0.0, 0
     for li in layers:
         W, ve = schedule[li]
-        p = Problem(B=1, T=T, Hq=HQ // HKV, Hkv=1, d=D, window=W, gain_std=0.1, ve=ve,
-                    vocab=VOCAB)
+        p = Problem(B=batch, T=T, Hq=kv_heads * (HQ // HKV), Hkv=kv_heads, d=D, window=W,
+                    gain_std=0.1, ve=ve, vocab=VOCAB)
         x = make_inputs(p, layer=li, seed=4242)
         f = {k: as_f64(t) for k, t in x.items()}
         tok = x["tok"].numpy() if x["tok"] is not None else None
@@ -156,10 +163,10 @@ def oracle_sample(schedule, layers=None):
         oracle.attention_forward(f["q"], f["k"], f["v"], f["gq"], f["gk"], **kw)
         oracle.attention_backward(f["q"], f["k"], f["v"], f["gq"], f["gk"], f["dO"], **kw)
         total_t += time.perf_counter() - t0
-        ff, fb = flops(1, T, HQ // HKV, D, W)
+        ff, fb = flops(batch, T, kv_heads * (HQ // HKV), D, W)
         total_f += ff + fb
-    desc = (f"float64 oracle fwd+bwd of layers {layers[0]}..{layers[-1]} of the stack on one "
-            f"(batch element, kv head) slice: B=1, T={T}, Hq={HQ // HKV}, Hkv=1, d={D}")
+    desc = (f"float64 oracle fwd+bwd of layers {layers} of the stack on a slice of "
+            f"B={batch}, T={T}, Hq={kv_heads * (HQ // HKV)}, Hkv={kv_heads}, d={D}")
     return total_t, total_f, desc
 
 
@@ -251,24 +258,32 @@ def run_ours(args, rank, world, dev):
     swa.load("bf16")
     stack = Stack(swa, dev)
     torch.cuda.synchronize()
-    for _ in range(args.warmup):
-        stack.step()
-    st = swa.swa_attn_check_status(stack.layers[0]["ws"])
-    if st != swa.SWA_OK:
-        raise swa.SwaError(st, "device status after warm-up")
-    torch.cuda.synchronize()
-    _barrier(world)
     ev = {k: [] for k in ("fwd", "bwd_pre", "bwd_main", "bwd_post")}
     start, stop = _ev_pair()
     gpu_index = torch.cuda.current_device()
+    # The clock sampler runs from the warm-up on; only samples taken inside
+    # the timed region are summarised.
     with ClockSampler(_physical_index(gpu_index)) as clocks:
+        for _ in range(args.warmup):
+            stack.step()
+        for L in stack.layers:
+            st = swa.swa_attn_check_status(L["ws"])
+            if st != swa.SWA_OK:
+                raise swa.SwaError(st, "device status after warm-up")
         torch.cuda.synchronize()
+        _barrier(world)
+        t0 = clocks.mark()
         start.record()
         for _ in range(args.steps):
             stack.step(ev)
         stop.record()
         torch.cuda.synchronize()
+        t1 = clocks.mark()
     _barrier(world)
+    for L in stack.layers:
+        st = swa.swa_attn_check_status(L["ws"])
+        if st != swa.SWA_OK:
+            raise swa.SwaError(st, "device status after the timed steps")
     ms_total = start.elapsed_time(stop)
     ms = _max_over_ranks(ms_total, world) / args.steps
     stage_ms = {k: sum(a.elapsed_time(b) for a, b in v) / args.steps for k, v in ev.items()}
@@ -300,12 +315,15 @@ def run_ours(args, rank, world, dev):
                      "frac": round(achieved / peak, 4), "traffic": NCU_TRAFFIC_BYTES,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops_sustained)"},
         "gpu_launches": Stack.LAUNCHES_PER_STEP * args.steps,
-        "clocks": clocks.summary(),
+        "clocks": clocks.summary(t0, t1),
     }
     if not args.skip_e2e:
         out["e2e"] = run_e2e(args, stack, world)
     if rank == 0 and world == 1 and not args.skip_cpu:
-        t, f, desc = oracle_sample(stack.sched, layers=[0, 3] if args.quick_cpu else None)
+        if args.quick_cpu:
+            t, f, desc = oracle_sample(stack.sched, layers=[0, 3])
+        else:
+            t, f, desc = oracle_sample(stack.sched, batch=2, kv_heads=HKV)
         out["cpu_baseline"] = {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s",
                                "cores": cores(), "kind": "oracle", "sample": desc,
                                "seconds": round(t, 2)}
@@ -418,7 +436,7 @@ def _max_over_ranks(x, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-e2e", action="store_true")

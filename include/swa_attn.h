@@ -142,6 +142,38 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
                         void* workspace, size_t ws_bytes, unsigned flags, void* stream);
 
 /*
+ * Forward without a caller-provided workspace: the same computation and
+ * outputs as swa_attn_fwd (flags 0), but its scratch (QK-norm / VE-mix
+ * outputs and the status word) lives in one fixed array of
+ * SWA_NOALLOC_SCRATCH_BYTES of device memory inside the library. The pages
+ * have no counterpart of this call; it exists for callers that cannot
+ * allocate device memory at the point where they run the attention, for
+ * example code that runs while a CUDA graph is being captured, a plug-in whose
+ * host framework owns every allocation, or a service that must not grow its
+ * memory after start-up.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *     routine. The array is part of the library's device code, so every GPU
+ *     that loads the library holds it until the process exits.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture begins.
+ *   - Problems whose forward workspace (swa_attn_workspace_size(p, 0)) is
+ *     larger than the array are rejected with SWA_ERR_WORKSPACE, launching
+ *     nothing.
+ *   - Every call, from any stream or thread, shares the one array and it
+ *     keeps the last call's contents: calls that overlap on the GPU race and
+ *     corrupt each other's results; order them (same stream or events).
+ *     Nothing in it has to start at zero (the prologue writes every value the
+ *     forward reads). Device-side checks are not reported: use swa_attn_fwd
+ *     with a workspace and swa_attn_check_status to see them.
+ */
+#define SWA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+swa_status swa_attn_fwd_noalloc(const swa_params* p, const void* q, const void* k,
+                                const void* v, const float* gq, const float* gk, const void* ve,
+                                const int32_t* tok, const float* ve_gate, void* o, float* lse,
+                                void* stream);
+
+/*
  * Synchronises `stream`, reads the workspace status word, clears it, and
  * returns SWA_OK, SWA_ERR_TIMEOUT or SWA_ERR_DEVICE_CHECK (timeout wins).
  */

@@ -25,6 +25,7 @@ from . import build as _build
 __all__ = [
     "swa_params", "SwaError", "load",
     "swa_attn_workspace_size", "swa_attn_workspace_init", "swa_attn_fwd", "swa_attn_bwd",
+    "swa_attn_fwd_noalloc",
     "swa_attn_check_status", "swa_sssl_window", "swa_has_ve", "swa_strerror",
     "swa_build_info", "attention_forward", "attention_backward", "make_params",
     "SWA_OK", "SWA_ERR_INVALID_ARG", "SWA_ERR_UNSUPPORTED", "SWA_ERR_CUDA", "SWA_ERR_TIMEOUT",
@@ -83,6 +84,8 @@ def load(kind: str = "bf16") -> ctypes.CDLL:
     lib.swa_attn_fwd.restype = ctypes.c_int
     lib.swa_attn_bwd.argtypes = [P] + [_vp] * 18 + [ctypes.c_size_t, ctypes.c_uint, _vp]
     lib.swa_attn_bwd.restype = ctypes.c_int
+    lib.swa_attn_fwd_noalloc.argtypes = [P] + [_vp] * 10 + [_vp]
+    lib.swa_attn_fwd_noalloc.restype = ctypes.c_int
     lib.swa_attn_check_status.argtypes = [_vp, _vp]
     lib.swa_attn_check_status.restype = ctypes.c_int
     lib.swa_sssl_window.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_char_p, ctypes.c_int]
@@ -157,6 +160,16 @@ def swa_attn_bwd(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, d
         ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(gq), _ptr(gk), _ptr(ve), _ptr(tok),
         _ptr(ve_gate), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgq),
         _ptr(dgk), _ptr(dve), _ptr(ws), n, int(flags), _stream(stream)))
+
+
+def swa_attn_fwd_noalloc(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, stream=None,
+                         kind=None) -> int:
+    """Forward whose scratch is the library's fixed device array (no
+    workspace argument, nothing allocated); see include/swa_attn.h."""
+    kind = kind or _kind_of(q)
+    return int(load(kind).swa_attn_fwd_noalloc(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(gq), _ptr(gk), _ptr(ve), _ptr(tok),
+        _ptr(ve_gate), _ptr(o), _ptr(lse), _stream(stream)))
 
 
 def swa_attn_check_status(ws, stream=None, kind: str = "bf16") -> int:

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/swa_attn.h"
 #include "common.cuh"
@@ -114,6 +115,36 @@ swa_status run_prologue(const Call& c, const elem_t* q, const elem_t* k, const e
   if (p.d == 64) prologue_kernel<64><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
   else prologue_kernel<128><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
   return launched();
+}
+
+}  // namespace
+
+// Scratch of swa_attn_fwd_noalloc: a fixed device array, so that the call
+// allocates nothing. Host code may not use this name as a device address (on
+// the host it names a stand-in); noalloc_scratch() looks the address up.
+static __device__ __align__(256) unsigned char swa_noalloc_scratch[SWA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 256;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of swa_noalloc_scratch on the current device, looked up once
+// per device with that device current.
+swa_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SWA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SWA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, swa_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return SWA_ERR_CUDA;
+    g_noalloc_addr[dev] = ptr;
+  }
+  *out = g_noalloc_addr[dev];
+  return SWA_OK;
 }
 
 }  // namespace
@@ -334,6 +365,21 @@ swa_status swa_attn_check_status(void* workspace, void* stream) {
   if (word & DEV_ERR_TIMEOUT) return SWA_ERR_TIMEOUT;
   if (word & (DEV_ERR_TOKEN | DEV_ERR_BOUNDS)) return SWA_ERR_DEVICE_CHECK;
   return SWA_OK;
+}
+
+swa_status swa_attn_fwd_noalloc(const swa_params* p, const void* q, const void* k,
+                                const void* v, const float* gq, const float* gk, const void* ve,
+                                const int32_t* tok, const float* ve_gate, void* o, float* lse,
+                                void* stream) {
+  const swa_status s = check_params(p);
+  if (s != SWA_OK) return s;
+  if (ws_layout(p->B, p->T, p->Hq, p->Hkv, p->d).fwd_end > SWA_NOALLOC_SCRATCH_BYTES)
+    return SWA_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const swa_status ss = noalloc_scratch(&scratch);
+  if (ss != SWA_OK) return ss;
+  return swa_attn_fwd(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, scratch,
+                      SWA_NOALLOC_SCRATCH_BYTES, 0, stream);
 }
 
 int swa_sssl_window(int layer, int n_layer, const char* pattern, int T) {

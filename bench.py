@@ -181,11 +181,26 @@ def cores():
 # GPU leg
 # ---------------------------------------------------------------------------
 
+WORKLOADS = {
+    "stack": WORKLOAD,
+    "s_layer": "one S layer (B=16, T=2048, Hq=6, Hkv=3, d=128, window 1024, no VE)",
+    "l_layer": "one L layer (B=16, T=2048, Hq=6, Hkv=3, d=128, full causal, no VE)",
+}
+
+
+def schedule_for(workload, window_fn, ve_fn):
+    if workload == "s_layer":
+        return [(T // 2, False)]
+    if workload == "l_layer":
+        return [(-1, False)]
+    return layer_schedule(window_fn, ve_fn)
+
+
 class Stack:
-    def __init__(self, swa, dev):
+    def __init__(self, swa, dev, workload="stack"):
         self.swa = swa
         self.dev = dev
-        self.sched = layer_schedule(swa.swa_sssl_window, swa.swa_has_ve)
+        self.sched = schedule_for(workload, swa.swa_sssl_window, swa.swa_has_ve)
         self.layers = []
         for li, (W, ve) in enumerate(self.sched):
             p = Problem(B=B, T=T, Hq=HQ, Hkv=HKV, d=D, window=W, gain_std=0.1, ve=ve, vocab=VOCAB)
@@ -244,9 +259,9 @@ class Stack:
                 if ev is not None:
                     ev[name][-1][1].record()
 
-    # launches of our kernels per step: fwd = prologue + attention; bwd =
-    # pre + main + post + gain sum
-    LAUNCHES_PER_STEP = N_LAYER * (2 + 4)
+    # launches of our kernels per layer and step: fwd = prologue + attention;
+    # bwd = pre + main + post + gain sum
+    LAUNCHES_PER_LAYER = 2 + 4
 
 
 def _ev_pair():
@@ -256,7 +271,8 @@ def _ev_pair():
 def run_ours(args, rank, world, dev):
     import sliding_window_gqa_qk_gb300 as swa
     swa.load("bf16")
-    stack = Stack(swa, dev)
+    stack = Stack(swa, dev, args.workload)
+    n_layer = len(stack.sched)
     torch.cuda.synchronize()
     ev = {k: [] for k in ("fwd", "bwd_pre", "bwd_main", "bwd_post")}
     start, stop = _ev_pair()
@@ -293,8 +309,8 @@ def run_ours(args, rank, world, dev):
     # dominant kernel: the backward main kernel (per launch = one layer)
     peaks, peak_kind = load_peaks()
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    bwd_main_launch_ms = stage_ms["bwd_main"] / N_LAYER
-    achieved = stack.flops_bwd / N_LAYER / (bwd_main_launch_ms * 1e-3) / 1e12
+    bwd_main_launch_ms = stage_ms["bwd_main"] / n_layer
+    achieved = stack.flops_bwd / n_layer / (bwd_main_launch_ms * 1e-3) / 1e12
     fwd_launch_tflops = stack.flops_fwd / (stage_ms["fwd"] * 1e-3) / 1e12
 
     out = {
@@ -302,9 +318,9 @@ def run_ours(args, rank, world, dev):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q/k/v/dO, gains 1+0.1N, VE N(0,0.02), tokens U[0,8192))",
-        "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": T,
+        "config": {"workload": WORKLOADS[args.workload], "global_batch": B * world, "seq_len": T,
                    "parallelism": f"replicas over batch x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2: 8 layers x ~0.4 GB of tensors per step",
+                   "l2": f"inputs larger than L2: {n_layer} layer(s) x ~0.4 GB of tensors per step",
                    "flops_per_step": flops_step,
                    "pct_of_peak": round(100 * value / world / peak, 2),
                    "peak_tflops": peak, "peak_source": f"{peak_kind} bf16_tflops_sustained",
@@ -314,12 +330,12 @@ def run_ours(args, rank, world, dev):
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": NCU_TRAFFIC_BYTES,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops_sustained)"},
-        "gpu_launches": Stack.LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": Stack.LAUNCHES_PER_LAYER * n_layer * args.steps,
         "clocks": clocks.summary(t0, t1),
     }
     if not args.skip_e2e:
         out["e2e"] = run_e2e(args, stack, world)
-    if rank == 0 and world == 1 and not args.skip_cpu:
+    if rank == 0 and world == 1 and not args.skip_cpu and args.workload == "stack":
         if args.quick_cpu:
             t, f, desc = oracle_sample(stack.sched, layers=[0, 3])
         else:
@@ -439,6 +455,8 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default="stack",
+                    help="stack (the headline) or one S / L layer (profiling)")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--quick-cpu", action="store_true", help="oracle sample of 2 layers only")

@@ -11,12 +11,15 @@
 //   dS^T = P^T (dP^T - D)   (smem, bf16), D = rowsum(dO * O)
 //   dV  += P^T dO,  dK += dS^T Q                                   (TMEM)
 //   dQ   = dS K  (computed as dQ^T = K^T dS^T when d = 128)         (TMEM)
-// and dQ * scale is added into an fp32 accumulator with vector/coalesced
-// reductions (the only cross-CTA exchange).
+// dQ * scale is staged in shared memory and added into the fp32 dQ
+// accumulator in global memory by TMA bulk reductions (the only cross-CTA
+// exchange).
 //
-// Roles: warp 4 TMA producer (K, V once; Q, dO, LSE, D per step, 2 stages),
-// warp 5 MMA issuer (one thread) and TMEM owner, warps 0-3 the element-wise
-// softmax backward (thread t owns key row t, TMEM lane t) and the dQ drain.
+// Roles: warp 8 TMA producer (K, V once; Q, dO, LSE, D per step, 2 stages),
+// warp 9 MMA issuer (one thread) and TMEM owner, warps 0-7 two warpgroups
+// that split each step's columns in halves: thread t of warpgroup w owns key
+// row t (TMEM lane t) and query columns [w BQ/2, (w+1) BQ/2) of S^T and dP^T,
+// and half of the dQ tile in the drain.
 //
 // Softmax backward written out from the forward of the attention block
 // (autoresearch Administrator & Developer Guide §8.2.1; train.py
@@ -34,7 +37,10 @@ namespace swa {
 namespace tc {
 
 constexpr int kBK = 128;          // keys per CTA
-constexpr int kBwdThreads = 192;  // 6 warps
+constexpr int kBwdWarps = 10;
+constexpr int kBwdThreads = kBwdWarps * 32;
+constexpr int kBwdProducerWarp = 8;
+constexpr int kBwdMmaWarp = 9;
 
 struct BwdLaunch {
   int B, T, Hq, Hkv, d, window, causal;
@@ -59,7 +65,6 @@ struct BwdParams {
   float scale, scale_log2;
   const float* lse2;
   const float* dvec;
-  float* dq_acc;
   float* dk_acc;
   float* dv_acc;
   uint32_t* status;
@@ -69,21 +74,27 @@ struct BwdParams {
 template <int D>
 struct BwdCfg {
   static constexpr int BQ = D == 128 ? 64 : 128;   // query rows per step
+  static constexpr int HC = BQ / 2;                // S^T columns per warpgroup
   static constexpr int kKV = kBK * D * 2;          // K or V tile bytes
   static constexpr int kQ = BQ * D * 2;            // Q or dO tile bytes
   static constexpr int kP = kBK * BQ * 2;          // P^T or dS^T bytes
+  static constexpr int kStage = 16384;             // dQ staging per warpgroup and buffer
+  static constexpr int kStageBufs = D == 128 ? 2 : 1;  // buffers (shared memory budget)
   static constexpr int oK = 0;
   static constexpr int oV = oK + kKV;
   static constexpr int oQ = oV + kKV;              // 2 stages
   static constexpr int oG = oQ + 2 * kQ;           // dO, 2 stages
   static constexpr int oP = oG + 2 * kQ;
   static constexpr int oS = oP + kP;
-  static constexpr int oL = oS + kP;               // LSE2, 2 stages of BQ floats
+  static constexpr int oR = oS + kP;               // dQ staging [buffers][2 warpgroups]
+  static constexpr int oL = oR + 2 * kStageBufs * kStage;  // LSE2, 2 stages of BQ floats
   static constexpr int oD = oL + 2 * BQ * 4;       // D, 2 stages
   static constexpr int kBytes = oD + 2 * BQ * 4;
   static constexpr int kAlloc = kBytes + 1024;
   // TMEM columns
   static constexpr uint32_t cS = 0, cDP = BQ, cDV = 2 * BQ, cDK = 2 * BQ + D, cDQ = 2 * BQ + 2 * D;
+  static_assert(kAlloc + 256 <= 232448, "shared memory budget (dynamic + static)");
+  static_assert(2 * BQ + 2 * D + 64 <= 512, "TMEM budget");
 };
 
 enum {
@@ -100,8 +111,8 @@ enum {
   BB_COUNT = 12
 };
 
-// Writes one bf16 row of 64-column swizzle regions: row r of a [rows][cols]
-// K-major SW128 tile (cols / 64 regions of rows * 128 bytes).
+// Writes one 16-byte chunk of row r of a [rows][cols] bf16 K-major tile in
+// the 128-byte swizzle layout (cols / 64 regions of rows * 128 bytes).
 __device__ __forceinline__ void st_sw128_chunk(uint32_t tile, int rows, int r, int chunk,
                                                uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   const uint32_t region = static_cast<uint32_t>(chunk >> 3) * rows * 128;
@@ -114,9 +125,10 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
-                  const BwdParams prm) {
+                  const __grid_constant__ CUtensorMap tmDQ, const BwdParams prm) {
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ;
+  constexpr int HC = C::HC;
   constexpr int KCH = D / 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -149,14 +161,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(bar(BB_SFULL), 1);
     mbar_init(bar(BB_DPFULL), 1);
-    mbar_init(bar(BB_PREADY), 4);
-    mbar_init(bar(BB_DSREADY), 4);
+    mbar_init(bar(BB_PREADY), 8);
+    mbar_init(bar(BB_DSREADY), 8);
     mbar_init(bar(BB_DQFULL), 1);
-    mbar_init(bar(BB_DQFREE), 4);
+    mbar_init(bar(BB_DQFREE), 8);
     mbar_init(bar(BB_FINAL), 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kBwdMmaWarp) {
     tmem_alloc(smem_u32(&tmem_base_sh), 512);
     tmem_relinquish();
   }
@@ -165,7 +177,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp == 4) {
+  if (warp == kBwdProducerWarp) {
     // ---------------- TMA producer ----------------
     if (lane == 0 && n_it > 0) {
       tma_prefetch_desc(&tmQ);
@@ -200,7 +212,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int s = 0; s < 2; ++s)
         if (last[s] >= 0) mbar_wait_drain(bar(BB_QFULL + s), (last[s] >> 1) & 1, prm.wait_limit_ns);
     }
-  } else if (warp == 5) {
+  } else if (warp == kBwdMmaWarp) {
     // ---------------- MMA issuer ----------------
     if (lane == 0 && n_it > 0) {
       constexpr uint32_t idST = idesc_bf16_f32(kBK, BQ, 0, 0);   // S^T, dP^T
@@ -264,22 +276,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_wait_drain(bar(BB_FINAL), 0, prm.wait_limit_ns);
     }
   } else {
-    // ---------------- softmax-backward warpgroup (warps 0-3) ----------------
-    const int t = threadIdx.x;                       // key row / TMEM lane
+    // ------------- softmax-backward warpgroups (warps 0-3 and 4-7) -------------
+    const int wg = warp >> 2;                        // 0 or 1: column half
+    const int t = threadIdx.x & 127;                 // key row / TMEM lane
     const int j = k0 + t;                            // key position
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int c0 = wg * HC;                          // first S^T column of this half
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float c = prm.scale_log2;
     const uint32_t sP = sbase + C::oP, sS = sbase + C::oS;
+    const bool leader = (t == 0);
+    // Wait outcomes are made warp-uniform (mbar_wait_warp) and warpgroup-
+    // uniform at the drain's named barrier, so that after a timeout every
+    // thread of the warpgroup leaves the loop at the same point.
     bool ok = true;
-    for (int it = 0; it < n_it && ok; ++it) {
+    for (int it = 0; it < n_it; ++it) {
       const int st = it & 1, ph = it & 1;
       const int h = hk * G + it / nq;
       const int q0 = (qlo + it % nq) * BQ;
-      const float* sL = reinterpret_cast<const float*>(smem + C::oL + st * BQ * 4);
-      const float* sDv = reinterpret_cast<const float*>(smem + C::oD + st * BQ * 4);
-      // visible query columns of this key row: [clo, chi]
-      int clo = 0, chi = BQ - 1;
       const bool full = tile_full(band, q0, BQ, k0, kBK);
+      // visible query columns of this key row (partial tiles): [clo, chi]
+      int clo = 0, chi = BQ - 1;
       if (!full) {
         if (j >= prm.T) {
           clo = 1; chi = 0;
@@ -294,113 +310,152 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
       }
-      if (!(ok = mbar_wait(bar(BB_QFULL + st), (it >> 1) & 1, ctl))) break;
-      if (!(ok = mbar_wait(bar(BB_SFULL), ph, ctl))) break;
-      tc_fence_after();
-      uint32_t sr[BQ / 32][32];
+      uint32_t sr[HC / 32][32];
+      // LSE2 and D of 32 of this half's columns, from shared memory
+      const uint32_t sL = sbase + C::oL + st * BQ * 4 + c0 * 4;
+      const uint32_t sDv = sbase + C::oD + st * BQ * 4 + c0 * 4;
+      auto load32 = [&](uint32_t base, int cc, float (&v)[32]) {
 #pragma unroll
-      for (int cc = 0; cc < BQ / 32; ++cc) tmem_ld32(tmem + C::cS + lane_off + cc * 32, sr[cc]);
-      tmem_wait_ld(sr[0]);
+        for (int e = 0; e < 32; e += 4) {
+          const float4 a = ld_shared_v4f(base + (cc * 32 + e) * 4);
+          v[e] = a.x; v[e + 1] = a.y; v[e + 2] = a.z; v[e + 3] = a.w;
+        }
+      };
+      ok = ok && mbar_wait_warp(bar(BB_QFULL + st), (it >> 1) & 1, ctl);
+      ok = ok && mbar_wait_warp(bar(BB_SFULL), ph, ctl);
+      if (ok) {
+        tc_fence_after();
 #pragma unroll
-      for (int cc = 1; cc < BQ / 32; ++cc) reg_fence(sr[cc]);
-      // P^T = exp2(S^T c - LSE2), masked; kept in fp32 registers for dS.
+        for (int cc = 0; cc < HC / 32; ++cc)
+          tmem_ld32(tmem + C::cS + lane_off + c0 + cc * 32, sr[cc]);
+        tmem_wait_ld(sr[0]);
 #pragma unroll
-      for (int cc = 0; cc < BQ / 32; ++cc)
+        for (int cc = 1; cc < HC / 32; ++cc) reg_fence(sr[cc]);
+        // P^T = exp2(S^T c - LSE2), masked on partial tiles
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int col = cc * 32 + e;
-          const float p = ex2_approx(fmaf(__uint_as_float(sr[cc][e]), c, -sL[col]));
-          sr[cc][e] = __float_as_uint((col >= clo && col <= chi) ? p : 0.f);
+        for (int cc = 0; cc < HC / 32; ++cc) {
+          float lse2[32];
+          load32(sL, cc, lse2);
+          if (full) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              sr[cc][e] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(sr[cc][e]), c, -lse2[e])));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int col = c0 + cc * 32 + e;
+              const float p = ex2_approx(fmaf(__uint_as_float(sr[cc][e]), c, -lse2[e]));
+              sr[cc][e] = __float_as_uint((col >= clo && col <= chi) ? p : 0.f);
+            }
+          }
         }
 #pragma unroll
-      for (int ch = 0; ch < BQ / 8; ++ch) {
-        const int cc = ch >> 2, e0 = (ch & 3) * 8;
-        st_sw128_chunk(sP, kBK, t, ch,
-                       pack_bf16x2(__uint_as_float(sr[cc][e0 + 0]), __uint_as_float(sr[cc][e0 + 1])),
-                       pack_bf16x2(__uint_as_float(sr[cc][e0 + 2]), __uint_as_float(sr[cc][e0 + 3])),
-                       pack_bf16x2(__uint_as_float(sr[cc][e0 + 4]), __uint_as_float(sr[cc][e0 + 5])),
-                       pack_bf16x2(__uint_as_float(sr[cc][e0 + 6]), __uint_as_float(sr[cc][e0 + 7])));
+        for (int ch = 0; ch < HC / 8; ++ch) {
+          const int cc = ch >> 2, e0 = (ch & 3) * 8;
+          st_sw128_chunk(sP, kBK, t, c0 / 8 + ch,
+                         pack_bf16x2(__uint_as_float(sr[cc][e0 + 0]), __uint_as_float(sr[cc][e0 + 1])),
+                         pack_bf16x2(__uint_as_float(sr[cc][e0 + 2]), __uint_as_float(sr[cc][e0 + 3])),
+                         pack_bf16x2(__uint_as_float(sr[cc][e0 + 4]), __uint_as_float(sr[cc][e0 + 5])),
+                         pack_bf16x2(__uint_as_float(sr[cc][e0 + 6]), __uint_as_float(sr[cc][e0 + 7])));
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BB_PREADY));
       }
-      fence_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BB_PREADY));
       // dS^T = P^T (dP^T - D)
-      if (!(ok = mbar_wait(bar(BB_DPFULL), ph, ctl))) break;
-      tc_fence_after();
+      ok = ok && mbar_wait_warp(bar(BB_DPFULL), ph, ctl);
+      if (ok) {
+        tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < BQ / 32; ++cc) {
-        uint32_t dp[32];
-        tmem_ld32(tmem + C::cDP + lane_off + cc * 32, dp);
-        tmem_wait_ld(dp);
+        for (int cc = 0; cc < HC / 32; ++cc) {
+          uint32_t dp[32];
+          float dd[32];
+          tmem_ld32(tmem + C::cDP + lane_off + c0 + cc * 32, dp);
+          load32(sDv, cc, dd);
+          tmem_wait_ld(dp);
+          if (full) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int col = cc * 32 + e;
-          const float p = __uint_as_float(sr[cc][e]);
-          const float ds = p * (__uint_as_float(dp[e]) - sDv[col]);
-          sr[cc][e] = __float_as_uint((col >= clo && col <= chi) ? ds : 0.f);
+            for (int e = 0; e < 32; ++e)
+              sr[cc][e] = __float_as_uint(__uint_as_float(sr[cc][e]) *
+                                          (__uint_as_float(dp[e]) - dd[e]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int col = c0 + cc * 32 + e;
+              const float ds = __uint_as_float(sr[cc][e]) * (__uint_as_float(dp[e]) - dd[e]);
+              sr[cc][e] = __float_as_uint((col >= clo && col <= chi) ? ds : 0.f);
+            }
+          }
         }
-      }
 #pragma unroll
-      for (int ch = 0; ch < BQ / 8; ++ch) {
-        const int cc = ch >> 2, e0 = (ch & 3) * 8;
-        st_sw128_chunk(sS, kBK, t, ch,
-                       pack_bf16x2(__uint_as_float(sr[cc][e0 + 0]), __uint_as_float(sr[cc][e0 + 1])),
-                       pack_bf16x2(__uint_as_float(sr[cc][e0 + 2]), __uint_as_float(sr[cc][e0 + 3])),
-                       pack_bf16x2(__uint_as_float(sr[cc][e0 + 4]), __uint_as_float(sr[cc][e0 + 5])),
-                       pack_bf16x2(__uint_as_float(sr[cc][e0 + 6]), __uint_as_float(sr[cc][e0 + 7])));
+        for (int ch = 0; ch < HC / 8; ++ch) {
+          const int cc = ch >> 2, e0 = (ch & 3) * 8;
+          st_sw128_chunk(sS, kBK, t, c0 / 8 + ch,
+                         pack_bf16x2(__uint_as_float(sr[cc][e0 + 0]), __uint_as_float(sr[cc][e0 + 1])),
+                         pack_bf16x2(__uint_as_float(sr[cc][e0 + 2]), __uint_as_float(sr[cc][e0 + 3])),
+                         pack_bf16x2(__uint_as_float(sr[cc][e0 + 4]), __uint_as_float(sr[cc][e0 + 5])),
+                         pack_bf16x2(__uint_as_float(sr[cc][e0 + 6]), __uint_as_float(sr[cc][e0 + 7])));
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BB_DSREADY));
+      }
+      // dQ drain: TMEM -> registers -> (scaled) shared staging -> TMA add.
+      // D=128: dQ^T, lane = head-dim index t, this half's 32 query columns.
+      // D=64:  dQ,   lane = query row t,     this half's 32 head-dim columns.
+      uint32_t dq[32];
+      ok = ok && mbar_wait_warp(bar(BB_DQFULL), ph, ctl);
+      if (ok) {
+        tc_fence_after();
+        tmem_ld32(tmem + C::cDQ + lane_off + wg * 32, dq);
+        tmem_wait_ld(dq);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BB_DQFREE));
+      }
+      const uint32_t stage = sbase + C::oR + ((it % C::kStageBufs) * 2 + wg) * C::kStage;
+      // the add issued from this buffer kStageBufs steps ago must have read it
+      if (leader) bulk_wait_group_read<C::kStageBufs - 1>();
+      ok = named_bar_and(1 + wg, 128, ok);
+      if (!ok) break;
+      if constexpr (D == 128) {
+        // staging [32 queries][128 d] fp32, row-major
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          st_shared_f32(stage + e * 512 + t * 4, __uint_as_float(dq[e]) * prm.scale);
+      } else {
+        // staging [128 queries][32 d] fp32, 128-byte swizzle
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint32_t addr = stage + (t >> 3) * 1024 + (t & 7) * 128 +
+                                static_cast<uint32_t>(ch ^ (t & 7)) * 16;
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                       "f"(__uint_as_float(dq[4 * ch]) * prm.scale),
+                       "f"(__uint_as_float(dq[4 * ch + 1]) * prm.scale),
+                       "f"(__uint_as_float(dq[4 * ch + 2]) * prm.scale),
+                       "f"(__uint_as_float(dq[4 * ch + 3]) * prm.scale)
+                       : "memory");
+        }
       }
       fence_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BB_DSREADY));
-      // dQ drain: scale and add into the fp32 accumulator.
-      if (!(ok = mbar_wait(bar(BB_DQFULL), ph, ctl))) break;
-      tc_fence_after();
-      const long long qrow0 = (static_cast<long long>(b) * prm.Hq + h) * prm.T + q0;
-      if constexpr (D == 128) {
-        // dQ^T: lane = head-dim index t, columns = BQ queries.
-#pragma unroll
-        for (int cc = 0; cc < BQ / 32; ++cc) {
-          uint32_t dq[32];
-          tmem_ld32(tmem + C::cDQ + lane_off + cc * 32, dq);
-          tmem_wait_ld(dq);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int qq = cc * 32 + e;
-            if (q0 + qq < prm.T)
-              atomicAdd(prm.dq_acc + (qrow0 + qq) * D + t, __uint_as_float(dq[e]) * prm.scale);
-          }
-        }
-      } else {
-        // dQ: lane = query row t, columns = D.
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t dq[32];
-          tmem_ld32(tmem + C::cDQ + lane_off + cc * 32, dq);
-          tmem_wait_ld(dq);
-          if (q0 + t < prm.T) {
-            float* dst = prm.dq_acc + (qrow0 + t) * D + cc * 32;
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              red_add_v4_f32(dst + e, __uint_as_float(dq[e]) * prm.scale,
-                             __uint_as_float(dq[e + 1]) * prm.scale,
-                             __uint_as_float(dq[e + 2]) * prm.scale,
-                             __uint_as_float(dq[e + 3]) * prm.scale);
-          }
-        }
+      named_bar_sync(1 + wg, 128);
+      if (leader) {
+        const int bh = b * prm.Hq + h;
+        if constexpr (D == 128) tma_reduce_add_3d(&tmDQ, stage, 0, q0 + wg * 32, bh);
+        else tma_reduce_add_3d(&tmDQ, stage, wg * 32, q0, bh);
+        bulk_commit_group();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BB_DQFREE));
     }
-    // ---- epilogue: dK (scaled) and dV rows of this key tile ----
+    if (leader) bulk_wait_group_all();
+    // ---- epilogue: dK (scaled) and dV rows of this key tile, half the columns each ----
     if (ok && j < prm.T) {
       const long long krow = (static_cast<long long>(b) * prm.Hkv + hk) * prm.T + j;
-      float* dkd = prm.dk_acc + krow * D;
-      float* dvd = prm.dv_acc + krow * D;
+      float* dkd = prm.dk_acc + krow * D + wg * (D / 2);
+      float* dvd = prm.dv_acc + krow * D + wg * (D / 2);
       if (n_it == 0) {
-        for (int e = 0; e < D; e += 4) {
+        for (int e = 0; e < D / 2; e += 4) {
           *reinterpret_cast<float4*>(dkd + e) = make_float4(0.f, 0.f, 0.f, 0.f);
           *reinterpret_cast<float4*>(dvd + e) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -410,15 +465,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       const long long krow = (static_cast<long long>(b) * prm.Hkv + hk) * prm.T + j;
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int col = wg * (D / 2) + cc * 32;
         uint32_t vk[32], vv[32];
-        tmem_ld32(tmem + C::cDK + lane_off + cc * 32, vk);
-        tmem_ld32(tmem + C::cDV + lane_off + cc * 32, vv);
+        tmem_ld32(tmem + C::cDK + lane_off + col, vk);
+        tmem_ld32(tmem + C::cDV + lane_off + col, vv);
         tmem_wait_ld(vk);
         reg_fence(vv);
         if (j < prm.T) {
-          float* dkd = prm.dk_acc + krow * D + cc * 32;
-          float* dvd = prm.dv_acc + krow * D + cc * 32;
+          float* dkd = prm.dk_acc + krow * D + col;
+          float* dvd = prm.dv_acc + krow * D + col;
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
             *reinterpret_cast<float4*>(dkd + e) =
@@ -434,21 +490,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kBwdMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
+// fp32 tensor map of the dQ accumulator [B*Hq][T][D] for the bulk adds:
+// D = 128: boxes of 32 query rows x 128 columns, no swizzle;
+// D = 64:  boxes of 128 query rows x 32 columns, 128-byte swizzle.
+inline bool map_dq_acc(CUtensorMap* m, float* base, int BH, int T, int D) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4, static_cast<cuuint64_t>(T) * D * 4};
+  cuuint32_t box[3] = {D == 128 ? 128u : 32u, D == 128 ? 32u : 128u, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            D == 128 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 inline swa_status launch_bwd_d(const BwdLaunch& f, cudaStream_t st) {
   using C = BwdCfg<D>;
-  CUtensorMap mq, mk, mv, mg;
+  CUtensorMap mq, mk, mv, mg, mdq;
   if (!make_map_4d(&mq, f.qn, D, f.T, f.Hq, f.B, D, static_cast<long long>(f.T) * D,
                    static_cast<long long>(f.Hq) * f.T * D, C::BQ) ||
       !make_map_4d(&mg, f.dO, D, f.T, f.Hq, f.B, static_cast<long long>(f.Hq) * D, D,
                    static_cast<long long>(f.T) * f.Hq * D, C::BQ) ||
-      !map_head_major(&mk, f.kn, f.B, f.Hkv, f.T, D))
+      !map_head_major(&mk, f.kn, f.B, f.Hkv, f.T, D) ||
+      !map_dq_acc(&mdq, f.dq_acc, f.B * f.Hq, f.T, D))
     return SWA_ERR_CUDA;
   const bool okv = f.v_head_major ? map_head_major(&mv, f.v, f.B, f.Hkv, f.T, D)
                                   : map_token_major(&mv, f.v, f.B, f.Hkv, f.T, D);
@@ -459,13 +533,13 @@ inline swa_status launch_bwd_d(const BwdLaunch& f, cudaStream_t st) {
   p.scale = f.scale;
   p.scale_log2 = f.scale * 1.4426950408889634f;
   p.lse2 = f.lse2; p.dvec = f.dvec;
-  p.dq_acc = f.dq_acc; p.dk_acc = f.dk_acc; p.dv_acc = f.dv_acc;
+  p.dk_acc = f.dk_acc; p.dv_acc = f.dv_acc;
   p.status = f.status; p.wait_limit_ns = f.wait_limit_ns;
   if (cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kAlloc) != cudaSuccess)
     return SWA_ERR_CUDA;
   dim3 grid(f.B * f.Hkv, p.n_ktiles);
-  bwd_tc_kernel<D><<<grid, kBwdThreads, C::kAlloc, st>>>(mq, mk, mv, mg, p);
+  bwd_tc_kernel<D><<<grid, kBwdThreads, C::kAlloc, st>>>(mq, mk, mv, mg, mdq, p);
   return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 

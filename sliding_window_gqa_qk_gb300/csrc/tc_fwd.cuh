@@ -67,6 +67,7 @@ struct FwdSmem {
   static constexpr int kP0 = kV0 + 2 * kTileBytes;
   static constexpr int kBytes = kP0 + 2 * kPBytes;
   static constexpr int kAlloc = kBytes + 1024;          // slack for 1024-byte alignment
+  static_assert(kAlloc + 256 <= 232448, "shared memory budget (dynamic + static)");
 };
 
 // Barrier indices

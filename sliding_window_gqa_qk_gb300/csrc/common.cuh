@@ -166,11 +166,15 @@ struct WsLayout {
   size_t dq_acc;    // f32  [B, Hq, T, d]   gradient of qn
   size_t dk_acc;    // f32  [B, Hkv, T, d]  gradient of kn
   size_t dv_acc;    // f32  [B, Hkv, T, d]  gradient of v_eff
-  size_t gpart;     // f32  [2, kPostBlocks, d] per-block partial gain gradients
+  size_t gpart;     // f32  [2, post_blocks, d] per-block partial gain gradients
   size_t bwd_end;
 };
 
-constexpr int kPostBlocks = 256;  // blocks of each backward-post segment
+// Blocks of one backward-post segment: runs of 256 positions x (batch, head)
+// pairs of the larger head count.
+__host__ __device__ __forceinline__ int post_blocks(int B, int T, int Hq) {
+  return (T + 255) / 256 * B * Hq;
+}
 
 __host__ __device__ __forceinline__ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -196,7 +200,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int T, int Hq, int Hkv, int
   L.dq_acc = o; o = align256(o + bt * Hq * d * 4);
   L.dk_acc = o; o = align256(o + bt * Hkv * d * 4);
   L.dv_acc = o; o = align256(o + bt * Hkv * d * 4);
-  L.gpart = o; o = align256(o + size_t(2) * kPostBlocks * d * 4);
+  L.gpart = o; o = align256(o + size_t(2) * post_blocks(B, T, Hq) * d * 4);
   L.bwd_end = o;
   return L;
 }
@@ -232,12 +236,14 @@ struct PostArgs {  // backward post: RMSNorm backward, dv, dVE, gain partials
   const float* dq_acc; const float* dk_acc; const float* dv_acc;
   elem_t* dq; elem_t* dk; elem_t* dv;
   float* dve;        // NULL: skip
-  float* gpart;      // [2, kPostBlocks, d]
+  float* gpart;      // [2, nblk_max, d]
+  int nblk_max;      // post_blocks(B, T, Hq)
   uint32_t* status;
 };
 
 struct GainArgs {
   int d;
+  int nblk_q, nblk_k, nblk_max;   // partials written by the q and k segments
   const float* gpart;
   float* dgq; float* dgk;
 };

@@ -49,11 +49,11 @@ swa_status check_params(const swa_params* p) {
   if (!std::isfinite(p->eps) || p->eps < 0.f) return SWA_ERR_INVALID_ARG;
   if (!std::isfinite(p->ve_scale)) return SWA_ERR_INVALID_ARG;
   if (p->d != 64 && p->d != 128) return SWA_ERR_UNSUPPORTED;
-  // Grid and index limits: (batch, head) pairs index grid x, tiles of 128
-  // positions index grid y (< 65536), positions are 32-bit TMA coordinates.
-  if (p->Hq > 65535 || p->B > 65535 || p->T > (1 << 22) ||
-      static_cast<long long>(p->B) * p->Hq > (1ll << 30))
-    return SWA_ERR_UNSUPPORTED;
+  // Grid and index limits: (batch, head) pairs index a grid dimension of at
+  // most 65535 blocks in the row-wise kernels, tiles of 128 positions index
+  // grid y of the attention kernels (< 65536), positions are 32-bit TMA
+  // coordinates.
+  if (p->T > (1 << 22) || static_cast<long long>(p->B) * p->Hq > 65535) return SWA_ERR_UNSUPPORTED;
   return SWA_OK;
 }
 
@@ -93,11 +93,6 @@ T* at(const Call& c, size_t off) {
   return reinterpret_cast<T*>(c.ws + off);
 }
 
-int row_grid(long long rows) {
-  long long blocks = (rows + kRowWarps * kRowsPerIter - 1) / (kRowWarps * kRowsPerIter);
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  return static_cast<int>(blocks < 1 ? 1 : blocks);
-}
 
 swa_status run_prologue(const Call& c, const elem_t* q, const elem_t* k, const elem_t* v,
                         const float* gq, const float* gk, const elem_t* ve, const int32_t* tok,
@@ -110,8 +105,7 @@ swa_status run_prologue(const Call& c, const elem_t* q, const elem_t* k, const e
   a.qn = at<elem_t>(c, c.L.qn); a.kn = at<elem_t>(c, c.L.kn); a.veff = at<elem_t>(c, c.L.veff);
   a.rstd_q = at<float>(c, c.L.rstd_q); a.rstd_k = at<float>(c, c.L.rstd_k);
   a.status = at<uint32_t>(c, c.L.status);
-  const long long rows = static_cast<long long>(p.B) * p.T * p.Hq;
-  dim3 grid(row_grid(rows), (ve != nullptr || copy_v) ? 3 : 2);
+  dim3 grid((p.T + kRowsPerBlock - 1) / kRowsPerBlock, p.B * p.Hq, (ve != nullptr || copy_v) ? 3 : 2);
   if (p.d == 64) prologue_kernel<64><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
   else prologue_kernel<128><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
   return launched();
@@ -268,7 +262,6 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
   if ((stages & SWA_BWD_STAGE_PRE) && !(flags & SWA_REUSE_PROLOGUE)) {
     if ((s = run_prologue(c, qe, ke, vin, gq, gk, vee, tok, ve_gate, copy_v)) != SWA_OK) return s;
   }
-  const long long qrows = static_cast<long long>(P.B) * P.T * P.Hq;
   if (stages & SWA_BWD_STAGE_PRE) {
     PreArgs a{};
     a.B = P.B; a.T = P.T; a.Tpad = t_pad(P.T); a.Hq = P.Hq; a.Hkv = P.Hkv; a.d = P.d;
@@ -276,8 +269,9 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
     a.dvec = at<float>(c, c.L.dvec); a.lse2 = at<float>(c, c.L.lse2);
     a.dq_acc = at<float>(c, c.L.dq_acc);
     a.clear_acc = clear_acc;
-    if (P.d == 64) bwd_pre_kernel<64><<<row_grid(qrows), kRowWarps * 32, 0, st>>>(a);
-    else bwd_pre_kernel<128><<<row_grid(qrows), kRowWarps * 32, 0, st>>>(a);
+    dim3 grid((P.T + kRowsPerBlock - 1) / kRowsPerBlock, P.B * P.Hq);
+    if (P.d == 64) bwd_pre_kernel<64><<<grid, kRowWarps * 32, 0, st>>>(a);
+    else bwd_pre_kernel<128><<<grid, kRowWarps * 32, 0, st>>>(a);
     if ((s = launched()) != SWA_OK) return s;
   }
   if (stages & SWA_BWD_STAGE_MAIN) {
@@ -337,14 +331,17 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
     a.dq = static_cast<elem_t*>(dq); a.dk = static_cast<elem_t*>(dk); a.dv = static_cast<elem_t*>(dv);
     a.dve = (ve != nullptr) ? dve : nullptr;
     a.gpart = at<float>(c, c.L.gpart);
+    a.nblk_max = post_blocks(P.B, P.T, P.Hq);
     a.status = at<uint32_t>(c, c.L.status);
-    dim3 grid(kPostBlocks, 3);
+    const int tblk = (P.T + kPostRowsPerBlock - 1) / kPostRowsPerBlock;
+    dim3 grid(tblk, P.B * P.Hq, 3);
     if (P.d == 64) bwd_post_kernel<64><<<grid, kRowWarps * 32, 0, st>>>(a);
     else bwd_post_kernel<128><<<grid, kRowWarps * 32, 0, st>>>(a);
     if ((s = launched()) != SWA_OK) return s;
     if (dgq || dgk) {
-      GainArgs g{P.d, at<float>(c, c.L.gpart), dgq, dgk};
-      gain_sum_kernel<<<2, 128, 0, st>>>(g);
+      GainArgs g{P.d, tblk * P.B * P.Hq, tblk * P.B * P.Hkv, post_blocks(P.B, P.T, P.Hq),
+                 at<float>(c, c.L.gpart), dgq, dgk};
+      gain_sum_kernel<<<dim3(2, P.d / 32), 256, 0, st>>>(g);
       if ((s = launched()) != SWA_OK) return s;
     }
   }

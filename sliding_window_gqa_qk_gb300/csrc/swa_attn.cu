@@ -16,6 +16,7 @@
 #include "simt.cuh"
 #else
 #include "tc_fwd.cuh"
+#include "tc_fwd_pair.cuh"
 #include "tc_bwd.cuh"
 #endif
 
@@ -214,7 +215,7 @@ swa_status swa_attn_fwd(const swa_params* p, const void* q, const void* k, const
   f.o = static_cast<elem_t*>(o); f.lse = lse;
   f.status = at<uint32_t>(c, c.L.status);
   f.wait_limit_ns = kWaitLimitNs;
-  return tc::launch_fwd(f, c.stream);
+  return tc::launch_fwd_any(f, c.stream);
 #endif
 }
 

@@ -177,6 +177,18 @@ __device__ __forceinline__ void bulk_wait_group_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Per-warpgroup register budget changes (all four warps of a warpgroup
+// execute the same one). The sum over warpgroups must not exceed the
+// registers the block was launched with.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Named barrier over `count` threads that also ANDs a per-thread flag.
 __device__ __forceinline__ bool named_bar_and(int id, int count, bool flag) {
   uint32_t out;

@@ -29,7 +29,15 @@
 namespace swa {
 namespace tc {
 
-constexpr int kPairThreads = 320;   // 10 warps
+// 12 warps: softmax warpgroups 0 and 1, warpgroup 2 = producer (warp 8),
+// MMA issuer (warp 9) and two idle warps. The launch gives every thread 168
+// registers (384 x 168 = 64512); warpgroup 2 drops to 88 and the softmax
+// warpgroups rise to 208 (2 x 128 x 208 + 128 x 88 = 64512).
+constexpr int kPairThreads = 384;
+constexpr int kPairRegsSoftmax = 208;
+constexpr int kPairRegsOther = 88;
+static_assert(2 * 128 * kPairRegsSoftmax + 128 * kPairRegsOther <= kPairThreads * 168,
+              "register split exceeds the launch's registers");
 
 template <int D>
 struct FwdPairSmem {
@@ -107,7 +115,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-
+  if (warp >= 8) {
+  setmaxnreg_dec<kPairRegsOther>();
   if (warp == 8) {
     // ---------------- TMA producer ----------------
     if (lane == 0 && n_tiles > 0) {
@@ -209,8 +218,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       umma_commit(bar(PB_FINAL));
       mbar_wait_drain(bar(PB_FINAL), 0, prm.wait_limit_ns);
     }
+  }
   } else {
     // ---------------- softmax warpgroups (A: warps 0-3, B: warps 4-7) ----------------
+    setmaxnreg_inc<kPairRegsSoftmax>();
     const int X = warp >> 2;
     const int h = hA + X;
     const int row = threadIdx.x & 127;        // TMEM lane
@@ -252,31 +263,20 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           }
         }
       };
-      // Pass 1: row maximum. Columns 64..127 stay in registers, 0..63 are
-      // read again in pass 2 (keeps the thread under its register budget).
-      uint32_t hi[2][32];
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
+      tmem_wait_ld(sr[0]);
+      reg_fence(sr[1]);
+      reg_fence(sr[2]);
+      reg_fence(sr[3]);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) mask(sr[cc], cc);
       float mx = -INFINITY;
-      {
-        uint32_t a[32];
-        tmem_ld32(tS, a);
-        tmem_wait_ld(a);
-        mask(a, 0);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(a[e]));
-        tmem_ld32(tS + 32, a);
-        tmem_ld32(tS + 64, hi[0]);
-        tmem_ld32(tS + 96, hi[1]);
-        tmem_wait_ld(a);
-        reg_fence(hi[0]);
-        reg_fence(hi[1]);
-        mask(a, 1);
-        mask(hi[0], 2);
-        mask(hi[1], 3);
+      for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          mx = fmaxf(mx, fmaxf(__uint_as_float(a[e]),
-                               fmaxf(__uint_as_float(hi[0][e]), __uint_as_float(hi[1][e]))));
-      }
+        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[cc][e]));
       const float mt = mx * c;
       float alpha = 1.f;
       bool rescale_o = false;
@@ -300,30 +300,22 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           tmem_st32(tO + cc * 32, orr);
         }
       }
-      // Pass 2: P = exp2(S c - m) as bf16 pairs into S's first 64 columns.
+      // P = exp2(S c - m) as bf16 pairs into S's first 64 columns.
       const float mref = (m == -INFINITY) ? 0.f : m;
       float lsum = 0.f;
-      auto emit = [&](const uint32_t (&r)[32], uint32_t dst) {
-        uint32_t pk[16];
 #pragma unroll
-        for (int w = 0; w < 16; ++w) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * w]), c, -mref));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * w + 1]), c, -mref));
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int w = 0; w < 32; ++w) {
+          const int cc = half * 2 + (w >> 4), e = (w & 15) * 2;
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[cc][e]), c, -mref));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[cc][e + 1]), c, -mref));
           lsum += p0 + p1;
           pk[w] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(dst, pk);
-      };
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t a[32];
-        tmem_ld32(tS + cc * 32, a);
-        tmem_wait_ld(a);
-        mask(a, cc);
-        emit(a, tS + cc * 16);
+        tmem_st32(tS + half * 32, pk);
       }
-      emit(hi[0], tS + 32);
-      emit(hi[1], tS + 48);
       l += lsum;
       tmem_wait_st();
       tc_fence_before();

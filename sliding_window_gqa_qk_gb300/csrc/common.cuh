@@ -167,6 +167,7 @@ struct WsLayout {
   size_t dk_acc;    // f32  [B, Hkv, T, d]  gradient of kn
   size_t dv_acc;    // f32  [B, Hkv, T, d]  gradient of v_eff
   size_t gpart;     // f32  [2, post_blocks, d] per-block partial gain gradients
+  size_t gpart_k;   // f32  [B * Hkv * ceil(T / 128), d] per-key-tile partials of dgk
   size_t bwd_end;
 };
 
@@ -201,6 +202,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int T, int Hq, int Hkv, int
   L.dk_acc = o; o = align256(o + bt * Hkv * d * 4);
   L.dv_acc = o; o = align256(o + bt * Hkv * d * 4);
   L.gpart = o; o = align256(o + size_t(2) * post_blocks(B, T, Hq) * d * 4);
+  L.gpart_k = o; o = align256(o + static_cast<size_t>(B) * Hkv * ((T + 127) / 128) * d * 4);
   L.bwd_end = o;
   return L;
 }
@@ -243,8 +245,8 @@ struct PostArgs {  // backward post: RMSNorm backward, dv, dVE, gain partials
 
 struct GainArgs {
   int d;
-  int nblk_q, nblk_k, nblk_max;   // partials written by the q and k segments
-  const float* gpart;
+  const float* part_q; int n_q;   // partials of dgq: [n_q][d]
+  const float* part_k; int n_k;   // partials of dgk: [n_k][d]
   float* dgq; float* dgk;
 };
 

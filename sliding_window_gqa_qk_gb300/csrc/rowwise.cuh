@@ -260,14 +260,15 @@ __global__ void __launch_bounds__(kRowWarps * 32) bwd_post_kernel(PostArgs a) {
   }
 }
 
-// dgq[c] = sum of the q partials, dgk[c] = sum of the k partials, in a fixed
-// order. Grid (2, d / 32), 256 threads: column = 32 * blockIdx.y + lane,
+// dgq[c] = sum of the q partials, dgk[c] = sum of the k partials (written by
+// the backward-post kernel, or by the attention backward's epilogue), in a
+// fixed order. Grid (2, d / 32), 256 threads: column = 32 * blockIdx.y + lane,
 // each warp sums every 8th partial, then the 8 sums are added in order.
 __global__ void __launch_bounds__(256) gain_sum_kernel(GainArgs a) {
   float* out = blockIdx.x == 0 ? a.dgq : a.dgk;
   if (out == nullptr) return;
-  const int nblk = blockIdx.x == 0 ? a.nblk_q : a.nblk_k;
-  const float* part = a.gpart + static_cast<long long>(blockIdx.x) * a.nblk_max * a.d;
+  const int nblk = blockIdx.x == 0 ? a.n_q : a.n_k;
+  const float* part = blockIdx.x == 0 ? a.part_q : a.part_k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = blockIdx.y * 32 + lane;
   float s = 0.f;

@@ -18,6 +18,7 @@
 #include "tc_fwd.cuh"
 #include "tc_fwd_pair.cuh"
 #include "tc_bwd.cuh"
+#include "tc_bwd_pp.cuh"
 #endif
 
 using namespace swa;
@@ -310,18 +311,31 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
     b.v_head_major = (ve != nullptr);
     b.dO = static_cast<const elem_t*>(dO);
     b.lse2 = at<float>(c, c.L.lse2); b.dvec = at<float>(c, c.L.dvec); b.Tpad = t_pad(P.T);
-    b.dq_acc = at<float>(c, c.L.dq_acc); b.dk_acc = at<float>(c, c.L.dk_acc);
-    b.dv_acc = at<float>(c, c.L.dv_acc);
+    b.dq_acc = at<float>(c, c.L.dq_acc);
+    // key-side gradients come out of the kernel's epilogue
+    b.k = ke; b.rstd_k = at<float>(c, c.L.rstd_k); b.gk = gk; b.tok = tok; b.gate = ve_gate;
+    b.dve = (ve != nullptr) ? dve : nullptr; b.ve_scale = P.ve_scale; b.vocab = P.vocab;
+    b.dk = static_cast<elem_t*>(dk); b.dv = static_cast<elem_t*>(dv);
+    b.gpart_k = at<float>(c, c.L.gpart_k);
     b.status = at<uint32_t>(c, c.L.status);
     b.wait_limit_ns = kWaitLimitNs;
-    if ((s = tc::launch_bwd(b, st)) != SWA_OK) return s;
-#endif
-  }
-  if (stages & SWA_BWD_STAGE_POST) {
     if (dve && ve) {
       if (cudaMemsetAsync(dve, 0, sizeof(float) * P.vocab * P.Hkv * P.d, st) != cudaSuccess)
         return SWA_ERR_CUDA;
     }
+    if ((s = tc::launch_bwd_any(b, st)) != SWA_OK) return s;
+#endif
+  }
+  if (stages & SWA_BWD_STAGE_POST) {
+#if defined(SWA_ELEM_FP32)
+    if (dve && ve) {
+      if (cudaMemsetAsync(dve, 0, sizeof(float) * P.vocab * P.Hkv * P.d, st) != cudaSuccess)
+        return SWA_ERR_CUDA;
+    }
+    const int post_segments = 3;   // q, k and v rows
+#else
+    const int post_segments = 1;   // q rows; k and v were done by the attention backward
+#endif
     PostArgs a{};
     a.B = P.B; a.T = P.T; a.Hq = P.Hq; a.Hkv = P.Hkv; a.d = P.d; a.vocab = P.vocab;
     a.ve_scale = P.ve_scale;
@@ -335,13 +349,19 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
     a.nblk_max = post_blocks(P.B, P.T, P.Hq);
     a.status = at<uint32_t>(c, c.L.status);
     const int tblk = (P.T + kPostRowsPerBlock - 1) / kPostRowsPerBlock;
-    dim3 grid(tblk, P.B * P.Hq, 3);
+    dim3 grid(tblk, P.B * P.Hq, post_segments);
     if (P.d == 64) bwd_post_kernel<64><<<grid, kRowWarps * 32, 0, st>>>(a);
     else bwd_post_kernel<128><<<grid, kRowWarps * 32, 0, st>>>(a);
     if ((s = launched()) != SWA_OK) return s;
     if (dgq || dgk) {
-      GainArgs g{P.d, tblk * P.B * P.Hq, tblk * P.B * P.Hkv, post_blocks(P.B, P.T, P.Hq),
-                 at<float>(c, c.L.gpart), dgq, dgk};
+#if defined(SWA_ELEM_FP32)
+      const float* part_k = at<float>(c, c.L.gpart) + static_cast<size_t>(post_blocks(P.B, P.T, P.Hq)) * P.d;
+      const int n_k = tblk * P.B * P.Hkv;
+#else
+      const float* part_k = at<float>(c, c.L.gpart_k);
+      const int n_k = P.B * P.Hkv * ((P.T + 127) / 128);
+#endif
+      GainArgs g{P.d, at<float>(c, c.L.gpart), tblk * P.B * P.Hq, part_k, n_k, dgq, dgk};
       gain_sum_kernel<<<dim3(2, P.d / 32), 256, 0, st>>>(g);
       if ((s = launched()) != SWA_OK) return s;
     }

@@ -54,8 +54,18 @@ struct BwdLaunch {
   const float* dvec;   // [B, Hq, Tpad]  D
   int Tpad;
   float* dq_acc;       // [B, Hq, T, d]
-  float* dk_acc;       // [B, Hkv, T, d]
-  float* dv_acc;       // [B, Hkv, T, d]
+  // key-side outputs, written by the epilogue of the kernel
+  const elem_t* k;     // raw k [B, T, Hkv, d]
+  const float* rstd_k; // [B, Hkv, T]
+  const float* gk;     // [d] or NULL
+  const int32_t* tok;  // [B, T] (VE layers)
+  const float* gate;   // [B, T, Hkv] or NULL
+  float* dve;          // [vocab, Hkv * d] or NULL
+  float ve_scale;
+  int vocab;
+  elem_t* dk;          // [B, T, Hkv, d]
+  elem_t* dv;          // [B, T, Hkv, d]
+  float* gpart_k;      // [B * Hkv * n_ktiles, d]
   uint32_t* status;
   uint64_t wait_limit_ns;
 };
@@ -65,11 +75,180 @@ struct BwdParams {
   float scale, scale_log2;
   const float* lse2;
   const float* dvec;
-  float* dk_acc;
-  float* dv_acc;
+  const elem_t* k;
+  const float* rstd_k;
+  const float* gk;
+  const int32_t* tok;
+  const float* gate;
+  float* dve;
+  float ve_scale;
+  int vocab;
+  elem_t* dk;
+  elem_t* dv;
+  float* gpart_k;
   uint32_t* status;
   uint64_t wait_limit_ns;
 };
+
+// Sum over the 32 lanes of each of 32 values: afterwards lane L holds the
+// sum of column L (a butterfly that halves the kept columns at each step).
+__device__ __forceinline__ float transpose_sum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? v[i] : v[i + off];
+      const float keep = upper ? v[i + off] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return v[0];
+}
+
+// Key-side epilogue of a backward CTA, fused so that dK and dV never leave
+// the chip in fp32. Thread t of warpgroup wg owns key row j = k0 + t and the
+// head-dim columns [wg D/2, (wg+1) D/2) of dK (scaled here) and dV in TMEM.
+//   dk  = RMSNorm backward of k: r (g dkn - xh mean(g dkn xh)),  xh = k r
+//   dgk partial of this key tile = sum over its rows of dkn xh
+//   dv  = dV (the gradient of v_eff);  dVE[tok] += ve_scale gate dV
+// (the RMSNorm and VE-mix backward of the autoresearch Administrator &
+// Developer Guide §8.2.1 blocks, differentiated). `have` is false when the
+// CTA visited no query tile (dK = dV = 0). The two warpgroups exchange their
+// half-row dot products through `sdot` and named barrier 3; `sgain` holds the
+// per-warp column sums. Every thread of both warpgroups must call this.
+template <int D>
+__device__ __forceinline__ void kv_epilogue(const BwdParams& prm, uint32_t tDK, uint32_t tDV,
+                                            bool have, int wg, int t, int b, int hk, int kt,
+                                            float* sdot, float* sgain, uint32_t sdk, uint32_t sdv,
+                                            const CUtensorMap* tmDK, const CUtensorMap* tmDV) {
+  constexpr int HD = D / 2, NCH = HD / 32;
+  float* sg = sdot + 256;                    // gains of this warpgroup's columns
+  sgain += HD * 2;                           // per-warp column sums follow the gains
+  const int lane = t & 31, warp4 = t >> 5;
+  const int j = kt * kBK + t;
+  const bool valid = j < prm.T;
+  const long long bt = static_cast<long long>(b) * prm.T + j;
+  const long long rowoff = (bt * prm.Hkv + hk) * D + wg * HD;   // into k / dk / dv
+  const float r = valid ? prm.rstd_k[(static_cast<long long>(b) * prm.Hkv + hk) * prm.T + j] : 0.f;
+  if (t < HD) sg[wg * HD + t] = prm.gk ? prm.gk[wg * HD + t] : 1.f;
+  // All loads first: dK (TMEM) and the k row (global).
+  uint32_t dkr[NCH][32];
+  if (have) {
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) tmem_ld32(tDK + ch * 32, dkr[ch]);
+  }
+  uint4 xr[NCH * 4];
+  if (valid) {
+    const uint4* src = reinterpret_cast<const uint4*>(prm.k + rowoff);
+#pragma unroll
+    for (int q = 0; q < NCH * 4; ++q) xr[q] = src[q];
+  } else {
+#pragma unroll
+    for (int q = 0; q < NCH * 4; ++q) xr[q] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (have) {
+    tmem_wait_ld(dkr[0]);
+#pragma unroll
+    for (int ch = 1; ch < NCH; ++ch) reg_fence(dkr[ch]);
+  } else {
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+      for (int e = 0; e < 32; ++e) dkr[ch][e] = 0u;
+  }
+  named_bar_sync(3, 256);                    // gains staged
+  auto xval = [&](int c) {                   // c in [0, HD)
+    const uint4 u = xr[c >> 3];
+    const uint32_t w = ((c & 7) >> 1) == 0 ? u.x : ((c & 7) >> 1) == 1 ? u.y : ((c & 7) >> 1) == 2 ? u.z : u.w;
+    return (c & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
+  };
+  float pdot = 0.f;
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int c = ch * 32 + e;
+      pdot = fmaf(sg[wg * HD + c] * __uint_as_float(dkr[ch][e]), xval(c), pdot);
+    }
+  pdot *= prm.scale * r;
+  sdot[wg * 128 + t] = pdot;
+  named_bar_sync(3, 256);
+  const float mean = (pdot + sdot[(1 - wg) * 128 + t]) / D;
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    uint32_t pk[16];
+    float gt[32];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const int c = ch * 32 + e;
+      const float dk0 = __uint_as_float(dkr[ch][e]) * prm.scale;
+      const float dk1 = __uint_as_float(dkr[ch][e + 1]) * prm.scale;
+      const float xh0 = xval(c) * r, xh1 = xval(c + 1) * r;
+      pk[e / 2] = pack_bf16x2(r * (sg[wg * HD + c] * dk0 - xh0 * mean),
+                              r * (sg[wg * HD + c + 1] * dk1 - xh1 * mean));
+      gt[e] = dk0 * xh0;                     // gain term, 0 on rows past T (r = 0)
+      gt[e + 1] = dk1 * xh1;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st_shared_v4(sw128_addr(sdk, kBK, t, (wg * HD + ch * 32) / 8 + q), pk[4 * q], pk[4 * q + 1],
+                   pk[4 * q + 2], pk[4 * q + 3]);
+    sgain[(wg * 4 + warp4) * HD + ch * 32 + lane] = transpose_sum32(gt, lane);
+  }
+  // dv and the VE-table gradient
+  const int tok = (prm.dve != nullptr && valid) ? prm.tok[bt] : -1;
+  const bool ve_ok = tok >= 0 && tok < prm.vocab;
+  const float vs = ve_ok ? prm.ve_scale * (prm.gate ? prm.gate[bt * prm.Hkv + hk] : 1.f) : 0.f;
+  uint32_t dvr[NCH][32];
+  if (have) {
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) tmem_ld32(tDV + ch * 32, dvr[ch]);
+    tmem_wait_ld(dvr[0]);
+#pragma unroll
+    for (int ch = 1; ch < NCH; ++ch) reg_fence(dvr[ch]);
+  } else {
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+      for (int e = 0; e < 32; ++e) dvr[ch][e] = 0u;
+  }
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    const uint32_t* a = dvr[ch];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st_shared_v4(sw128_addr(sdv, kBK, t, (wg * HD + ch * 32) / 8 + q),
+                   pack_bf16x2(__uint_as_float(a[8 * q]), __uint_as_float(a[8 * q + 1])),
+                   pack_bf16x2(__uint_as_float(a[8 * q + 2]), __uint_as_float(a[8 * q + 3])),
+                   pack_bf16x2(__uint_as_float(a[8 * q + 4]), __uint_as_float(a[8 * q + 5])),
+                   pack_bf16x2(__uint_as_float(a[8 * q + 6]), __uint_as_float(a[8 * q + 7])));
+    if (ve_ok) {
+      float* dst = prm.dve + static_cast<long long>(tok) * prm.Hkv * D + hk * D + wg * HD + ch * 32;
+#pragma unroll
+      for (int e = 0; e < 32; e += 4)
+        red_add_v4_f32(dst + e, vs * __uint_as_float(a[e]), vs * __uint_as_float(a[e + 1]),
+                       vs * __uint_as_float(a[e + 2]), vs * __uint_as_float(a[e + 3]));
+    }
+  }
+  fence_async_smem();
+  named_bar_sync(3, 256);
+  if (wg == 0 && t == 0) {
+    // rows past T fall outside the tensors and are not written
+    for (int c = 0; c < D / 64; ++c) {
+      tma_store_4d(tmDK, sdk + c * kBK * 128, 64 * c, kt * kBK, hk, b);
+      tma_store_4d(tmDV, sdv + c * kBK * 128, 64 * c, kt * kBK, hk, b);
+    }
+    bulk_commit_group();
+    bulk_wait_group_all();
+  }
+  if (t < HD) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) sum += sgain[(wg * 4 + w) * HD + t];
+    prm.gpart_k[(static_cast<long long>(b * prm.Hkv + hk) * prm.n_ktiles + kt) * D + wg * HD + t] = sum;
+  }
+}
 
 template <int D>
 struct BwdCfg {
@@ -125,7 +304,8 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
-                  const __grid_constant__ CUtensorMap tmDQ, const BwdParams prm) {
+                  const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmDK,
+                  const __grid_constant__ CUtensorMap tmDV, const BwdParams prm) {
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ;
   constexpr int HC = C::HC;
@@ -449,44 +629,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
     if (leader) bulk_wait_group_all();
-    // ---- epilogue: dK (scaled) and dV rows of this key tile, half the columns each ----
-    if (ok && j < prm.T) {
-      const long long krow = (static_cast<long long>(b) * prm.Hkv + hk) * prm.T + j;
-      float* dkd = prm.dk_acc + krow * D + wg * (D / 2);
-      float* dvd = prm.dv_acc + krow * D + wg * (D / 2);
-      if (n_it == 0) {
-        for (int e = 0; e < D / 2; e += 4) {
-          *reinterpret_cast<float4*>(dkd + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-          *reinterpret_cast<float4*>(dvd + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-    }
-    if (ok && n_it > 0) {
-      tc_fence_after();
-      const long long krow = (static_cast<long long>(b) * prm.Hkv + hk) * prm.T + j;
-#pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc) {
-        const int col = wg * (D / 2) + cc * 32;
-        uint32_t vk[32], vv[32];
-        tmem_ld32(tmem + C::cDK + lane_off + col, vk);
-        tmem_ld32(tmem + C::cDV + lane_off + col, vv);
-        tmem_wait_ld(vk);
-        reg_fence(vv);
-        if (j < prm.T) {
-          float* dkd = prm.dk_acc + krow * D + col;
-          float* dvd = prm.dv_acc + krow * D + col;
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            *reinterpret_cast<float4*>(dkd + e) =
-                make_float4(__uint_as_float(vk[e]) * prm.scale, __uint_as_float(vk[e + 1]) * prm.scale,
-                            __uint_as_float(vk[e + 2]) * prm.scale, __uint_as_float(vk[e + 3]) * prm.scale);
-            *reinterpret_cast<float4*>(dvd + e) =
-                make_float4(__uint_as_float(vv[e]), __uint_as_float(vv[e + 1]),
-                            __uint_as_float(vv[e + 2]), __uint_as_float(vv[e + 3]));
-          }
-        }
-      }
-    }
+    // ---- epilogue: key-side gradients (scratch in the free Q stage buffer) ----
+    tc_fence_after();
+    float* scratch = reinterpret_cast<float*>(smem + C::oQ);
+    const uint32_t sdk = sbase + C::oQ + 4096, sdv = sdk + kBK * D * 2;
+    kv_epilogue<D>(prm, tmem + C::cDK + lane_off + wg * (D / 2), tmem + C::cDV + lane_off + wg * (D / 2),
+                   ok && n_it > 0, wg, t, b, hk, kt, scratch, scratch + 256, sdk, sdv, &tmDK, &tmDV);
   }
   tc_fence_before();
   __syncthreads();
@@ -516,7 +664,9 @@ inline bool map_dq_acc(CUtensorMap* m, float* base, int BH, int T, int D) {
 template <int D>
 inline swa_status launch_bwd_d(const BwdLaunch& f, cudaStream_t st) {
   using C = BwdCfg<D>;
-  CUtensorMap mq, mk, mv, mg, mdq;
+  CUtensorMap mq, mk, mv, mg, mdq, mdk, mdv;
+  if (!map_token_major(&mdk, f.dk, f.B, f.Hkv, f.T, D) || !map_token_major(&mdv, f.dv, f.B, f.Hkv, f.T, D))
+    return SWA_ERR_CUDA;
   if (!make_map_4d(&mq, f.qn, D, f.T, f.Hq, f.B, D, static_cast<long long>(f.T) * D,
                    static_cast<long long>(f.Hq) * f.T * D, C::BQ) ||
       !make_map_4d(&mg, f.dO, D, f.T, f.Hq, f.B, static_cast<long long>(f.Hq) * D, D,
@@ -533,13 +683,14 @@ inline swa_status launch_bwd_d(const BwdLaunch& f, cudaStream_t st) {
   p.scale = f.scale;
   p.scale_log2 = f.scale * 1.4426950408889634f;
   p.lse2 = f.lse2; p.dvec = f.dvec;
-  p.dk_acc = f.dk_acc; p.dv_acc = f.dv_acc;
+  p.k = f.k; p.rstd_k = f.rstd_k; p.gk = f.gk; p.tok = f.tok; p.gate = f.gate; p.dve = f.dve;
+  p.ve_scale = f.ve_scale; p.vocab = f.vocab; p.dk = f.dk; p.dv = f.dv; p.gpart_k = f.gpart_k;
   p.status = f.status; p.wait_limit_ns = f.wait_limit_ns;
   if (cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kAlloc) != cudaSuccess)
     return SWA_ERR_CUDA;
   dim3 grid(f.B * f.Hkv, p.n_ktiles);
-  bwd_tc_kernel<D><<<grid, kBwdThreads, C::kAlloc, st>>>(mq, mk, mv, mg, mdq, p);
+  bwd_tc_kernel<D><<<grid, kBwdThreads, C::kAlloc, st>>>(mq, mk, mv, mg, mdq, mdk, mdv, p);
   return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 

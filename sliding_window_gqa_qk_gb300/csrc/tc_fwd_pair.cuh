@@ -67,7 +67,8 @@ enum {
 template <int D>
 __global__ void __launch_bounds__(kPairThreads, 1)
     fwd_tc_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const FwdParams prm) {
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                       const FwdParams prm) {
   using L = FwdPairSmem<D>;
   constexpr int KCH = D / 64;
   extern __shared__ uint8_t smem_raw[];
@@ -117,35 +118,38 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const uint32_t tmem = tmem_base_sh;
   if (warp >= 8) {
   setmaxnreg_dec<kPairRegsOther>();
+  const uint32_t one = (lane == 0);   // the lane that issues in warp-wide loops
   if (warp == 8) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0 && n_tiles > 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(bar(PB_Q), 2 * L::kTile);
+    // ---------------- TMA producer (whole warp, lane 0 issues) ----------------
+    if (n_tiles > 0) {
+      if (one) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+      }
+      mbar_arrive_expect_tx_w(bar(PB_Q), 2 * L::kTile, one);
       for (int c = 0; c < KCH; ++c) {
-        tma_load_4d(sbase + L::kQA + c * 16384, &tmQ, bar(PB_Q), 64 * c, q0, hA, b);
-        tma_load_4d(sbase + L::kQB + c * 16384, &tmQ, bar(PB_Q), 64 * c, q0, hA + 1, b);
+        tma_load_4d_w(sbase + L::kQA + c * 16384, &tmQ, bar(PB_Q), 64 * c, q0, hA, b, one);
+        tma_load_4d_w(sbase + L::kQB + c * 16384, &tmQ, bar(PB_Q), 64 * c, q0, hA + 1, b, one);
       }
       bool ok = true;
       int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
       for (int j = 0; j < n_tiles && ok; ++j) {
         const int s = j & 1;
         const int k0 = (kt_lo + j) * kBN;
-        if (j >= 2) ok = mbar_wait(bar(PB_KEMPTY + s), ((j - 2) >> 1) & 1, ctl);
+        if (j >= 2) ok = mbar_wait_warp(bar(PB_KEMPTY + s), ((j - 2) >> 1) & 1, ctl);
         if (!ok) break;
-        mbar_arrive_expect_tx(bar(PB_KFULL + s), L::kTile);
+        mbar_arrive_expect_tx_w(bar(PB_KFULL + s), L::kTile, one);
         for (int c = 0; c < KCH; ++c)
-          tma_load_4d(sbase + L::kK0 + s * L::kTile + c * 16384, &tmK, bar(PB_KFULL + s), 64 * c,
-                      k0, hk, b);
+          tma_load_4d_w(sbase + L::kK0 + s * L::kTile + c * 16384, &tmK, bar(PB_KFULL + s), 64 * c,
+                        k0, hk, b, one);
         last_k[s] = j;
-        if (j >= 2) ok = mbar_wait(bar(PB_VEMPTY + s), ((j - 2) >> 1) & 1, ctl);
+        if (j >= 2) ok = mbar_wait_warp(bar(PB_VEMPTY + s), ((j - 2) >> 1) & 1, ctl);
         if (!ok) break;
-        mbar_arrive_expect_tx(bar(PB_VFULL + s), L::kTile);
+        mbar_arrive_expect_tx_w(bar(PB_VFULL + s), L::kTile, one);
         for (int c = 0; c < KCH; ++c)
-          tma_load_4d(sbase + L::kV0 + s * L::kTile + c * 16384, &tmV, bar(PB_VFULL + s), 64 * c,
-                      k0, hk, b);
+          tma_load_4d_w(sbase + L::kV0 + s * L::kTile + c * 16384, &tmV, bar(PB_VFULL + s), 64 * c,
+                        k0, hk, b, one);
         last_v[s] = j;
       }
       mbar_wait_drain(bar(PB_Q), 0, prm.wait_limit_ns);
@@ -155,67 +159,71 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
     }
   } else if (warp == 9) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0 && n_tiles > 0) {
+    // ---------------- MMA issuer (whole warp, lane 0 issues) ----------------
+    if (n_tiles > 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0, 0);
       constexpr uint32_t idO = idesc_bf16_f32(kBM, D, 0, 1);
+      // Descriptor bases, computed once; every MMA adds a constant offset.
+      const uint64_t dQ0 = sdesc_sw128(sbase + L::kQA, 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(sbase + L::kK0, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(sbase + L::kV0, 16384, 1024);
       auto issue_s = [&](int X, int j) {
-        const uint32_t qa = sbase + (X == 0 ? L::kQA : L::kQB);
-        const uint32_t ka = sbase + L::kK0 + (j & 1) * L::kTile;
+        const uint64_t qd = sdesc_add(dQ0, X * L::kTile), kd = sdesc_add(dK0, (j & 1) * L::kTile);
+        const uint32_t dst = tmem + X * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_bf16_ss(tmem + X * 128, sdesc_sw128(qa + off, 16, 1024),
-                       sdesc_sw128(ka + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          umma_bf16_ss_w(dst, sdesc_add(qd, off), sdesc_add(kd, off), idS, kk > 0 ? 1u : 0u, one);
         }
-        umma_commit(bar(PB_SFULL + X));
+        umma_commit_w(bar(PB_SFULL + X), one);
       };
       auto issue_pv = [&](int X, int j) {
-        const uint32_t va = sbase + L::kV0 + (j & 1) * L::kTile;
+        const uint64_t vd = sdesc_add(dV0, (j & 1) * L::kTile);
+        const uint32_t dst = tmem + 256 + X * D, pa = tmem + X * 128;
+        umma_bf16_ts_w(dst, pa, vd, idO, j > 0 ? 1u : 0u, one);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_bf16_ts(tmem + 256 + X * D, tmem + X * 128 + kk * 8,
-                       sdesc_sw128(va + kk * 2048, 16384, 1024), idO, (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(PB_PV + X));
+        for (int kk = 1; kk < kBN / 16; ++kk)
+          umma_bf16_ts_w(dst, pa + kk * 8, sdesc_add(vd, kk * 2048), idO, 1u, one);
+        umma_commit_w(bar(PB_PV + X), one);
       };
-      bool ok = mbar_wait(bar(PB_Q), 0, ctl) && mbar_wait(bar(PB_KFULL), 0, ctl);
+      bool ok = mbar_wait_warp(bar(PB_Q), 0, ctl) && mbar_wait_warp(bar(PB_KFULL), 0, ctl);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
         issue_s(1, 0);
-        umma_commit(bar(PB_KEMPTY));
+        umma_commit_w(bar(PB_KEMPTY), one);
       }
       for (int j = 1; j < n_tiles && ok; ++j) {
         const int s = j & 1, sp = (j - 1) & 1;
-        ok = mbar_wait(bar(PB_KFULL + s), (j >> 1) & 1, ctl) &&
-             mbar_wait(bar(PB_PFULL + 0), (j - 1) & 1, ctl) &&
-             mbar_wait(bar(PB_VFULL + sp), ((j - 1) >> 1) & 1, ctl);
+        ok = mbar_wait_warp(bar(PB_KFULL + s), (j >> 1) & 1, ctl) &&
+             mbar_wait_warp(bar(PB_PFULL + 0), (j - 1) & 1, ctl) &&
+             mbar_wait_warp(bar(PB_VFULL + sp), ((j - 1) >> 1) & 1, ctl);
         if (!ok) break;
         tc_fence_after();
         issue_pv(0, j - 1);
         issue_s(0, j);
-        if (!(ok = mbar_wait(bar(PB_PFULL + 1), (j - 1) & 1, ctl))) break;
+        if (!(ok = mbar_wait_warp(bar(PB_PFULL + 1), (j - 1) & 1, ctl))) break;
         tc_fence_after();
         issue_pv(1, j - 1);
-        umma_commit(bar(PB_VEMPTY + sp));
+        umma_commit_w(bar(PB_VEMPTY + sp), one);
         issue_s(1, j);
-        umma_commit(bar(PB_KEMPTY + s));
+        umma_commit_w(bar(PB_KEMPTY + s), one);
       }
       if (ok) {
         const int j = n_tiles - 1;
-        ok = mbar_wait(bar(PB_PFULL + 0), j & 1, ctl) &&
-             mbar_wait(bar(PB_VFULL + (j & 1)), (j >> 1) & 1, ctl);
+        ok = mbar_wait_warp(bar(PB_PFULL + 0), j & 1, ctl) &&
+             mbar_wait_warp(bar(PB_VFULL + (j & 1)), (j >> 1) & 1, ctl);
         if (ok) {
           tc_fence_after();
           issue_pv(0, j);
-          if ((ok = mbar_wait(bar(PB_PFULL + 1), j & 1, ctl))) {
+          if ((ok = mbar_wait_warp(bar(PB_PFULL + 1), j & 1, ctl))) {
             tc_fence_after();
             issue_pv(1, j);
-            umma_commit(bar(PB_VEMPTY + (j & 1)));
+            umma_commit_w(bar(PB_VEMPTY + (j & 1)), one);
           }
         }
       }
-      umma_commit(bar(PB_FINAL));
+      umma_commit_w(bar(PB_FINAL), one);
       mbar_wait_drain(bar(PB_FINAL), 0, prm.wait_limit_ns);
     }
   }
@@ -324,32 +332,37 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
     // ---- epilogue: O / l, LSE ----
     if (ok) ok = mbar_wait_warp(bar(PB_PV + X), (n_tiles - 1) & 1, ctl);
+    // O / l goes through this warpgroup's Q tile (no longer read by any MMA)
+    // in the 128-byte swizzle layout, then out with bulk tensor stores.
+    const uint32_t sOut = sbase + (X == 0 ? L::kQA : L::kQB);
     if (ok) {
       tc_fence_after();
       const bool empty = !(l > 0.f);
       const float inv = empty ? 0.f : 1.0f / l;
-      elem_t* orow = prm.o + ((static_cast<long long>(b) * prm.T + i) * prm.Hq + h) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t orr[32];
         tmem_ld32(tO + cc * 32, orr);
         tmem_wait_ld(orr);
-        if (i < prm.T) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 pk;
-            pk.x = pack_bf16x2(__uint_as_float(orr[e + 0]) * inv, __uint_as_float(orr[e + 1]) * inv);
-            pk.y = pack_bf16x2(__uint_as_float(orr[e + 2]) * inv, __uint_as_float(orr[e + 3]) * inv);
-            pk.z = pack_bf16x2(__uint_as_float(orr[e + 4]) * inv, __uint_as_float(orr[e + 5]) * inv);
-            pk.w = pack_bf16x2(__uint_as_float(orr[e + 6]) * inv, __uint_as_float(orr[e + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + cc * 32 + e) = pk;
-          }
-        }
+        for (int e = 0; e < 32; e += 8)
+          st_shared_v4(sw128_addr(sOut, kBM, row, (cc * 32 + e) / 8),
+                       pack_bf16x2(__uint_as_float(orr[e + 0]) * inv, __uint_as_float(orr[e + 1]) * inv),
+                       pack_bf16x2(__uint_as_float(orr[e + 2]) * inv, __uint_as_float(orr[e + 3]) * inv),
+                       pack_bf16x2(__uint_as_float(orr[e + 4]) * inv, __uint_as_float(orr[e + 5]) * inv),
+                       pack_bf16x2(__uint_as_float(orr[e + 6]) * inv, __uint_as_float(orr[e + 7]) * inv));
       }
       if (i < prm.T) {
         prm.lse[(static_cast<long long>(b) * prm.Hq + h) * prm.T + i] =
             empty ? -INFINITY : (m + log2f(l)) * 0.69314718055994531f;
       }
+      fence_async_smem();
+    }
+    ok = named_bar_and(1 + X, 128, ok);
+    if (ok && row == 0) {
+      for (int c = 0; c < KCH; ++c) tma_store_4d(&tmO, sOut + c * 16384, 64 * c, q0, h, b);
+      bulk_commit_group();
+      bulk_wait_group_all();
     }
   }
   tc_fence_before();
@@ -362,8 +375,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
 template <int D>
 inline swa_status launch_fwd_pair_d(const FwdLaunch& f, cudaStream_t st) {
-  CUtensorMap mq, mk, mv;
-  if (!map_head_major(&mq, f.qn, f.B, f.Hq, f.T, D) || !map_head_major(&mk, f.kn, f.B, f.Hkv, f.T, D))
+  CUtensorMap mq, mk, mv, mo;
+  if (!map_head_major(&mq, f.qn, f.B, f.Hq, f.T, D) || !map_head_major(&mk, f.kn, f.B, f.Hkv, f.T, D) ||
+      !map_token_major(&mo, f.o, f.B, f.Hq, f.T, D))
     return SWA_ERR_CUDA;
   const bool okv = f.v_head_major ? map_head_major(&mv, f.v, f.B, f.Hkv, f.T, D)
                                   : map_token_major(&mv, f.v, f.B, f.Hkv, f.T, D);
@@ -377,7 +391,7 @@ inline swa_status launch_fwd_pair_d(const FwdLaunch& f, cudaStream_t st) {
                            FwdPairSmem<D>::kAlloc) != cudaSuccess)
     return SWA_ERR_CUDA;
   dim3 grid(f.B * (f.Hq / 2), p.n_qtiles);
-  fwd_tc_pair_kernel<D><<<grid, kPairThreads, FwdPairSmem<D>::kAlloc, st>>>(mq, mk, mv, p);
+  fwd_tc_pair_kernel<D><<<grid, kPairThreads, FwdPairSmem<D>::kAlloc, st>>>(mq, mk, mv, mo, p);
   return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 

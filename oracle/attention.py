@@ -55,6 +55,8 @@ __all__ = [
     "attention_forward",
     "attention_backward",
     "attention_forward_rows",
+    "attention_backward_rows",
+    "attention_backward_cols",
 ]
 
 
@@ -316,3 +318,79 @@ def attention_backward(q, k, v, gq=None, gk=None, dO=None, *, window: int,
         dve = np.zeros((np.asarray(ve).shape[0], Hd))
         np.add.at(dve, np.asarray(tok, dtype=np.int64).reshape(-1), contrib)
     return {"dq": dq, "dk": dk, "dv": dveff, "dgq": dgq, "dgk": dgk, "dve": dve}
+
+
+def _one_batch(q, k, v, dO, tok, gate, b):
+    """Batch element b of the inputs, kept 4-D (leading axis of size 1)."""
+    sl = slice(b, b + 1)
+    f = lambda x: None if x is None else np.asarray(x[sl], dtype=np.float64)
+    tk = None if tok is None else np.asarray(tok)[sl]
+    return f(q), f(k), f(v), f(dO), tk, f(gate)
+
+
+def attention_backward_rows(q, k, v, gq=None, gk=None, dO=None, *, b: int, h: int, rows,
+                            window: int, causal: bool = True, scale=None, eps: float = 1e-6,
+                            ve=None, tok=None, gate=None, ve_scale: float = 0.5):
+    """dq of ``attention_backward`` at the query rows ``rows`` of one (b, h).
+
+    Row i of dq depends only on row i of the softmax: dA_i = dO_i v_eff^T,
+    dS_i = A_i * (dA_i - <dA_i, A_i>), dqn_i = scale * dS_i kn, then the
+    RMSNorm backward of that row. Returns dq [len(rows), d]. Used to sample
+    the gradient of full-size problems one row at a time.
+    """
+    q, k, v, dO, tk, gt = _one_batch(q, k, v, dO, tok, gate, b)
+    T, d = q.shape[1], q.shape[3]
+    G = q.shape[2] // k.shape[2]
+    hk = h // G
+    sc = _scale(d, scale)
+    rows = np.asarray(rows, dtype=np.int64)
+    qn, _ = rms_norm(q[0, rows, h, :], gq, eps)
+    kn, _ = rms_norm(k[0, :, hk, :], gk, eps)
+    v_eff = ve_mix(v, ve, tk, gt, ve_scale)[0, :, hk, :]
+    A, _ = _softmax_rows(sc * (qn @ kn.T), band_mask(rows, T, window, causal))
+    dA = dO[0, rows, h, :] @ v_eff.T
+    dS = A * (dA - np.sum(dA * A, axis=1, keepdims=True))
+    dq, _ = rms_norm_backward(q[0, rows, h, :], gq, eps, sc * (dS @ kn))
+    return dq
+
+
+def attention_backward_cols(q, k, v, gq=None, gk=None, dO=None, *, b: int, hk: int, cols,
+                            window: int, causal: bool = True, scale=None, eps: float = 1e-6,
+                            ve=None, tok=None, gate=None, ve_scale: float = 0.5,
+                            row_chunk: int = 512):
+    """dk and dv of ``attention_backward`` at the key positions ``cols`` of one
+    (b, kv head hk).
+
+    Column j collects, over the G query heads of the group and every query
+    row i: dv_j += A_ij dO_i and dkn_j += scale * dS_ij qn_i, with A and dS
+    the full rows of the softmax and its backward (a row must be seen whole
+    to be normalised). Only rows whose band holds one of ``cols`` are
+    visited; the others add exact zeros. Then the RMSNorm backward of the k
+    rows. Returns (dk [len(cols), d], dv [len(cols), d]).
+    """
+    q, k, v, dO, tk, gt = _one_batch(q, k, v, dO, tok, gate, b)
+    T, Hq, d = q.shape[1], q.shape[2], q.shape[3]
+    G = Hq // k.shape[2]
+    sc = _scale(d, scale)
+    cols = np.asarray(cols, dtype=np.int64)
+    kn, _ = rms_norm(k[0, :, hk, :], gk, eps)
+    v_eff = ve_mix(v, ve, tk, gt, ve_scale)[0, :, hk, :]
+    dkn = np.zeros((cols.size, d))
+    dv = np.zeros((cols.size, d))
+    for r0 in range(0, T, row_chunk):
+        rows = np.arange(r0, min(T, r0 + row_chunk))
+        M = band_mask(rows, T, window, causal)
+        keep = M[:, cols].any(axis=1)
+        if not keep.any():
+            continue
+        rows, M = rows[keep], M[keep]
+        for h in range(hk * G, (hk + 1) * G):
+            qn, _ = rms_norm(q[0, rows, h, :], gq, eps)
+            A, _ = _softmax_rows(sc * (qn @ kn.T), M)
+            dOr = dO[0, rows, h, :]
+            dA = dOr @ v_eff.T
+            dS = A * (dA - np.sum(dA * A, axis=1, keepdims=True))
+            dv += A[:, cols].T @ dOr
+            dkn += sc * (dS[:, cols].T @ qn)
+    dk, _ = rms_norm_backward(k[0, cols, hk, :], gk, eps, dkn)
+    return dk, dv

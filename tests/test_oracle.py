@@ -448,3 +448,58 @@ def test_row_chunking_does_not_change_results():
     g2 = bwd(x, window=9, row_chunk=5)
     for k in ("dq", "dk", "dv", "dgq", "dgk"):
         np.testing.assert_allclose(g1[k], g2[k], rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("window,causal", [(6, True), (-1, True), (4, False)])
+def test_backward_samplers_against_float64_torch_autograd(window, causal):
+    """The row (dq) and column (dk, dv) samplers of the backward, checked
+    against torch float64 autograd through SDPA with an explicit mask, and
+    against the full oracle backward."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    B, T, Hq, Hkv, d = 2, 23, 4, 2, 8
+    x = rand_problem(19, B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, with_ve=True, with_gate=True)
+    eps, s_ve = 1e-6, 0.5
+    t = {k: (torch.tensor(v, dtype=torch.float64, requires_grad=k in ("q", "k", "v"))
+             if v is not None and k != "tok" else v) for k, v in x.items()}
+    tok = torch.tensor(x["tok"], dtype=torch.long)
+    qn = F.rms_norm(t["q"], (d,), t["gq"], eps)
+    kn = F.rms_norm(t["k"], (d,), t["gk"], eps)
+    v = t["v"] + s_ve * t["gate"].unsqueeze(-1) * t["ve"][tok].view(B, T, Hkv, d)
+    i = torch.arange(T)[:, None]
+    j = torch.arange(T)[None, :]
+    if causal:
+        mask = (j <= i) & ((i - j <= window) if window >= 0 else True)
+    else:
+        mask = (i - j).abs() <= window
+    out = F.scaled_dot_product_attention(qn.transpose(1, 2), kn.transpose(1, 2),
+                                         v.transpose(1, 2), attn_mask=mask,
+                                         enable_gqa=True).transpose(1, 2)
+    (out * t["dO"]).sum().backward()
+    full = bwd(x, window=window, causal=causal, eps=eps, ve_scale=s_ve)
+    kw = dict(window=window, causal=causal, eps=eps, ve=x["ve"], tok=x["tok"], gate=x["gate"],
+              ve_scale=s_ve)
+    args = (x["q"], x["k"], x["v"], x["gq"], x["gk"], x["dO"])
+    rows = [0, 3, 11, 22]
+    for b, h in [(0, 0), (1, 3), (1, 2)]:
+        dq = orc.attention_backward_rows(*args, b=b, h=h, rows=rows, **kw)
+        np.testing.assert_allclose(dq, t["q"].grad[b, rows, h].numpy(), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(dq, full["dq"][b, rows, h], rtol=1e-10, atol=1e-12)
+    cols = [0, 1, 9, 21, 22]
+    for b, hk in [(0, 0), (1, 1)]:
+        dk, dv = orc.attention_backward_cols(*args, b=b, hk=hk, cols=cols, row_chunk=5, **kw)
+        np.testing.assert_allclose(dk, t["k"].grad[b, cols, hk].numpy(), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(dv, t["v"].grad[b, cols, hk].numpy(), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(dv, full["dv"][b, cols, hk], rtol=1e-10, atol=1e-12)
+
+
+def test_backward_column_sampler_skips_only_rows_that_add_zero():
+    """A key seen by no row of a chunk: the sampler's result does not depend
+    on the chunking (rows outside every band are skipped, not dropped)."""
+    x = rand_problem(20, B=1, T=40, Hq=2, Hkv=1, d=8)
+    args = (x["q"], x["k"], x["v"], x["gq"], x["gk"], x["dO"])
+    a = orc.attention_backward_cols(*args, b=0, hk=0, cols=[2, 30, 39], window=3, row_chunk=4)
+    c = orc.attention_backward_cols(*args, b=0, hk=0, cols=[2, 30, 39], window=3, row_chunk=64)
+    full = bwd(x, window=3)
+    for got, ref in ((a[0], full["dk"]), (c[0], full["dk"]), (a[1], full["dv"])):
+        np.testing.assert_allclose(got, ref[0, [2, 30, 39], 0], rtol=1e-11, atol=1e-13)

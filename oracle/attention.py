@@ -158,8 +158,9 @@ def ve_mix(v: np.ndarray, ve, tok, gate, ve_scale: float) -> np.ndarray:
 # Mask and attention
 # ----------------------------------------------------------------------------
 
-def band_mask(rows, T: int, window: int, causal: bool) -> np.ndarray:
-    """Boolean visibility matrix for query rows ``rows`` against keys 0..T-1.
+def band_mask(rows, T: int, window: int, causal: bool, keys=None) -> np.ndarray:
+    """Boolean visibility matrix for query rows ``rows`` against keys 0..T-1
+    (or against the key positions ``keys`` only, when given).
 
     Causal: key j visible to query i iff j <= i and (window < 0 or i - j <= window).
     Non-causal: iff window < 0 or |i - j| <= window.
@@ -167,13 +168,13 @@ def band_mask(rows, T: int, window: int, causal: bool) -> np.ndarray:
     [Guide] §6.3 "Sliding-window attention".
     """
     i = np.asarray(rows, dtype=np.int64)[:, None]
-    j = np.arange(T, dtype=np.int64)[None, :]
+    j = (np.arange(T, dtype=np.int64) if keys is None else np.asarray(keys, dtype=np.int64))[None, :]
     if causal:
         m = j <= i
         if window >= 0:
             m &= (i - j) <= window
     else:
-        m = np.ones((i.shape[0], T), dtype=bool)
+        m = np.ones((i.shape[0], j.shape[1]), dtype=bool)
         if window >= 0:
             m &= np.abs(i - j) <= window
     return m
@@ -379,11 +380,11 @@ def attention_backward_cols(q, k, v, gq=None, gk=None, dO=None, *, b: int, hk: i
     dv = np.zeros((cols.size, d))
     for r0 in range(0, T, row_chunk):
         rows = np.arange(r0, min(T, r0 + row_chunk))
-        M = band_mask(rows, T, window, causal)
-        keep = M[:, cols].any(axis=1)
+        keep = band_mask(rows, T, window, causal, keys=cols).any(axis=1)
         if not keep.any():
             continue
-        rows, M = rows[keep], M[keep]
+        rows = rows[keep]
+        M = band_mask(rows, T, window, causal)
         for h in range(hk * G, (hk + 1) * G):
             qn, _ = rms_norm(q[0, rows, h, :], gq, eps)
             A, _ = _softmax_rows(sc * (qn @ kn.T), M)

@@ -503,3 +503,12 @@ def test_backward_column_sampler_skips_only_rows_that_add_zero():
     full = bwd(x, window=3)
     for got, ref in ((a[0], full["dk"]), (c[0], full["dk"]), (a[1], full["dv"])):
         np.testing.assert_allclose(got, ref[0, [2, 30, 39], 0], rtol=1e-11, atol=1e-13)
+
+
+def test_band_mask_on_chosen_keys_is_a_column_selection():
+    rows = np.arange(0, 50, 3)
+    cols = [0, 7, 8, 33, 49]
+    for window, causal in [(5, True), (-1, True), (4, False), (-1, False), (0, True)]:
+        full = orc.band_mask(rows, 50, window, causal)
+        np.testing.assert_array_equal(orc.band_mask(rows, 50, window, causal, keys=cols),
+                                      full[:, cols])

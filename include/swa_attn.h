@@ -87,8 +87,10 @@ typedef struct swa_params {
                                   inputs: skip recomputing them                       */
 #define SWA_BWD_STAGE_PRE 2u   /* backward stages to run; none of the three bits set */
 #define SWA_BWD_STAGE_MAIN 4u  /* means all of them. PRE: D = rowsum(dO * O), clear   */
-#define SWA_BWD_STAGE_POST 8u  /* the accumulators; MAIN: the attention backward;
-                                  POST: RMSNorm backward, gain and VE gradients.
+#define SWA_BWD_STAGE_POST 8u  /* the accumulators (and dve); MAIN: the attention
+                                  backward with the key-side RMSNorm backward (dk,
+                                  dv, dve); POST: query-side RMSNorm backward and
+                                  the gain gradients.
                                   Running them one call at a time, in this order,
                                   gives the same result as one call with all three.  */
 

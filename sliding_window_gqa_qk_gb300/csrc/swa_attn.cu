@@ -275,6 +275,13 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
     if (P.d == 64) bwd_pre_kernel<64><<<grid, kRowWarps * 32, 0, st>>>(a);
     else bwd_pre_kernel<128><<<grid, kRowWarps * 32, 0, st>>>(a);
     if ((s = launched()) != SWA_OK) return s;
+#if !defined(SWA_ELEM_FP32)
+    // the attention backward adds the VE-table gradient into dve
+    if (dve && ve) {
+      if (cudaMemsetAsync(dve, 0, sizeof(float) * P.vocab * P.Hkv * P.d, st) != cudaSuccess)
+        return SWA_ERR_CUDA;
+    }
+#endif
   }
   if (stages & SWA_BWD_STAGE_MAIN) {
 #if defined(SWA_ELEM_FP32)
@@ -319,10 +326,6 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
     b.gpart_k = at<float>(c, c.L.gpart_k);
     b.status = at<uint32_t>(c, c.L.status);
     b.wait_limit_ns = kWaitLimitNs;
-    if (dve && ve) {
-      if (cudaMemsetAsync(dve, 0, sizeof(float) * P.vocab * P.Hkv * P.d, st) != cudaSuccess)
-        return SWA_ERR_CUDA;
-    }
     if ((s = tc::launch_bwd_any(b, st)) != SWA_OK) return s;
 #endif
   }

@@ -54,36 +54,41 @@ LONG_S = Problem(B=2, T=16384, Hq=16, Hkv=4, d=128, window=8192, gain_std=0.1)
 LONG_L = Problem(B=2, T=16384, Hq=16, Hkv=4, d=128, window=-1, gain_std=0.1)
 
 
-def _gen(seed: int) -> torch.Generator:
-    g = torch.Generator(device="cpu")
+def _gen(seed: int, device="cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
     g.manual_seed(seed)
     return g
 
 
 def make_inputs(p: Problem, layer: int = 0, dtype: torch.dtype = torch.bfloat16,
-                seed: int = BASE_SEED) -> dict:
-    """Draw the inputs of one layer on the CPU.
+                seed: int = BASE_SEED, device="cpu") -> dict:
+    """Draw the inputs of one layer.
 
     Returns a dict with q, k, v, dO (``dtype``), gq, gk (fp32 [d] or None),
     ve ([vocab, Hkv*d] in ``dtype`` or None) and tok (int32 [B, T] or None).
+    With ``device`` a CUDA device the same recipe draws from that device's
+    generator (another stream of numbers than the CPU's, same distributions),
+    for sizes whose CPU draw would take minutes.
     """
     s = seed + 100 * layer
     B, T, Hq, Hkv, d = p.B, p.T, p.Hq, p.Hkv, p.d
+    kw = dict(device=device)
     out = {}
-    out["q"] = torch.randn(B, T, Hq, d, generator=_gen(s + 0)).to(dtype)
-    out["k"] = torch.randn(B, T, Hkv, d, generator=_gen(s + 1)).to(dtype)
-    out["v"] = torch.randn(B, T, Hkv, d, generator=_gen(s + 2)).to(dtype)
+    out["q"] = torch.randn(B, T, Hq, d, generator=_gen(s + 0, device), **kw).to(dtype)
+    out["k"] = torch.randn(B, T, Hkv, d, generator=_gen(s + 1, device), **kw).to(dtype)
+    out["v"] = torch.randn(B, T, Hkv, d, generator=_gen(s + 2, device), **kw).to(dtype)
     if p.gain_std is None:
         out["gq"] = None
         out["gk"] = None
     else:
-        out["gq"] = 1.0 + p.gain_std * torch.randn(d, generator=_gen(s + 3))
-        out["gk"] = 1.0 + p.gain_std * torch.randn(d, generator=_gen(s + 4))
-    out["dO"] = torch.randn(B, T, Hq, d, generator=_gen(s + 5)).to(dtype)
+        out["gq"] = 1.0 + p.gain_std * torch.randn(d, generator=_gen(s + 3, device), **kw)
+        out["gk"] = 1.0 + p.gain_std * torch.randn(d, generator=_gen(s + 4, device), **kw)
+    out["dO"] = torch.randn(B, T, Hq, d, generator=_gen(s + 5, device), **kw).to(dtype)
     if p.ve:
-        out["ve"] = (0.02 * torch.randn(p.vocab, Hkv * d, generator=_gen(s + 6))).to(dtype)
-        out["tok"] = torch.randint(0, p.vocab, (B, T), generator=_gen(s + 7),
-                                   dtype=torch.int64).to(torch.int32)
+        out["ve"] = (0.02 * torch.randn(p.vocab, Hkv * d, generator=_gen(s + 6, device),
+                                        **kw)).to(dtype)
+        out["tok"] = torch.randint(0, p.vocab, (B, T), generator=_gen(s + 7, device),
+                                   dtype=torch.int64, **kw).to(torch.int32)
     else:
         out["ve"] = None
         out["tok"] = None

@@ -46,7 +46,7 @@ def run_library(p, x, reuse_prologue=True):
 def run_oracle(p, x, b_slice=None):
     f = {k: as_f64(t) for k, t in x.items()}
     tok = x["tok"].numpy() if x["tok"] is not None else None
-    gate = f["gate"]
+    gate = f.get("gate")
     q, k, v, dO = f["q"], f["k"], f["v"], f["dO"]
     if b_slice is not None:
         sl = slice(b_slice, b_slice + 1)
@@ -91,3 +91,51 @@ def compare(got, ref, tol, keys=("o", "lse", "dq", "dk", "dv", "dgq", "dgk", "dv
     bad = {k: e for k, e in errs.items() if not e <= tol}
     assert not bad, f"relative errors above {tol}: {bad} (all: {errs})"
     return errs
+
+
+def run_staged(p, x, dev=None):
+    """Forward + backward through the C ABI exactly as the benchmark calls
+    it: swa_attn_fwd with the ve gate left out, then the three backward
+    stages one call at a time with the prologue outputs reused. Returns CPU
+    tensors (bf16 outputs as stored, fp32 gradients of the shared
+    parameters)."""
+    dev = dev or torch.device("cuda:0")
+    g = {k: (t.to(dev).contiguous() if t is not None else None) for k, t in x.items()}
+    kind = "fp32" if x["q"].dtype == torch.float32 else "bf16"
+    prm = swa.make_params(p.B, p.T, p.Hq, p.Hkv, p.d, p.window, p.causal, 0.0, p.eps,
+                          p.ve_scale, p.vocab if p.ve else 0)
+    ws = swa.new_workspace(prm, True, dev, kind)
+    o = torch.empty_like(g["q"])
+    lse = torch.empty(p.B, p.Hq, p.T, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(g["q"]), torch.empty_like(g["k"]), torch.empty_like(g["v"])
+    dgq = torch.empty(p.d, device=dev) if g["gq"] is not None else None
+    dgk = torch.empty(p.d, device=dev) if g["gk"] is not None else None
+    dve = torch.empty(g["ve"].shape, device=dev) if p.ve else None
+    gate = g.get("gate")
+    st = swa.swa_attn_fwd(prm, g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"], g["tok"], gate,
+                          o, lse, ws, kind=kind)
+    assert st == swa.SWA_OK, swa.swa_strerror(st)
+    for stage in (swa.SWA_BWD_STAGE_PRE, swa.SWA_BWD_STAGE_MAIN, swa.SWA_BWD_STAGE_POST):
+        st = swa.swa_attn_bwd(prm, g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"], g["tok"],
+                              gate, o, lse, g["dO"], dq, dk, dv, dgq, dgk, dve, ws,
+                              flags=swa.SWA_REUSE_PROLOGUE | stage, kind=kind)
+        assert st == swa.SWA_OK, swa.swa_strerror(st)
+    status = swa.swa_attn_check_status(ws, kind=kind)
+    torch.cuda.synchronize()
+    out = {"o": o.cpu(), "lse": lse.cpu(), "dq": dq.cpu(), "dk": dk.cpu(), "dv": dv.cpu(),
+           "dgq": dgq.cpu() if dgq is not None else None,
+           "dgk": dgk.cpu() if dgk is not None else None,
+           "dve": dve.cpu() if dve is not None else None, "status": status}
+    del ws, g
+    return out
+
+
+def batch_slice(x, b):
+    """The inputs of batch element b alone (a B=1 problem); shared tensors kept."""
+    out = {}
+    for k, t in x.items():
+        if t is None or k in ("gq", "gk", "ve"):
+            out[k] = t
+        else:
+            out[k] = t[b:b + 1].contiguous()
+    return out

@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <type_traits>
 
 namespace swa {
 
@@ -318,6 +319,50 @@ __device__ __forceinline__ void umma_commit_w(uint32_t bar, uint32_t issue) {
       "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
       "r"(issue)
       : "memory");
+}
+
+// Forms with the per-instruction descriptor offsets as immediates (in 16-byte
+// units for shared-memory descriptors, in columns for TMEM addresses) and the
+// instruction descriptor as an immediate. The offset is added inside the asm,
+// so the compiler keeps one base descriptor per operand live instead of
+// hoisting one 64-bit descriptor per K step out of the issue loop (which
+// spills in the 88-register MMA warp).
+template <uint32_t ID, uint32_t AOFF, uint32_t BOFF>
+__device__ __forceinline__ void umma_ss_imm(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t accumulate, uint32_t issue) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b64 da, db;\n\t"
+      "add.s64 da, %1, %5;\n\t"
+      "add.s64 db, %2, %6;\n\t"
+      "setp.ne.b32 p, %3, 0;\n\t"
+      "setp.ne.b32 q, %4, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %7, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(accumulate), "r"(issue), "n"(AOFF), "n"(BOFF), "n"(ID)
+      : "memory");
+}
+
+template <uint32_t ID, uint32_t AOFF, uint32_t BOFF>
+__device__ __forceinline__ void umma_ts_imm(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t accumulate, uint32_t issue) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b64 db;\n\t.reg .b32 ta;\n\t"
+      "add.u32 ta, %1, %5;\n\t"
+      "add.s64 db, %2, %6;\n\t"
+      "setp.ne.b32 p, %3, 0;\n\t"
+      "setp.ne.b32 q, %4, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %7, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(accumulate), "r"(issue), "n"(AOFF), "n"(BOFF), "n"(ID)
+      : "memory");
+}
+
+// Calls f(std::integral_constant<int, I>) for I = 0 .. N-1 (so that I can be a
+// template argument).
+template <int I, int N, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+  if constexpr (I < N) {
+    f(std::integral_constant<int, I>{});
+    static_for<I + 1, N>(f);
+  }
 }
 
 // Arrives once on the mbarrier when every tcgen05.mma issued so far by this

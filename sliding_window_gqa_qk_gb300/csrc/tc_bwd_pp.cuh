@@ -17,8 +17,8 @@
 //     with A = S^T, dP^T; B = dV; C = dK, dQ.
 // TMEM: S^T_0/dQ^T_0 [0,64), dP^T_0 [64,128), S^T_1/dQ^T_1 [128,192),
 // dP^T_1 [192,256), dV [256,384), dK [384,512).
-// Registers: the softmax warpgroups run with 208 per thread, warpgroup 2
-// (producer, MMA, two idle warps) with 88 (setmaxnreg; 384 x 168 at launch).
+// Registers: the softmax warpgroups run with 216 per thread, warpgroup 2
+// (producer, MMA, two idle warps) with 72 (setmaxnreg; 384 x 168 at launch).
 //
 // Softmax backward written out from the forward of the attention block
 // (autoresearch Administrator & Developer Guide §8.2.1; train.py
@@ -31,8 +31,8 @@ namespace swa {
 namespace tc {
 
 constexpr int kPPThreads = 384;
-constexpr int kPPRegsSoftmax = 208;
-constexpr int kPPRegsOther = 88;
+constexpr int kPPRegsSoftmax = 216;
+constexpr int kPPRegsOther = 72;
 static_assert(2 * 128 * kPPRegsSoftmax + 128 * kPPRegsOther <= kPPThreads * 168,
               "register split exceeds the launch's registers");
 
@@ -183,19 +183,19 @@ __global__ void __launch_bounds__(kPPThreads, 1)
         tc_fence_after();
         const uint64_t qd = sdesc_add(dQk0, st * C::kQ), gd = sdesc_add(dGk0, st * C::kQ);
         const uint32_t tS = tmem + X * 128;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t offA = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
-          const uint32_t offB = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-          umma_bf16_ss(tS, sdesc_add(dKk, offA), sdesc_add(qd, offB), idST, kk > 0);
-        }
+        static_for<0, D / 16>([&](auto kc) {
+          constexpr int kk = decltype(kc)::value;
+          constexpr uint32_t offA = ((kk >> 2) * (kBK * 128) + (kk & 3) * 32) >> 4;
+          constexpr uint32_t offB = ((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4;
+          umma_ss_imm<idST, offA, offB>(tS, dKk, qd, kk > 0, 1u);
+        });
         umma_commit(bar(QB_SFULL + X));
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t offA = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
-          const uint32_t offB = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-          umma_bf16_ss(tS + 64, sdesc_add(dVk, offA), sdesc_add(gd, offB), idST, kk > 0);
-        }
+        static_for<0, D / 16>([&](auto kc) {
+          constexpr int kk = decltype(kc)::value;
+          constexpr uint32_t offA = ((kk >> 2) * (kBK * 128) + (kk & 3) * 32) >> 4;
+          constexpr uint32_t offB = ((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4;
+          umma_ss_imm<idST, offA, offB>(tS + 64, dVk, gd, kk > 0, 1u);
+        });
         umma_commit(bar(QB_DPFULL + X));
         return true;
       };
@@ -204,10 +204,10 @@ __global__ void __launch_bounds__(kPPThreads, 1)
         if (!mbar_wait(bar(QB_PREADY + X), (i >> 1) & 1, ctl)) return false;
         tc_fence_after();
         const uint64_t pd = sdesc_add(dPk0, X * C::kPS), gd = sdesc_add(dGmn0, st * C::kQ);
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-          umma_bf16_ss(tmem + cDV, sdesc_add(pd, kk * 32), sdesc_add(gd, kk * 2048), idKV,
-                       (i > 0 || kk > 0));
+        static_for<0, BQ / 16>([&](auto kc) {
+          constexpr int kk = decltype(kc)::value;
+          umma_ss_imm<idKV, kk * 2, kk * 128>(tmem + cDV, pd, gd, (i > 0 || kk > 0), 1u);
+        });
         return true;
       };
       auto opC = [&](int i) -> bool {   // dK += dS^T Q; dQ^T = K^T dS^T
@@ -216,14 +216,14 @@ __global__ void __launch_bounds__(kPPThreads, 1)
         tc_fence_after();
         const uint64_t sd = sdesc_add(dPk0, X * C::kPS + kBK * BQ * 2);
         const uint64_t qd = sdesc_add(dQmn0, st * C::kQ), smn = sdesc_add(dSmn0, X * C::kPS);
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-          umma_bf16_ss(tmem + cDK, sdesc_add(sd, kk * 32), sdesc_add(qd, kk * 2048), idKV,
-                       (i > 0 || kk > 0));
-#pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          umma_bf16_ss(tmem + X * 128, sdesc_add(dKmn, kk * 2048), sdesc_add(smn, kk * 2048), idQ,
-                       kk > 0);
+        static_for<0, BQ / 16>([&](auto kc) {
+          constexpr int kk = decltype(kc)::value;
+          umma_ss_imm<idKV, kk * 2, kk * 128>(tmem + cDK, sd, qd, (i > 0 || kk > 0), 1u);
+        });
+        static_for<0, kBK / 16>([&](auto kc) {
+          constexpr int kk = decltype(kc)::value;
+          umma_ss_imm<idQ, kk * 128, kk * 128>(tmem + X * 128, dKmn, smn, kk > 0, 1u);
+        });
         umma_commit(bar(QB_DQFULL + X));
         umma_commit(bar(QB_QEMPTY + st));
         return true;

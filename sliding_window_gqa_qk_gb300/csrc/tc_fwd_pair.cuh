@@ -31,11 +31,11 @@ namespace tc {
 
 // 12 warps: softmax warpgroups 0 and 1, warpgroup 2 = producer (warp 8),
 // MMA issuer (warp 9) and two idle warps. The launch gives every thread 168
-// registers (384 x 168 = 64512); warpgroup 2 drops to 88 and the softmax
-// warpgroups rise to 208 (2 x 128 x 208 + 128 x 88 = 64512).
+// registers (384 x 168 = 64512); warpgroup 2 drops to 72 and the softmax
+// warpgroups rise to 216 (2 x 128 x 216 + 128 x 72 = 64512).
 constexpr int kPairThreads = 384;
-constexpr int kPairRegsSoftmax = 208;
-constexpr int kPairRegsOther = 88;
+constexpr int kPairRegsSoftmax = 216;
+constexpr int kPairRegsOther = 72;
 static_assert(2 * 128 * kPairRegsSoftmax + 128 * kPairRegsOther <= kPairThreads * 168,
               "register split exceeds the launch's registers");
 
@@ -170,20 +170,21 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       auto issue_s = [&](int X, int j) {
         const uint64_t qd = sdesc_add(dQ0, X * L::kTile), kd = sdesc_add(dK0, (j & 1) * L::kTile);
         const uint32_t dst = tmem + X * 128;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_bf16_ss_w(dst, sdesc_add(qd, off), sdesc_add(kd, off), idS, kk > 0 ? 1u : 0u, one);
-        }
+        static_for<0, D / 16>([&](auto kc) {
+          constexpr int kk = decltype(kc)::value;
+          constexpr uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          umma_ss_imm<idS, off, off>(dst, qd, kd, kk > 0 ? 1u : 0u, one);
+        });
         umma_commit_w(bar(PB_SFULL + X), one);
       };
       auto issue_pv = [&](int X, int j) {
         const uint64_t vd = sdesc_add(dV0, (j & 1) * L::kTile);
         const uint32_t dst = tmem + 256 + X * D, pa = tmem + X * 128;
-        umma_bf16_ts_w(dst, pa, vd, idO, j > 0 ? 1u : 0u, one);
-#pragma unroll
-        for (int kk = 1; kk < kBN / 16; ++kk)
-          umma_bf16_ts_w(dst, pa + kk * 8, sdesc_add(vd, kk * 2048), idO, 1u, one);
+        umma_ts_imm<idO, 0, 0>(dst, pa, vd, j > 0 ? 1u : 0u, one);
+        static_for<1, kBN / 16>([&](auto kc) {
+          constexpr int kk = decltype(kc)::value;
+          umma_ts_imm<idO, kk * 8, kk * 2048 / 16>(dst, pa, vd, 1u, one);
+        });
         umma_commit_w(bar(PB_PV + X), one);
       };
       bool ok = mbar_wait_warp(bar(PB_Q), 0, ctl) && mbar_wait_warp(bar(PB_KFULL), 0, ctl);

@@ -281,11 +281,20 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       reg_fence(sr[3]);
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) mask(sr[cc], cc);
-      float mx = -INFINITY;
+      // Row maximum: eight independent three-input chains, then a short tree.
+      float mq[8];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
+      for (int q = 0; q < 8; ++q) {
+        const int cc = q >> 1, e0 = (q & 1) * 16;
+        float a = fmax3(__uint_as_float(sr[cc][e0]), __uint_as_float(sr[cc][e0 + 1]),
+                        __uint_as_float(sr[cc][e0 + 2]));
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[cc][e]));
+        for (int e = 3; e < 15; e += 2)
+          a = fmax3(a, __uint_as_float(sr[cc][e0 + e]), __uint_as_float(sr[cc][e0 + e + 1]));
+        mq[q] = fmaxf(a, __uint_as_float(sr[cc][e0 + 15]));
+      }
+      const float mx = fmaxf(fmax3(mq[0], mq[1], mq[2]),
+                             fmax3(fmax3(mq[3], mq[4], mq[5]), mq[6], mq[7]));
       const float mt = mx * c;
       float alpha = 1.f;
       bool rescale_o = false;
@@ -309,22 +318,25 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           tmem_st32(tO + cc * 32, orr);
         }
       }
-      // P = exp2(S c - m) as bf16 pairs into S's first 64 columns.
-      const float mref = (m == -INFINITY) ? 0.f : m;
-      float lsum = 0.f;
+      // P = exp2(S c - m) as bf16 pairs into S's first 64 columns; the
+      // scale-and-shift and the row sum run two lanes per instruction.
+      const float nm = (m == -INFINITY) ? 0.f : -m;
+      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
         for (int w = 0; w < 32; ++w) {
           const int cc = half * 2 + (w >> 4), e = (w & 15) * 2;
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[cc][e]), c, -mref));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[cc][e + 1]), c, -mref));
-          lsum += p0 + p1;
+          float x0, x1;
+          ffma2(x0, x1, __uint_as_float(sr[cc][e]), __uint_as_float(sr[cc][e + 1]), c, c, nm, nm);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          fadd2_acc(ls[2 * (w & 3)], ls[2 * (w & 3) + 1], p0, p1);
           pk[w] = pack_bf16x2(p0, p1);
         }
         tmem_st32(tS + half * 32, pk);
       }
+      const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       l += lsum;
       tmem_wait_st();
       tc_fence_before();

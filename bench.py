@@ -326,7 +326,7 @@ def run_ours(args, rank, world, dev):
                    "peak_tflops": peak, "peak_source": f"{peak_kind} bf16_tflops_sustained",
                    "stage_ms_per_step": {k: round(v, 4) for k, v in stage_ms.items()},
                    "fwd_tflops": round(fwd_launch_tflops, 1)},
-        "roofline": {"kernel": "bwd_tc_pp_kernel (backward main, d=128; one launch per layer)",
+        "roofline": {"kernel": "bwd_tc128_kernel (backward main, d=128; one launch per layer)",
                      "bound": "tensor",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": NCU_TRAFFIC_BYTES,

@@ -226,6 +226,9 @@ struct PreArgs {  // backward preprocess: D = rowsum(dO * O), LSE2, clear dQ acc
   const elem_t* o; const elem_t* dO; const float* lse;
   float* dvec; float* lse2; float* dq_acc;
   int clear_acc;
+  // dvec = d_mul * D, lse2 = lse2_mul * LSE + lse2_add (the forms the
+  // attention backward kernels consume)
+  float d_mul, lse2_mul, lse2_add;
 };
 
 struct PostArgs {  // backward post: RMSNorm backward, dv, dVE, gain partials

@@ -171,6 +171,17 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+__device__ __forceinline__ void bulk_load_w(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                            uint32_t issue) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.ne.b32 q, %4, 0;\n\t"
+      "@q cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "r"(issue)
+      : "memory");
+}
+
 // Bulk tensor reduction shared -> global: element-wise fp32 add of a box
 // into the tensor (tracked by the issuing thread's bulk async-groups). Boxes
 // may extend past the tensor's end (those elements are skipped); the
@@ -508,6 +519,26 @@ __device__ __forceinline__ void fadd2_acc(float& d0, float& d1, float a0, float 
       : "+f"(d0), "+f"(d1)
       : "f"(a0), "f"(a1));
 }
+//   (d0, d1) = (a0 + b0, a1 + b1)
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+//   (d0, d1) = (a0 * b0, a1 * b1)
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
 //   (d0, d1) = (a0 * s, a1 * s)
 __device__ __forceinline__ void fmul2_s(float& d0, float& d1, float a0, float a1, float s) {
   asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
@@ -572,6 +603,11 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
 __device__ __forceinline__ uint32_t sw128_addr(uint32_t tile, int rows, int r, int chunk) {
   return tile + static_cast<uint32_t>(chunk >> 3) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 +
          static_cast<uint32_t>((chunk & 7) ^ (r & 7)) * 16;
+}
+
+// Fire-and-forget fp32 add into global memory (no return value).
+__device__ __forceinline__ void red_add_f32(float* gaddr, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(gaddr), "f"(a) : "memory");
 }
 
 __device__ __forceinline__ void red_add_v4_f32(float* gaddr, float a, float b, float c, float d) {

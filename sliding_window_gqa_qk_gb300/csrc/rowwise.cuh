@@ -141,8 +141,8 @@ __global__ void __launch_bounds__(kRowWarps * 32) bwd_pre_kernel(PreArgs a) {
     s = warp_sum(s);
     const long long prow = static_cast<long long>(bh) * a.Tpad + t;
     if (lane == 0) {
-      a.dvec[prow] = s;
-      a.lse2[prow] = a.lse[static_cast<long long>(bh) * a.T + t] * 1.4426950408889634f;
+      a.dvec[prow] = s * a.d_mul;
+      a.lse2[prow] = fmaf(a.lse[static_cast<long long>(bh) * a.T + t], a.lse2_mul, a.lse2_add);
     }
     if (a.clear_acc) {
       float z[NV];

@@ -18,7 +18,7 @@
 #include "tc_fwd.cuh"
 #include "tc_fwd_pair.cuh"
 #include "tc_bwd.cuh"
-#include "tc_bwd_pp.cuh"
+#include "tc_bwd128.cuh"
 #endif
 
 using namespace swa;
@@ -257,9 +257,11 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
 #if defined(SWA_ELEM_FP32)
   const bool copy_v = true;
   const int clear_acc = 0;
+  constexpr bool kFp32Build = true;
 #else
   const bool copy_v = false;
   const int clear_acc = 1;
+  constexpr bool kFp32Build = false;
 #endif
   if ((stages & SWA_BWD_STAGE_PRE) && !(flags & SWA_REUSE_PROLOGUE)) {
     if ((s = run_prologue(c, qe, ke, vin, gq, gk, vee, tok, ve_gate, copy_v)) != SWA_OK) return s;
@@ -271,6 +273,12 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
     a.dvec = at<float>(c, c.L.dvec); a.lse2 = at<float>(c, c.L.lse2);
     a.dq_acc = at<float>(c, c.L.dq_acc);
     a.clear_acc = clear_acc;
+    // The d = 128 tensor-core backward takes -D and log2(scale) - LSE log2(e)
+    // (its P carries the softmax scale); the others take D and LSE log2(e).
+    const bool scaled_p = !kFp32Build && P.d == 128;
+    a.d_mul = scaled_p ? -1.f : 1.f;
+    a.lse2_mul = scaled_p ? -1.4426950408889634f : 1.4426950408889634f;
+    a.lse2_add = scaled_p ? log2f(c.scale) : 0.f;
     dim3 grid((P.T + kRowsPerBlock - 1) / kRowsPerBlock, P.B * P.Hq);
     if (P.d == 64) bwd_pre_kernel<64><<<grid, kRowWarps * 32, 0, st>>>(a);
     else bwd_pre_kernel<128><<<grid, kRowWarps * 32, 0, st>>>(a);
@@ -326,7 +334,7 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
     b.gpart_k = at<float>(c, c.L.gpart_k);
     b.status = at<uint32_t>(c, c.L.status);
     b.wait_limit_ns = kWaitLimitNs;
-    if ((s = tc::launch_bwd_any(b, st)) != SWA_OK) return s;
+    if ((s = (P.d == 128 ? tc::launch_bwd128(b, st) : tc::launch_bwd(b, st))) != SWA_OK) return s;
 #endif
   }
   if (stages & SWA_BWD_STAGE_POST) {

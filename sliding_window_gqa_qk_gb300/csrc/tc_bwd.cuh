@@ -73,6 +73,8 @@ struct BwdLaunch {
 struct BwdParams {
   int T, Tpad, Hq, Hkv, window, causal, n_ktiles;
   float scale, scale_log2;
+  float dk_mul, dv_mul;   // factors applied to the dK and dV accumulators
+  float* dq_acc;          // fp32 [B, Hq, T, d] (kernels that add into it directly)
   const float* lse2;
   const float* dvec;
   const elem_t* k;
@@ -171,7 +173,7 @@ __device__ __forceinline__ void kv_epilogue(const BwdParams& prm, uint32_t tDK, 
       const int c = ch * 32 + e;
       pdot = fmaf(sg[wg * HD + c] * __uint_as_float(dkr[ch][e]), xval(c), pdot);
     }
-  pdot *= prm.scale * r;
+  pdot *= prm.dk_mul * r;
   sdot[wg * 128 + t] = pdot;
   named_bar_sync(3, 256);
   const float mean = (pdot + sdot[(1 - wg) * 128 + t]) / D;
@@ -182,8 +184,8 @@ __device__ __forceinline__ void kv_epilogue(const BwdParams& prm, uint32_t tDK, 
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
       const int c = ch * 32 + e;
-      const float dk0 = __uint_as_float(dkr[ch][e]) * prm.scale;
-      const float dk1 = __uint_as_float(dkr[ch][e + 1]) * prm.scale;
+      const float dk0 = __uint_as_float(dkr[ch][e]) * prm.dk_mul;
+      const float dk1 = __uint_as_float(dkr[ch][e + 1]) * prm.dk_mul;
       const float xh0 = xval(c) * r, xh1 = xval(c + 1) * r;
       pk[e / 2] = pack_bf16x2(r * (sg[wg * HD + c] * dk0 - xh0 * mean),
                               r * (sg[wg * HD + c + 1] * dk1 - xh1 * mean));
@@ -199,7 +201,9 @@ __device__ __forceinline__ void kv_epilogue(const BwdParams& prm, uint32_t tDK, 
   // dv and the VE-table gradient
   const int tok = (prm.dve != nullptr && valid) ? prm.tok[bt] : -1;
   const bool ve_ok = tok >= 0 && tok < prm.vocab;
-  const float vs = ve_ok ? prm.ve_scale * (prm.gate ? prm.gate[bt * prm.Hkv + hk] : 1.f) : 0.f;
+  const float vs =
+      ve_ok ? prm.dv_mul * prm.ve_scale * (prm.gate ? prm.gate[bt * prm.Hkv + hk] : 1.f) : 0.f;
+  const float dvm = prm.dv_mul;
   uint32_t dvr[NCH][32];
   if (have) {
 #pragma unroll
@@ -219,10 +223,10 @@ __device__ __forceinline__ void kv_epilogue(const BwdParams& prm, uint32_t tDK, 
 #pragma unroll
     for (int q = 0; q < 4; ++q)
       st_shared_v4(sw128_addr(sdv, kBK, t, (wg * HD + ch * 32) / 8 + q),
-                   pack_bf16x2(__uint_as_float(a[8 * q]), __uint_as_float(a[8 * q + 1])),
-                   pack_bf16x2(__uint_as_float(a[8 * q + 2]), __uint_as_float(a[8 * q + 3])),
-                   pack_bf16x2(__uint_as_float(a[8 * q + 4]), __uint_as_float(a[8 * q + 5])),
-                   pack_bf16x2(__uint_as_float(a[8 * q + 6]), __uint_as_float(a[8 * q + 7])));
+                   pack_bf16x2(__uint_as_float(a[8 * q]) * dvm, __uint_as_float(a[8 * q + 1]) * dvm),
+                   pack_bf16x2(__uint_as_float(a[8 * q + 2]) * dvm, __uint_as_float(a[8 * q + 3]) * dvm),
+                   pack_bf16x2(__uint_as_float(a[8 * q + 4]) * dvm, __uint_as_float(a[8 * q + 5]) * dvm),
+                   pack_bf16x2(__uint_as_float(a[8 * q + 6]) * dvm, __uint_as_float(a[8 * q + 7]) * dvm));
     if (ve_ok) {
       float* dst = prm.dve + static_cast<long long>(tok) * prm.Hkv * D + hk * D + wg * HD + ch * 32;
 #pragma unroll
@@ -683,6 +687,7 @@ inline swa_status launch_bwd_d(const BwdLaunch& f, cudaStream_t st) {
   p.scale = f.scale;
   p.scale_log2 = f.scale * 1.4426950408889634f;
   p.lse2 = f.lse2; p.dvec = f.dvec;
+  p.dk_mul = f.scale; p.dv_mul = 1.f;
   p.k = f.k; p.rstd_k = f.rstd_k; p.gk = f.gk; p.tok = f.tok; p.gate = f.gate; p.dve = f.dve;
   p.ve_scale = f.ve_scale; p.vocab = f.vocab; p.dk = f.dk; p.dv = f.dv; p.gpart_k = f.gpart_k;
   p.status = f.status; p.wait_limit_ns = f.wait_limit_ns;

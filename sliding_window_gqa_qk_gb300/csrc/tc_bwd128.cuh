@@ -1,0 +1,573 @@
+// Backward attention core for d = 128 with 128-query steps (sm_103a).
+//
+// One CTA per 128-key tile of a (batch, kv head): K and V stay in shared
+// memory, dK and dV accumulate in TMEM over the GQA group and the in-band
+// 128-row query tiles, so the GQA reduction of dK and dV happens inside the
+// CTA. Every product of a step is a full M = 128, N = 128 tcgen05 MMA:
+//   S^T  = K Q_i^T            (TMEM [0,128): lanes = keys, columns = queries)
+//   dP^T = V dO_i^T           (TMEM [128,256))
+//   P^T  = scale exp2(S^T c - LSE log2 e)     -> bf16 into S^T's columns
+//   dS^T = P^T (dP^T - D)                     -> bf16 into dP^T's columns,
+//                                                and to shared memory
+//   dV  += P^T dO_i           (A operand from TMEM)
+//   dK  += dS^T Q_i           (A operand from TMEM)
+//   dQ_i^T = K^T dS^T         (into dP^T's columns once dK has read dS^T)
+// P^T and dS^T carry the softmax scale, so dK and dQ come out final and dV
+// is divided by it in the epilogue.
+//
+// Roles (12 warps): warpgroups 0 and 1 do the element-wise work, each on 64
+// of the step's 128 query columns (thread = key row = TMEM lane); warp 8 is
+// the TMA producer (K, V once; Q with LSE and D, and dO per step, two stages
+// each) and also issues the bulk reductions of the staged dQ boxes, so that
+// it can reload a Q stage as soon as they have been read; warp 9 issues the
+// MMAs from one thread, in the order
+//   S(0) dP(0) | dV(i) S(i+1) [dK(i) dQ(i)] dP(i+1) | ...
+// while the warpgroups run dS(i), P(i+1), drain(i): S^T(i+1) lands while
+// they compute dS^T(i), their exponentials of step i+1 overlap dK(i) and
+// dQ^T(i), and dP^T(i+1) waits only for the drain of dQ^T(i) from TMEM.
+// dQ^T(i) goes from TMEM to shared memory in two [32 queries][128] fp32
+// boxes per warpgroup, one in half of the step's Q stage (free once the dK
+// product has read it) and one in half of its dO stage (free once the dV
+// product has read it), and from there into the fp32 dQ accumulator by TMA
+// bulk reductions. Those reductions run at the rate the L2 accepts fp32
+// adds (about 6.6 TB/s over the whole GPU, about 21 bytes per clock per
+// SM), 64 KB per step: no element-wise work waits for them, only the
+// reloading of the two stages two steps later.
+// Registers: the element-wise warpgroups run with 216 per thread, warpgroup
+// 2 with 72 (setmaxnreg; 384 x 168 at launch).
+//
+// Softmax backward written out from the forward of the attention block
+// (autoresearch Administrator & Developer Guide §8.2.1; train.py
+// walkthrough post, model paragraph).
+#pragma once
+
+#include "tc_bwd.cuh"
+
+namespace swa {
+namespace tc {
+
+constexpr int kB2Threads = 384;
+constexpr int kB2RegsSoftmax = 216;
+constexpr int kB2RegsOther = 72;
+// Issue S^T(i+1) right after dV(i) (true) or after dK(i), dQ^T(i) (false);
+// the element-wise warpgroups follow the same order.
+constexpr bool kB2EarlyS = false;
+// Stage the first dQ box of each warpgroup in the step's Q stage (true; the Q
+// stage is reloaded once it has been read) or in the dS^T buffer (false; the
+// next dS^T waits until it has been read).
+constexpr bool kB2StageInQ = true;
+static_assert(2 * 128 * kB2RegsSoftmax + 128 * kB2RegsOther <= kB2Threads * 168,
+              "register split exceeds the launch's registers");
+
+struct B2Cfg {
+  static constexpr int D = 128;
+  static constexpr int BQ = 128;                 // queries per step
+  static constexpr int kTile = 128 * 128 * 2;    // 32 KB: K, V, a Q or dO stage, dS^T
+  static constexpr int kHalf = kTile / 2;        // a 64-column half (one SW128 region)
+  static constexpr int oK = 0;
+  static constexpr int oV = oK + kTile;
+  static constexpr int oQ = oV + kTile;          // 2 stages
+  static constexpr int oG = oQ + 2 * kTile;      // dO, 2 stages
+  static constexpr int oS = oG + 2 * kTile;      // dS^T [128 keys][128 queries]
+  static constexpr int oL = oS + kTile;          // 2 stages x BQ floats: log2(scale) - LSE log2(e)
+  static constexpr int oD = oL + 2 * BQ * 4;     // 2 stages x BQ floats: -D
+  static constexpr int oBar = oD + 2 * BQ * 4;   // mbarriers, TMEM base, abort flag
+  static constexpr int kBytes = oBar + 256;
+  // The whole budget is dynamic shared memory (no static shared variables),
+  // so the dynamic base is the start of the CTA's window (1024-aligned).
+  static_assert(kBytes <= 232448, "shared memory budget");
+};
+
+enum {
+  B2_KV = 0,
+  B2_QFULL = 1,      // +stage: Q, LSE, D of a step landed
+  B2_QEMPTY = 3,     // +stage: the dK product of the step completed (Q stage reusable)
+  B2_GFULL = 5,      // +stage: dO landed
+  B2_GFREE = 7,      // +stage: the dO-stage dQ boxes of the step were read (dO stage reusable)
+  B2_SFULL = 9,      // S^T in TMEM
+  B2_DPFULL = 10,    // dP^T in TMEM
+  B2_PREADY = 11,    // P^T in TMEM (8 warps)
+  B2_DSREADY = 12,   // dS^T in TMEM and shared memory (8 warps)
+  B2_DQFULL = 13,    // dQ^T in TMEM
+  B2_DQFREE = 14,    // dQ^T read out of TMEM (8 warps)
+  B2_STAGED = 15,    // the step's four dQ boxes are in shared memory (8 warps)
+  B2_DSFREE = 16,    // the dQ boxes staged in the dS^T buffer were read
+  B2_DQREAD = 17,    // every dQ box of the CTA was read (once, at the end)
+  B2_FINAL = 18,
+  B2_COUNT = 19
+};
+
+// Visible query columns [clo, chi] of key row j among the 64 queries
+// starting at qb, on a tile that is not entirely inside the band.
+__device__ __forceinline__ void key_row_span(const Band& band, int j, int qb, int& clo, int& chi) {
+  clo = 0;
+  chi = 63;
+  if (j >= band.T) {
+    clo = 1;
+    chi = 0;
+    return;
+  }
+  if (band.T - 1 - qb < chi) chi = band.T - 1 - qb;
+  if (band.causal) {
+    if (j - qb > clo) clo = j - qb;
+    if (band.window >= 0 && j + band.window - qb < chi) chi = j + band.window - qb;
+  } else if (band.window >= 0) {
+    if (j - band.window - qb > clo) clo = j - band.window - qb;
+    if (j + band.window - qb < chi) chi = j + band.window - qb;
+  }
+}
+
+// 64 fp32 values (two 32-column TMEM loads) -> 32 bf16 pairs of consecutive
+// columns.
+__device__ __forceinline__ void pack64(const uint32_t (&v)[2][32], uint32_t (&pk)[32]) {
+#pragma unroll
+  for (int w = 0; w < 32; ++w)
+    pk[w] = pack_bf16x2(__uint_as_float(v[w >> 4][(w & 15) * 2]),
+                        __uint_as_float(v[w >> 4][(w & 15) * 2 + 1]));
+}
+
+__global__ void __launch_bounds__(kB2Threads, 1)
+    bwd_tc128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                     const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmDK,
+                     const __grid_constant__ CUtensorMap tmDV, const BwdParams prm) {
+  using C = B2Cfg;
+  constexpr int D = C::D, BQ = C::BQ;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {   // swizzle atoms need 1024-byte aligned tiles (uniform over the CTA)
+    if (threadIdx.x == 0) atomicOr(prm.status, DEV_ERR_BOUNDS);
+    return;
+  }
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(smem + C::oBar + B2_COUNT * 8);
+  uint32_t* abort_flag = tmem_base_sh + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kt = static_cast<int>(blockIdx.x);        // key tiles of one (b, kv head) run together
+  const int bhk = static_cast<int>(blockIdx.y);
+  const int b = bhk / prm.Hkv, hk = bhk % prm.Hkv;
+  const int k0 = kt * kBK;
+  const int G = prm.Hq / prm.Hkv;
+  const Band band{prm.T, prm.window, prm.causal};
+  int qlo = 0, qhi = -1;
+  q_tile_range(band, k0, kBK, BQ, qlo, qhi);
+  const int nq = qhi - qlo + 1;
+  const int n_it = nq > 0 ? nq * G : 0;
+  const WaitCtl ctl{abort_flag, prm.status, prm.wait_limit_ns};
+  auto bar = [&](int i) { return sbase + C::oBar + 8u * static_cast<uint32_t>(i); };
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(B2_KV), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B2_QFULL + s), 1);
+      mbar_init(bar(B2_QEMPTY + s), 1);
+      mbar_init(bar(B2_GFULL + s), 1);
+      mbar_init(bar(B2_GFREE + s), 1);
+    }
+    mbar_init(bar(B2_SFULL), 1);
+    mbar_init(bar(B2_DPFULL), 1);
+    mbar_init(bar(B2_PREADY), 8);
+    mbar_init(bar(B2_DSREADY), 8);
+    mbar_init(bar(B2_DQFULL), 1);
+    mbar_init(bar(B2_DQFREE), 8);
+    mbar_init(bar(B2_STAGED), 8);
+    mbar_init(bar(B2_DSFREE), 1);
+    mbar_init(bar(B2_DQREAD), 1);
+    mbar_init(bar(B2_FINAL), 1);
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_base_sh), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_sh;
+  constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 384;
+
+  if (warp >= 8) {
+    setmaxnreg_dec<kB2RegsOther>();
+    if (warp == 8 && lane == 0 && n_it > 0) {
+      // ---------------- TMA producer of K, V, and per step Q, LSE, D ----------------
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(bar(B2_KV), 2 * C::kTile);
+      for (int c = 0; c < 2; ++c) {
+        tma_load_4d(sbase + C::oK + c * C::kHalf, &tmK, bar(B2_KV), 64 * c, k0, hk, b);
+        tma_load_4d(sbase + C::oV + c * C::kHalf, &tmV, bar(B2_KV), 64 * c, k0, hk, b);
+      }
+      int last[2] = {-1, -1};
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it & 1;
+        const int h = hk * G + it / nq;
+        const int q0 = (qlo + it % nq) * BQ;
+        // the stage is free once the dK product two steps back completed (and,
+        // with dQ boxes staged in it, once those were read)
+        if (it >= 2 && !mbar_wait(bar(B2_QEMPTY + s), ((it >> 1) - 1) & 1, ctl)) break;
+        last[s] = it;
+        mbar_arrive_expect_tx(bar(B2_QFULL + s), C::kTile + 2 * BQ * 4);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(sbase + C::oQ + s * C::kTile + c * C::kHalf, &tmQ, bar(B2_QFULL + s), 64 * c,
+                      q0, h, b);
+        const long long row = (static_cast<long long>(b) * prm.Hq + h) * prm.Tpad + q0;
+        bulk_load(sbase + C::oL + s * BQ * 4, prm.lse2 + row, BQ * 4, bar(B2_QFULL + s));
+        bulk_load(sbase + C::oD + s * BQ * 4, prm.dvec + row, BQ * 4, bar(B2_QFULL + s));
+      }
+      mbar_wait_drain(bar(B2_KV), 0, prm.wait_limit_ns);
+      for (int s = 0; s < 2; ++s)
+        if (last[s] >= 0) mbar_wait_drain(bar(B2_QFULL + s), (last[s] >> 1) & 1, prm.wait_limit_ns);
+    } else if (warp == 11 && lane == 0 && n_it > 0) {
+      // ---------------- TMA producer of dO ----------------
+      tma_prefetch_desc(&tmG);
+      int last[2] = {-1, -1};
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it & 1;
+        const int h = hk * G + it / nq;
+        const int q0 = (qlo + it % nq) * BQ;
+        // the stage held dQ boxes of step it - 2: free once they were read
+        if (it >= 2 && !mbar_wait(bar(B2_GFREE + s), ((it >> 1) - 1) & 1, ctl)) break;
+        last[s] = it;
+        mbar_arrive_expect_tx(bar(B2_GFULL + s), C::kTile);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(sbase + C::oG + s * C::kTile + c * C::kHalf, &tmG, bar(B2_GFULL + s), 64 * c,
+                      q0, h, b);
+      }
+      for (int s = 0; s < 2; ++s)
+        if (last[s] >= 0) mbar_wait_drain(bar(B2_GFULL + s), (last[s] >> 1) & 1, prm.wait_limit_ns);
+    } else if (warp == 10 && lane == 0 && n_it > 0) {
+      // ---------------- dQ reducer ----------------
+      // Step m's dQ boxes, for each warpgroup X: queries qb.. in half X of the
+      // dS^T buffer, qb+32.. in half X of the step's dO stage, added into the
+      // fp32 accumulator by bulk reductions. These run at the rate the L2
+      // accepts fp32 adds (about 6.6 TB/s over the whole GPU, about 21 bytes
+      // per clock per SM, so about 3000 clocks per step); the buffers are
+      // handed back as soon as their boxes have been read.
+      tma_prefetch_desc(&tmDQ);
+      for (int m = 0; m < n_it; ++m) {
+        if (!mbar_wait(bar(B2_STAGED), m & 1, ctl)) break;
+        const int h = hk * G + m / nq;
+        const int q0 = (qlo + m % nq) * BQ;
+        const uint32_t boxA = kB2StageInQ ? sbase + C::oQ + (m & 1) * C::kTile : sbase + C::oS;
+        for (int X = 0; X < 2; ++X)
+          tma_reduce_add_3d(&tmDQ, boxA + X * C::kHalf, 0, q0 + 64 * X, b * prm.Hq + h);
+        bulk_commit_group();
+        for (int X = 0; X < 2; ++X)
+          tma_reduce_add_3d(&tmDQ, sbase + C::oG + (m & 1) * C::kTile + X * C::kHalf, 0,
+                            q0 + 64 * X + 32, b * prm.Hq + h);
+        bulk_commit_group();
+        bulk_wait_group_read<1>();
+        mbar_arrive(bar(kB2StageInQ ? B2_QEMPTY + (m & 1) : B2_DSFREE));
+        bulk_wait_group_read<0>();
+        mbar_arrive(bar(B2_GFREE + (m & 1)));
+      }
+      bulk_wait_group_all();
+      mbar_arrive(bar(B2_DQREAD));
+    } else if (warp == 9 && lane == 0 && n_it > 0) {
+      // ---------------- MMA issuer (one thread) ----------------
+      constexpr uint32_t idN = idesc_bf16_f32(128, 128, 0, 0);    // S^T, dP^T
+      constexpr uint32_t idKV = idesc_bf16_f32(128, 128, 0, 1);   // dV, dK (A from TMEM)
+      constexpr uint32_t idQ = idesc_bf16_f32(128, 128, 1, 1);    // dQ^T = K^T dS^T
+      const uint64_t dKk = sdesc_sw128(sbase + C::oK, 16, 1024);
+      const uint64_t dVk = sdesc_sw128(sbase + C::oV, 16, 1024);
+      const uint64_t dKmn = sdesc_sw128(sbase + C::oK, C::kHalf, 1024);
+      const uint64_t dQk0 = sdesc_sw128(sbase + C::oQ, 16, 1024);
+      const uint64_t dGk0 = sdesc_sw128(sbase + C::oG, 16, 1024);
+      const uint64_t dQmn0 = sdesc_sw128(sbase + C::oQ, C::kHalf, 1024);
+      const uint64_t dGmn0 = sdesc_sw128(sbase + C::oG, C::kHalf, 1024);
+      const uint64_t dSmn = sdesc_sw128(sbase + C::oS, C::kHalf, 1024);
+      // K-major operands: K step kk is 32 bytes into a row of its 64-column region.
+      auto issue_S = [&](int i) {    // S^T = K Q_i^T
+        const uint64_t qd = sdesc_add(dQk0, (i & 1) * C::kTile);
+        static_for<0, 8>([&](auto kc) {
+          constexpr int kk = decltype(kc)::value;
+          constexpr uint32_t off = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;
+          umma_ss_imm<idN, off, off>(tmem + cS, dKk, qd, kk > 0, 1u);
+        });
+        umma_commit(bar(B2_SFULL));
+      };
+      auto issue_dP = [&](int i) {   // dP^T = V dO_i^T
+        const uint64_t gd = sdesc_add(dGk0, (i & 1) * C::kTile);
+        static_for<0, 8>([&](auto kc) {
+          constexpr int kk = decltype(kc)::value;
+          constexpr uint32_t off = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;
+          umma_ss_imm<idN, off, off>(tmem + cDP, dVk, gd, kk > 0, 1u);
+        });
+        umma_commit(bar(B2_DPFULL));
+      };
+      // A operands from TMEM: K step kk (16 queries) is 8 columns; queries
+      // 0-63 sit in the first 32 columns of warpgroup 0's 64, queries 64-127
+      // in warpgroup 1's. MN-major B: K step kk is 16 rows (2048 bytes) on.
+      auto issue_dV = [&](int i) {   // dV += P^T dO_i
+        const uint64_t gd = sdesc_add(dGmn0, (i & 1) * C::kTile);
+        static_for<0, 8>([&](auto kc) {
+          constexpr int kk = decltype(kc)::value;
+          umma_ts_imm<idKV, (kk >> 2) * 64 + (kk & 3) * 8, kk * 128>(tmem + cDV, tmem + cS, gd,
+                                                                      (i > 0 || kk > 0), 1u);
+        });
+      };
+      auto issue_dKdQ = [&](int i) {   // dK += dS^T Q_i; dQ_i^T = K^T dS^T
+        const uint64_t qd = sdesc_add(dQmn0, (i & 1) * C::kTile);
+        static_for<0, 8>([&](auto kc) {
+          constexpr int kk = decltype(kc)::value;
+          umma_ts_imm<idKV, (kk >> 2) * 64 + (kk & 3) * 8, kk * 128>(tmem + cDK, tmem + cDP, qd,
+                                                                      (i > 0 || kk > 0), 1u);
+        });
+        if (!kB2StageInQ) umma_commit(bar(B2_QEMPTY + (i & 1)));
+        static_for<0, 8>([&](auto kc) {
+          constexpr int kk = decltype(kc)::value;
+          umma_ss_imm<idQ, kk * 128, kk * 128>(tmem + cDP, dKmn, dSmn, kk > 0, 1u);
+        });
+        umma_commit(bar(B2_DQFULL));
+      };
+      bool ok = mbar_wait(bar(B2_KV), 0, ctl) && mbar_wait(bar(B2_QFULL), 0, ctl);
+      if (ok) {
+        tc_fence_after();
+        issue_S(0);
+      }
+      ok = ok && mbar_wait(bar(B2_GFULL), 0, ctl);
+      if (ok) {
+        tc_fence_after();
+        issue_dP(0);
+      }
+      for (int i = 0; i < n_it && ok; ++i) {
+        const int ph = i & 1;
+        const bool more = i + 1 < n_it;
+        const int s1 = (i + 1) & 1, ph1 = ((i + 1) >> 1) & 1;
+        if (!(ok = mbar_wait(bar(B2_PREADY), ph, ctl))) break;
+        tc_fence_after();
+        issue_dV(i);
+        if (kB2EarlyS && more) {
+          // S^T(i+1) overwrites P^T(i), which dV(i) (issued before) reads.
+          if (!(ok = mbar_wait(bar(B2_QFULL + s1), ph1, ctl))) break;
+          tc_fence_after();
+          issue_S(i + 1);
+        }
+        if (!(ok = mbar_wait(bar(B2_DSREADY), ph, ctl))) break;
+        tc_fence_after();
+        issue_dKdQ(i);
+        if (!kB2EarlyS && more) {
+          if (!(ok = mbar_wait(bar(B2_QFULL + s1), ph1, ctl))) break;
+          tc_fence_after();
+          issue_S(i + 1);
+        }
+        if (more) {
+          // dP^T(i+1) overwrites dQ^T(i): wait until it was read out.
+          if (!(ok = mbar_wait(bar(B2_DQFREE), ph, ctl) && mbar_wait(bar(B2_GFULL + s1), ph1, ctl)))
+            break;
+          tc_fence_after();
+          issue_dP(i + 1);
+        }
+      }
+      umma_commit(bar(B2_FINAL));
+      mbar_wait_drain(bar(B2_FINAL), 0, prm.wait_limit_ns);
+    }
+  } else {
+    // --------- element-wise warpgroups: X = warp / 4 owns query columns [64X, 64X + 64) ---------
+    setmaxnreg_inc<kB2RegsSoftmax>();
+    const int X = warp >> 2;
+    const int t = threadIdx.x & 127;                // key row / TMEM lane (head-dim row of dQ^T)
+    const int j = k0 + t;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float c = prm.scale_log2;
+    const uint32_t tS = tmem + cS + 64 * X + lane_off;     // S^T, then P^T in its first 32 columns
+    const uint32_t tDP = tmem + cDP + 64 * X + lane_off;   // dP^T, then dS^T, then dQ^T
+    const uint32_t sSx = sbase + C::oS + X * C::kHalf;     // dS^T region X
+    // Per step the order is dS(i), P(i+1), drain(i) (kB2EarlyS): the
+    // exponentials of the next step run while the tensor core computes dK(i)
+    // and dQ^T(i); otherwise P(i), dS(i), drain(i).
+    uint32_t sr[2][32];   // P^T of the step whose dS^T comes next (fp32)
+    // ---- P^T(i) = scale exp2(S^T c - LSE log2 e), zero off the band ----
+    auto p_phase = [&](int i) -> bool {
+      const int s = i & 1;
+      const int q0 = (qlo + i % nq) * BQ;
+      const int qb = q0 + 64 * X;
+      const float4* L4 = reinterpret_cast<const float4*>(smem + C::oL + s * BQ * 4 + X * 256);
+      if (!(mbar_wait_warp(bar(B2_QFULL + s), (i >> 1) & 1, ctl) &&
+            mbar_wait_warp(bar(B2_SFULL), i & 1, ctl)))
+        return false;
+      tc_fence_after();
+      tmem_ld32(tS, sr[0]);
+      tmem_ld32(tS + 32, sr[1]);
+      tmem_wait_ld(sr[0]);
+      reg_fence(sr[1]);
+#pragma unroll
+      for (int k4 = 0; k4 < 16; ++k4) {
+        const float4 lv = L4[k4];
+        const int cc = k4 >> 3, e = (k4 & 7) * 4;
+        float x0, x1, x2, x3;
+        ffma2(x0, x1, __uint_as_float(sr[cc][e]), __uint_as_float(sr[cc][e + 1]), c, c, lv.x, lv.y);
+        ffma2(x2, x3, __uint_as_float(sr[cc][e + 2]), __uint_as_float(sr[cc][e + 3]), c, c, lv.z, lv.w);
+        sr[cc][e] = __float_as_uint(ex2_approx(x0));
+        sr[cc][e + 1] = __float_as_uint(ex2_approx(x1));
+        sr[cc][e + 2] = __float_as_uint(ex2_approx(x2));
+        sr[cc][e + 3] = __float_as_uint(ex2_approx(x3));
+      }
+      if (!tile_full(band, q0, BQ, k0, kBK)) {
+        int clo, chi;
+        key_row_span(band, j, qb, clo, chi);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int col = cc * 32 + e;
+            if (col < clo || col > chi) sr[cc][e] = 0u;
+          }
+      }
+      uint32_t pk[32];
+      pack64(sr, pk);
+      tmem_st32(tS, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B2_PREADY));
+      return true;
+    };
+    // ---- dS^T(i) = P^T (dP^T - D) with the scaled P^T ----
+    auto ds_phase = [&](int i) -> bool {
+      const float4* D4 = reinterpret_cast<const float4*>(smem + C::oD + (i & 1) * BQ * 4 + X * 256);
+      if (!mbar_wait_warp(bar(B2_DPFULL), i & 1, ctl)) return false;
+      tc_fence_after();
+      uint32_t dp[2][32];
+      tmem_ld32(tDP, dp[0]);
+      tmem_ld32(tDP + 32, dp[1]);
+      tmem_wait_ld(dp[0]);
+      reg_fence(dp[1]);
+#pragma unroll
+      for (int k4 = 0; k4 < 16; ++k4) {
+        const float4 dv = D4[k4];
+        const int cc = k4 >> 3, e = (k4 & 7) * 4;
+        float x0, x1, x2, x3;
+        fadd2(x0, x1, __uint_as_float(dp[cc][e]), __uint_as_float(dp[cc][e + 1]), dv.x, dv.y);
+        fadd2(x2, x3, __uint_as_float(dp[cc][e + 2]), __uint_as_float(dp[cc][e + 3]), dv.z, dv.w);
+        fmul2(x0, x1, x0, x1, __uint_as_float(sr[cc][e]), __uint_as_float(sr[cc][e + 1]));
+        fmul2(x2, x3, x2, x3, __uint_as_float(sr[cc][e + 2]), __uint_as_float(sr[cc][e + 3]));
+        dp[cc][e] = __float_as_uint(x0);
+        dp[cc][e + 1] = __float_as_uint(x1);
+        dp[cc][e + 2] = __float_as_uint(x2);
+        dp[cc][e + 3] = __float_as_uint(x3);
+      }
+      uint32_t pk[32];
+      pack64(dp, pk);
+      tmem_st32(tDP, pk);   // A operand of dK
+      // MN-major B operand of dQ^T, in this warpgroup's half of the dS^T
+      // buffer, once the dQ box of step i - 1 staged there has been read
+      if (!kB2StageInQ && i > 0 && !mbar_wait_warp(bar(B2_DSFREE), (i - 1) & 1, ctl)) return false;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        st_sw128_chunk(sSx, kBK, t, ch, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+      tmem_wait_st();
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B2_DSREADY));
+      return true;
+    };
+    // ---- dQ^T(i) (lane = head-dim index, 64 query columns) -> staged boxes ----
+    auto drain = [&](int i) -> bool {
+      const int s = i & 1;
+      if (!mbar_wait_warp(bar(B2_DQFULL), i & 1, ctl)) return false;
+      tc_fence_after();
+      uint32_t dq[2][32];
+      tmem_ld32(tDP, dq[0]);
+      tmem_ld32(tDP + 32, dq[1]);
+      tmem_wait_ld(dq[0]);
+      reg_fence(dq[1]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B2_DQFREE));
+      // boxes [32 queries][128] fp32: queries qb.. in this warpgroup's half of
+      // the dS^T buffer (last read by dQ^T(i)), qb+32.. in half X of the dO
+      // stage (last read by dV(i)); both products completed before DQFULL
+      const uint32_t box0 = kB2StageInQ ? sbase + C::oQ + s * C::kTile + X * C::kHalf : sSx;
+      const uint32_t box1 = sbase + C::oG + s * C::kTile + X * C::kHalf;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) st_shared_f32(box0 + e * 512 + t * 4, __uint_as_float(dq[0][e]));
+#pragma unroll
+      for (int e = 0; e < 32; ++e) st_shared_f32(box1 + e * 512 + t * 4, __uint_as_float(dq[1][e]));
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B2_STAGED));   // the producer reduces them
+      return true;
+    };
+    bool ok = n_it > 0;
+    if (kB2EarlyS) {
+      ok = ok && p_phase(0);
+      for (int i = 0; i < n_it && ok; ++i) {
+        ok = ds_phase(i);
+        if (ok && i + 1 < n_it) ok = p_phase(i + 1);
+        ok = ok && drain(i);
+      }
+    } else {
+      for (int i = 0; i < n_it && ok; ++i) ok = p_phase(i) && ds_phase(i) && drain(i);
+    }
+    // All dQ boxes are read before the epilogue reuses the stage buffers as
+    // scratch.
+    const bool final_ok = ok && n_it > 0 && mbar_wait_warp(bar(B2_DQREAD), 0, ctl) &&
+                          mbar_wait_warp(bar(B2_FINAL), 0, ctl);
+    tc_fence_after();
+    float* scratch = reinterpret_cast<float*>(smem + C::oQ);
+    const uint32_t sdk = sbase + C::oQ + 4096, sdv = sdk + kBK * D * 2;
+    kv_epilogue<D>(prm, tmem + cDK + lane_off + X * 64, tmem + cDV + lane_off + X * 64, final_ok, X,
+                   t, b, hk, kt, scratch, scratch + 256, sdk, sdv, &tmDK, &tmDV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// fp32 tensor map of the dQ accumulator [B*Hq][T][128] with boxes of `rows`
+// query rows x 128 columns (no swizzle) for bulk reductions.
+inline bool map_dq_acc_rows(CUtensorMap* m, float* base, int BH, int T, int rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {128 * 4, static_cast<cuuint64_t>(T) * 128 * 4};
+  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(rows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline swa_status launch_bwd128(const BwdLaunch& f, cudaStream_t st) {
+  using C = B2Cfg;
+  CUtensorMap mq, mk, mv, mg, mdq, mdk, mdv;
+  if (!map_token_major(&mdk, f.dk, f.B, f.Hkv, f.T, 128) ||
+      !map_token_major(&mdv, f.dv, f.B, f.Hkv, f.T, 128) ||
+      !map_head_major(&mq, f.qn, f.B, f.Hq, f.T, 128) ||
+      !map_token_major(&mg, f.dO, f.B, f.Hq, f.T, 128) ||
+      !map_head_major(&mk, f.kn, f.B, f.Hkv, f.T, 128) ||
+      !map_dq_acc_rows(&mdq, f.dq_acc, f.B * f.Hq, f.T, 32))
+    return SWA_ERR_CUDA;
+  const bool okv = f.v_head_major ? map_head_major(&mv, f.v, f.B, f.Hkv, f.T, 128)
+                                  : map_token_major(&mv, f.v, f.B, f.Hkv, f.T, 128);
+  if (!okv) return SWA_ERR_CUDA;
+  BwdParams p{};
+  p.T = f.T; p.Tpad = f.Tpad; p.Hq = f.Hq; p.Hkv = f.Hkv; p.window = f.window; p.causal = f.causal;
+  p.n_ktiles = (f.T + kBK - 1) / kBK;
+  p.scale = f.scale;
+  p.scale_log2 = f.scale * 1.4426950408889634f;
+  p.lse2 = f.lse2; p.dvec = f.dvec;
+  // P^T and dS^T carry the softmax scale: dK and dQ come out final, dV is
+  // divided by it in the epilogue.
+  p.dk_mul = 1.f; p.dv_mul = 1.f / f.scale;
+  p.dq_acc = f.dq_acc;
+  p.k = f.k; p.rstd_k = f.rstd_k; p.gk = f.gk; p.tok = f.tok; p.gate = f.gate; p.dve = f.dve;
+  p.ve_scale = f.ve_scale; p.vocab = f.vocab; p.dk = f.dk; p.dv = f.dv; p.gpart_k = f.gpart_k;
+  p.status = f.status; p.wait_limit_ns = f.wait_limit_ns;
+  if (cudaFuncSetAttribute(bwd_tc128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kBytes) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  dim3 grid(p.n_ktiles, f.B * f.Hkv);
+  bwd_tc128_kernel<<<grid, kB2Threads, C::kBytes, st>>>(mq, mk, mv, mg, mdq, mdk, mdv, p);
+  return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
+}  // namespace tc
+}  // namespace swa

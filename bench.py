@@ -47,7 +47,9 @@ WORKLOAD = "8-layer SSSL stack (B=16, T=2048, Hq=6, Hkv=3, d=128, W=1024 on S la
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
 # kernel, from the ncu capture summarised in profiles/ (None until captured
 # for the current kernel).
-NCU_TRAFFIC_BYTES = None
+# DRAM bytes (read + write) per launch of bwd_tc128_kernel from one ncu capture:
+# the mean over the stack's 6 S-layer and 2 L-layer launches.
+NCU_TRAFFIC_BYTES = 388_820_000
 
 
 def layer_schedule(window_fn, ve_fn):

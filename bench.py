@@ -44,11 +44,10 @@ VOCAB, VE_SCALE = 8192, 0.5
 METRIC = "masked TFLOP/s fwd+bwd, T=2048 SSSL layers; % of GB300 bf16 tensor-core peak"
 WORKLOAD = "8-layer SSSL stack (B=16, T=2048, Hq=6, Hkv=3, d=128, W=1024 on S layers, VE on odd layers)"
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
-# kernel, from the ncu capture summarised in profiles/ (None until captured
-# for the current kernel).
-# DRAM bytes (read + write) per launch of bwd_tc128_kernel from one ncu capture:
-# the mean over the stack's 6 S-layer and 2 L-layer launches.
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
+# kernel (bwd_tc128_kernel) from one ncu capture, summarised in profiles/:
+# the mean over the stack's 6 S-layer and 2 L-layer launches (None whenever
+# the kernel has changed since the capture).
 NCU_TRAFFIC_BYTES = 388_820_000
 
 

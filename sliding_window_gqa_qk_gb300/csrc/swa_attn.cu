@@ -17,6 +17,7 @@
 #else
 #include "tc_fwd.cuh"
 #include "tc_fwd_pair.cuh"
+#include "tc_fwd_persist.cuh"
 #include "tc_bwd.cuh"
 #include "tc_bwd128.cuh"
 #endif
@@ -216,7 +217,7 @@ swa_status swa_attn_fwd(const swa_params* p, const void* q, const void* k, const
   f.o = static_cast<elem_t*>(o); f.lse = lse;
   f.status = at<uint32_t>(c, c.L.status);
   f.wait_limit_ns = kWaitLimitNs;
-  return tc::launch_fwd_any(f, c.stream);
+  return tc::launch_fwd_any2(f, c.stream);
 #endif
 }
 

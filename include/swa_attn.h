@@ -149,10 +149,10 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
  * outputs and the status word) lives in one fixed array of
  * SWA_NOALLOC_SCRATCH_BYTES of device memory inside the library. The pages
  * have no counterpart of this call; it exists for callers that cannot
- * allocate device memory at the point where they run the attention, for
- * example code that runs while a CUDA graph is being captured, a plug-in whose
- * host framework owns every allocation, or a service that must not grow its
- * memory after start-up.
+ * allocate device memory at the point where they run the attention: a
+ * plug-in whose host framework owns every allocation, a service that must not
+ * grow its memory after start-up, or a latency-critical path that cannot
+ * afford cudaMalloc's implicit device synchronisation.
  *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  *     routine. The array is part of the library's device code, so every GPU
  *     that loads the library holds it until the process exits.

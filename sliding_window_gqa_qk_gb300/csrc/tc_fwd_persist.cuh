@@ -473,15 +473,18 @@ __global__ void __launch_bounds__(kPerThreads, 1)
   }
 }
 
+// SM count of the current device (looked up once per device).
 inline int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 1;
+  constexpr int kMaxDev = 64;
+  static int n_sm[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 1;
+  if (n_sm[dev] <= 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    n_sm[dev] = n;
   }
-  return n;
+  return n_sm[dev];
 }
 
 template <int D>

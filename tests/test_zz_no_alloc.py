@@ -1,10 +1,11 @@
 """The forward entry point that allocates nothing (swa_attn_fwd_noalloc).
 
 Some callers cannot allocate device memory where they run the attention:
-code running while a CUDA graph is being captured, plug-ins whose host
-framework owns every allocation, services that must not grow their memory
-after start-up. For them the library keeps the forward's scratch in one
-fixed device array instead of a caller-provided workspace. This test calls
+plug-ins whose host framework owns every allocation, services that must not
+grow their memory after start-up, latency-critical paths that cannot afford
+cudaMalloc's implicit device synchronisation. For them the library keeps the
+forward's scratch in one fixed device array instead of a caller-provided
+workspace. This test calls
 that entry point through the C ABI and checks that its outputs equal those of
 the regular swa_attn_fwd (with a workspace) within the parity tolerance, on
 two calls in a row with different inputs (the array keeps the previous

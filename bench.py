@@ -305,7 +305,7 @@ def run_ours(args, rank, world, dev):
     ms = _max_over_ranks(ms_total, world) / args.steps
     stage_ms = {k: sum(a.elapsed_time(b) for a, b in v) / args.steps for k, v in ev.items()}
     flops_step = stack.flops_fwd + stack.flops_bwd
-    value = flops_step * world / (ms * 1e-3) / 1e12
+    value = _aggregate(flops_step, world, ms)
 
     # dominant kernel: the backward main kernel (per launch = one layer)
     peaks, peak_kind = load_peaks()
@@ -390,7 +390,7 @@ def run_e2e(args, stack, world):
     b.record()
     torch.cuda.synchronize()
     ms = _max_over_ranks(a.elapsed_time(b), world) / args.steps
-    value = (stack.flops_fwd + stack.flops_bwd) * world / (ms * 1e-3) / 1e12
+    value = _aggregate(stack.flops_fwd + stack.flops_bwd, world, ms)
     return {"value": round(value, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
@@ -443,12 +443,19 @@ def _barrier(world):
 
 
 def _max_over_ranks(x, world):
+    """The maximum of x over the ranks (the slowest rank's time)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def _aggregate(flops_per_rank_step, world, ms_per_step):
+    """Whole-job TFLOP/s: every rank's work over the slowest rank's time."""
+    return flops_per_rank_step * world / (ms_per_step * 1e-3) / 1e12
 
 
 def main():

@@ -271,16 +271,8 @@ __global__ void __launch_bounds__(256) gain_sum_kernel(GainArgs a) {
   const float* part = blockIdx.x == 0 ? a.part_q : a.part_k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = blockIdx.y * 32 + lane;
-  // Eight independent accumulators per warp (rows warp + 8u + 64k), so that
-  // eight loads are in flight; the order of the additions is fixed.
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  int blk = warp;
-  for (; blk + 56 < nblk; blk += 64) {
-#pragma unroll
-    for (int u = 0; u < 8; ++u) acc[u] += part[static_cast<long long>(blk + 8 * u) * a.d + c];
-  }
-  for (; blk < nblk; blk += 8) acc[0] += part[static_cast<long long>(blk) * a.d + c];
-  const float s = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+  float s = 0.f;
+  for (int blk = warp; blk < nblk; blk += 8) s += part[static_cast<long long>(blk) * a.d + c];
   __shared__ float red[8][32];
   red[warp][lane] = s;
   __syncthreads();

@@ -92,6 +92,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   return false;
 }
 
+
+// Non-blocking check that all three barriers completed the given phases
+// (one instruction sequence, no branches), for the fast path of waits that
+// are usually already satisfied.
+__device__ __forceinline__ uint32_t mbar_test3(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1,
+                                               uint32_t b2, uint32_t p2) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred a, b, c;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 a, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 b, [%3], %4;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 c, [%5], %6;\n\t"
+      "and.pred a, a, b;\n\t"
+      "and.pred a, a, c;\n\t"
+      "selp.u32 %0, 1, 0, a;\n\t}"
+      : "=r"(done)
+      : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+      : "memory");
+  return done;
+}
+
 // mbar_wait whose outcome is the same for every lane of the warp (so that the
 // warp stays converged for the warp-collective tcgen05 loads that follow).
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {

@@ -256,9 +256,13 @@ __global__ void __launch_bounds__(kPerThreads, 1)
         umma_commit_w(bar(QP_KEMPTY + (g0 & 1)), one);
         for (int j = 1; j < n && ok; ++j) {
           const int gj = g0 + j, gp = gj - 1;
-          ok = mbar_wait_warp(bar(QP_KFULL + (gj & 1)), (gj >> 1) & 1, ctl) &&
-               mbar_wait_warp(bar(QP_PFULL + 0), gp & 1, ctl) &&
-               mbar_wait_warp(bar(QP_VFULL + (gp & 1)), (gp >> 1) & 1, ctl) && (j > 1 || wait_ofree(0));
+          const bool ready = __all_sync(0xffffffffu, mbar_test3(bar(QP_KFULL + (gj & 1)), (gj >> 1) & 1,
+                                                                  bar(QP_PFULL + 0), gp & 1,
+                                                                  bar(QP_VFULL + (gp & 1)), (gp >> 1) & 1) != 0);
+          ok = (ready || (mbar_wait_warp(bar(QP_KFULL + (gj & 1)), (gj >> 1) & 1, ctl) &&
+                          mbar_wait_warp(bar(QP_PFULL + 0), gp & 1, ctl) &&
+                          mbar_wait_warp(bar(QP_VFULL + (gp & 1)), (gp >> 1) & 1, ctl))) &&
+               (j > 1 || wait_ofree(0));
           if (!ok) break;
           tc_fence_after();
           issue_pv(0, gp, j == 1);

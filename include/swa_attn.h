@@ -87,7 +87,8 @@ typedef struct swa_params {
                                   inputs: skip recomputing them                       */
 #define SWA_BWD_STAGE_PRE 2u   /* backward stages to run; none of the three bits set */
 #define SWA_BWD_STAGE_MAIN 4u  /* means all of them. PRE: D = rowsum(dO * O), clear   */
-#define SWA_BWD_STAGE_POST 8u  /* the accumulators (and dve); MAIN: the attention
+#define SWA_BWD_STAGE_POST 8u  /* the accumulators unless the forward left them
+                                  zeroed (and dve); MAIN: the attention
                                   backward with the key-side RMSNorm backward (dk,
                                   dv, dve); POST: query-side RMSNorm backward and
                                   the gain gradients.
@@ -97,7 +98,8 @@ typedef struct swa_params {
 /*
  * Bytes of workspace a problem needs (forward only, or forward + backward).
  * Returns 0 when the parameters are invalid. The workspace holds a 256-byte
- * header (device status word), the QK-norm outputs qn, kn and their inverse
+ * header (device status word, record of a zeroed dQ accumulator), the
+ * QK-norm outputs qn, kn and their inverse
  * RMS, v_eff on VE layers, and for the backward the fp32 accumulators.
  * A fresh workspace must be initialised once with swa_attn_workspace_init().
  */
@@ -116,7 +118,13 @@ swa_status swa_attn_workspace_init(void* workspace, size_t ws_bytes, void* strea
  *            initialisation: 2 * sigmoid(0)).
  *   flags    0 or SWA_REUSE_PROLOGUE.
  * Writes o and lse, and the prologue outputs into the workspace (kept for the
- * backward's SWA_REUSE_PROLOGUE).
+ * backward's SWA_REUSE_PROLOGUE). When ws_bytes is at least the backward
+ * size (swa_attn_workspace_size(p, 1)) and Hq / Hkv is even, the forward
+ * kernel also zeroes the backward's fp32 dQ accumulator and records that in
+ * the workspace header; the next backward of the same problem on this
+ * workspace then skips that clear. Any later call that may overwrite the
+ * accumulator drops the record (a forward that does not zero it, the
+ * backward's main stage).
  */
 swa_status swa_attn_fwd(const swa_params* p, const void* q, const void* k, const void* v,
                         const float* gq, const float* gk, const void* ve, const int32_t* tok,

@@ -17,6 +17,20 @@ using elem_t = __nv_bfloat16;
 
 namespace swa {
 
+// SM count of the current device (looked up once per device).
+inline int num_sms() {
+  constexpr int kMaxDev = 64;
+  static int n_sm[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 1;
+  if (n_sm[dev] <= 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    n_sm[dev] = n;
+  }
+  return n_sm[dev];
+}
+
 // ---------------------------------------------------------------------------
 // Element conversions
 // ---------------------------------------------------------------------------
@@ -154,7 +168,8 @@ __host__ __device__ __forceinline__ bool tile_full(const Band& b, int q0, int bm
 // attention kernels stream, so that one head's rows are contiguous.
 // ---------------------------------------------------------------------------
 struct WsLayout {
-  size_t status;    // uint32 status word (header, 256 bytes)
+  size_t status;    // uint32 status word (header, 256 bytes); bytes 8..23:
+                    // record of a zeroed dQ accumulator (offset, length)
   size_t qn;        // elem [B, Hq, T, d]
   size_t kn;        // elem [B, Hkv, T, d]
   size_t veff;      // elem [B, Hkv, T, d]
@@ -212,6 +227,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int T, int Hq, int Hkv, int
 // ---------------------------------------------------------------------------
 struct ProArgs {  // QK-norm + VE-mix prologue
   int B, T, Hq, Hkv, d, vocab;
+  int nseg;         // 2: q and k rows; 3: also v rows
   float eps, ve_scale;
   const elem_t* q; const elem_t* k; const elem_t* v;
   const float* gq; const float* gk;
@@ -226,6 +242,10 @@ struct PreArgs {  // backward preprocess: D = rowsum(dO * O), LSE2, clear dQ acc
   const elem_t* o; const elem_t* dO; const float* lse;
   float* dvec; float* lse2; float* dq_acc;
   int clear_acc;
+  // Record (offset, length) of a zeroed dQ accumulator left by the forward;
+  // the clear is skipped when it names exactly this call's accumulator.
+  const unsigned long long* acc_flag;
+  unsigned long long acc_off, acc_len;
   // dvec = d_mul * D, lse2 = lse2_mul * LSE + lse2_add (the forms the
   // attention backward kernels consume)
   float d_mul, lse2_mul, lse2_add;

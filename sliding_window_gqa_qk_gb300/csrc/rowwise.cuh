@@ -1,250 +1,358 @@
 // Row-wise, HBM-bound kernels around the attention core:
 //   prologue   QK-norm of q and k, value-embedding mix of v   (forward)
 //   bwd_pre    D = rowsum(dO * O), LSE * log2 e, clear the dQ accumulator
+//              (unless the forward left it zeroed)
 //   bwd_post   RMSNorm backward of q and k, dv, VE-table gradient, gain
 //              gradient partials                               (backward)
 //   gain_sum   deterministic sum of the gain partials           (backward)
 //
-// Grids are 2-D: blockIdx.y = b * H + h, blockIdx.x = a run of consecutive
-// positions t, so no per-row integer division is needed. One warp owns one
-// row of d elements (each lane d/32 consecutive elements) and keeps
-// kRowsPerIter rows in flight, all loads issued before any arithmetic.
+// The first three are persistent: a grid of a few blocks per SM whose warps
+// walk a flat list of row groups (kRowSlots x rows-per-instruction
+// consecutive positions of one (batch, head) row), group w, w + W, w + 2W,
+// ... for warp w of W, so every warp gets the same amount of work. Each lane
+// moves one 16-byte vector of a row per access (8 bf16 or 4 fp32 elements),
+// LPR lanes cover a row, and a warp keeps kRowSlots such accesses per tensor
+// in flight before any arithmetic. Row reductions are shuffles over the LPR
+// lanes of a row.
 #pragma once
 
 #include "common.cuh"
 
 namespace swa {
 
-constexpr int kRowWarps = 8;                              // warps per block
-constexpr int kRowsPerIter = 4;                           // rows in flight per warp
-constexpr int kRowsPerBlock = kRowWarps * kRowsPerIter;   // 32 positions per block
-constexpr int kPostRowsPerBlock = 256;                    // positions per post block
+constexpr int kRowWarps = 8;        // warps per block of the row-wise kernels
+constexpr int kPreBlocksPerSm = 4;  // persistent blocks per SM (register budget 64)
+constexpr int kProBlocksPerSm = 3;  // prologue: register budget 80
+constexpr int kPostBlocksPerSm = 2; // post: register budget 128
+constexpr int kRowSlots = 4;        // 16-byte accesses in flight per lane and tensor
+
+// Lane layout of a D-element row of elem_t.
+template <int D>
+struct RowMap {
+  static constexpr int EPL = 16 / static_cast<int>(sizeof(elem_t));  // elements per lane
+  static constexpr int LPR = D / EPL;                                // lanes per row
+  static constexpr int RPI = 32 / LPR;                               // rows per warp access
+  static constexpr int RG = kRowSlots * RPI;                         // rows per group
+  static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0, "row layout");
+};
+
+// 16 bytes of elem_t <-> EPL floats.
+__device__ __forceinline__ void unpack16(const uint4& r, float (&f)[8]) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ void unpack16(const uint4& r, float (&f)[4]) {
+  f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+  f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+}
+__device__ __forceinline__ uint4 pack16(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+__device__ __forceinline__ uint4 pack16(const float (&f)[4]) {
+  return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                    __float_as_uint(f[3]));
+}
+__device__ __forceinline__ uint4 ld16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ void st16(void* p, const uint4& v) { *reinterpret_cast<uint4*>(p) = v; }
+
+// n consecutive fp32 values (n = 4 or 8) as 16-byte accesses.
+template <int N>
+__device__ __forceinline__ void ldf(const float* p, float (&f)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; i += 4) {
+    const float4 t = *reinterpret_cast<const float4*>(p + i);
+    f[i] = t.x; f[i + 1] = t.y; f[i + 2] = t.z; f[i + 3] = t.w;
+  }
+}
+template <int N>
+__device__ __forceinline__ void stf(float* p, const float (&f)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; i += 4) *reinterpret_cast<float4*>(p + i) = make_float4(f[i], f[i + 1], f[i + 2], f[i + 3]);
+}
+
+// Sum over the LPR lanes of a row.
+template <int LPR>
+__device__ __forceinline__ float row_sum(float x) {
+#pragma unroll
+  for (int o = LPR / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Warp index over the grid and the number of warps of the grid.
+__device__ __forceinline__ long long grid_warp() {
+  return static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+}
+__device__ __forceinline__ long long grid_warps() {
+  return static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+}
 
 // QK-norm ("RMSNorm of queries and keys right before the attention dot
 // product", autoresearch train.py walkthrough post, model paragraph; the
 // Administrator & Developer Guide §8.2.1 names F.rms_norm) and the
 // value-embedding mix v + ve_scale * gate * VE[tok] (Guide §8.2.1,
-// value-embedding row). blockIdx.z selects the segment: 0 = q rows,
-// 1 = k rows, 2 = v rows (launched on value-embedding layers, and by the fp32
-// build on every layer to make a head-major copy of v).
-// Inputs are [B, T, H, d]; outputs are written head-major [B, H, T, d].
+// value-embedding row). The group list holds the q rows, then the k rows,
+// then (nseg = 3: value-embedding layers, and every layer of the fp32 build,
+// which makes a head-major copy of v) the v rows. Inputs are [B, T, H, d];
+// outputs are written head-major [B, H, T, d].
 template <int D>
-__global__ void __launch_bounds__(kRowWarps * 32) prologue_kernel(ProArgs a) {
-  constexpr int NV = D / 32;
-  const int seg = blockIdx.z;
-  const int H = seg == 0 ? a.Hq : a.Hkv;
-  const int bh = blockIdx.y;
-  if (bh >= a.B * H) return;
-  const int b = bh / H, h = bh - (bh / H) * H;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c0 = lane * NV;
-  const int t0 = blockIdx.x * kRowsPerBlock + warp;      // rows t0 + u * kRowWarps
-  const long long in_stride = static_cast<long long>(H) * D;
-  const long long in0 = (static_cast<long long>(b) * a.T * H + h) * D + c0;   // t = 0
-  const long long out0 = static_cast<long long>(bh) * a.T * D + c0;
-
-  if (seg < 2) {
-    const elem_t* x = seg == 0 ? a.q : a.k;
-    const float* gain = seg == 0 ? a.gq : a.gk;
-    elem_t* y = seg == 0 ? a.qn : a.kn;
-    float* rs = seg == 0 ? a.rstd_q : a.rstd_k;
-    float xv[kRowsPerIter][NV];
+__global__ void __launch_bounds__(kRowWarps * 32, kProBlocksPerSm) prologue_kernel(ProArgs a) {
+  using M = RowMap<D>;
+  constexpr int EPL = M::EPL;
+  const int lane = threadIdx.x & 31;
+  const int slot = lane / M::LPR, c0 = (lane % M::LPR) * EPL;
+  const int ngt = (a.T + M::RG - 1) / M::RG;
+  const long long n_q = static_cast<long long>(a.B) * a.Hq * ngt;
+  const long long n_k = static_cast<long long>(a.B) * a.Hkv * ngt;
+  const long long n_all = n_q + n_k * (a.nseg == 3 ? 2 : 1);
+  float gq[EPL], gk[EPL];
 #pragma unroll
-    for (int u = 0; u < kRowsPerIter; ++u) {
-      const int t = t0 + u * kRowWarps;
-      if (t < a.T) load_vec<NV>(x + in0 + t * in_stride, xv[u]);
-    }
-    float g[NV];
+  for (int i = 0; i < EPL; ++i) {
+    gq[i] = a.gq ? a.gq[c0 + i] : 1.0f;
+    gk[i] = a.gk ? a.gk[c0 + i] : 1.0f;
+  }
+  const int Hd = a.Hkv * D;
+  for (long long gi = grid_warp(); gi < n_all; gi += grid_warps()) {
+    const int seg = gi < n_q ? 0 : (gi < n_q + n_k ? 1 : 2);
+    const long long loc = gi - (seg == 0 ? 0 : (seg == 1 ? n_q : n_q + n_k));
+    const int H = seg == 0 ? a.Hq : a.Hkv;
+    const int bh = static_cast<int>(loc / ngt);
+    const int tg = static_cast<int>(loc - static_cast<long long>(bh) * ngt) * M::RG + slot;
+    const int b = bh / H, h = bh - b * H;
+    const long long in0 = (static_cast<long long>(b) * a.T * H + h) * D + c0;   // t = 0
+    const long long in_stride = static_cast<long long>(H) * D;
+    const long long out0 = static_cast<long long>(bh) * a.T * D + c0;
+    if (seg < 2) {
+      const elem_t* x = seg == 0 ? a.q : a.k;
+      elem_t* y = seg == 0 ? a.qn : a.kn;
+      float* rs = seg == 0 ? a.rstd_q : a.rstd_k;
+      uint4 xr[kRowSlots];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) g[i] = gain ? gain[c0 + i] : 1.0f;
-#pragma unroll
-    for (int u = 0; u < kRowsPerIter; ++u) {
-      const int t = t0 + u * kRowWarps;
-      if (t >= a.T) break;
-      float ss = 0.f;
-#pragma unroll
-      for (int i = 0; i < NV; ++i) ss = fmaf(xv[u][i], xv[u][i], ss);
-      ss = warp_sum(ss);
-      const float rstd = rsqrtf(ss / D + a.eps);
-      float o[NV];
-#pragma unroll
-      for (int i = 0; i < NV; ++i) o[i] = xv[u][i] * rstd * g[i];
-      store_vec<NV>(y + out0 + static_cast<long long>(t) * D, o);
-      if (lane == 0) rs[static_cast<long long>(bh) * a.T + t] = rstd;
-    }
-  } else {
-    const int Hd = a.Hkv * D;
-    float vv[kRowsPerIter][NV], ev[kRowsPerIter][NV], sc[kRowsPerIter];
-#pragma unroll
-    for (int u = 0; u < kRowsPerIter; ++u) {
-      const int t = t0 + u * kRowWarps;
-      if (t >= a.T) break;
-      const long long bt = static_cast<long long>(b) * a.T + t;
-      load_vec<NV>(a.v + in0 + t * in_stride, vv[u]);
-      sc[u] = a.ve_scale * (a.gate ? a.gate[bt * a.Hkv + h] : 1.0f);
-      const int tok = a.ve ? a.tok[bt] : 0;
-      if (a.ve == nullptr) {
-        // Plain layer (fp32 build only): v_eff is a head-major copy of v.
-#pragma unroll
-        for (int i = 0; i < NV; ++i) ev[u][i] = 0.f;
-      } else if (tok >= 0 && tok < a.vocab) {
-        load_vec<NV>(a.ve + static_cast<long long>(tok) * Hd + h * D + c0, ev[u]);
-      } else {
-        // An id outside the table contributes nothing and is reported.
-#pragma unroll
-        for (int i = 0; i < NV; ++i) ev[u][i] = 0.f;
-        if (lane == 0) atomicOr(a.status, DEV_ERR_TOKEN);
+      for (int u = 0; u < kRowSlots; ++u) {
+        const int t = tg + u * M::RPI;
+        xr[u] = t < a.T ? ld16(x + in0 + t * in_stride) : make_uint4(0u, 0u, 0u, 0u);
       }
-    }
 #pragma unroll
-    for (int u = 0; u < kRowsPerIter; ++u) {
-      const int t = t0 + u * kRowWarps;
-      if (t >= a.T) break;
-      float o[NV];
+      for (int u = 0; u < kRowSlots; ++u) {
+        const int t = tg + u * M::RPI;
+        float xv[EPL];
+        unpack16(xr[u], xv);
+        float ss = 0.f;
 #pragma unroll
-      for (int i = 0; i < NV; ++i) o[i] = fmaf(sc[u], ev[u][i], vv[u][i]);
-      store_vec<NV>(a.veff + out0 + static_cast<long long>(t) * D, o);
+        for (int i = 0; i < EPL; ++i) ss = fmaf(xv[i], xv[i], ss);
+        ss = row_sum<M::LPR>(ss);
+        const float rstd = rsqrtf(ss / D + a.eps);
+        float o[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) o[i] = xv[i] * rstd * (seg == 0 ? gq[i] : gk[i]);
+        if (t < a.T) {
+          st16(y + out0 + static_cast<long long>(t) * D, pack16(o));
+          if (c0 == 0) rs[static_cast<long long>(bh) * a.T + t] = rstd;
+        }
+      }
+    } else {
+      uint4 vr[kRowSlots], er[kRowSlots];
+      float sc[kRowSlots];
+#pragma unroll
+      for (int u = 0; u < kRowSlots; ++u) {
+        const int t = tg + u * M::RPI;
+        er[u] = make_uint4(0u, 0u, 0u, 0u);
+        sc[u] = 0.f;
+        if (t >= a.T) continue;
+        const long long bt = static_cast<long long>(b) * a.T + t;
+        vr[u] = ld16(a.v + in0 + t * in_stride);
+        if (a.ve == nullptr) continue;   // plain layer (fp32 build only): v_eff is a copy of v
+        const int tok = a.tok[bt];
+        if (tok >= 0 && tok < a.vocab) {
+          er[u] = ld16(a.ve + static_cast<long long>(tok) * Hd + h * D + c0);
+          sc[u] = a.ve_scale * (a.gate ? a.gate[bt * a.Hkv + h] : 1.0f);
+        } else if (c0 == 0) {
+          // An id outside the table contributes nothing and is reported.
+          atomicOr(a.status, DEV_ERR_TOKEN);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kRowSlots; ++u) {
+        const int t = tg + u * M::RPI;
+        if (t >= a.T) continue;
+        float vv[EPL], ev[EPL], o[EPL];
+        unpack16(vr[u], vv);
+        unpack16(er[u], ev);
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) o[i] = fmaf(sc[u], ev[i], vv[i]);
+        st16(a.veff + out0 + static_cast<long long>(t) * D, pack16(o));
+      }
     }
   }
 }
 
 // D[b, h, t] = sum_c dO[b, t, h, c] * O[b, t, h, c] (the softmax-backward row
-// term), LSE2[b, h, t] = LSE[b, h, t] * log2(e) (both in rows padded to Tpad),
-// and (clear_acc) zero the fp32 dQ accumulator row [b, h, t, :].
-// Grid (ceil(T / 32), B * Hq).
+// term), LSE2[b, h, t] = LSE[b, h, t] * log2(e) (both in rows padded to Tpad;
+// the d_mul / lse2_mul / lse2_add forms), and (unless the forward left it
+// zeroed) zero the fp32 dQ accumulator row [b, h, t, :].
 template <int D>
-__global__ void __launch_bounds__(kRowWarps * 32) bwd_pre_kernel(PreArgs a) {
-  constexpr int NV = D / 32;
-  const int bh = blockIdx.y;
-  const int b = bh / a.Hq, h = bh - (bh / a.Hq) * a.Hq;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c0 = lane * NV;
-  const int t0 = blockIdx.x * kRowsPerBlock + warp;
+__global__ void __launch_bounds__(kRowWarps * 32, kPreBlocksPerSm) bwd_pre_kernel(PreArgs a) {
+  using M = RowMap<D>;
+  constexpr int EPL = M::EPL;
+  const int lane = threadIdx.x & 31;
+  const int slot = lane / M::LPR, c0 = (lane % M::LPR) * EPL;
+  // the forward may already have zeroed exactly this accumulator
+  const bool clear = a.clear_acc &&
+                     !(a.acc_flag != nullptr && a.acc_flag[0] == a.acc_off && a.acc_flag[1] == a.acc_len);
+  const int ngt = (a.T + M::RG - 1) / M::RG;
+  const long long n_all = static_cast<long long>(a.B) * a.Hq * ngt;
   const long long in_stride = static_cast<long long>(a.Hq) * D;
-  const long long in0 = (static_cast<long long>(b) * a.T * a.Hq + h) * D + c0;
-  float ov[kRowsPerIter][NV], gv[kRowsPerIter][NV];
+  for (long long gi = grid_warp(); gi < n_all; gi += grid_warps()) {
+    const int bh = static_cast<int>(gi / ngt);
+    const int tg = static_cast<int>(gi - static_cast<long long>(bh) * ngt) * M::RG + slot;
+    const int b = bh / a.Hq, h = bh - b * a.Hq;
+    const long long in0 = (static_cast<long long>(b) * a.T * a.Hq + h) * D + c0;
+    uint4 orw[kRowSlots], grw[kRowSlots];
 #pragma unroll
-  for (int u = 0; u < kRowsPerIter; ++u) {
-    const int t = t0 + u * kRowWarps;
-    if (t < a.T) {
-      load_vec<NV>(a.o + in0 + t * in_stride, ov[u]);
-      load_vec<NV>(a.dO + in0 + t * in_stride, gv[u]);
+    for (int u = 0; u < kRowSlots; ++u) {
+      const int t = tg + u * M::RPI;
+      orw[u] = grw[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (t < a.T) {
+        orw[u] = ld16(a.o + in0 + t * in_stride);
+        grw[u] = ld16(a.dO + in0 + t * in_stride);
+      }
     }
-  }
 #pragma unroll
-  for (int u = 0; u < kRowsPerIter; ++u) {
-    const int t = t0 + u * kRowWarps;
-    if (t >= a.T) break;
-    float s = 0.f;
+    for (int u = 0; u < kRowSlots; ++u) {
+      const int t = tg + u * M::RPI;
+      float ov[EPL], gv[EPL];
+      unpack16(orw[u], ov);
+      unpack16(grw[u], gv);
+      float s = 0.f;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) s = fmaf(ov[u][i], gv[u][i], s);
-    s = warp_sum(s);
-    const long long prow = static_cast<long long>(bh) * a.Tpad + t;
-    if (lane == 0) {
-      a.dvec[prow] = s * a.d_mul;
-      a.lse2[prow] = fmaf(a.lse[static_cast<long long>(bh) * a.T + t], a.lse2_mul, a.lse2_add);
-    }
-    if (a.clear_acc) {
-      float z[NV];
+      for (int i = 0; i < EPL; ++i) s = fmaf(ov[i], gv[i], s);
+      s = row_sum<M::LPR>(s);
+      if (t >= a.T) continue;
+      const long long prow = static_cast<long long>(bh) * a.Tpad + t;
+      if (c0 == 0) {
+        a.dvec[prow] = s * a.d_mul;
+        a.lse2[prow] = fmaf(a.lse[static_cast<long long>(bh) * a.T + t], a.lse2_mul, a.lse2_add);
+      }
+      if (clear) {
+        float z[EPL];
 #pragma unroll
-      for (int i = 0; i < NV; ++i) z[i] = 0.f;
-      store_vec<NV>(a.dq_acc + (static_cast<long long>(bh) * a.T + t) * D + c0, z);
+        for (int i = 0; i < EPL; ++i) z[i] = 0.f;
+        stf<EPL>(a.dq_acc + (static_cast<long long>(bh) * a.T + t) * D + c0, z);
+      }
     }
   }
 }
 
-// Backward of the prologue. Grid (ceil(T / 256), B * max(Hq, Hkv), 3);
-// blockIdx.z: 0 = q rows (RMSNorm backward of q from the gradient of qn, dgq
-// partials), 1 = k rows (same for k), 2 = v rows (dv = gradient of v_eff;
-// scatter ve_scale * gate * dv_eff into dVE). RMSNorm backward, with
-// r = rstd, xh = x r, y = g xh:
+// Backward of the prologue. Grid (nblk, segments); blockIdx.y: 0 = q rows
+// (RMSNorm backward of q from the gradient of qn, dgq partials), 1 = k rows
+// (same for k), 2 = v rows (dv = gradient of v_eff; scatter
+// ve_scale * gate * dv_eff into dVE). RMSNorm backward, with r = rstd,
+// xh = x r, y = g xh:
 //   dxh = g dy;  dx = r (dxh - xh mean(dxh xh));  dg += dy xh.
-// The gain partial of block (x, y) of segment s goes to
-// gpart[s][y * gridDim.x + x][:].
+// The gain partial of block x of segment s goes to gpart[s][x][:].
 template <int D>
-__global__ void __launch_bounds__(kRowWarps * 32) bwd_post_kernel(PostArgs a) {
-  constexpr int NV = D / 32;
-  const int seg = blockIdx.z;
+__global__ void __launch_bounds__(kRowWarps * 32, kPostBlocksPerSm) bwd_post_kernel(PostArgs a) {
+  using M = RowMap<D>;
+  constexpr int EPL = M::EPL;
+  const int seg = blockIdx.y;
   const int H = seg == 0 ? a.Hq : a.Hkv;
-  const int bh = blockIdx.y;
-  if (bh >= a.B * H) return;
-  const int b = bh / H, h = bh - (bh / H) * H;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c0 = lane * NV;
+  const int slot = lane / M::LPR, c0 = (lane % M::LPR) * EPL;
+  const int ngt = (a.T + M::RG - 1) / M::RG;
+  const long long n_all = static_cast<long long>(a.B) * H * ngt;
   const long long in_stride = static_cast<long long>(H) * D;
-  const long long in0 = (static_cast<long long>(b) * a.T * H + h) * D + c0;
-  const long long acc0 = static_cast<long long>(bh) * a.T * D + c0;
-  const int tb = blockIdx.x * kPostRowsPerBlock;
-  const int tend = min(a.T, tb + kPostRowsPerBlock);
-
+  const int Hd = a.Hkv * D;
   if (seg < 2) {
     const elem_t* x = seg == 0 ? a.q : a.k;
     const float* gain = seg == 0 ? a.gq : a.gk;
     const float* rs = seg == 0 ? a.rstd_q : a.rstd_k;
     const float* acc = seg == 0 ? a.dq_acc : a.dk_acc;
     elem_t* dx = seg == 0 ? a.dq : a.dk;
-    float g[NV], gacc[NV];
+    float g[EPL], gacc[EPL];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
+    for (int i = 0; i < EPL; ++i) {
       g[i] = gain ? gain[c0 + i] : 1.0f;
       gacc[i] = 0.f;
     }
-    for (int base = tb + warp; base < tend; base += kRowWarps * kRowsPerIter) {
-      float xv[kRowsPerIter][NV], dy[kRowsPerIter][NV], rr[kRowsPerIter];
+    for (long long gi = grid_warp(); gi < n_all; gi += grid_warps()) {
+      const int bh = static_cast<int>(gi / ngt);
+      const int tg = static_cast<int>(gi - static_cast<long long>(bh) * ngt) * M::RG + slot;
+      const int b = bh / H, h = bh - b * H;
+      const long long in0 = (static_cast<long long>(b) * a.T * H + h) * D + c0;
+      const long long acc0 = static_cast<long long>(bh) * a.T * D + c0;
+      uint4 xr[kRowSlots];
+      float dy[kRowSlots][EPL], rr[kRowSlots];
 #pragma unroll
-      for (int u = 0; u < kRowsPerIter; ++u) {
-        const int t = base + u * kRowWarps;
-        if (t >= tend) break;
-        load_vec<NV>(x + in0 + t * in_stride, xv[u]);
-        load_vec<NV>(acc + acc0 + static_cast<long long>(t) * D, dy[u]);
-        rr[u] = rs[static_cast<long long>(bh) * a.T + t];
+      for (int u = 0; u < kRowSlots; ++u) {
+        const int t = tg + u * M::RPI;
+        rr[u] = 0.f;
+        if (t < a.T) {
+          xr[u] = ld16(x + in0 + t * in_stride);
+          ldf<EPL>(acc + acc0 + static_cast<long long>(t) * D, dy[u]);
+          rr[u] = rs[static_cast<long long>(bh) * a.T + t];
+        } else {
+          xr[u] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int i = 0; i < EPL; ++i) dy[u][i] = 0.f;
+        }
       }
 #pragma unroll
-      for (int u = 0; u < kRowsPerIter; ++u) {
-        const int t = base + u * kRowWarps;
-        if (t >= tend) break;
-        float xh[NV], dxh[NV], dot = 0.f;
+      for (int u = 0; u < kRowSlots; ++u) {
+        const int t = tg + u * M::RPI;
+        float xh[EPL], dxh[EPL], dot = 0.f;
+        unpack16(xr[u], xh);
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-          xh[i] = xv[u][i] * rr[u];
+        for (int i = 0; i < EPL; ++i) {
+          xh[i] *= rr[u];
           dxh[i] = g[i] * dy[u][i];
           dot = fmaf(dxh[i], xh[i], dot);
           gacc[i] = fmaf(dy[u][i], xh[i], gacc[i]);
         }
-        dot = warp_sum(dot) / D;
-        float o[NV];
+        dot = row_sum<M::LPR>(dot) / D;
+        if (t >= a.T) continue;
+        float o[EPL];
 #pragma unroll
-        for (int i = 0; i < NV; ++i) o[i] = rr[u] * (dxh[i] - xh[i] * dot);
-        store_vec<NV>(dx + in0 + t * in_stride, o);
+        for (int i = 0; i < EPL; ++i) o[i] = rr[u] * (dxh[i] - xh[i] * dot);
+        st16(dx + in0 + t * in_stride, pack16(o));
       }
     }
-    // Block reduction of the gain partials: fixed order, no atomics.
-    __shared__ float red[kRowWarps][D];
+    // Block reduction of the gain partials, in a fixed order: the row slots
+    // of a warp (lanes c, c + LPR, ...), then the warps.
 #pragma unroll
-    for (int i = 0; i < NV; ++i) red[warp][c0 + i] = gacc[i];
+    for (int i = 0; i < EPL; ++i) {
+#pragma unroll
+      for (int o = M::LPR; o < 32; o <<= 1) gacc[i] += __shfl_xor_sync(0xffffffffu, gacc[i], o);
+    }
+    __shared__ float red[kRowWarps][D];
+    if (slot == 0) {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) red[warp][c0 + i] = gacc[i];
+    }
     __syncthreads();
-    const long long blk = static_cast<long long>(bh) * gridDim.x + blockIdx.x;
     for (int c = threadIdx.x; c < D; c += blockDim.x) {
       float s = 0.f;
 #pragma unroll
       for (int w = 0; w < kRowWarps; ++w) s += red[w][c];
-      a.gpart[(static_cast<long long>(seg) * a.nblk_max + blk) * D + c] = s;
+      a.gpart[(static_cast<long long>(seg) * a.nblk_max + blockIdx.x) * D + c] = s;
     }
   } else {
-    const int Hd = a.Hkv * D;
-    for (int base = tb + warp; base < tend; base += kRowWarps * kRowsPerIter) {
-      float dv[kRowsPerIter][NV];
+    for (long long gi = grid_warp(); gi < n_all; gi += grid_warps()) {
+      const int bh = static_cast<int>(gi / ngt);
+      const int tg = static_cast<int>(gi - static_cast<long long>(bh) * ngt) * M::RG + slot;
+      const int b = bh / H, h = bh - b * H;
+      const long long in0 = (static_cast<long long>(b) * a.T * H + h) * D + c0;
+      const long long acc0 = static_cast<long long>(bh) * a.T * D + c0;
 #pragma unroll
-      for (int u = 0; u < kRowsPerIter; ++u) {
-        const int t = base + u * kRowWarps;
-        if (t >= tend) break;
-        load_vec<NV>(a.dv_acc + acc0 + static_cast<long long>(t) * D, dv[u]);
-      }
-#pragma unroll
-      for (int u = 0; u < kRowsPerIter; ++u) {
-        const int t = base + u * kRowWarps;
-        if (t >= tend) break;
-        store_vec<NV>(a.dv + in0 + t * in_stride, dv[u]);
+      for (int u = 0; u < kRowSlots; ++u) {
+        const int t = tg + u * M::RPI;
+        if (t >= a.T) continue;
+        float dv[EPL];
+        ldf<EPL>(a.dv_acc + acc0 + static_cast<long long>(t) * D, dv);
+        st16(a.dv + in0 + t * in_stride, pack16(dv));
         if (a.dve) {
           const long long bt = static_cast<long long>(b) * a.T + t;
           const int tok = a.tok[bt];
@@ -252,7 +360,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) bwd_post_kernel(PostArgs a) {
             const float s = a.ve_scale * (a.gate ? a.gate[bt * a.Hkv + h] : 1.0f);
             float* dst = a.dve + static_cast<long long>(tok) * Hd + h * D + c0;
 #pragma unroll
-            for (int i = 0; i < NV; ++i) atomicAdd(dst + i, s * dv[u][i]);
+            for (int i = 0; i < EPL; ++i) atomicAdd(dst + i, s * dv[i]);
           }
         }
       }
@@ -260,11 +368,23 @@ __global__ void __launch_bounds__(kRowWarps * 32) bwd_post_kernel(PostArgs a) {
   }
 }
 
+// Blocks of a persistent row-wise launch: `per_sm` per SM, no more than
+// there are row groups (nor than `cap`).
+inline int row_grid(long long groups, int per_sm, int cap) {
+  long long n = static_cast<long long>(num_sms()) * per_sm;
+  const long long per = (groups + kRowWarps - 1) / kRowWarps;
+  if (per < n) n = per;
+  if (cap > 0 && cap < n) n = cap;
+  return n < 1 ? 1 : static_cast<int>(n);
+}
+
 // dgq[c] = sum of the q partials, dgk[c] = sum of the k partials (written by
 // the backward-post kernel, or by the attention backward's epilogue), in a
-// fixed order. Grid (2, d / 32), 256 threads: column = 32 * blockIdx.y + lane,
-// each warp sums every 8th partial, then the 8 sums are added in order.
-__global__ void __launch_bounds__(256) gain_sum_kernel(GainArgs a) {
+// fixed order. Grid (2, d / 32), 1024 threads: column = 32 * blockIdx.y +
+// lane; warp w sums partials w, w + 32, w + 64, ... in that order (eight
+// loads in flight), then warp 0 adds the 32 warp sums in order.
+constexpr int kGainWarps = 32;
+__global__ void __launch_bounds__(kGainWarps * 32) gain_sum_kernel(GainArgs a) {
   float* out = blockIdx.x == 0 ? a.dgq : a.dgk;
   if (out == nullptr) return;
   const int nblk = blockIdx.x == 0 ? a.n_q : a.n_k;
@@ -272,14 +392,22 @@ __global__ void __launch_bounds__(256) gain_sum_kernel(GainArgs a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = blockIdx.y * 32 + lane;
   float s = 0.f;
-  for (int blk = warp; blk < nblk; blk += 8) s += part[static_cast<long long>(blk) * a.d + c];
-  __shared__ float red[8][32];
+  int blk = warp;
+  for (; blk + 7 * kGainWarps < nblk; blk += 8 * kGainWarps) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = part[static_cast<long long>(blk + u * kGainWarps) * a.d + c];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) s += v[u];
+  }
+  for (; blk < nblk; blk += kGainWarps) s += part[static_cast<long long>(blk) * a.d + c];
+  __shared__ float red[kGainWarps][32];
   red[warp][lane] = s;
   __syncthreads();
   if (warp == 0) {
     float tot = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) tot += red[w][lane];
+    for (int w = 0; w < kGainWarps; ++w) tot += red[w][lane];
     out[c] = tot;
   }
 }

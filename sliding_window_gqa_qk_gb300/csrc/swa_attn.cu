@@ -16,7 +16,6 @@
 #include "simt.cuh"
 #else
 #include "tc_fwd.cuh"
-#include "tc_fwd_pair.cuh"
 #include "tc_fwd_persist.cuh"
 #include "tc_bwd.cuh"
 #include "tc_bwd128.cuh"
@@ -108,7 +107,11 @@ swa_status run_prologue(const Call& c, const elem_t* q, const elem_t* k, const e
   a.qn = at<elem_t>(c, c.L.qn); a.kn = at<elem_t>(c, c.L.kn); a.veff = at<elem_t>(c, c.L.veff);
   a.rstd_q = at<float>(c, c.L.rstd_q); a.rstd_k = at<float>(c, c.L.rstd_k);
   a.status = at<uint32_t>(c, c.L.status);
-  dim3 grid((p.T + kRowsPerBlock - 1) / kRowsPerBlock, p.B * p.Hq, (ve != nullptr || copy_v) ? 3 : 2);
+  a.nseg = (ve != nullptr || copy_v) ? 3 : 2;
+  const int rg = p.d == 64 ? RowMap<64>::RG : RowMap<128>::RG;
+  const long long ngt = (p.T + rg - 1) / rg;
+  const long long groups = ngt * p.B * (p.Hq + p.Hkv * (a.nseg - 1));
+  const int grid = row_grid(groups, kProBlocksPerSm, 0);
   if (p.d == 64) prologue_kernel<64><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
   else prologue_kernel<128><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
   return launched();
@@ -146,28 +149,15 @@ swa_status noalloc_scratch(void** out) {
 
 }  // namespace
 
-// ---------------------------------------------------------------------------
-// Exported C ABI
-// ---------------------------------------------------------------------------
-extern "C" {
+namespace {
 
-size_t swa_attn_workspace_size(const swa_params* p, int for_backward) {
-  if (check_params(p) != SWA_OK) return 0;
-  const WsLayout L = ws_layout(p->B, p->T, p->Hq, p->Hkv, p->d);
-  return for_backward ? L.bwd_end : L.fwd_end;
-}
-
-swa_status swa_attn_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
-  if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < 256) return SWA_ERR_INVALID_ARG;
-  if (cudaMemsetAsync(workspace, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return SWA_ERR_CUDA;
-  return SWA_OK;
-}
-
-swa_status swa_attn_fwd(const swa_params* p, const void* q, const void* k, const void* v,
-                        const float* gq, const float* gk, const void* ve, const int32_t* tok,
-                        const float* ve_gate, void* o, float* lse, void* workspace,
-                        size_t ws_bytes, unsigned flags, void* stream) {
+// The forward of swa_attn_fwd. prepare_bwd: a workspace sized for the
+// backward also gets its dQ accumulator zeroed by the forward kernel (the
+// no-allocation entry point passes false).
+swa_status fwd_impl(const swa_params* p, const void* q, const void* k, const void* v,
+                    const float* gq, const float* gk, const void* ve, const int32_t* tok,
+                    const float* ve_gate, void* o, float* lse, void* workspace, size_t ws_bytes,
+                    unsigned flags, void* stream, bool prepare_bwd) {
   Call c;
   swa_status s = begin(c, p, workspace, ws_bytes, false, stream);
   if (s != SWA_OK) return s;
@@ -217,8 +207,44 @@ swa_status swa_attn_fwd(const swa_params* p, const void* q, const void* k, const
   f.o = static_cast<elem_t*>(o); f.lse = lse;
   f.status = at<uint32_t>(c, c.L.status);
   f.wait_limit_ns = kWaitLimitNs;
+  // The forward is compute-bound, so it can zero the backward's dQ
+  // accumulator at little cost; the backward's preprocess then skips it.
+  f.acc_flag = at<unsigned long long>(c, c.L.status + 8);
+  if (prepare_bwd && ws_bytes >= c.L.bwd_end) {
+    f.dq_acc = at<float>(c, c.L.dq_acc);
+    f.acc_off = c.L.dq_acc;
+    f.acc_len = static_cast<unsigned long long>(p->B) * p->T * p->Hq * p->d * sizeof(float);
+  }
   return tc::launch_fwd_any2(f, c.stream);
 #endif
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Exported C ABI
+// ---------------------------------------------------------------------------
+extern "C" {
+
+size_t swa_attn_workspace_size(const swa_params* p, int for_backward) {
+  if (check_params(p) != SWA_OK) return 0;
+  const WsLayout L = ws_layout(p->B, p->T, p->Hq, p->Hkv, p->d);
+  return for_backward ? L.bwd_end : L.fwd_end;
+}
+
+swa_status swa_attn_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+  if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < 256) return SWA_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(workspace, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  return SWA_OK;
+}
+
+swa_status swa_attn_fwd(const swa_params* p, const void* q, const void* k, const void* v,
+                        const float* gq, const float* gk, const void* ve, const int32_t* tok,
+                        const float* ve_gate, void* o, float* lse, void* workspace,
+                        size_t ws_bytes, unsigned flags, void* stream) {
+  return fwd_impl(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, workspace, ws_bytes, flags, stream,
+                  true);
 }
 
 swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const void* v,
@@ -274,13 +300,17 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
     a.dvec = at<float>(c, c.L.dvec); a.lse2 = at<float>(c, c.L.lse2);
     a.dq_acc = at<float>(c, c.L.dq_acc);
     a.clear_acc = clear_acc;
+    a.acc_flag = at<unsigned long long>(c, c.L.status + 8);
+    a.acc_off = c.L.dq_acc;
+    a.acc_len = static_cast<unsigned long long>(P.B) * P.T * P.Hq * P.d * sizeof(float);
     // The d = 128 tensor-core backward takes -D and log2(scale) - LSE log2(e)
     // (its P carries the softmax scale); the others take D and LSE log2(e).
     const bool scaled_p = !kFp32Build && P.d == 128;
     a.d_mul = scaled_p ? -1.f : 1.f;
     a.lse2_mul = scaled_p ? -1.4426950408889634f : 1.4426950408889634f;
     a.lse2_add = scaled_p ? log2f(c.scale) : 0.f;
-    dim3 grid((P.T + kRowsPerBlock - 1) / kRowsPerBlock, P.B * P.Hq);
+    const int rg = P.d == 64 ? RowMap<64>::RG : RowMap<128>::RG;
+    const int grid = row_grid(static_cast<long long>((P.T + rg - 1) / rg) * P.B * P.Hq, kPreBlocksPerSm, 0);
     if (P.d == 64) bwd_pre_kernel<64><<<grid, kRowWarps * 32, 0, st>>>(a);
     else bwd_pre_kernel<128><<<grid, kRowWarps * 32, 0, st>>>(a);
     if ((s = launched()) != SWA_OK) return s;
@@ -335,6 +365,7 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
     b.gpart_k = at<float>(c, c.L.gpart_k);
     b.status = at<uint32_t>(c, c.L.status);
     b.wait_limit_ns = kWaitLimitNs;
+    b.acc_flag = at<unsigned long long>(c, c.L.status + 8);
     if ((s = (P.d == 128 ? tc::launch_bwd128(b, st) : tc::launch_bwd(b, st))) != SWA_OK) return s;
 #endif
   }
@@ -360,21 +391,24 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
     a.gpart = at<float>(c, c.L.gpart);
     a.nblk_max = post_blocks(P.B, P.T, P.Hq);
     a.status = at<uint32_t>(c, c.L.status);
-    const int tblk = (P.T + kPostRowsPerBlock - 1) / kPostRowsPerBlock;
-    dim3 grid(tblk, P.B * P.Hq, post_segments);
+    // one gain partial per block: no more blocks than the workspace holds
+    const int rg = P.d == 64 ? RowMap<64>::RG : RowMap<128>::RG;
+    const int nblk = row_grid(static_cast<long long>((P.T + rg - 1) / rg) * P.B * P.Hq, kPostBlocksPerSm,
+                               a.nblk_max);
+    dim3 grid(nblk, post_segments);
     if (P.d == 64) bwd_post_kernel<64><<<grid, kRowWarps * 32, 0, st>>>(a);
     else bwd_post_kernel<128><<<grid, kRowWarps * 32, 0, st>>>(a);
     if ((s = launched()) != SWA_OK) return s;
     if (dgq || dgk) {
 #if defined(SWA_ELEM_FP32)
       const float* part_k = at<float>(c, c.L.gpart) + static_cast<size_t>(post_blocks(P.B, P.T, P.Hq)) * P.d;
-      const int n_k = tblk * P.B * P.Hkv;
+      const int n_k = nblk;
 #else
       const float* part_k = at<float>(c, c.L.gpart_k);
       const int n_k = P.B * P.Hkv * ((P.T + 127) / 128);
 #endif
-      GainArgs g{P.d, at<float>(c, c.L.gpart), tblk * P.B * P.Hq, part_k, n_k, dgq, dgk};
-      gain_sum_kernel<<<dim3(2, P.d / 32), 256, 0, st>>>(g);
+      GainArgs g{P.d, at<float>(c, c.L.gpart), nblk, part_k, n_k, dgq, dgk};
+      gain_sum_kernel<<<dim3(2, P.d / 32), kGainWarps * 32, 0, st>>>(g);
       if ((s = launched()) != SWA_OK) return s;
     }
   }
@@ -408,8 +442,8 @@ swa_status swa_attn_fwd_noalloc(const swa_params* p, const void* q, const void* 
   void* scratch = nullptr;
   const swa_status ss = noalloc_scratch(&scratch);
   if (ss != SWA_OK) return ss;
-  return swa_attn_fwd(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, scratch,
-                      SWA_NOALLOC_SCRATCH_BYTES, 0, stream);
+  return fwd_impl(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, scratch, SWA_NOALLOC_SCRATCH_BYTES, 0,
+                  stream, false);
 }
 
 int swa_sssl_window(int layer, int n_layer, const char* pattern, int T) {

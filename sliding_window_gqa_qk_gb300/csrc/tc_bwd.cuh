@@ -68,6 +68,7 @@ struct BwdLaunch {
   float* gpart_k;      // [B * Hkv * n_ktiles, d]
   uint32_t* status;
   uint64_t wait_limit_ns;
+  unsigned long long* acc_flag;   // dQ-accumulator record in the workspace header
 };
 
 struct BwdParams {
@@ -90,6 +91,11 @@ struct BwdParams {
   float* gpart_k;
   uint32_t* status;
   uint64_t wait_limit_ns;
+  int n_bhk;                  // B * Hkv
+  int chunk;                  // (batch, kv head) pairs per scheduling chunk (1-D grids)
+  // Record of a forward that zeroed the dQ accumulator (offset, length);
+  // the kernels that add into the accumulator mark it used (length 0).
+  unsigned long long* acc_flag;
 };
 
 // Sum over the 32 lanes of each of 32 values: afterwards lane L holds the
@@ -337,6 +343,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   if (threadIdx.x == 0) {
+    // the accumulator is about to receive this launch's additions
+    if (blockIdx.x == 0 && blockIdx.y == 0 && prm.acc_flag != nullptr) prm.acc_flag[1] = 0ull;
     abort_flag = 0;
     mbar_init(bar(BB_KV), 1);
     for (int s = 0; s < 2; ++s) {
@@ -691,6 +699,7 @@ inline swa_status launch_bwd_d(const BwdLaunch& f, cudaStream_t st) {
   p.k = f.k; p.rstd_k = f.rstd_k; p.gk = f.gk; p.tok = f.tok; p.gate = f.gate; p.dve = f.dve;
   p.ve_scale = f.ve_scale; p.vocab = f.vocab; p.dk = f.dk; p.dv = f.dv; p.gpart_k = f.gpart_k;
   p.status = f.status; p.wait_limit_ns = f.wait_limit_ns;
+  p.acc_flag = f.acc_flag;
   if (cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kAlloc) != cudaSuccess)
     return SWA_ERR_CUDA;

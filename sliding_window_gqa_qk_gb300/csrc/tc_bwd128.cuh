@@ -143,8 +143,23 @@ __global__ void __launch_bounds__(kB2Threads, 1)
   uint32_t* abort_flag = tmem_base_sh + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kt = static_cast<int>(blockIdx.x);        // key tiles of one (b, kv head) run together
-  const int bhk = static_cast<int>(blockIdx.y);
+  // CTA -> (key tile, batch x kv head). The (batch, kv head) pairs are cut
+  // into chunks of prm.chunk; within a chunk the CTAs go key tile by key tile
+  // (all pairs of key tile 0, then of key tile 1, ...). On a causal band the
+  // early key tiles see the most query tiles, so the heavy CTAs of a chunk
+  // start first and the grid ends on light ones, while the Q, dO and dQ rows
+  // that the running CTAs share (one chunk's worth) stay in L2.
+  int kt, bhk;
+  {
+    const int id = static_cast<int>(blockIdx.x);
+    const int per = prm.chunk * prm.n_ktiles;
+    const int ch = id / per;
+    const int r = id - ch * per;
+    const int rest = prm.n_bhk - ch * prm.chunk;
+    const int cn = rest < prm.chunk ? rest : prm.chunk;
+    kt = r / cn;
+    bhk = ch * prm.chunk + (r - kt * cn);
+  }
   const int b = bhk / prm.Hkv, hk = bhk % prm.Hkv;
   const int k0 = kt * kBK;
   const int G = prm.Hq / prm.Hkv;
@@ -157,6 +172,8 @@ __global__ void __launch_bounds__(kB2Threads, 1)
   auto bar = [&](int i) { return sbase + C::oBar + 8u * static_cast<uint32_t>(i); };
 
   if (threadIdx.x == 0) {
+    // the accumulator is about to receive this launch's additions
+    if (blockIdx.x == 0 && prm.acc_flag != nullptr) prm.acc_flag[1] = 0ull;
     *abort_flag = 0;
     mbar_init(bar(B2_KV), 1);
     for (int s = 0; s < 2; ++s) {
@@ -564,8 +581,15 @@ inline swa_status launch_bwd128(const BwdLaunch& f, cudaStream_t st) {
   if (cudaFuncSetAttribute(bwd_tc128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kBytes) != cudaSuccess)
     return SWA_ERR_CUDA;
-  dim3 grid(p.n_ktiles, f.B * f.Hkv);
-  bwd_tc128_kernel<<<grid, kB2Threads, C::kBytes, st>>>(mq, mk, mv, mg, mdq, mdk, mdv, p);
+  // chunks of about 2.5 waves of CTAs
+  p.n_bhk = f.B * f.Hkv;
+  const int want = (5 * num_sms() + 2 * p.n_ktiles - 1) / (2 * p.n_ktiles);
+  p.chunk = want < 1 ? 1 : (want > p.n_bhk ? p.n_bhk : want);
+  p.acc_flag = f.acc_flag;
+  const long long n_cta = static_cast<long long>(p.n_ktiles) * p.n_bhk;
+  if (n_cta > 0x7fffffffLL) return SWA_ERR_UNSUPPORTED;
+  bwd_tc128_kernel<<<static_cast<unsigned>(n_cta), kB2Threads, C::kBytes, st>>>(mq, mk, mv, mg, mdq, mdk,
+                                                                                mdv, p);
   return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 

@@ -46,6 +46,11 @@ struct FwdLaunch {
   float* lse;        // [B, Hq, T]
   uint32_t* status;
   uint64_t wait_limit_ns;
+  // Optional (persistent kernel only): fp32 dQ accumulator of the backward
+  // [B, Hq, T, d] to zero, and where to record the zeroed byte range.
+  float* dq_acc;
+  unsigned long long* acc_flag;
+  unsigned long long acc_off, acc_len;
 };
 
 struct FwdParams {

@@ -10,7 +10,10 @@
 //               row t (TMEM lane t), keeps the running max m and sum l,
 //               rescales its O row only when m grows by more than 2^8, and
 //               writes P = exp2(S c - m) as bf16 pairs back into S's columns
-//               of TMEM, where the PV MMA reads it as its A operand.
+//               of TMEM, where the PV MMA reads it as its A operand. After an
+//               item's first tile the exponentials use the running m at
+//               once (the tile's own maximum is reduced alongside and P is
+//               recomputed only when it exceeds m by more than 2^8).
 // Across items: the Q tiles of the next item load as soon as the last S MMA
 // of the current one completed, so the next item's first S products run
 // while the softmax warpgroups finish the current item's epilogue (O / l
@@ -75,6 +78,12 @@ struct FwdPerParams {
   float* lse;
   uint32_t* status;
   uint64_t wait_limit_ns;
+  // With a workspace sized for the backward: zero the fp32 dQ accumulator
+  // [B, Hq, T, D] of the rows each item covers (null: leave it), and record
+  // the zeroed byte range (acc_off, acc_len) in acc_flag[0..1].
+  float* dq_acc;
+  unsigned long long* acc_flag;
+  unsigned long long acc_off, acc_len;
 };
 
 // The k-th item of CTA c of G: rounds of G items, even rounds dealt in CTA
@@ -198,6 +207,24 @@ __global__ void __launch_bounds__(kPerThreads, 1)
             tma_load_4d_w(sbase + L::kV0 + s * L::kTile + c * L::kHalf, &tmV, bar(QP_VFULL + s), 64 * c,
                           k0, hk, I.b, one);
           last_v[s] = g;
+          if (prm.dq_acc != nullptr) {
+            // A share of the item's rows of the backward's dQ accumulator
+            // (both heads, 128 rows, D floats each), spread over its key
+            // tiles: 512 bytes per warp store, lane = 16 bytes.
+            constexpr int kUnits = 2 * kBM * D * 4 / 512;
+            constexpr int kRowsPerUnit = 512 / (D * 4);
+            const int u1 = (j + 1) * kUnits / I.n_tiles;
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int u = j * kUnits / I.n_tiles; u < u1; ++u) {
+              const int row = u * kRowsPerUnit + lane / (32 / kRowsPerUnit);   // 0 .. 2 kBM - 1
+              const int t = I.q0 + (row % kBM);
+              if (t < prm.T) {
+                float4* acc = reinterpret_cast<float4*>(
+                    prm.dq_acc + ((static_cast<long long>(I.b) * prm.Hq + hA + row / kBM) * prm.T + t) * D);
+                acc[lane % (32 / kRowsPerUnit)] = z;
+              }
+            }
+          }
         }
         ++it;
       }
@@ -339,77 +366,118 @@ __global__ void __launch_bounds__(kPerThreads, 1)
             }
           }
         }
+        // S in two halves of 64 columns: the second half's TMEM load runs
+        // while the first half is masked and reduced.
         uint32_t sr[4][32];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
+        tmem_ld32(tS, sr[0]);
+        tmem_ld32(tS + 32, sr[1]);
         tmem_wait_ld(sr[0]);
         reg_fence(sr[1]);
-        reg_fence(sr[2]);
-        reg_fence(sr[3]);
-        if (!full) {
+        tmem_ld32(tS + 64, sr[2]);
+        tmem_ld32(tS + 96, sr[3]);
+        auto mask_half = [&](int hf) {
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
+          for (int cc = 2 * hf; cc < 2 * hf + 2; ++cc)
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               const int col = cc * 32 + e;
               if (col < clo || col > chi) sr[cc][e] = __float_as_uint(-INFINITY);
             }
-        }
-        // Row maximum: eight independent three-input chains, then a short tree.
-        float mq[8];
+        };
+        // Maximum of one half: four independent three-input chains.
+        auto max_half = [&](int hf) -> float {
+          float mq[4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int cc = q >> 1, e0 = (q & 1) * 16;
-          float a = fmax3(__uint_as_float(sr[cc][e0]), __uint_as_float(sr[cc][e0 + 1]),
-                          __uint_as_float(sr[cc][e0 + 2]));
+          for (int q = 0; q < 4; ++q) {
+            const int cc = 2 * hf + (q >> 1), e0 = (q & 1) * 16;
+            float a = fmax3(__uint_as_float(sr[cc][e0]), __uint_as_float(sr[cc][e0 + 1]),
+                            __uint_as_float(sr[cc][e0 + 2]));
 #pragma unroll
-          for (int e = 3; e < 15; e += 2)
-            a = fmax3(a, __uint_as_float(sr[cc][e0 + e]), __uint_as_float(sr[cc][e0 + e + 1]));
-          mq[q] = fmaxf(a, __uint_as_float(sr[cc][e0 + 15]));
-        }
-        const float mx = fmaxf(fmax3(mq[0], mq[1], mq[2]),
-                               fmax3(fmax3(mq[3], mq[4], mq[5]), mq[6], mq[7]));
-        const float mt = mx * c;
-        float alpha = 1.f;
-        bool rescale_o = false;
-        if (mt > m + kRescaleLog2) {     // also the first finite maximum (m = -inf)
-          if (m != -INFINITY) {
-            alpha = ex2_approx(m - mt);
-            rescale_o = true;
+            for (int e = 3; e < 15; e += 2)
+              a = fmax3(a, __uint_as_float(sr[cc][e0 + e]), __uint_as_float(sr[cc][e0 + e + 1]));
+            mq[q] = fmaxf(a, __uint_as_float(sr[cc][e0 + 15]));
           }
-          l *= alpha;
-          m = mt;
-        }
-        // PV_X of the previous tile has completed: the commit that signalled
-        // this S covers it (only within the item: O is not rescaled at j = 0).
-        if (__any_sync(0xffffffffu, rescale_o)) {
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t orr[32];
-            tmem_ld32(tO + cc * 32, orr);
-            tmem_wait_ld(orr);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-            tmem_st32(tO + cc * 32, orr);
-          }
-        }
-        // P = exp2(S c - m) as bf16 pairs into S's first 64 columns; the
-        // scale-and-shift and the row sum run two lanes per instruction.
-        const float nm = (m == -INFINITY) ? 0.f : -m;
-        float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
+          return fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        };
+        // P = exp2(S c - m) of one half as bf16 pairs into S's columns
+        // [32 hf, 32 hf + 32); scale-and-shift and row sum two lanes per
+        // instruction.
+        float ls[8];
+        auto exp_half = [&](int hf, float nm) {
           uint32_t pk[32];
 #pragma unroll
           for (int w2 = 0; w2 < 32; ++w2) {
-            const int cc = half * 2 + (w2 >> 4), e = (w2 & 15) * 2;
+            const int cc = hf * 2 + (w2 >> 4), e = (w2 & 15) * 2;
             float x0, x1;
             ffma2(x0, x1, __uint_as_float(sr[cc][e]), __uint_as_float(sr[cc][e + 1]), c, c, nm, nm);
             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             fadd2_acc(ls[2 * (w2 & 3)], ls[2 * (w2 & 3) + 1], p0, p1);
             pk[w2] = pack_bf16x2(p0, p1);
           }
-          tmem_st32(tS + half * 32, pk);
+          tmem_st32(tS + hf * 32, pk);
+        };
+#pragma unroll
+        for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+        float mx;
+        bool redo;
+        if (j > 0) {
+          // Exponentials against the running maximum m straight away; the
+          // tile's own maximum is reduced alongside, and only if it exceeds
+          // m by more than 2^8 (rare after the first tile) is P recomputed
+          // against the new maximum below. Either way P, l and O refer to
+          // the same m, so the result is exact.
+          const float nm0 = (m == -INFINITY) ? 0.f : -m;
+          if (!full) mask_half(0);
+          const float mx0 = max_half(0);
+          exp_half(0, nm0);
+          tmem_wait_ld(sr[2]);
+          reg_fence(sr[3]);
+          if (!full) mask_half(1);
+          mx = fmaxf(mx0, max_half(1));
+          exp_half(1, nm0);
+          redo = __any_sync(0xffffffffu, mx * c > m + kRescaleLog2);
+        } else {
+          tmem_wait_ld(sr[2]);
+          reg_fence(sr[3]);
+          if (!full) {
+            mask_half(0);
+            mask_half(1);
+          }
+          mx = fmaxf(max_half(0), max_half(1));
+          redo = true;
+        }
+        if (redo) {
+          if (j > 0) tmem_wait_st();   // the first P stores land before they are redone
+          const float mt = mx * c;
+          float alpha = 1.f;
+          bool rescale_o = false;
+          if (mt > m + kRescaleLog2) {     // also the first finite maximum (m = -inf)
+            if (m != -INFINITY) {
+              alpha = ex2_approx(m - mt);
+              rescale_o = true;
+            }
+            l *= alpha;
+            m = mt;
+          }
+          // PV_X of the previous tile has completed: the commit that
+          // signalled this S covers it (only within the item: O is not
+          // rescaled at j = 0).
+          if (__any_sync(0xffffffffu, rescale_o)) {
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t orr[32];
+              tmem_ld32(tO + cc * 32, orr);
+              tmem_wait_ld(orr);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+              tmem_st32(tO + cc * 32, orr);
+            }
+          }
+          const float nm = (m == -INFINITY) ? 0.f : -m;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+          exp_half(0, nm);
+          exp_half(1, nm);
         }
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         tmem_wait_st();
@@ -468,6 +536,11 @@ __global__ void __launch_bounds__(kPerThreads, 1)
       ++it;
     }
     if (leader) bulk_wait_group_all();
+    if (cta == 0 && threadIdx.x == 0 && prm.acc_flag != nullptr) {
+      // a forward that did not zero the accumulator may have overwritten it
+      prm.acc_flag[0] = prm.acc_off;
+      prm.acc_flag[1] = (ok && prm.dq_acc != nullptr) ? prm.acc_len : 0ull;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -475,20 +548,6 @@ __global__ void __launch_bounds__(kPerThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-}
-
-// SM count of the current device (looked up once per device).
-inline int num_sms() {
-  constexpr int kMaxDev = 64;
-  static int n_sm[kMaxDev] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 1;
-  if (n_sm[dev] <= 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-    n_sm[dev] = n;
-  }
-  return n_sm[dev];
 }
 
 template <int D>
@@ -507,6 +566,8 @@ inline swa_status launch_fwd_persist_d(const FwdLaunch& f, cudaStream_t st) {
   p.n_items = f.B * (f.Hq / 2) * p.n_qtiles;
   p.scale_log2 = f.scale * 1.4426950408889634f;
   p.lse = f.lse; p.status = f.status; p.wait_limit_ns = f.wait_limit_ns;
+  p.dq_acc = f.dq_acc; p.acc_flag = f.acc_flag;
+  p.acc_off = f.acc_off; p.acc_len = f.acc_len;
   if (cudaFuncSetAttribute(fwd_tc_persist_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            L::kBytes) != cudaSuccess)
     return SWA_ERR_CUDA;
@@ -520,6 +581,9 @@ inline swa_status launch_fwd_persist_d(const FwdLaunch& f, cudaStream_t st) {
 inline swa_status launch_fwd_any2(const FwdLaunch& f, cudaStream_t st) {
   if ((f.Hq / f.Hkv) % 2 == 0)
     return f.d == 64 ? launch_fwd_persist_d<64>(f, st) : launch_fwd_persist_d<128>(f, st);
+  // This kernel leaves the dQ accumulator alone: drop any record of it.
+  if (f.acc_flag != nullptr && cudaMemsetAsync(f.acc_flag, 0, 2 * sizeof(unsigned long long), st) != cudaSuccess)
+    return SWA_ERR_CUDA;
   return launch_fwd(f, st);
 }
 

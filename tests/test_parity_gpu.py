@@ -118,3 +118,72 @@ def test_empty_problem_backward_zeroes_shared_gradients():
     assert st == swa.SWA_OK
     assert dgq.abs().sum().item() == 0 and dgk.abs().sum().item() == 0
     assert dve.abs().sum().item() == 0
+
+
+def _grads_bf16(p, g, o, lse, ws, ws_bytes=None, flags=0):
+    dev = torch.device("cuda:0")
+    prm = swa.make_params(p.B, p.T, p.Hq, p.Hkv, p.d, p.window, p.causal, 0.0, p.eps, p.ve_scale,
+                          p.vocab if p.ve else 0)
+    dq, dk, dv = torch.empty_like(g["q"]), torch.empty_like(g["k"]), torch.empty_like(g["v"])
+    dgq = torch.empty(p.d, device=dev)
+    dgk = torch.empty(p.d, device=dev)
+    dve = torch.empty(g["ve"].shape, device=dev) if p.ve else None
+    st = swa.swa_attn_bwd(prm, g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"], g["tok"], None,
+                          o, lse, g["dO"], dq, dk, dv, dgq, dgk, dve, ws, ws_bytes=ws_bytes,
+                          flags=flags)
+    assert st == swa.SWA_OK, swa.swa_strerror(st)
+    torch.cuda.synchronize()
+    out = {"dq": dq.cpu(), "dk": dk.cpu(), "dv": dv.cpu(), "dgq": dgq.cpu(), "dgk": dgk.cpu()}
+    if dve is not None:
+        out["dve"] = dve.cpu()
+    return out
+
+
+def test_second_backward_after_one_forward_clears_the_accumulator_again():
+    # The forward leaves the dQ accumulator zeroed for the backward that
+    # follows; the backward's main kernel marks it used, so a second backward
+    # on the same workspace must clear it itself.
+    p = CASES["ragged_gqa_ve"]
+    x = inputs(p, "bf16")
+    ref = run_oracle(p, x)
+    dev = torch.device("cuda:0")
+    g = {k: (t.to(dev) if t is not None else None) for k, t in x.items()}
+    o, lse, ws = swa.attention_forward(g["q"], g["k"], g["v"], g["gq"], g["gk"], window=p.window,
+                                       ve=g["ve"], tok=g["tok"], ve_scale=p.ve_scale)
+    for _ in range(2):
+        got = _grads_bf16(p, g, o, lse, ws, flags=swa.SWA_REUSE_PROLOGUE)
+        compare(got, ref, TOL["bf16"], keys=("dq", "dk", "dv", "dgq", "dgk", "dve"))
+
+
+@pytest.mark.parametrize("zeroing", [True, False])
+def test_forward_of_another_problem_in_between_keeps_the_backward_right(zeroing):
+    # Forward of X, then a forward of a larger problem Y in the same
+    # workspace (its prologue outputs land where X's accumulator lies), then
+    # the backward of X without prologue reuse. With zeroing=False the second
+    # forward gets a forward-only workspace size and must drop the record of
+    # X's zeroed accumulator; with zeroing=True it records its own, which
+    # does not name X's.
+    X = Problem(B=1, T=256, Hq=2, Hkv=1, d=128, window=100, gain_std=0.1)
+    Y = Problem(B=2, T=1024, Hq=4, Hkv=2, d=128, window=-1, gain_std=0.1)
+    dev = torch.device("cuda:0")
+    px = swa.make_params(X.B, X.T, X.Hq, X.Hkv, X.d, X.window, X.causal, 0.0, X.eps, X.ve_scale, 0)
+    py = swa.make_params(Y.B, Y.T, Y.Hq, Y.Hkv, Y.d, Y.window, Y.causal, 0.0, Y.eps, Y.ve_scale, 0)
+    nbytes = max(swa.swa_attn_workspace_size(px, 1), swa.swa_attn_workspace_size(py, 1))
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    xx, xy = inputs(X, "bf16"), inputs(Y, "bf16", layer=2)
+    gx = {k: (t.to(dev) if t is not None else None) for k, t in xx.items()}
+    gy = {k: (t.to(dev) if t is not None else None) for k, t in xy.items()}
+
+    def fwd(p, prm, g, ws_bytes):
+        o = torch.empty_like(g["q"])
+        lse = torch.empty(p.B, p.Hq, p.T, dtype=torch.float32, device=dev)
+        st = swa.swa_attn_fwd(prm, g["q"], g["k"], g["v"], g["gq"], g["gk"], None, None, None, o,
+                              lse, ws, ws_bytes=ws_bytes)
+        assert st == swa.SWA_OK, swa.swa_strerror(st)
+        return o, lse
+
+    ox, lx = fwd(X, px, gx, nbytes)
+    fwd(Y, py, gy, nbytes if zeroing else swa.swa_attn_workspace_size(py, 0))
+    got = _grads_bf16(X, gx, ox, lx, ws, ws_bytes=nbytes, flags=0)
+    assert swa.swa_attn_check_status(ws) == swa.SWA_OK
+    compare(got, run_oracle(X, xx), TOL["bf16"], keys=("dq", "dk", "dv", "dgq", "dgk"))

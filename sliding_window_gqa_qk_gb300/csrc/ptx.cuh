@@ -216,6 +216,13 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32
       : "memory");
 }
 
+// Bulk copy shared -> global (both 16-byte aligned, bytes a multiple of 16),
+// completion tracked by the bulk async-groups of the issuing thread.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

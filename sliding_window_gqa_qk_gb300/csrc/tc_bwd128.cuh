@@ -7,32 +7,30 @@
 //   S^T  = K Q_i^T            (TMEM [0,128): lanes = keys, columns = queries)
 //   dP^T = V dO_i^T           (TMEM [128,256))
 //   P^T  = scale exp2(S^T c - LSE log2 e)     -> bf16 into S^T's columns
-//   dS^T = P^T (dP^T - D)                     -> bf16 into dP^T's columns,
-//                                                and to shared memory
+//   dS^T = P^T (dP^T - D)                     -> bf16 to shared memory
 //   dV  += P^T dO_i           (A operand from TMEM)
-//   dK  += dS^T Q_i           (A operand from TMEM)
-//   dQ_i^T = K^T dS^T         (into dP^T's columns once dK has read dS^T)
+//   dQ_i^T = K^T dS^T         (into dP^T's columns)
+//   dK  += dS^T Q_i           (A operand dS^T from shared memory)
 // P^T and dS^T carry the softmax scale, so dK and dQ come out final and dV
 // is divided by it in the epilogue.
 //
 // Roles (12 warps): warpgroups 0 and 1 do the element-wise work, each on 64
-// of the step's 128 query columns (thread = key row = TMEM lane); warp 8 is
-// the TMA producer (K, V once; Q with LSE and D, and dO per step, two stages
-// each) and also issues the bulk reductions of the staged dQ boxes, so that
-// it can reload a Q stage as soon as they have been read; warp 9 issues the
-// MMAs from one thread, in the order
-//   S(0) dP(0) | dV(i) S(i+1) [dK(i) dQ(i)] dP(i+1) | ...
-// while the warpgroups run dS(i), P(i+1), drain(i): S^T(i+1) lands while
-// they compute dS^T(i), their exponentials of step i+1 overlap dK(i) and
-// dQ^T(i), and dP^T(i+1) waits only for the drain of dQ^T(i) from TMEM.
+// of the step's 128 query columns (thread = key row = TMEM lane): per step
+// P(i), dS(i), then the drain of dQ^T(i). Warp 8 is the TMA producer of K, V
+// (once) and of Q with LSE and D (two stages); warp 11 of dO (one stage,
+// reloaded as soon as dV of the step completed); warp 10 adds the staged dQ
+// boxes into the fp32 accumulator; warp 9 issues the MMAs from one thread,
+// in the order
+//   S(0) dP(0) | dV(i) [dQ(i) dK(i)] S(i+1) dP(i+1) | ...
+// dQ^T(i) comes before dK(i) so that its drain starts one product earlier;
+// dP^T(i+1) waits for that drain (it reuses the columns).
 // dQ^T(i) goes from TMEM to shared memory in two [32 queries][128] fp32
-// boxes per warpgroup, one in half of the step's Q stage (free once the dK
-// product has read it) and one in half of its dO stage (free once the dV
-// product has read it), and from there into the fp32 dQ accumulator by TMA
-// bulk reductions. Those reductions run at the rate the L2 accepts fp32
-// adds (about 6.6 TB/s over the whole GPU, about 21 bytes per clock per
-// SM), 64 KB per step: no element-wise work waits for them, only the
-// reloading of the two stages two steps later.
+// boxes per warpgroup, one in half of the dedicated staging buffer (free once
+// the previous step's boxes there were read) and one in half of the step's Q
+// stage (free once dK(i) has read it), and from there into the fp32 dQ
+// accumulator by TMA bulk reductions. Those run at the rate the L2 accepts
+// fp32 adds (about 6.6 TB/s over the whole GPU, about 21 bytes per clock per
+// SM), 64 KB per step.
 // Registers: the element-wise warpgroups run with 216 per thread, warpgroup
 // 2 with 72 (setmaxnreg; 384 x 168 at launch).
 //
@@ -49,13 +47,6 @@ namespace tc {
 constexpr int kB2Threads = 384;
 constexpr int kB2RegsSoftmax = 216;
 constexpr int kB2RegsOther = 72;
-// Issue S^T(i+1) right after dV(i) (true) or after dK(i), dQ^T(i) (false);
-// the element-wise warpgroups follow the same order.
-constexpr bool kB2EarlyS = false;
-// Stage the first dQ box of each warpgroup in the step's Q stage (true; the Q
-// stage is reloaded once it has been read) or in the dS^T buffer (false; the
-// next dS^T waits until it has been read).
-constexpr bool kB2StageInQ = true;
 static_assert(2 * 128 * kB2RegsSoftmax + 128 * kB2RegsOther <= kB2Threads * 168,
               "register split exceeds the launch's registers");
 
@@ -67,9 +58,10 @@ struct B2Cfg {
   static constexpr int oK = 0;
   static constexpr int oV = oK + kTile;
   static constexpr int oQ = oV + kTile;          // 2 stages
-  static constexpr int oG = oQ + 2 * kTile;      // dO, 2 stages
-  static constexpr int oS = oG + 2 * kTile;      // dS^T [128 keys][128 queries]
-  static constexpr int oL = oS + kTile;          // 2 stages x BQ floats: log2(scale) - LSE log2(e)
+  static constexpr int oG = oQ + 2 * kTile;      // dO, one stage
+  static constexpr int oS = oG + kTile;          // dS^T [128 keys][128 queries]
+  static constexpr int oX = oS + kTile;          // dQ staging: the second box of each warpgroup
+  static constexpr int oL = oX + kTile;          // 2 stages x BQ floats: log2(scale) - LSE log2(e)
   static constexpr int oD = oL + 2 * BQ * 4;     // 2 stages x BQ floats: -D
   static constexpr int oBar = oD + 2 * BQ * 4;   // mbarriers, TMEM base, abort flag
   static constexpr int kBytes = oBar + 256;
@@ -81,9 +73,9 @@ struct B2Cfg {
 enum {
   B2_KV = 0,
   B2_QFULL = 1,      // +stage: Q, LSE, D of a step landed
-  B2_QEMPTY = 3,     // +stage: the dK product of the step completed (Q stage reusable)
-  B2_GFULL = 5,      // +stage: dO landed
-  B2_GFREE = 7,      // +stage: the dO-stage dQ boxes of the step were read (dO stage reusable)
+  B2_QEMPTY = 3,     // +stage: the dQ boxes staged in the Q stage were read (Q stage reusable)
+  B2_GFULL = 5,      // dO landed
+  B2_GFREE = 7,      // the dV product of the step completed (dO stage reusable)
   B2_SFULL = 9,      // S^T in TMEM
   B2_DPFULL = 10,    // dP^T in TMEM
   B2_PREADY = 11,    // P^T in TMEM (8 warps)
@@ -91,10 +83,11 @@ enum {
   B2_DQFULL = 13,    // dQ^T in TMEM
   B2_DQFREE = 14,    // dQ^T read out of TMEM (8 warps)
   B2_STAGED = 15,    // the step's four dQ boxes are in shared memory (8 warps)
-  B2_DSFREE = 16,    // the dQ boxes staged in the dS^T buffer were read
+  B2_XFREE = 16,     // the dQ boxes in the staging buffer were read
   B2_DQREAD = 17,    // every dQ box of the CTA was read (once, at the end)
   B2_FINAL = 18,
-  B2_COUNT = 19
+  B2_DKDONE = 19,    // the dK product of the step completed (dQ-first order)
+  B2_COUNT = 20
 };
 
 // Visible query columns [clo, chi] of key row j among the 64 queries
@@ -179,9 +172,9 @@ __global__ void __launch_bounds__(kB2Threads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B2_QFULL + s), 1);
       mbar_init(bar(B2_QEMPTY + s), 1);
-      mbar_init(bar(B2_GFULL + s), 1);
-      mbar_init(bar(B2_GFREE + s), 1);
     }
+    mbar_init(bar(B2_GFULL), 1);
+    mbar_init(bar(B2_GFREE), 1);
     mbar_init(bar(B2_SFULL), 1);
     mbar_init(bar(B2_DPFULL), 1);
     mbar_init(bar(B2_PREADY), 8);
@@ -189,9 +182,10 @@ __global__ void __launch_bounds__(kB2Threads, 1)
     mbar_init(bar(B2_DQFULL), 1);
     mbar_init(bar(B2_DQFREE), 8);
     mbar_init(bar(B2_STAGED), 8);
-    mbar_init(bar(B2_DSFREE), 1);
+    mbar_init(bar(B2_XFREE), 1);
     mbar_init(bar(B2_DQREAD), 1);
     mbar_init(bar(B2_FINAL), 1);
+    mbar_init(bar(B2_DKDONE), 1);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -237,48 +231,44 @@ __global__ void __launch_bounds__(kB2Threads, 1)
       for (int s = 0; s < 2; ++s)
         if (last[s] >= 0) mbar_wait_drain(bar(B2_QFULL + s), (last[s] >> 1) & 1, prm.wait_limit_ns);
     } else if (warp == 11 && lane == 0 && n_it > 0) {
-      // ---------------- TMA producer of dO ----------------
+      // ---------------- TMA producer of dO (one stage) ----------------
       tma_prefetch_desc(&tmG);
-      int last[2] = {-1, -1};
+      int last = -1;
       for (int it = 0; it < n_it; ++it) {
-        const int s = it & 1;
         const int h = hk * G + it / nq;
         const int q0 = (qlo + it % nq) * BQ;
-        // the stage held dQ boxes of step it - 2: free once they were read
-        if (it >= 2 && !mbar_wait(bar(B2_GFREE + s), ((it >> 1) - 1) & 1, ctl)) break;
-        last[s] = it;
-        mbar_arrive_expect_tx(bar(B2_GFULL + s), C::kTile);
+        // the stage is free once dV of the previous step completed
+        if (it >= 1 && !mbar_wait(bar(B2_GFREE), (it - 1) & 1, ctl)) break;
+        last = it;
+        mbar_arrive_expect_tx(bar(B2_GFULL), C::kTile);
         for (int c = 0; c < 2; ++c)
-          tma_load_4d(sbase + C::oG + s * C::kTile + c * C::kHalf, &tmG, bar(B2_GFULL + s), 64 * c,
-                      q0, h, b);
+          tma_load_4d(sbase + C::oG + c * C::kHalf, &tmG, bar(B2_GFULL), 64 * c, q0, h, b);
       }
-      for (int s = 0; s < 2; ++s)
-        if (last[s] >= 0) mbar_wait_drain(bar(B2_GFULL + s), (last[s] >> 1) & 1, prm.wait_limit_ns);
+      if (last >= 0) mbar_wait_drain(bar(B2_GFULL), last & 1, prm.wait_limit_ns);
     } else if (warp == 10 && lane == 0 && n_it > 0) {
       // ---------------- dQ reducer ----------------
       // Step m's dQ boxes, for each warpgroup X: queries qb.. in half X of the
-      // dS^T buffer, qb+32.. in half X of the step's dO stage, added into the
-      // fp32 accumulator by bulk reductions. These run at the rate the L2
+      // step's Q stage, qb+32.. in half X of the staging buffer, added into
+      // the fp32 accumulator by bulk reductions. These run at the rate the L2
       // accepts fp32 adds (about 6.6 TB/s over the whole GPU, about 21 bytes
-      // per clock per SM, so about 3000 clocks per step); the buffers are
-      // handed back as soon as their boxes have been read.
+      // per clock per SM, so about 3000 clocks per step); each buffer is
+      // handed back as soon as its boxes have been read, the Q stage first.
       tma_prefetch_desc(&tmDQ);
       for (int m = 0; m < n_it; ++m) {
         if (!mbar_wait(bar(B2_STAGED), m & 1, ctl)) break;
         const int h = hk * G + m / nq;
         const int q0 = (qlo + m % nq) * BQ;
-        const uint32_t boxA = kB2StageInQ ? sbase + C::oQ + (m & 1) * C::kTile : sbase + C::oS;
         for (int X = 0; X < 2; ++X)
-          tma_reduce_add_3d(&tmDQ, boxA + X * C::kHalf, 0, q0 + 64 * X, b * prm.Hq + h);
+          tma_reduce_add_3d(&tmDQ, sbase + C::oQ + (m & 1) * C::kTile + X * C::kHalf, 0, q0 + 64 * X,
+                            b * prm.Hq + h);
         bulk_commit_group();
         for (int X = 0; X < 2; ++X)
-          tma_reduce_add_3d(&tmDQ, sbase + C::oG + (m & 1) * C::kTile + X * C::kHalf, 0,
-                            q0 + 64 * X + 32, b * prm.Hq + h);
+          tma_reduce_add_3d(&tmDQ, sbase + C::oX + X * C::kHalf, 0, q0 + 64 * X + 32, b * prm.Hq + h);
         bulk_commit_group();
         bulk_wait_group_read<1>();
-        mbar_arrive(bar(kB2StageInQ ? B2_QEMPTY + (m & 1) : B2_DSFREE));
+        mbar_arrive(bar(B2_QEMPTY + (m & 1)));
         bulk_wait_group_read<0>();
-        mbar_arrive(bar(B2_GFREE + (m & 1)));
+        mbar_arrive(bar(B2_XFREE));
       }
       bulk_wait_group_all();
       mbar_arrive(bar(B2_DQREAD));
@@ -291,10 +281,11 @@ __global__ void __launch_bounds__(kB2Threads, 1)
       const uint64_t dVk = sdesc_sw128(sbase + C::oV, 16, 1024);
       const uint64_t dKmn = sdesc_sw128(sbase + C::oK, C::kHalf, 1024);
       const uint64_t dQk0 = sdesc_sw128(sbase + C::oQ, 16, 1024);
-      const uint64_t dGk0 = sdesc_sw128(sbase + C::oG, 16, 1024);
+      const uint64_t dGk = sdesc_sw128(sbase + C::oG, 16, 1024);
       const uint64_t dQmn0 = sdesc_sw128(sbase + C::oQ, C::kHalf, 1024);
-      const uint64_t dGmn0 = sdesc_sw128(sbase + C::oG, C::kHalf, 1024);
+      const uint64_t dGmn = sdesc_sw128(sbase + C::oG, C::kHalf, 1024);
       const uint64_t dSmn = sdesc_sw128(sbase + C::oS, C::kHalf, 1024);
+      const uint64_t dSk = sdesc_sw128(sbase + C::oS, 16, 1024);
       // K-major operands: K step kk is 32 bytes into a row of its 64-column region.
       auto issue_S = [&](int i) {    // S^T = K Q_i^T
         const uint64_t qd = sdesc_add(dQk0, (i & 1) * C::kTile);
@@ -306,38 +297,37 @@ __global__ void __launch_bounds__(kB2Threads, 1)
         umma_commit(bar(B2_SFULL));
       };
       auto issue_dP = [&](int i) {   // dP^T = V dO_i^T
-        const uint64_t gd = sdesc_add(dGk0, (i & 1) * C::kTile);
         static_for<0, 8>([&](auto kc) {
           constexpr int kk = decltype(kc)::value;
           constexpr uint32_t off = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;
-          umma_ss_imm<idN, off, off>(tmem + cDP, dVk, gd, kk > 0, 1u);
+          umma_ss_imm<idN, off, off>(tmem + cDP, dVk, dGk, kk > 0, 1u);
         });
         umma_commit(bar(B2_DPFULL));
       };
       // A operands from TMEM: K step kk (16 queries) is 8 columns; queries
       // 0-63 sit in the first 32 columns of warpgroup 0's 64, queries 64-127
       // in warpgroup 1's. MN-major B: K step kk is 16 rows (2048 bytes) on.
-      auto issue_dV = [&](int i) {   // dV += P^T dO_i
-        const uint64_t gd = sdesc_add(dGmn0, (i & 1) * C::kTile);
+      auto issue_dV = [&](int i) {   // dV += P^T dO_i; then the dO stage is free
         static_for<0, 8>([&](auto kc) {
           constexpr int kk = decltype(kc)::value;
-          umma_ts_imm<idKV, (kk >> 2) * 64 + (kk & 3) * 8, kk * 128>(tmem + cDV, tmem + cS, gd,
+          umma_ts_imm<idKV, (kk >> 2) * 64 + (kk & 3) * 8, kk * 128>(tmem + cDV, tmem + cS, dGmn,
                                                                       (i > 0 || kk > 0), 1u);
         });
+        umma_commit(bar(B2_GFREE));
       };
-      auto issue_dKdQ = [&](int i) {   // dK += dS^T Q_i; dQ_i^T = K^T dS^T
-        const uint64_t qd = sdesc_add(dQmn0, (i & 1) * C::kTile);
-        static_for<0, 8>([&](auto kc) {
-          constexpr int kk = decltype(kc)::value;
-          umma_ts_imm<idKV, (kk >> 2) * 64 + (kk & 3) * 8, kk * 128>(tmem + cDK, tmem + cDP, qd,
-                                                                      (i > 0 || kk > 0), 1u);
-        });
-        if (!kB2StageInQ) umma_commit(bar(B2_QEMPTY + (i & 1)));
+      auto issue_dQdK = [&](int i) {   // dQ_i^T = K^T dS^T, then dK += dS^T Q_i (A from shared memory)
         static_for<0, 8>([&](auto kc) {
           constexpr int kk = decltype(kc)::value;
           umma_ss_imm<idQ, kk * 128, kk * 128>(tmem + cDP, dKmn, dSmn, kk > 0, 1u);
         });
         umma_commit(bar(B2_DQFULL));
+        const uint64_t qd = sdesc_add(dQmn0, (i & 1) * C::kTile);
+        static_for<0, 8>([&](auto kc) {
+          constexpr int kk = decltype(kc)::value;
+          constexpr uint32_t aoff = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;
+          umma_ss_imm<idKV, aoff, kk * 128>(tmem + cDK, dSk, qd, (i > 0 || kk > 0), 1u);
+        });
+        umma_commit(bar(B2_DKDONE));
       };
       bool ok = mbar_wait(bar(B2_KV), 0, ctl) && mbar_wait(bar(B2_QFULL), 0, ctl);
       if (ok) {
@@ -356,23 +346,17 @@ __global__ void __launch_bounds__(kB2Threads, 1)
         if (!(ok = mbar_wait(bar(B2_PREADY), ph, ctl))) break;
         tc_fence_after();
         issue_dV(i);
-        if (kB2EarlyS && more) {
-          // S^T(i+1) overwrites P^T(i), which dV(i) (issued before) reads.
-          if (!(ok = mbar_wait(bar(B2_QFULL + s1), ph1, ctl))) break;
-          tc_fence_after();
-          issue_S(i + 1);
-        }
         if (!(ok = mbar_wait(bar(B2_DSREADY), ph, ctl))) break;
         tc_fence_after();
-        issue_dKdQ(i);
-        if (!kB2EarlyS && more) {
+        issue_dQdK(i);
+        if (more) {
           if (!(ok = mbar_wait(bar(B2_QFULL + s1), ph1, ctl))) break;
           tc_fence_after();
           issue_S(i + 1);
         }
         if (more) {
           // dP^T(i+1) overwrites dQ^T(i): wait until it was read out.
-          if (!(ok = mbar_wait(bar(B2_DQFREE), ph, ctl) && mbar_wait(bar(B2_GFULL + s1), ph1, ctl)))
+          if (!(ok = mbar_wait(bar(B2_DQFREE), ph, ctl) && mbar_wait(bar(B2_GFULL), (i + 1) & 1, ctl)))
             break;
           tc_fence_after();
           issue_dP(i + 1);
@@ -392,9 +376,7 @@ __global__ void __launch_bounds__(kB2Threads, 1)
     const uint32_t tS = tmem + cS + 64 * X + lane_off;     // S^T, then P^T in its first 32 columns
     const uint32_t tDP = tmem + cDP + 64 * X + lane_off;   // dP^T, then dS^T, then dQ^T
     const uint32_t sSx = sbase + C::oS + X * C::kHalf;     // dS^T region X
-    // Per step the order is dS(i), P(i+1), drain(i) (kB2EarlyS): the
-    // exponentials of the next step run while the tensor core computes dK(i)
-    // and dQ^T(i); otherwise P(i), dS(i), drain(i).
+    // Per step the order is P(i), dS(i), drain(i).
     uint32_t sr[2][32];   // P^T of the step whose dS^T comes next (fp32)
     // ---- P^T(i) = scale exp2(S^T c - LSE log2 e), zero off the band ----
     auto p_phase = [&](int i) -> bool {
@@ -468,14 +450,11 @@ __global__ void __launch_bounds__(kB2Threads, 1)
       }
       uint32_t pk[32];
       pack64(dp, pk);
-      tmem_st32(tDP, pk);   // A operand of dK
       // MN-major B operand of dQ^T, in this warpgroup's half of the dS^T
       // buffer, once the dQ box of step i - 1 staged there has been read
-      if (!kB2StageInQ && i > 0 && !mbar_wait_warp(bar(B2_DSFREE), (i - 1) & 1, ctl)) return false;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch)
         st_sw128_chunk(sSx, kBK, t, ch, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-      tmem_wait_st();
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -498,28 +477,23 @@ __global__ void __launch_bounds__(kB2Threads, 1)
       // boxes [32 queries][128] fp32: queries qb.. in this warpgroup's half of
       // the dS^T buffer (last read by dQ^T(i)), qb+32.. in half X of the dO
       // stage (last read by dV(i)); both products completed before DQFULL
-      const uint32_t box0 = kB2StageInQ ? sbase + C::oQ + s * C::kTile + X * C::kHalf : sSx;
-      const uint32_t box1 = sbase + C::oG + s * C::kTile + X * C::kHalf;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) st_shared_f32(box0 + e * 512 + t * 4, __uint_as_float(dq[0][e]));
+      const uint32_t box0 = sbase + C::oQ + s * C::kTile + X * C::kHalf;
+      const uint32_t box1 = sbase + C::oX + X * C::kHalf;
+      // box1 once the reducer has read the previous step's boxes out of the
+      // staging buffer; box0 once dK(i), which reads the Q stage, completed
+      if (i > 0 && !mbar_wait_warp(bar(B2_XFREE), (i - 1) & 1, ctl)) return false;
 #pragma unroll
       for (int e = 0; e < 32; ++e) st_shared_f32(box1 + e * 512 + t * 4, __uint_as_float(dq[1][e]));
+      if (!mbar_wait_warp(bar(B2_DKDONE), i & 1, ctl)) return false;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) st_shared_f32(box0 + e * 512 + t * 4, __uint_as_float(dq[0][e]));
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B2_STAGED));   // the producer reduces them
       return true;
     };
     bool ok = n_it > 0;
-    if (kB2EarlyS) {
-      ok = ok && p_phase(0);
-      for (int i = 0; i < n_it && ok; ++i) {
-        ok = ds_phase(i);
-        if (ok && i + 1 < n_it) ok = p_phase(i + 1);
-        ok = ok && drain(i);
-      }
-    } else {
-      for (int i = 0; i < n_it && ok; ++i) ok = p_phase(i) && ds_phase(i) && drain(i);
-    }
+    for (int i = 0; i < n_it && ok; ++i) ok = p_phase(i) && ds_phase(i) && drain(i);
     // All dQ boxes are read before the epilogue reuses the stage buffers as
     // scratch.
     const bool final_ok = ok && n_it > 0 && mbar_wait_warp(bar(B2_DQREAD), 0, ctl) &&

@@ -10,10 +10,7 @@
 //               row t (TMEM lane t), keeps the running max m and sum l,
 //               rescales its O row only when m grows by more than 2^8, and
 //               writes P = exp2(S c - m) as bf16 pairs back into S's columns
-//               of TMEM, where the PV MMA reads it as its A operand. After an
-//               item's first tile the exponentials use the running m at
-//               once (the tile's own maximum is reduced alongside and P is
-//               recomputed only when it exceeds m by more than 2^8).
+//               of TMEM, where the PV MMA reads it as its A operand.
 // Across items: the Q tiles of the next item load as soon as the last S MMA
 // of the current one completed, so the next item's first S products run
 // while the softmax warpgroups finish the current item's epilogue (O / l
@@ -51,7 +48,9 @@ struct FwdPerSmem {
   static constexpr int kV0 = kK0 + 2 * kTile; // 2 stages
   static constexpr int kO0 = kV0 + 2 * kTile; // O staging: one 64-column half per warpgroup
   static constexpr int kBar = kO0 + 2 * kHalf;
-  static constexpr int kBytes = kBar + 256;
+  static constexpr int kZero = kBar + 256;     // zeros, the source of the dQ-accumulator clears
+  static constexpr int kZeroBytes = 2048;
+  static constexpr int kBytes = kZero + kZeroBytes;
   // Dynamic shared memory only (no static shared variables), so its base is
   // the start of the CTA's window and 1024-byte aligned.
   static_assert(kBytes <= 232448, "shared memory budget");
@@ -159,6 +158,10 @@ __global__ void __launch_bounds__(kPerThreads, 1)
     tmem_alloc(smem_u32(tmem_base_sh), 512);
     tmem_relinquish();
   }
+  if (prm.dq_acc != nullptr && threadIdx.x < L::kZeroBytes / 16) {
+    reinterpret_cast<uint4*>(smem + L::kZero)[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
+    fence_async_smem();   // visible to the bulk copies that read it
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -207,23 +210,24 @@ __global__ void __launch_bounds__(kPerThreads, 1)
             tma_load_4d_w(sbase + L::kV0 + s * L::kTile + c * L::kHalf, &tmV, bar(QP_VFULL + s), 64 * c,
                           k0, hk, I.b, one);
           last_v[s] = g;
-          if (prm.dq_acc != nullptr) {
+          if (prm.dq_acc != nullptr && one) {
             // A share of the item's rows of the backward's dQ accumulator
-            // (both heads, 128 rows, D floats each), spread over its key
-            // tiles: 512 bytes per warp store, lane = 16 bytes.
-            constexpr int kUnits = 2 * kBM * D * 4 / 512;
-            constexpr int kRowsPerUnit = 512 / (D * 4);
-            const int u1 = (j + 1) * kUnits / I.n_tiles;
-            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int u = j * kUnits / I.n_tiles; u < u1; ++u) {
-              const int row = u * kRowsPerUnit + lane / (32 / kRowsPerUnit);   // 0 .. 2 kBM - 1
-              const int t = I.q0 + (row % kBM);
-              if (t < prm.T) {
-                float4* acc = reinterpret_cast<float4*>(
-                    prm.dq_acc + ((static_cast<long long>(I.b) * prm.Hq + hA + row / kBM) * prm.T + t) * D);
-                acc[lane % (32 / kRowsPerUnit)] = z;
-              }
+            // (per head one contiguous run of up to 128 rows of D floats),
+            // spread over its key tiles, as bulk copies of the zero block.
+            const int nrows = prm.T - I.q0 < kBM ? prm.T - I.q0 : kBM;
+            const uint32_t run = static_cast<uint32_t>(nrows) * D * 4;
+            const int per_head = static_cast<int>((run + L::kZeroBytes - 1) / L::kZeroBytes);
+            const int total = 2 * per_head;
+            const int c1 = (j + 1) * total / I.n_tiles;
+            for (int cpy = j * total / I.n_tiles; cpy < c1; ++cpy) {
+              const int hx = cpy / per_head;
+              const uint32_t off = static_cast<uint32_t>(cpy - hx * per_head) * L::kZeroBytes;
+              const uint32_t bytes = run - off < static_cast<uint32_t>(L::kZeroBytes) ? run - off
+                                                                                     : L::kZeroBytes;
+              float* dst = prm.dq_acc + ((static_cast<long long>(I.b) * prm.Hq + hA + hx) * prm.T + I.q0) * D;
+              bulk_store(reinterpret_cast<uint8_t*>(dst) + off, sbase + L::kZero, bytes);
             }
+            bulk_commit_group();
           }
         }
         ++it;
@@ -233,6 +237,7 @@ __global__ void __launch_bounds__(kPerThreads, 1)
         if (last_k[s] >= 0) mbar_wait_drain(bar(QP_KFULL + s), (last_k[s] >> 1) & 1, prm.wait_limit_ns);
         if (last_v[s] >= 0) mbar_wait_drain(bar(QP_VFULL + s), (last_v[s] >> 1) & 1, prm.wait_limit_ns);
       }
+      if (one) bulk_wait_group_all();   // the zero-block copies have finished
     } else if (warp == 9) {
       // ---------------- MMA issuer (whole warp, lane 0 issues) ----------------
       constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0, 0);
@@ -366,118 +371,77 @@ __global__ void __launch_bounds__(kPerThreads, 1)
             }
           }
         }
-        // S in two halves of 64 columns: the second half's TMEM load runs
-        // while the first half is masked and reduced.
         uint32_t sr[4][32];
-        tmem_ld32(tS, sr[0]);
-        tmem_ld32(tS + 32, sr[1]);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
         tmem_wait_ld(sr[0]);
         reg_fence(sr[1]);
-        tmem_ld32(tS + 64, sr[2]);
-        tmem_ld32(tS + 96, sr[3]);
-        auto mask_half = [&](int hf) {
+        reg_fence(sr[2]);
+        reg_fence(sr[3]);
+        if (!full) {
 #pragma unroll
-          for (int cc = 2 * hf; cc < 2 * hf + 2; ++cc)
+          for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               const int col = cc * 32 + e;
               if (col < clo || col > chi) sr[cc][e] = __float_as_uint(-INFINITY);
             }
-        };
-        // Maximum of one half: four independent three-input chains.
-        auto max_half = [&](int hf) -> float {
-          float mq[4];
+        }
+        // Row maximum: eight independent three-input chains, then a short tree.
+        float mq[8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int cc = 2 * hf + (q >> 1), e0 = (q & 1) * 16;
-            float a = fmax3(__uint_as_float(sr[cc][e0]), __uint_as_float(sr[cc][e0 + 1]),
-                            __uint_as_float(sr[cc][e0 + 2]));
+        for (int q = 0; q < 8; ++q) {
+          const int cc = q >> 1, e0 = (q & 1) * 16;
+          float a = fmax3(__uint_as_float(sr[cc][e0]), __uint_as_float(sr[cc][e0 + 1]),
+                          __uint_as_float(sr[cc][e0 + 2]));
 #pragma unroll
-            for (int e = 3; e < 15; e += 2)
-              a = fmax3(a, __uint_as_float(sr[cc][e0 + e]), __uint_as_float(sr[cc][e0 + e + 1]));
-            mq[q] = fmaxf(a, __uint_as_float(sr[cc][e0 + 15]));
+          for (int e = 3; e < 15; e += 2)
+            a = fmax3(a, __uint_as_float(sr[cc][e0 + e]), __uint_as_float(sr[cc][e0 + e + 1]));
+          mq[q] = fmaxf(a, __uint_as_float(sr[cc][e0 + 15]));
+        }
+        const float mx = fmaxf(fmax3(mq[0], mq[1], mq[2]),
+                               fmax3(fmax3(mq[3], mq[4], mq[5]), mq[6], mq[7]));
+        const float mt = mx * c;
+        float alpha = 1.f;
+        bool rescale_o = false;
+        if (mt > m + kRescaleLog2) {     // also the first finite maximum (m = -inf)
+          if (m != -INFINITY) {
+            alpha = ex2_approx(m - mt);
+            rescale_o = true;
           }
-          return fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-        };
-        // P = exp2(S c - m) of one half as bf16 pairs into S's columns
-        // [32 hf, 32 hf + 32); scale-and-shift and row sum two lanes per
-        // instruction.
-        float ls[8];
-        auto exp_half = [&](int hf, float nm) {
+          l *= alpha;
+          m = mt;
+        }
+        // PV_X of the previous tile has completed: the commit that signalled
+        // this S covers it (only within the item: O is not rescaled at j = 0).
+        if (__any_sync(0xffffffffu, rescale_o)) {
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t orr[32];
+            tmem_ld32(tO + cc * 32, orr);
+            tmem_wait_ld(orr);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+            tmem_st32(tO + cc * 32, orr);
+          }
+        }
+        // P = exp2(S c - m) as bf16 pairs into S's first 64 columns; the
+        // scale-and-shift and the row sum run two lanes per instruction.
+        const float nm = (m == -INFINITY) ? 0.f : -m;
+        float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
           uint32_t pk[32];
 #pragma unroll
           for (int w2 = 0; w2 < 32; ++w2) {
-            const int cc = hf * 2 + (w2 >> 4), e = (w2 & 15) * 2;
+            const int cc = half * 2 + (w2 >> 4), e = (w2 & 15) * 2;
             float x0, x1;
             ffma2(x0, x1, __uint_as_float(sr[cc][e]), __uint_as_float(sr[cc][e + 1]), c, c, nm, nm);
             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             fadd2_acc(ls[2 * (w2 & 3)], ls[2 * (w2 & 3) + 1], p0, p1);
             pk[w2] = pack_bf16x2(p0, p1);
           }
-          tmem_st32(tS + hf * 32, pk);
-        };
-#pragma unroll
-        for (int u = 0; u < 8; ++u) ls[u] = 0.f;
-        float mx;
-        bool redo;
-        if (j > 0) {
-          // Exponentials against the running maximum m straight away; the
-          // tile's own maximum is reduced alongside, and only if it exceeds
-          // m by more than 2^8 (rare after the first tile) is P recomputed
-          // against the new maximum below. Either way P, l and O refer to
-          // the same m, so the result is exact.
-          const float nm0 = (m == -INFINITY) ? 0.f : -m;
-          if (!full) mask_half(0);
-          const float mx0 = max_half(0);
-          exp_half(0, nm0);
-          tmem_wait_ld(sr[2]);
-          reg_fence(sr[3]);
-          if (!full) mask_half(1);
-          mx = fmaxf(mx0, max_half(1));
-          exp_half(1, nm0);
-          redo = __any_sync(0xffffffffu, mx * c > m + kRescaleLog2);
-        } else {
-          tmem_wait_ld(sr[2]);
-          reg_fence(sr[3]);
-          if (!full) {
-            mask_half(0);
-            mask_half(1);
-          }
-          mx = fmaxf(max_half(0), max_half(1));
-          redo = true;
-        }
-        if (redo) {
-          if (j > 0) tmem_wait_st();   // the first P stores land before they are redone
-          const float mt = mx * c;
-          float alpha = 1.f;
-          bool rescale_o = false;
-          if (mt > m + kRescaleLog2) {     // also the first finite maximum (m = -inf)
-            if (m != -INFINITY) {
-              alpha = ex2_approx(m - mt);
-              rescale_o = true;
-            }
-            l *= alpha;
-            m = mt;
-          }
-          // PV_X of the previous tile has completed: the commit that
-          // signalled this S covers it (only within the item: O is not
-          // rescaled at j = 0).
-          if (__any_sync(0xffffffffu, rescale_o)) {
-#pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-              uint32_t orr[32];
-              tmem_ld32(tO + cc * 32, orr);
-              tmem_wait_ld(orr);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-              tmem_st32(tO + cc * 32, orr);
-            }
-          }
-          const float nm = (m == -INFINITY) ? 0.f : -m;
-#pragma unroll
-          for (int u = 0; u < 8; ++u) ls[u] = 0.f;
-          exp_half(0, nm);
-          exp_half(1, nm);
+          tmem_st32(tS + half * 32, pk);
         }
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         tmem_wait_st();

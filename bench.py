@@ -186,6 +186,7 @@ WORKLOADS = {
     "stack": WORKLOAD,
     "s_layer": "one S layer (B=16, T=2048, Hq=6, Hkv=3, d=128, window 1024, no VE)",
     "l_layer": "one L layer (B=16, T=2048, Hq=6, Hkv=3, d=128, full causal, no VE)",
+    "stack_rope": WORKLOAD[:-1] + ", rotary tables (base 10000) fused before the QK-norm)",
 }
 
 
@@ -201,6 +202,14 @@ class Stack:
     def __init__(self, swa, dev, workload="stack"):
         self.swa = swa
         self.dev = dev
+        self.rope = None
+        if workload == "stack_rope":
+            # standard rotary tables: angle t * 10000^(-2c/d), positions 0..T-1
+            inv = 10000.0 ** (-torch.arange(D // 2, dtype=torch.float64) * 2.0 / D)
+            ang = torch.arange(T, dtype=torch.float64)[:, None] * inv[None, :]
+            self.rope_t = (torch.cos(ang).float().to(dev).contiguous(),
+                           torch.sin(ang).float().to(dev).contiguous())
+            self.rope = swa.make_rope(*self.rope_t)
         self.sched = schedule_for(workload, swa.swa_sssl_window, swa.swa_has_ve)
         self.layers = []
         for li, (W, ve) in enumerate(self.sched):
@@ -224,17 +233,24 @@ class Stack:
 
     def fwd(self, L):
         g = L["g"]
-        st = self.swa.swa_attn_fwd(L["prm"], g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"],
-                                   g["tok"], None, L["o"], L["lse"], L["ws"])
+        if self.rope is not None:
+            st = self.swa.swa_attn_fwd_rope(L["prm"], self.rope, g["q"], g["k"], g["v"], g["gq"], g["gk"],
+                                            g["ve"], g["tok"], None, L["o"], L["lse"], L["ws"])
+        else:
+            st = self.swa.swa_attn_fwd(L["prm"], g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"],
+                                       g["tok"], None, L["o"], L["lse"], L["ws"])
         if st != 0:
             raise self.swa.SwaError(st, "swa_attn_fwd")
 
     def bwd(self, L, stage):
         g = L["g"]
-        st = self.swa.swa_attn_bwd(L["prm"], g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"],
-                                   g["tok"], None, L["o"], L["lse"], g["dO"], L["dq"], L["dk"],
-                                   L["dv"], L["dgq"], L["dgk"], L["dve"], L["ws"],
-                                   flags=self.swa.SWA_REUSE_PROLOGUE | stage)
+        args = (g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"], g["tok"], None, L["o"], L["lse"],
+                g["dO"], L["dq"], L["dk"], L["dv"], L["dgq"], L["dgk"], L["dve"], L["ws"])
+        if self.rope is not None:
+            st = self.swa.swa_attn_bwd_rope(L["prm"], self.rope, *args,
+                                            flags=self.swa.SWA_REUSE_PROLOGUE | stage)
+        else:
+            st = self.swa.swa_attn_bwd(L["prm"], *args, flags=self.swa.SWA_REUSE_PROLOGUE | stage)
         if st != 0:
             raise self.swa.SwaError(st, "swa_attn_bwd")
 

@@ -152,6 +152,42 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
                         void* workspace, size_t ws_bytes, unsigned flags, void* stream);
 
 /*
+ * Rotary position embedding fused into the QK-norm prologue (rotation first,
+ * then the norm, so the norm comes right before the dot product, as in the
+ * autoresearch train.py walkthrough post, model paragraph; the Administrator
+ * & Developer Guide §8.2.1 model table, "Rotary embeddings" row, has the
+ * cos / sin tables precomputed once by the caller). The pages print neither
+ * the channel pairing nor the sign; this library pairs channel c with
+ * c + d/2 and turns the pair of position t by the angle of row t, column c:
+ *   y_c       =  x_c cos[t][c] + x_{c+d/2} sin[t][c]
+ *   y_{c+d/2} = -x_c sin[t][c] + x_{c+d/2} cos[t][c]        (c < d/2)
+ * Tables: fp32, row-major [rows][d/2], device pointers, 16-byte aligned,
+ * rows >= T (row t is position t). cos and sin both NULL (or rope NULL):
+ * no rotation, identical to swa_attn_fwd / swa_attn_bwd.
+ */
+typedef struct {
+  const float* cos;
+  const float* sin;
+  int rows;
+} swa_rope;
+
+/* swa_attn_fwd with the rotary tables (arguments otherwise identical). */
+swa_status swa_attn_fwd_rope(const swa_params* p, const swa_rope* rope, const void* q, const void* k,
+                             const void* v, const float* gq, const float* gk, const void* ve,
+                             const int32_t* tok, const float* ve_gate, void* o, float* lse,
+                             void* workspace, size_t ws_bytes, unsigned flags, void* stream);
+
+/* swa_attn_bwd with the rotary tables: dq and dk are the gradients of the
+ * unrotated q and k (the transposed rotation of the norm backward's result).
+ * A backward with SWA_REUSE_PROLOGUE needs the same tables as its forward. */
+swa_status swa_attn_bwd_rope(const swa_params* p, const swa_rope* rope, const void* q, const void* k,
+                             const void* v, const float* gq, const float* gk, const void* ve,
+                             const int32_t* tok, const float* ve_gate, const void* o,
+                             const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                             float* dgq, float* dgk, float* dve, void* workspace, size_t ws_bytes,
+                             unsigned flags, void* stream);
+
+/*
  * Forward without a caller-provided workspace: the same computation and
  * outputs as swa_attn_fwd (flags 0), but its scratch (QK-norm / VE-mix
  * outputs and the status word) lives in one fixed array of

@@ -32,6 +32,10 @@ Readings where the pages are silent (each one is listed in the design doc):
   * VE mix: v_eff = v + ve_scale * gate[b, t, hkv] * VE[tok[b, t], hkv*d:(hkv+1)*d]
     (gate None = 1). The pages' learned gate is an input of this function.
   * Layout: q [B, T, Hq, d], k/v [B, T, Hkv, d], LSE [B, Hq, T] in natural log.
+  * Rotary (optional, ``rope=(cos, sin)`` tables [>= T, d/2] given by the
+    caller): applied to q and k before the norm, pairing channel c with
+    c + d/2 and turning the pair by the angle of table entry [t, c]:
+    y_c = x_c cos + x_{c+d/2} sin, y_{c+d/2} = -x_c sin + x_{c+d/2} cos.
 
 parity pinned: every function here is checked in ``tests/test_oracle.py``
 against the pages' worked examples, closed forms, invariants, brute force,
@@ -47,6 +51,8 @@ import numpy as np
 __all__ = [
     "sssl_window",
     "has_ve",
+    "rotary",
+    "rotary_backward",
     "rms_norm",
     "rms_norm_backward",
     "ve_mix",
@@ -98,6 +104,37 @@ def has_ve(layer: int, n_layer: int) -> bool:
 # ----------------------------------------------------------------------------
 # QK-norm and the value-embedding mix
 # ----------------------------------------------------------------------------
+
+def rotary(x: np.ndarray, cos, sin, positions=None) -> np.ndarray:
+    """Rotary position embedding over the last axis of x [..., T or len(positions), H, d].
+
+    [Guide] §8.2.1, model table, "Rotary embeddings" row: the cos / sin tables
+    are precomputed once for a length beyond the sequence and applied to q and
+    k; [Post] model paragraph: the QK-norm comes right before the dot product,
+    so the rotation comes first. The pages print neither the pairing nor the
+    sign; the reading taken here pairs channel c with c + d/2 and turns each
+    pair by the table's angle for its position:
+      y_c       =  x_c cos[t, c] + x_{c+d/2} sin[t, c]
+      y_{c+d/2} = -x_c sin[t, c] + x_{c+d/2} cos[t, c]
+    The position axis is axis -3 (rows t of the tables, or the rows
+    ``positions``).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    half = x.shape[-1] // 2
+    n = x.shape[-3]
+    pos = np.arange(n) if positions is None else np.asarray(positions, dtype=np.int64)
+    c = np.asarray(cos, dtype=np.float64)[pos][:, None, :]    # [n, 1, d/2]
+    sn = np.asarray(sin, dtype=np.float64)[pos][:, None, :]
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c + x2 * sn, -x1 * sn + x2 * c], axis=-1)
+
+
+def rotary_backward(dy: np.ndarray, cos, sin, positions=None) -> np.ndarray:
+    """Gradient of ``rotary``: the transposed rotation of every pair,
+      dx_c = dy_c cos - dy_{c+d/2} sin,  dx_{c+d/2} = dy_c sin + dy_{c+d/2} cos,
+    i.e. the rotation by the opposite angle."""
+    return rotary(dy, cos, -np.asarray(sin, dtype=np.float64), positions)
+
 
 def rms_norm(x: np.ndarray, g, eps: float):
     """RMSNorm over the last axis: y = g * x / sqrt(mean(x^2) + eps).
@@ -180,9 +217,17 @@ def band_mask(rows, T: int, window: int, causal: bool, keys=None) -> np.ndarray:
     return m
 
 
-def _prep(q, k, v, gq, gk, eps, ve, tok, gate, ve_scale):
-    qn, rq = rms_norm(q, gq, eps)
-    kn, rk = rms_norm(k, gk, eps)
+def _rot(x, rope, positions=None):
+    return x if rope is None else rotary(x, rope[0], rope[1], positions)
+
+
+def _unrot(dx, rope, positions=None):
+    return dx if rope is None else rotary_backward(dx, rope[0], rope[1], positions)
+
+
+def _prep(q, k, v, gq, gk, eps, ve, tok, gate, ve_scale, rope=None):
+    qn, rq = rms_norm(_rot(q, rope), gq, eps)
+    kn, rk = rms_norm(_rot(k, rope), gk, eps)
     v_eff = ve_mix(v, ve, tok, gate, ve_scale)
     return qn, kn, v_eff
 
@@ -213,10 +258,11 @@ def _softmax_rows(S: np.ndarray, M: np.ndarray):
 
 def attention_forward(q, k, v, gq=None, gk=None, *, window: int, causal: bool = True,
                       scale=None, eps: float = 1e-6, ve=None, tok=None, gate=None,
-                      ve_scale: float = 0.5, row_chunk: int = 1024):
+                      ve_scale: float = 0.5, row_chunk: int = 1024, rope=None):
     """Forward of the attention block: returns (o [B,T,Hq,d], lse [B,Hq,T]).
 
-    Steps in the pages' order: QK-norm of q and k ([Post]; [Guide] §8.2.1),
+    Steps in the pages' order: rotary of q and k when ``rope`` is given
+    ([Guide] §8.2.1 rotary row), QK-norm of q and k ([Post]; [Guide] §8.2.1),
     value-embedding mix into v on VE layers ([Guide] §8.2.1), then for every
     batch b and query head h (kv head h // G, [Guide] §8.2.1 GQA row):
     S = scale * qn kn^T, masked to the causal / sliding band, A = softmax(S),
@@ -229,7 +275,7 @@ def attention_forward(q, k, v, gq=None, gk=None, *, window: int, causal: bool = 
         raise ValueError("Hq must be a multiple of Hkv")
     G = Hq // Hkv
     sc = _scale(d, scale)
-    qn, kn, v_eff = _prep(q, k, v, gq, gk, eps, ve, tok, gate, ve_scale)
+    qn, kn, v_eff = _prep(q, k, v, gq, gk, eps, ve, tok, gate, ve_scale, rope)
     o = np.zeros((B, T, Hq, d))
     lse = np.zeros((B, Hq, T))
     for b in range(B):
@@ -247,7 +293,7 @@ def attention_forward(q, k, v, gq=None, gk=None, *, window: int, causal: bool = 
 def attention_forward_rows(q, k, v, gq=None, gk=None, *, b: int, h: int, rows,
                            window: int, causal: bool = True, scale=None,
                            eps: float = 1e-6, ve=None, tok=None, gate=None,
-                           ve_scale: float = 0.5):
+                           ve_scale: float = 0.5, rope=None):
     """Same as ``attention_forward`` for the query rows ``rows`` of one (b, h)
     only; returns (o [len(rows), d], lse [len(rows)]). Used to sample outputs
     of full-size problems one by one."""
@@ -259,8 +305,8 @@ def attention_forward_rows(q, k, v, gq=None, gk=None, *, b: int, h: int, rows,
     sc = _scale(d, scale)
     tk = None if tok is None else np.asarray(tok)[b:b + 1]
     gt = None if gate is None else np.asarray(gate)[b:b + 1]
-    qn, _ = rms_norm(q[:, :, h:h + 1, :], gq, eps)
-    kn, _ = rms_norm(k[:, :, h // G:h // G + 1, :], gk, eps)
+    qn, _ = rms_norm(_rot(q[:, :, h:h + 1, :], rope), gq, eps)
+    kn, _ = rms_norm(_rot(k[:, :, h // G:h // G + 1, :], rope), gk, eps)
     v_eff = ve_mix(v, ve, tk, gt, ve_scale)[:, :, h // G, :]
     rows = np.asarray(rows, dtype=np.int64)
     S = sc * (qn[0, rows, 0, :] @ kn[0, :, 0, :].T)
@@ -271,7 +317,7 @@ def attention_forward_rows(q, k, v, gq=None, gk=None, *, b: int, h: int, rows,
 def attention_backward(q, k, v, gq=None, gk=None, dO=None, *, window: int,
                        causal: bool = True, scale=None, eps: float = 1e-6, ve=None,
                        tok=None, gate=None, ve_scale: float = 0.5,
-                       row_chunk: int = 1024):
+                       row_chunk: int = 1024, rope=None):
     """Analytic backward of ``attention_forward`` for the loss <O, dO>.
 
     Per (b, h), with A the masked softmax and kv head hk = h // G:
@@ -280,8 +326,10 @@ def attention_backward(q, k, v, gq=None, gk=None, dO=None, *, window: int,
       dqn = scale * dS kn
       dkn[hk] += scale * dS^T qn                   (summed over the G heads of a group)
       dv_eff[hk] += A^T dO
-    then the RMSNorm backward of q and k (dq, dgq, dk, dgk), dv = dv_eff and
-    dVE[tok] += ve_scale * gate * dv_eff ([Guide] §8.2.1 VE mix, differentiated).
+    then the RMSNorm backward of q and k (dq, dgq, dk, dgk; of the rotated q
+    and k, followed by the transposed rotation, when ``rope`` is given),
+    dv = dv_eff and dVE[tok] += ve_scale * gate * dv_eff ([Guide] §8.2.1 VE
+    mix, differentiated).
 
     Returns a dict with dq, dk, dv, dgq, dgk (None when the gain is None) and
     dve ([vocab, Hkv*d], None without VE).
@@ -292,7 +340,7 @@ def attention_backward(q, k, v, gq=None, gk=None, dO=None, *, window: int,
     Hkv = np.asarray(k).shape[2]
     G = Hq // Hkv
     sc = _scale(d, scale)
-    qn, kn, v_eff = _prep(q, k, v, gq, gk, eps, ve, tok, gate, ve_scale)
+    qn, kn, v_eff = _prep(q, k, v, gq, gk, eps, ve, tok, gate, ve_scale, rope)
     dqn = np.zeros_like(qn)
     dkn = np.zeros_like(kn)
     dveff = np.zeros_like(v_eff)
@@ -309,8 +357,9 @@ def attention_backward(q, k, v, gq=None, gk=None, dO=None, *, window: int,
                 dqn[b, rows, h, :] += sc * (dS @ kn[b, :, hk, :])
                 dkn[b, :, hk, :] += sc * (dS.T @ qn[b, rows, h, :])
                 dveff[b, :, hk, :] += A.T @ dOr
-    dq, dgq = rms_norm_backward(q, gq, eps, dqn)
-    dk, dgk = rms_norm_backward(k, gk, eps, dkn)
+    dq, dgq = rms_norm_backward(_rot(q, rope), gq, eps, dqn)
+    dk, dgk = rms_norm_backward(_rot(np.asarray(k, dtype=np.float64), rope), gk, eps, dkn)
+    dq, dk = _unrot(dq, rope), _unrot(dk, rope)
     dve = None
     if ve is not None:
         Hd = Hkv * d
@@ -331,7 +380,7 @@ def _one_batch(q, k, v, dO, tok, gate, b):
 
 def attention_backward_rows(q, k, v, gq=None, gk=None, dO=None, *, b: int, h: int, rows,
                             window: int, causal: bool = True, scale=None, eps: float = 1e-6,
-                            ve=None, tok=None, gate=None, ve_scale: float = 0.5):
+                            ve=None, tok=None, gate=None, ve_scale: float = 0.5, rope=None):
     """dq of ``attention_backward`` at the query rows ``rows`` of one (b, h).
 
     Row i of dq depends only on row i of the softmax: dA_i = dO_i v_eff^T,
@@ -345,20 +394,21 @@ def attention_backward_rows(q, k, v, gq=None, gk=None, dO=None, *, b: int, h: in
     hk = h // G
     sc = _scale(d, scale)
     rows = np.asarray(rows, dtype=np.int64)
-    qn, _ = rms_norm(q[0, rows, h, :], gq, eps)
-    kn, _ = rms_norm(k[0, :, hk, :], gk, eps)
+    qr = _rot(q[0, rows, h:h + 1, :], rope, rows)[:, 0, :]
+    qn, _ = rms_norm(qr, gq, eps)
+    kn, _ = rms_norm(_rot(k[0, :, hk:hk + 1, :], rope)[:, 0, :], gk, eps)
     v_eff = ve_mix(v, ve, tk, gt, ve_scale)[0, :, hk, :]
     A, _ = _softmax_rows(sc * (qn @ kn.T), band_mask(rows, T, window, causal))
     dA = dO[0, rows, h, :] @ v_eff.T
     dS = A * (dA - np.sum(dA * A, axis=1, keepdims=True))
-    dq, _ = rms_norm_backward(q[0, rows, h, :], gq, eps, sc * (dS @ kn))
-    return dq
+    dq, _ = rms_norm_backward(qr, gq, eps, sc * (dS @ kn))
+    return _unrot(dq[:, None, :], rope, rows)[:, 0, :]
 
 
 def attention_backward_cols(q, k, v, gq=None, gk=None, dO=None, *, b: int, hk: int, cols,
                             window: int, causal: bool = True, scale=None, eps: float = 1e-6,
                             ve=None, tok=None, gate=None, ve_scale: float = 0.5,
-                            row_chunk: int = 512):
+                            row_chunk: int = 512, rope=None):
     """dk and dv of ``attention_backward`` at the key positions ``cols`` of one
     (b, kv head hk).
 
@@ -374,7 +424,8 @@ def attention_backward_cols(q, k, v, gq=None, gk=None, dO=None, *, b: int, hk: i
     G = Hq // k.shape[2]
     sc = _scale(d, scale)
     cols = np.asarray(cols, dtype=np.int64)
-    kn, _ = rms_norm(k[0, :, hk, :], gk, eps)
+    kr = _rot(k[0, :, hk:hk + 1, :], rope)[:, 0, :]
+    kn, _ = rms_norm(kr, gk, eps)
     v_eff = ve_mix(v, ve, tk, gt, ve_scale)[0, :, hk, :]
     dkn = np.zeros((cols.size, d))
     dv = np.zeros((cols.size, d))
@@ -386,12 +437,12 @@ def attention_backward_cols(q, k, v, gq=None, gk=None, dO=None, *, b: int, hk: i
         rows = rows[keep]
         M = band_mask(rows, T, window, causal)
         for h in range(hk * G, (hk + 1) * G):
-            qn, _ = rms_norm(q[0, rows, h, :], gq, eps)
+            qn, _ = rms_norm(_rot(q[0, rows, h:h + 1, :], rope, rows)[:, 0, :], gq, eps)
             A, _ = _softmax_rows(sc * (qn @ kn.T), M)
             dOr = dO[0, rows, h, :]
             dA = dOr @ v_eff.T
             dS = A * (dA - np.sum(dA * A, axis=1, keepdims=True))
             dv += A[:, cols].T @ dOr
             dkn += sc * (dS[:, cols].T @ qn)
-    dk, _ = rms_norm_backward(k[0, cols, hk, :], gk, eps, dkn)
-    return dk, dv
+    dk, _ = rms_norm_backward(kr[cols], gk, eps, dkn)
+    return _unrot(dk[:, None, :], rope, cols)[:, 0, :], dv

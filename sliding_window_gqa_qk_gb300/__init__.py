@@ -25,6 +25,7 @@ from . import build as _build
 __all__ = [
     "swa_params", "SwaError", "load",
     "swa_attn_workspace_size", "swa_attn_workspace_init", "swa_attn_fwd", "swa_attn_bwd",
+    "swa_attn_fwd_rope", "swa_attn_bwd_rope",
     "swa_attn_fwd_noalloc",
     "swa_attn_check_status", "swa_sssl_window", "swa_has_ve", "swa_strerror",
     "swa_build_info", "attention_forward", "attention_backward", "make_params",
@@ -62,6 +63,11 @@ class SwaError(RuntimeError):
         self.status = status
 
 
+class swa_rope(ctypes.Structure):
+    """Rotary tables of the _rope entry points (see include/swa_attn.h)."""
+    _fields_ = [("cos", ctypes.c_void_p), ("sin", ctypes.c_void_p), ("rows", ctypes.c_int)]
+
+
 _LIBS: dict = {}
 _vp = ctypes.c_void_p
 
@@ -84,6 +90,11 @@ def load(kind: str = "bf16") -> ctypes.CDLL:
     lib.swa_attn_fwd.restype = ctypes.c_int
     lib.swa_attn_bwd.argtypes = [P] + [_vp] * 18 + [ctypes.c_size_t, ctypes.c_uint, _vp]
     lib.swa_attn_bwd.restype = ctypes.c_int
+    R = ctypes.POINTER(swa_rope)
+    lib.swa_attn_fwd_rope.argtypes = [P, R] + [_vp] * 11 + [ctypes.c_size_t, ctypes.c_uint, _vp]
+    lib.swa_attn_fwd_rope.restype = ctypes.c_int
+    lib.swa_attn_bwd_rope.argtypes = [P, R] + [_vp] * 18 + [ctypes.c_size_t, ctypes.c_uint, _vp]
+    lib.swa_attn_bwd_rope.restype = ctypes.c_int
     lib.swa_attn_fwd_noalloc.argtypes = [P] + [_vp] * 10 + [_vp]
     lib.swa_attn_fwd_noalloc.restype = ctypes.c_int
     lib.swa_attn_check_status.argtypes = [_vp, _vp]
@@ -162,6 +173,34 @@ def swa_attn_bwd(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, d
         _ptr(dgk), _ptr(dve), _ptr(ws), n, int(flags), _stream(stream)))
 
 
+def make_rope(cos, sin) -> swa_rope:
+    """swa_rope of two [rows, d/2] fp32 device tensors (None, None: no rotary)."""
+    if cos is None and sin is None:
+        return swa_rope(None, None, 0)
+    return swa_rope(_ptr(cos), _ptr(sin), int(cos.shape[0]))
+
+
+def swa_attn_fwd_rope(p, rope, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, ws, ws_bytes=None,
+                      flags=0, stream=None, kind=None) -> int:
+    kind = kind or _kind_of(q)
+    n = ws.numel() if ws_bytes is None else ws_bytes
+    rp = None if rope is None else ctypes.byref(rope)
+    return int(load(kind).swa_attn_fwd_rope(
+        ctypes.byref(p), rp, _ptr(q), _ptr(k), _ptr(v), _ptr(gq), _ptr(gk), _ptr(ve), _ptr(tok),
+        _ptr(ve_gate), _ptr(o), _ptr(lse), _ptr(ws), n, int(flags), _stream(stream)))
+
+
+def swa_attn_bwd_rope(p, rope, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, dgq, dgk,
+                      dve, ws, ws_bytes=None, flags=0, stream=None, kind=None) -> int:
+    kind = kind or _kind_of(q)
+    n = ws.numel() if ws_bytes is None else ws_bytes
+    rp = None if rope is None else ctypes.byref(rope)
+    return int(load(kind).swa_attn_bwd_rope(
+        ctypes.byref(p), rp, _ptr(q), _ptr(k), _ptr(v), _ptr(gq), _ptr(gk), _ptr(ve), _ptr(tok),
+        _ptr(ve_gate), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgq),
+        _ptr(dgk), _ptr(dve), _ptr(ws), n, int(flags), _stream(stream)))
+
+
 def swa_attn_fwd_noalloc(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, stream=None,
                          kind=None) -> int:
     """Forward whose scratch is the library's fixed device array (no
@@ -215,10 +254,12 @@ def new_workspace(p: swa_params, for_backward: bool, device, kind: str, stream=N
 
 def attention_forward(q, k, v, gq=None, gk=None, *, window: int = -1, causal: bool = True,
                       softmax_scale: float = 0.0, eps: float = 1e-6, ve=None, tok=None,
-                      ve_gate=None, ve_scale: float = 0.5, workspace=None, stream=None):
+                      ve_gate=None, ve_scale: float = 0.5, workspace=None, stream=None,
+                      rope=None):
     """o, lse, workspace = attention_forward(q, k, v, ...). The workspace is
     allocated for the backward too, so it can be passed on to
-    ``attention_backward`` with the prologue outputs kept."""
+    ``attention_backward`` with the prologue outputs kept. ``rope``: None or
+    (cos, sin) fp32 device tensors [rows >= T, d/2] (rotary before the norm)."""
     B, T, Hq, d = q.shape
     Hkv = k.shape[2]
     kind = _kind_of(q)
@@ -227,15 +268,19 @@ def attention_forward(q, k, v, gq=None, gk=None, *, window: int = -1, causal: bo
     ws = workspace if workspace is not None else new_workspace(p, True, q.device, kind, stream)
     o = torch.empty_like(q)
     lse = torch.empty(B, Hq, T, dtype=torch.float32, device=q.device)
-    _check(swa_attn_fwd(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, ws, stream=stream),
-           "swa_attn_fwd")
+    if rope is None:
+        _check(swa_attn_fwd(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, ws, stream=stream),
+               "swa_attn_fwd")
+    else:
+        _check(swa_attn_fwd_rope(p, make_rope(*rope), q, k, v, gq, gk, ve, tok, ve_gate, o, lse, ws,
+                                 stream=stream), "swa_attn_fwd_rope")
     return o, lse, ws
 
 
 def attention_backward(q, k, v, gq, gk, o, lse, dO, *, window: int = -1, causal: bool = True,
                        softmax_scale: float = 0.0, eps: float = 1e-6, ve=None, tok=None,
                        ve_gate=None, ve_scale: float = 0.5, workspace=None,
-                       reuse_prologue: bool = False, stream=None) -> dict:
+                       reuse_prologue: bool = False, stream=None, rope=None) -> dict:
     """Gradients dq, dk, dv, dgq, dgk, dve (dve None without a VE table)."""
     B, T, Hq, d = q.shape
     Hkv = k.shape[2]
@@ -248,6 +293,11 @@ def attention_backward(q, k, v, gq, gk, o, lse, dO, *, window: int = -1, causal:
     dgk = torch.empty(d, dtype=torch.float32, device=q.device)
     dve = torch.empty(ve.shape, dtype=torch.float32, device=q.device) if ve is not None else None
     flags = SWA_REUSE_PROLOGUE if (reuse_prologue and workspace is not None) else 0
-    _check(swa_attn_bwd(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, dgq, dgk,
-                        dve, ws, flags=flags, stream=stream), "swa_attn_bwd")
+    if rope is None:
+        _check(swa_attn_bwd(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, dgq, dgk,
+                            dve, ws, flags=flags, stream=stream), "swa_attn_bwd")
+    else:
+        _check(swa_attn_bwd_rope(p, make_rope(*rope), q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq,
+                                 dk, dv, dgq, dgk, dve, ws, flags=flags, stream=stream),
+               "swa_attn_bwd_rope")
     return {"dq": dq, "dk": dk, "dv": dv, "dgq": dgq, "dgk": dgk, "dve": dve, "workspace": ws}

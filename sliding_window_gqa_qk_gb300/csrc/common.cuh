@@ -234,6 +234,7 @@ struct ProArgs {  // QK-norm + VE-mix prologue
   const elem_t* ve; const int32_t* tok; const float* gate;
   elem_t* qn; elem_t* kn; elem_t* veff;
   float* rstd_q; float* rstd_k;
+  const float* rcos; const float* rsin;   // rotary tables [rows, d/2], NULL: none
   uint32_t* status;
 };
 
@@ -263,6 +264,7 @@ struct PostArgs {  // backward post: RMSNorm backward, dv, dVE, gain partials
   float* dve;        // NULL: skip
   float* gpart;      // [2, nblk_max, d]
   int nblk_max;      // post_blocks(B, T, Hq)
+  const float* rcos; const float* rsin;   // rotary tables [rows, d/2], NULL: none
   uint32_t* status;
 };
 

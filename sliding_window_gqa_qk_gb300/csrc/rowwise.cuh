@@ -83,6 +83,35 @@ __device__ __forceinline__ float row_sum(float x) {
   return x;
 }
 
+// Rotary position embedding of one row, as the lanes hold it: channel c is
+// paired with c + D/2, which sits LPR/2 lanes away, and the pair at position
+// t turns by the angle whose cosine and sine are cos[t, c], sin[t, c]
+// (c < D/2):  y_c = x_c cos + x_{c+D/2} sin,  y_{c+D/2} = -x_c sin + x_{c+D/2} cos.
+// sgn = +1 applies the rotation, -1 its transpose (the backward). Every lane
+// of the warp calls this (shuffles); rows past the end pass valid = false.
+template <int D>
+__device__ __forceinline__ void rotate_row(float (&x)[RowMap<D>::EPL], const float* rcos, const float* rsin,
+                                           int t, bool valid, float sgn) {
+  using M = RowMap<D>;
+  constexpr int EPL = M::EPL;
+  const int cl = (threadIdx.x & 31) % M::LPR;
+  const bool first = cl < M::LPR / 2;
+  float p[EPL], cs[EPL], sn[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) p[i] = __shfl_xor_sync(0xffffffffu, x[i], M::LPR / 2);
+  if (valid) {
+    const long long base = static_cast<long long>(t) * (D / 2) + (cl % (M::LPR / 2)) * EPL;
+    ldf<EPL>(rcos + base, cs);
+    ldf<EPL>(rsin + base, sn);
+  } else {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) cs[i] = sn[i] = 0.f;
+  }
+  const float s = first ? sgn : -sgn;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) x[i] = fmaf(x[i], cs[i], s * p[i] * sn[i]);
+}
+
 // Warp index over the grid and the number of warps of the grid.
 __device__ __forceinline__ long long grid_warp() {
   return static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -98,9 +127,11 @@ __device__ __forceinline__ long long grid_warps() {
 // value-embedding row). The group list holds the q rows, then the k rows,
 // then (nseg = 3: value-embedding layers, and every layer of the fp32 build,
 // which makes a head-major copy of v) the v rows. Inputs are [B, T, H, d];
-// outputs are written head-major [B, H, T, d].
-template <int D>
-__global__ void __launch_bounds__(kRowWarps * 32, kProBlocksPerSm) prologue_kernel(ProArgs a) {
+// outputs are written head-major [B, H, T, d]. ROPE: q and k rows are
+// rotated (rotate_row) before the norm.
+template <int D, bool ROPE>
+__global__ void __launch_bounds__(kRowWarps * 32, ROPE ? kProBlocksPerSm - 1 : kProBlocksPerSm)
+    prologue_kernel(ProArgs a) {
   using M = RowMap<D>;
   constexpr int EPL = M::EPL;
   const int lane = threadIdx.x & 31;
@@ -141,6 +172,7 @@ __global__ void __launch_bounds__(kRowWarps * 32, kProBlocksPerSm) prologue_kern
         const int t = tg + u * M::RPI;
         float xv[EPL];
         unpack16(xr[u], xv);
+        if (ROPE) rotate_row<D>(xv, a.rcos, a.rsin, t, t < a.T, 1.f);
         float ss = 0.f;
 #pragma unroll
         for (int i = 0; i < EPL; ++i) ss = fmaf(xv[i], xv[i], ss);
@@ -305,6 +337,7 @@ __global__ void __launch_bounds__(kRowWarps * 32, kPostBlocksPerSm) bwd_post_ker
         const int t = tg + u * M::RPI;
         float xh[EPL], dxh[EPL], dot = 0.f;
         unpack16(xr[u], xh);
+        if (a.rcos != nullptr) rotate_row<D>(xh, a.rcos, a.rsin, t, t < a.T, 1.f);
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
           xh[i] *= rr[u];
@@ -313,10 +346,12 @@ __global__ void __launch_bounds__(kRowWarps * 32, kPostBlocksPerSm) bwd_post_ker
           gacc[i] = fmaf(dy[u][i], xh[i], gacc[i]);
         }
         dot = row_sum<M::LPR>(dot) / D;
-        if (t >= a.T) continue;
         float o[EPL];
 #pragma unroll
         for (int i = 0; i < EPL; ++i) o[i] = rr[u] * (dxh[i] - xh[i] * dot);
+        // the gradient of the rotated row, turned back by the transpose
+        if (a.rcos != nullptr) rotate_row<D>(o, a.rcos, a.rsin, t, t < a.T, -1.f);
+        if (t >= a.T) continue;
         st16(dx + in0 + t * in_stride, pack16(o));
       }
     }

@@ -39,7 +39,21 @@ struct Call {
   WsLayout L;
   uint8_t* ws;
   cudaStream_t stream;
+  const float* rcos = nullptr;   // rotary tables [rows, d/2], NULL: none
+  const float* rsin = nullptr;
 };
+
+// Rotary tables of a call: none (NULL or NULL tables), or both tables,
+// 16-byte aligned, with at least T rows.
+swa_status set_rope(Call& c, const swa_rope* r) {
+  if (r == nullptr || (r->cos == nullptr && r->sin == nullptr)) return SWA_OK;
+  if (r->cos == nullptr || r->sin == nullptr || !aligned(r->cos, 16) || !aligned(r->sin, 16) ||
+      r->rows < c.p.T)
+    return SWA_ERR_INVALID_ARG;
+  c.rcos = r->cos;
+  c.rsin = r->sin;
+  return SWA_OK;
+}
 
 swa_status check_params(const swa_params* p) {
   if (p == nullptr) return SWA_ERR_INVALID_ARG;
@@ -106,14 +120,21 @@ swa_status run_prologue(const Call& c, const elem_t* q, const elem_t* k, const e
   a.q = q; a.k = k; a.v = v; a.gq = gq; a.gk = gk; a.ve = ve; a.tok = tok; a.gate = gate;
   a.qn = at<elem_t>(c, c.L.qn); a.kn = at<elem_t>(c, c.L.kn); a.veff = at<elem_t>(c, c.L.veff);
   a.rstd_q = at<float>(c, c.L.rstd_q); a.rstd_k = at<float>(c, c.L.rstd_k);
+  a.rcos = c.rcos; a.rsin = c.rsin;
   a.status = at<uint32_t>(c, c.L.status);
   a.nseg = (ve != nullptr || copy_v) ? 3 : 2;
   const int rg = p.d == 64 ? RowMap<64>::RG : RowMap<128>::RG;
   const long long ngt = (p.T + rg - 1) / rg;
   const long long groups = ngt * p.B * (p.Hq + p.Hkv * (a.nseg - 1));
-  const int grid = row_grid(groups, kProBlocksPerSm, 0);
-  if (p.d == 64) prologue_kernel<64><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
-  else prologue_kernel<128><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
+  const bool rope = a.rcos != nullptr;
+  const int grid = row_grid(groups, rope ? kProBlocksPerSm - 1 : kProBlocksPerSm, 0);
+  if (p.d == 64) {
+    if (rope) prologue_kernel<64, true><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
+    else prologue_kernel<64, false><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
+  } else {
+    if (rope) prologue_kernel<128, true><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
+    else prologue_kernel<128, false><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
+  }
   return launched();
 }
 
@@ -154,13 +175,14 @@ namespace {
 // The forward of swa_attn_fwd. prepare_bwd: a workspace sized for the
 // backward also gets its dQ accumulator zeroed by the forward kernel (the
 // no-allocation entry point passes false).
-swa_status fwd_impl(const swa_params* p, const void* q, const void* k, const void* v,
-                    const float* gq, const float* gk, const void* ve, const int32_t* tok,
-                    const float* ve_gate, void* o, float* lse, void* workspace, size_t ws_bytes,
-                    unsigned flags, void* stream, bool prepare_bwd) {
+swa_status fwd_impl(const swa_params* p, const swa_rope* rope, const void* q, const void* k,
+                    const void* v, const float* gq, const float* gk, const void* ve,
+                    const int32_t* tok, const float* ve_gate, void* o, float* lse, void* workspace,
+                    size_t ws_bytes, unsigned flags, void* stream, bool prepare_bwd) {
   Call c;
   swa_status s = begin(c, p, workspace, ws_bytes, false, stream);
   if (s != SWA_OK) return s;
+  if ((s = set_rope(c, rope)) != SWA_OK) return s;
   if ((flags & ~SWA_REUSE_PROLOGUE) != 0) return SWA_ERR_INVALID_ARG;
   if (!tensor_ok(q) || !tensor_ok(k) || !tensor_ok(v) || !tensor_ok(o) || lse == nullptr)
     return SWA_ERR_INVALID_ARG;
@@ -219,42 +241,15 @@ swa_status fwd_impl(const swa_params* p, const void* q, const void* k, const voi
 #endif
 }
 
-}  // namespace
-
-// ---------------------------------------------------------------------------
-// Exported C ABI
-// ---------------------------------------------------------------------------
-extern "C" {
-
-size_t swa_attn_workspace_size(const swa_params* p, int for_backward) {
-  if (check_params(p) != SWA_OK) return 0;
-  const WsLayout L = ws_layout(p->B, p->T, p->Hq, p->Hkv, p->d);
-  return for_backward ? L.bwd_end : L.fwd_end;
-}
-
-swa_status swa_attn_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
-  if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < 256) return SWA_ERR_INVALID_ARG;
-  if (cudaMemsetAsync(workspace, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return SWA_ERR_CUDA;
-  return SWA_OK;
-}
-
-swa_status swa_attn_fwd(const swa_params* p, const void* q, const void* k, const void* v,
-                        const float* gq, const float* gk, const void* ve, const int32_t* tok,
-                        const float* ve_gate, void* o, float* lse, void* workspace,
-                        size_t ws_bytes, unsigned flags, void* stream) {
-  return fwd_impl(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, workspace, ws_bytes, flags, stream,
-                  true);
-}
-
-swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const void* v,
-                        const float* gq, const float* gk, const void* ve, const int32_t* tok,
-                        const float* ve_gate, const void* o, const float* lse, const void* dO,
-                        void* dq, void* dk, void* dv, float* dgq, float* dgk, float* dve,
-                        void* workspace, size_t ws_bytes, unsigned flags, void* stream) {
+swa_status bwd_impl(const swa_params* p, const swa_rope* rope, const void* q, const void* k,
+                    const void* v, const float* gq, const float* gk, const void* ve,
+                    const int32_t* tok, const float* ve_gate, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, float* dgq, float* dgk, float* dve,
+                    void* workspace, size_t ws_bytes, unsigned flags, void* stream) {
   Call c;
   swa_status s = begin(c, p, workspace, ws_bytes, true, stream);
   if (s != SWA_OK) return s;
+  if ((s = set_rope(c, rope)) != SWA_OK) return s;
   const unsigned known = SWA_REUSE_PROLOGUE | SWA_BWD_STAGE_PRE | SWA_BWD_STAGE_MAIN | SWA_BWD_STAGE_POST;
   if ((flags & ~known) != 0) return SWA_ERR_INVALID_ARG;
   if (!tensor_ok(q) || !tensor_ok(k) || !tensor_ok(v) || !tensor_ok(o) || !tensor_ok(dO) ||
@@ -366,6 +361,8 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
     b.status = at<uint32_t>(c, c.L.status);
     b.wait_limit_ns = kWaitLimitNs;
     b.acc_flag = at<unsigned long long>(c, c.L.status + 8);
+    // with rotary the k-side norm backward moves to the post kernel
+    b.dkn_out = c.rcos != nullptr ? at<float>(c, c.L.dk_acc) : nullptr;
     if ((s = (P.d == 128 ? tc::launch_bwd128(b, st) : tc::launch_bwd(b, st))) != SWA_OK) return s;
 #endif
   }
@@ -377,7 +374,9 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
     }
     const int post_segments = 3;   // q, k and v rows
 #else
-    const int post_segments = 1;   // q rows; k and v were done by the attention backward
+    // q rows; k and v were done by the attention backward, except the k-side
+    // norm and rotary backward when there are rotary tables
+    const int post_segments = c.rcos != nullptr ? 2 : 1;
 #endif
     PostArgs a{};
     a.B = P.B; a.T = P.T; a.Hq = P.Hq; a.Hkv = P.Hkv; a.d = P.d; a.vocab = P.vocab;
@@ -389,6 +388,7 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
     a.dq = static_cast<elem_t*>(dq); a.dk = static_cast<elem_t*>(dk); a.dv = static_cast<elem_t*>(dv);
     a.dve = (ve != nullptr) ? dve : nullptr;
     a.gpart = at<float>(c, c.L.gpart);
+    a.rcos = c.rcos; a.rsin = c.rsin;
     a.nblk_max = post_blocks(P.B, P.T, P.Hq);
     a.status = at<uint32_t>(c, c.L.status);
     // one gain partial per block: no more blocks than the workspace holds
@@ -404,8 +404,10 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
       const float* part_k = at<float>(c, c.L.gpart) + static_cast<size_t>(post_blocks(P.B, P.T, P.Hq)) * P.d;
       const int n_k = nblk;
 #else
-      const float* part_k = at<float>(c, c.L.gpart_k);
-      const int n_k = P.B * P.Hkv * ((P.T + 127) / 128);
+      const bool post_k = c.rcos != nullptr;
+      const float* part_k = post_k ? at<float>(c, c.L.gpart) + static_cast<size_t>(post_blocks(P.B, P.T, P.Hq)) * P.d
+                                   : at<float>(c, c.L.gpart_k);
+      const int n_k = post_k ? nblk : P.B * P.Hkv * ((P.T + 127) / 128);
 #endif
       GainArgs g{P.d, at<float>(c, c.L.gpart), nblk, part_k, n_k, dgq, dgk};
       gain_sum_kernel<<<dim3(2, P.d / 32), kGainWarps * 32, 0, st>>>(g);
@@ -413,6 +415,61 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
     }
   }
   return SWA_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Exported C ABI
+// ---------------------------------------------------------------------------
+extern "C" {
+
+size_t swa_attn_workspace_size(const swa_params* p, int for_backward) {
+  if (check_params(p) != SWA_OK) return 0;
+  const WsLayout L = ws_layout(p->B, p->T, p->Hq, p->Hkv, p->d);
+  return for_backward ? L.bwd_end : L.fwd_end;
+}
+
+swa_status swa_attn_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+  if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < 256) return SWA_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(workspace, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SWA_ERR_CUDA;
+  return SWA_OK;
+}
+
+swa_status swa_attn_fwd(const swa_params* p, const void* q, const void* k, const void* v,
+                        const float* gq, const float* gk, const void* ve, const int32_t* tok,
+                        const float* ve_gate, void* o, float* lse, void* workspace,
+                        size_t ws_bytes, unsigned flags, void* stream) {
+  return fwd_impl(p, nullptr, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, workspace, ws_bytes, flags,
+                  stream, true);
+}
+
+swa_status swa_attn_fwd_rope(const swa_params* p, const swa_rope* rope, const void* q, const void* k,
+                             const void* v, const float* gq, const float* gk, const void* ve,
+                             const int32_t* tok, const float* ve_gate, void* o, float* lse,
+                             void* workspace, size_t ws_bytes, unsigned flags, void* stream) {
+  return fwd_impl(p, rope, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, workspace, ws_bytes, flags,
+                  stream, true);
+}
+
+swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const void* v,
+                        const float* gq, const float* gk, const void* ve, const int32_t* tok,
+                        const float* ve_gate, const void* o, const float* lse, const void* dO,
+                        void* dq, void* dk, void* dv, float* dgq, float* dgk, float* dve,
+                        void* workspace, size_t ws_bytes, unsigned flags, void* stream) {
+  return bwd_impl(p, nullptr, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, dgq, dgk, dve,
+                  workspace, ws_bytes, flags, stream);
+}
+
+swa_status swa_attn_bwd_rope(const swa_params* p, const swa_rope* rope, const void* q, const void* k,
+                             const void* v, const float* gq, const float* gk, const void* ve,
+                             const int32_t* tok, const float* ve_gate, const void* o,
+                             const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                             float* dgq, float* dgk, float* dve, void* workspace, size_t ws_bytes,
+                             unsigned flags, void* stream) {
+  return bwd_impl(p, rope, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, dgq, dgk, dve,
+                  workspace, ws_bytes, flags, stream);
 }
 
 swa_status swa_attn_check_status(void* workspace, void* stream) {
@@ -442,8 +499,8 @@ swa_status swa_attn_fwd_noalloc(const swa_params* p, const void* q, const void* 
   void* scratch = nullptr;
   const swa_status ss = noalloc_scratch(&scratch);
   if (ss != SWA_OK) return ss;
-  return fwd_impl(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, scratch, SWA_NOALLOC_SCRATCH_BYTES, 0,
-                  stream, false);
+  return fwd_impl(p, nullptr, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, scratch,
+                  SWA_NOALLOC_SCRATCH_BYTES, 0, stream, false);
 }
 
 int swa_sssl_window(int layer, int n_layer, const char* pattern, int T) {

@@ -69,6 +69,7 @@ struct BwdLaunch {
   uint32_t* status;
   uint64_t wait_limit_ns;
   unsigned long long* acc_flag;   // dQ-accumulator record in the workspace header
+  float* dkn_out;      // rotary: fp32 dkn [B, Hkv, T, d] for the post kernel (NULL: none)
 };
 
 struct BwdParams {
@@ -91,6 +92,10 @@ struct BwdParams {
   float* gpart_k;
   uint32_t* status;
   uint64_t wait_limit_ns;
+  // Rotary (non-null): the epilogue writes dkn = dK (fp32, [B, Hkv, T, d])
+  // here and leaves the RMSNorm and rotary backward of k, with its gain
+  // partials, to the post kernel (they need whole rotated rows).
+  float* dkn_out;
   int n_bhk;                  // B * Hkv
   int chunk;                  // (batch, kv head) pairs per scheduling chunk (1-D grids)
   // Record of a forward that zeroed the dQ accumulator (offset, length);
@@ -139,70 +144,101 @@ __device__ __forceinline__ void kv_epilogue(const BwdParams& prm, uint32_t tDK, 
   const long long bt = static_cast<long long>(b) * prm.T + j;
   const long long rowoff = (bt * prm.Hkv + hk) * D + wg * HD;   // into k / dk / dv
   const float r = valid ? prm.rstd_k[(static_cast<long long>(b) * prm.Hkv + hk) * prm.T + j] : 0.f;
-  if (t < HD) sg[wg * HD + t] = prm.gk ? prm.gk[wg * HD + t] : 1.f;
-  // All loads first: dK (TMEM) and the k row (global).
-  uint32_t dkr[NCH][32];
-  if (have) {
+  const bool rope = prm.dkn_out != nullptr;
+  if (rope) {
+    // dkn rows (fp32) for the post kernel, this warpgroup's half of the row
+    uint32_t dkr[NCH][32];
+    if (have) {
 #pragma unroll
-    for (int ch = 0; ch < NCH; ++ch) tmem_ld32(tDK + ch * 32, dkr[ch]);
+      for (int ch = 0; ch < NCH; ++ch) tmem_ld32(tDK + ch * 32, dkr[ch]);
+      tmem_wait_ld(dkr[0]);
+#pragma unroll
+      for (int ch = 1; ch < NCH; ++ch) reg_fence(dkr[ch]);
+    } else {
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) dkr[ch][e] = 0u;
+    }
+    if (valid) {
+      float4* dst = reinterpret_cast<float4*>(
+          prm.dkn_out + ((static_cast<long long>(b) * prm.Hkv + hk) * prm.T + j) * D + wg * HD);
+      const float m = prm.dk_mul;
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          dst[(ch * 32 + e) / 4] =
+              make_float4(__uint_as_float(dkr[ch][e]) * m, __uint_as_float(dkr[ch][e + 1]) * m,
+                          __uint_as_float(dkr[ch][e + 2]) * m, __uint_as_float(dkr[ch][e + 3]) * m);
+    }
   }
-  uint4 xr[NCH * 4];
-  if (valid) {
-    const uint4* src = reinterpret_cast<const uint4*>(prm.k + rowoff);
+  if (!rope && t < HD) sg[wg * HD + t] = prm.gk ? prm.gk[wg * HD + t] : 1.f;
+  if (!rope) {
+    // All loads first: dK (TMEM) and the k row (global).
+    uint32_t dkr[NCH][32];
+    if (have) {
 #pragma unroll
-    for (int q = 0; q < NCH * 4; ++q) xr[q] = src[q];
-  } else {
+      for (int ch = 0; ch < NCH; ++ch) tmem_ld32(tDK + ch * 32, dkr[ch]);
+    }
+    uint4 xr[NCH * 4];
+    if (valid) {
+      const uint4* src = reinterpret_cast<const uint4*>(prm.k + rowoff);
 #pragma unroll
-    for (int q = 0; q < NCH * 4; ++q) xr[q] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  if (have) {
-    tmem_wait_ld(dkr[0]);
+      for (int q = 0; q < NCH * 4; ++q) xr[q] = src[q];
+    } else {
 #pragma unroll
-    for (int ch = 1; ch < NCH; ++ch) reg_fence(dkr[ch]);
-  } else {
+      for (int q = 0; q < NCH * 4; ++q) xr[q] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (have) {
+      tmem_wait_ld(dkr[0]);
+#pragma unroll
+      for (int ch = 1; ch < NCH; ++ch) reg_fence(dkr[ch]);
+    } else {
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) dkr[ch][e] = 0u;
+    }
+    named_bar_sync(3, 256);                    // gains staged
+    auto xval = [&](int c) {                   // c in [0, HD)
+      const uint4 u = xr[c >> 3];
+      const uint32_t w = ((c & 7) >> 1) == 0 ? u.x : ((c & 7) >> 1) == 1 ? u.y : ((c & 7) >> 1) == 2 ? u.z : u.w;
+      return (c & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
+    };
+    float pdot = 0.f;
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
-      for (int e = 0; e < 32; ++e) dkr[ch][e] = 0u;
-  }
-  named_bar_sync(3, 256);                    // gains staged
-  auto xval = [&](int c) {                   // c in [0, HD)
-    const uint4 u = xr[c >> 3];
-    const uint32_t w = ((c & 7) >> 1) == 0 ? u.x : ((c & 7) >> 1) == 1 ? u.y : ((c & 7) >> 1) == 2 ? u.z : u.w;
-    return (c & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
-  };
-  float pdot = 0.f;
+      for (int e = 0; e < 32; ++e) {
+        const int c = ch * 32 + e;
+        pdot = fmaf(sg[wg * HD + c] * __uint_as_float(dkr[ch][e]), xval(c), pdot);
+      }
+    pdot *= prm.dk_mul * r;
+    sdot[wg * 128 + t] = pdot;
+    named_bar_sync(3, 256);
+    const float mean = (pdot + sdot[(1 - wg) * 128 + t]) / D;
 #pragma unroll
-  for (int ch = 0; ch < NCH; ++ch)
+    for (int ch = 0; ch < NCH; ++ch) {
+      uint32_t pk[16];
+      float gt[32];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const int c = ch * 32 + e;
-      pdot = fmaf(sg[wg * HD + c] * __uint_as_float(dkr[ch][e]), xval(c), pdot);
+      for (int e = 0; e < 32; e += 2) {
+        const int c = ch * 32 + e;
+        const float dk0 = __uint_as_float(dkr[ch][e]) * prm.dk_mul;
+        const float dk1 = __uint_as_float(dkr[ch][e + 1]) * prm.dk_mul;
+        const float xh0 = xval(c) * r, xh1 = xval(c + 1) * r;
+        pk[e / 2] = pack_bf16x2(r * (sg[wg * HD + c] * dk0 - xh0 * mean),
+                                r * (sg[wg * HD + c + 1] * dk1 - xh1 * mean));
+        gt[e] = dk0 * xh0;                     // gain term, 0 on rows past T (r = 0)
+        gt[e + 1] = dk1 * xh1;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st_shared_v4(sw128_addr(sdk, kBK, t, (wg * HD + ch * 32) / 8 + q), pk[4 * q], pk[4 * q + 1],
+                     pk[4 * q + 2], pk[4 * q + 3]);
+      sgain[(wg * 4 + warp4) * HD + ch * 32 + lane] = transpose_sum32(gt, lane);
     }
-  pdot *= prm.dk_mul * r;
-  sdot[wg * 128 + t] = pdot;
-  named_bar_sync(3, 256);
-  const float mean = (pdot + sdot[(1 - wg) * 128 + t]) / D;
-#pragma unroll
-  for (int ch = 0; ch < NCH; ++ch) {
-    uint32_t pk[16];
-    float gt[32];
-#pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      const int c = ch * 32 + e;
-      const float dk0 = __uint_as_float(dkr[ch][e]) * prm.dk_mul;
-      const float dk1 = __uint_as_float(dkr[ch][e + 1]) * prm.dk_mul;
-      const float xh0 = xval(c) * r, xh1 = xval(c + 1) * r;
-      pk[e / 2] = pack_bf16x2(r * (sg[wg * HD + c] * dk0 - xh0 * mean),
-                              r * (sg[wg * HD + c + 1] * dk1 - xh1 * mean));
-      gt[e] = dk0 * xh0;                     // gain term, 0 on rows past T (r = 0)
-      gt[e + 1] = dk1 * xh1;
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      st_shared_v4(sw128_addr(sdk, kBK, t, (wg * HD + ch * 32) / 8 + q), pk[4 * q], pk[4 * q + 1],
-                   pk[4 * q + 2], pk[4 * q + 3]);
-    sgain[(wg * 4 + warp4) * HD + ch * 32 + lane] = transpose_sum32(gt, lane);
   }
   // dv and the VE-table gradient
   const int tok = (prm.dve != nullptr && valid) ? prm.tok[bt] : -1;
@@ -246,13 +282,13 @@ __device__ __forceinline__ void kv_epilogue(const BwdParams& prm, uint32_t tDK, 
   if (wg == 0 && t == 0) {
     // rows past T fall outside the tensors and are not written
     for (int c = 0; c < D / 64; ++c) {
-      tma_store_4d(tmDK, sdk + c * kBK * 128, 64 * c, kt * kBK, hk, b);
+      if (!rope) tma_store_4d(tmDK, sdk + c * kBK * 128, 64 * c, kt * kBK, hk, b);
       tma_store_4d(tmDV, sdv + c * kBK * 128, 64 * c, kt * kBK, hk, b);
     }
     bulk_commit_group();
-    bulk_wait_group_all();
+    bulk_wait_group_read<0>();   // the tiles are read out of shared memory
   }
-  if (t < HD) {
+  if (!rope && t < HD) {
     float sum = 0.f;
 #pragma unroll
     for (int w = 0; w < 4; ++w) sum += sgain[(wg * 4 + w) * HD + t];
@@ -700,6 +736,7 @@ inline swa_status launch_bwd_d(const BwdLaunch& f, cudaStream_t st) {
   p.ve_scale = f.ve_scale; p.vocab = f.vocab; p.dk = f.dk; p.dv = f.dv; p.gpart_k = f.gpart_k;
   p.status = f.status; p.wait_limit_ns = f.wait_limit_ns;
   p.acc_flag = f.acc_flag;
+  p.dkn_out = f.dkn_out;
   if (cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kAlloc) != cudaSuccess)
     return SWA_ERR_CUDA;
@@ -708,8 +745,9 @@ inline swa_status launch_bwd_d(const BwdLaunch& f, cudaStream_t st) {
   return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 
+// d = 64 (d = 128 has its own kernel, tc_bwd128.cuh).
 inline swa_status launch_bwd(const BwdLaunch& f, cudaStream_t st) {
-  return f.d == 64 ? launch_bwd_d<64>(f, st) : launch_bwd_d<128>(f, st);
+  return f.d == 64 ? launch_bwd_d<64>(f, st) : SWA_ERR_UNSUPPORTED;
 }
 
 }  // namespace tc

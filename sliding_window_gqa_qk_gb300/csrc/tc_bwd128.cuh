@@ -14,25 +14,25 @@
 // P^T and dS^T carry the softmax scale, so dK and dQ come out final and dV
 // is divided by it in the epilogue.
 //
-// Roles (12 warps): warpgroups 0 and 1 do the element-wise work, each on 64
+// Roles (16 warps): warpgroups 0 and 1 do the element-wise work, each on 64
 // of the step's 128 query columns (thread = key row = TMEM lane): per step
-// P(i), dS(i), then the drain of dQ^T(i). Warp 8 is the TMA producer of K, V
-// (once) and of Q with LSE and D (two stages); warp 11 of dO (one stage,
-// reloaded as soon as dV of the step completed); warp 10 adds the staged dQ
-// boxes into the fp32 accumulator; warp 9 issues the MMAs from one thread,
+// P(i), then dS(i). Warpgroup 2 drains dQ^T(i) from TMEM into the staging
+// boxes, off the element-wise warps' path. Warp 12 is the TMA producer of K,
+// V (once) and of Q with LSE and D (two stages); warp 15 of dO (one stage,
+// reloaded as soon as dV of the step completed); warp 14 adds the staged dQ
+// boxes into the fp32 accumulator; warp 13 issues the MMAs from one thread,
 // in the order
 //   S(0) dP(0) | dV(i) [dQ(i) dK(i)] S(i+1) dP(i+1) | ...
 // dQ^T(i) comes before dK(i) so that its drain starts one product earlier;
 // dP^T(i+1) waits for that drain (it reuses the columns).
-// dQ^T(i) goes from TMEM to shared memory in two [32 queries][128] fp32
-// boxes per warpgroup, one in half of the dedicated staging buffer (free once
-// the previous step's boxes there were read) and one in half of the step's Q
-// stage (free once dK(i) has read it), and from there into the fp32 dQ
-// accumulator by TMA bulk reductions. Those run at the rate the L2 accepts
-// fp32 adds (about 6.6 TB/s over the whole GPU, about 21 bytes per clock per
-// SM), 64 KB per step.
-// Registers: the element-wise warpgroups run with 216 per thread, warpgroup
-// 2 with 72 (setmaxnreg; 384 x 168 at launch).
+// dQ^T(i) goes from TMEM to shared memory in four [32 queries][128] fp32
+// boxes, two in the dedicated staging buffer (free once the previous step's
+// boxes there were read) and two in the step's Q stage (free once dK(i) has
+// read it), and from there into the fp32 dQ accumulator by TMA bulk
+// reductions. Those run at the rate the L2 accepts fp32 adds (about 6.6 TB/s
+// over the whole GPU, about 21 bytes per clock per SM), 64 KB per step.
+// Registers (setmaxnreg; 512 x 128 at launch): element-wise warpgroups 176
+// per thread, drain warpgroup 96, the four single-role warps 56.
 //
 // Softmax backward written out from the forward of the attention block
 // (autoresearch Administrator & Developer Guide §8.2.1; train.py
@@ -44,10 +44,12 @@
 namespace swa {
 namespace tc {
 
-constexpr int kB2Threads = 384;
-constexpr int kB2RegsSoftmax = 216;
-constexpr int kB2RegsOther = 72;
-static_assert(2 * 128 * kB2RegsSoftmax + 128 * kB2RegsOther <= kB2Threads * 168,
+constexpr int kB2Threads = 512;
+constexpr int kB2RegsSoftmax = 176;   // element-wise warpgroups 0, 1
+constexpr int kB2RegsDrain = 96;      // drain warpgroup (warps 8-11)
+constexpr int kB2RegsOther = 56;      // producers, MMA issuer, reducer (warps 12-15)
+constexpr int kB2ProdWarp = 12, kB2MmaWarp = 13, kB2RedWarp = 14, kB2GWarp = 15;
+static_assert(2 * 128 * kB2RegsSoftmax + 128 * kB2RegsDrain + 128 * kB2RegsOther <= kB2Threads * 128,
               "register split exceeds the launch's registers");
 
 struct B2Cfg {
@@ -84,7 +86,6 @@ enum {
   B2_DQFREE = 14,    // dQ^T read out of TMEM (8 warps)
   B2_STAGED = 15,    // the step's four dQ boxes are in shared memory (8 warps)
   B2_XFREE = 16,     // the dQ boxes in the staging buffer were read
-  B2_DQREAD = 17,    // every dQ box of the CTA was read (once, at the end)
   B2_FINAL = 18,
   B2_DKDONE = 19,    // the dK product of the step completed (dQ-first order)
   B2_COUNT = 20
@@ -180,15 +181,14 @@ __global__ void __launch_bounds__(kB2Threads, 1)
     mbar_init(bar(B2_PREADY), 8);
     mbar_init(bar(B2_DSREADY), 8);
     mbar_init(bar(B2_DQFULL), 1);
-    mbar_init(bar(B2_DQFREE), 8);
-    mbar_init(bar(B2_STAGED), 8);
+    mbar_init(bar(B2_DQFREE), 4);
+    mbar_init(bar(B2_STAGED), 4);
     mbar_init(bar(B2_XFREE), 1);
-    mbar_init(bar(B2_DQREAD), 1);
     mbar_init(bar(B2_FINAL), 1);
     mbar_init(bar(B2_DKDONE), 1);
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kB2MmaWarp) {
     tmem_alloc(smem_u32(tmem_base_sh), 512);
     tmem_relinquish();
   }
@@ -198,9 +198,9 @@ __global__ void __launch_bounds__(kB2Threads, 1)
   const uint32_t tmem = *tmem_base_sh;
   constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 384;
 
-  if (warp >= 8) {
+  if (warp >= kB2ProdWarp) {
     setmaxnreg_dec<kB2RegsOther>();
-    if (warp == 8 && lane == 0 && n_it > 0) {
+    if (warp == kB2ProdWarp && lane == 0 && n_it > 0) {
       // ---------------- TMA producer of K, V, and per step Q, LSE, D ----------------
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kB2Threads, 1)
       mbar_wait_drain(bar(B2_KV), 0, prm.wait_limit_ns);
       for (int s = 0; s < 2; ++s)
         if (last[s] >= 0) mbar_wait_drain(bar(B2_QFULL + s), (last[s] >> 1) & 1, prm.wait_limit_ns);
-    } else if (warp == 11 && lane == 0 && n_it > 0) {
+    } else if (warp == kB2GWarp && lane == 0 && n_it > 0) {
       // ---------------- TMA producer of dO (one stage) ----------------
       tma_prefetch_desc(&tmG);
       int last = -1;
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kB2Threads, 1)
           tma_load_4d(sbase + C::oG + c * C::kHalf, &tmG, bar(B2_GFULL), 64 * c, q0, h, b);
       }
       if (last >= 0) mbar_wait_drain(bar(B2_GFULL), last & 1, prm.wait_limit_ns);
-    } else if (warp == 10 && lane == 0 && n_it > 0) {
+    } else if (warp == kB2RedWarp && lane == 0 && n_it > 0) {
       // ---------------- dQ reducer ----------------
       // Step m's dQ boxes, for each warpgroup X: queries qb.. in half X of the
       // step's Q stage, qb+32.. in half X of the staging buffer, added into
@@ -270,9 +270,8 @@ __global__ void __launch_bounds__(kB2Threads, 1)
         bulk_wait_group_read<0>();
         mbar_arrive(bar(B2_XFREE));
       }
-      bulk_wait_group_all();
-      mbar_arrive(bar(B2_DQREAD));
-    } else if (warp == 9 && lane == 0 && n_it > 0) {
+      bulk_wait_group_read<0>();   // shared memory stays valid until read
+    } else if (warp == kB2MmaWarp && lane == 0 && n_it > 0) {
       // ---------------- MMA issuer (one thread) ----------------
       constexpr uint32_t idN = idesc_bf16_f32(128, 128, 0, 0);    // S^T, dP^T
       constexpr uint32_t idKV = idesc_bf16_f32(128, 128, 0, 1);   // dV, dK (A from TMEM)
@@ -364,6 +363,49 @@ __global__ void __launch_bounds__(kB2Threads, 1)
       }
       umma_commit(bar(B2_FINAL));
       mbar_wait_drain(bar(B2_FINAL), 0, prm.wait_limit_ns);
+    }
+  } else if (warp >= 8) {
+    // --------- drain warpgroup: dQ^T(i) (lane = head-dim index) -> staged boxes ---------
+    // Boxes [32 queries][128] fp32: queries 64X .. 64X + 31 in half X of the
+    // step's Q stage (free once dK(i) has read it), 64X + 32 .. 64X + 63 in
+    // half X of the staging buffer (free once the reducer read the previous
+    // step's boxes there). TMEM is handed back (DQFREE) as soon as every
+    // column has been read.
+    setmaxnreg_dec<kB2RegsDrain>();
+    const int t = threadIdx.x & 127;
+    const uint32_t tDQ = tmem + cDP + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    for (int i = 0; i < n_it; ++i) {
+      const int s = i & 1;
+      if (!mbar_wait_warp(bar(B2_DQFULL), i & 1, ctl)) break;
+      tc_fence_after();
+      uint32_t a[2][32];
+      tmem_ld32(tDQ + 32, a[0]);
+      tmem_ld32(tDQ + 96, a[1]);
+      tmem_wait_ld(a[0]);
+      reg_fence(a[1]);
+      if (i > 0 && !mbar_wait_warp(bar(B2_XFREE), (i - 1) & 1, ctl)) break;
+#pragma unroll
+      for (int X = 0; X < 2; ++X)
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          st_shared_f32(sbase + C::oX + X * C::kHalf + e * 512 + t * 4, __uint_as_float(a[X][e]));
+      tmem_ld32(tDQ, a[0]);
+      tmem_ld32(tDQ + 64, a[1]);
+      tmem_wait_ld(a[0]);
+      reg_fence(a[1]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B2_DQFREE));
+      if (!mbar_wait_warp(bar(B2_DKDONE), i & 1, ctl)) break;
+#pragma unroll
+      for (int X = 0; X < 2; ++X)
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          st_shared_f32(sbase + C::oQ + s * C::kTile + X * C::kHalf + e * 512 + t * 4,
+                        __uint_as_float(a[X][e]));
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B2_STAGED));   // the reducer adds them
     }
   } else {
     // --------- element-wise warpgroups: X = warp / 4 owns query columns [64X, 64X + 64) ---------
@@ -461,52 +503,22 @@ __global__ void __launch_bounds__(kB2Threads, 1)
       if (lane == 0) mbar_arrive(bar(B2_DSREADY));
       return true;
     };
-    // ---- dQ^T(i) (lane = head-dim index, 64 query columns) -> staged boxes ----
-    auto drain = [&](int i) -> bool {
-      const int s = i & 1;
-      if (!mbar_wait_warp(bar(B2_DQFULL), i & 1, ctl)) return false;
-      tc_fence_after();
-      uint32_t dq[2][32];
-      tmem_ld32(tDP, dq[0]);
-      tmem_ld32(tDP + 32, dq[1]);
-      tmem_wait_ld(dq[0]);
-      reg_fence(dq[1]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B2_DQFREE));
-      // boxes [32 queries][128] fp32: queries qb.. in this warpgroup's half of
-      // the dS^T buffer (last read by dQ^T(i)), qb+32.. in half X of the dO
-      // stage (last read by dV(i)); both products completed before DQFULL
-      const uint32_t box0 = sbase + C::oQ + s * C::kTile + X * C::kHalf;
-      const uint32_t box1 = sbase + C::oX + X * C::kHalf;
-      // box1 once the reducer has read the previous step's boxes out of the
-      // staging buffer; box0 once dK(i), which reads the Q stage, completed
-      if (i > 0 && !mbar_wait_warp(bar(B2_XFREE), (i - 1) & 1, ctl)) return false;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) st_shared_f32(box1 + e * 512 + t * 4, __uint_as_float(dq[1][e]));
-      if (!mbar_wait_warp(bar(B2_DKDONE), i & 1, ctl)) return false;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) st_shared_f32(box0 + e * 512 + t * 4, __uint_as_float(dq[0][e]));
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B2_STAGED));   // the producer reduces them
-      return true;
-    };
     bool ok = n_it > 0;
-    for (int i = 0; i < n_it && ok; ++i) ok = p_phase(i) && ds_phase(i) && drain(i);
-    // All dQ boxes are read before the epilogue reuses the stage buffers as
-    // scratch.
-    const bool final_ok = ok && n_it > 0 && mbar_wait_warp(bar(B2_DQREAD), 0, ctl) &&
-                          mbar_wait_warp(bar(B2_FINAL), 0, ctl);
+    for (int i = 0; i < n_it && ok; ++i) ok = p_phase(i) && ds_phase(i);
+    // Once every product has completed, K, V and the dS^T buffer are free:
+    // the epilogue stages dk and dv there (and its scratch in the dS^T
+    // buffer) while the reducer may still be reading the last dQ boxes out
+    // of the Q stage and the staging buffer.
+    const bool final_ok = ok && n_it > 0 && mbar_wait_warp(bar(B2_FINAL), 0, ctl);
     tc_fence_after();
-    float* scratch = reinterpret_cast<float*>(smem + C::oQ);
-    const uint32_t sdk = sbase + C::oQ + 4096, sdv = sdk + kBK * D * 2;
+    float* scratch = reinterpret_cast<float*>(smem + C::oS);
+    const uint32_t sdk = sbase + C::oK, sdv = sbase + C::oV;
     kv_epilogue<D>(prm, tmem + cDK + lane_off + X * 64, tmem + cDV + lane_off + X * 64, final_ok, X,
                    t, b, hk, kt, scratch, scratch + 256, sdk, sdv, &tmDK, &tmDV);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kB2MmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -560,6 +572,7 @@ inline swa_status launch_bwd128(const BwdLaunch& f, cudaStream_t st) {
   const int want = (5 * num_sms() + 2 * p.n_ktiles - 1) / (2 * p.n_ktiles);
   p.chunk = want < 1 ? 1 : (want > p.n_bhk ? p.n_bhk : want);
   p.acc_flag = f.acc_flag;
+  p.dkn_out = f.dkn_out;
   const long long n_cta = static_cast<long long>(p.n_ktiles) * p.n_bhk;
   if (n_cta > 0x7fffffffLL) return SWA_ERR_UNSUPPORTED;
   bwd_tc128_kernel<<<static_cast<unsigned>(n_cta), kB2Threads, C::kBytes, st>>>(mq, mk, mv, mg, mdq, mdk,

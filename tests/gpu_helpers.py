@@ -23,17 +23,28 @@ def inputs(p, kind, layer=0, with_gate=False):
     return x
 
 
-def run_library(p, x, reuse_prologue=True):
-    """Forward + backward through the C ABI on cuda:0. Returns CPU tensors."""
+def rope_tables(rows, d, base=10000.0):
+    """Standard rotary tables (angle t * base^(-2c/d)) as fp32 CPU tensors
+    [rows, d/2]; the oracle gets the same fp32 values."""
+    half = d // 2
+    inv = base ** (-np.arange(half) * 2.0 / d)
+    ang = np.arange(rows)[:, None] * inv[None, :]
+    return (torch.tensor(np.cos(ang), dtype=torch.float32), torch.tensor(np.sin(ang), dtype=torch.float32))
+
+
+def run_library(p, x, reuse_prologue=True, rope=None):
+    """Forward + backward through the C ABI on cuda:0. Returns CPU tensors.
+    rope: None or (cos, sin) CPU fp32 tensors."""
     dev = torch.device("cuda:0")
     g = {k: (t.to(dev).contiguous() if t is not None else None) for k, t in x.items()}
+    rp = None if rope is None else tuple(t.to(dev).contiguous() for t in rope)
     o, lse, ws = swa.attention_forward(
         g["q"], g["k"], g["v"], g["gq"], g["gk"], window=p.window, causal=p.causal, eps=p.eps,
-        ve=g["ve"], tok=g["tok"], ve_gate=g["gate"], ve_scale=p.ve_scale)
+        ve=g["ve"], tok=g["tok"], ve_gate=g["gate"], ve_scale=p.ve_scale, rope=rp)
     grads = swa.attention_backward(
         g["q"], g["k"], g["v"], g["gq"], g["gk"], o, lse, g["dO"], window=p.window,
         causal=p.causal, eps=p.eps, ve=g["ve"], tok=g["tok"], ve_gate=g["gate"],
-        ve_scale=p.ve_scale, workspace=ws, reuse_prologue=reuse_prologue)
+        ve_scale=p.ve_scale, workspace=ws, reuse_prologue=reuse_prologue, rope=rp)
     kind = "fp32" if x["q"].dtype == torch.float32 else "bf16"
     status = swa.swa_attn_check_status(ws, kind=kind)
     torch.cuda.synchronize()
@@ -43,7 +54,7 @@ def run_library(p, x, reuse_prologue=True):
     return out
 
 
-def run_oracle(p, x, b_slice=None):
+def run_oracle(p, x, b_slice=None, rope=None):
     f = {k: as_f64(t) for k, t in x.items()}
     tok = x["tok"].numpy() if x["tok"] is not None else None
     gate = f.get("gate")
@@ -55,6 +66,8 @@ def run_oracle(p, x, b_slice=None):
         gate = gate[sl] if gate is not None else None
     kw = dict(window=p.window, causal=p.causal, eps=p.eps, ve=f["ve"], tok=tok, gate=gate,
               ve_scale=p.ve_scale)
+    if rope is not None:
+        kw["rope"] = (rope[0].double().numpy(), rope[1].double().numpy())
     o, lse = oracle.attention_forward(q, k, v, f["gq"], f["gk"], **kw)
     ref = oracle.attention_backward(q, k, v, f["gq"], f["gk"], dO, **kw)
     ref["o"], ref["lse"] = o, lse

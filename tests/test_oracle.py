@@ -512,3 +512,145 @@ def test_band_mask_on_chosen_keys_is_a_column_selection():
         full = orc.band_mask(rows, 50, window, causal)
         np.testing.assert_array_equal(orc.band_mask(rows, 50, window, causal, keys=cols),
                                       full[:, cols])
+
+
+# ---------------------------------------------------------------------------
+# Rotary position embedding (applied to q and k before the QK-norm)
+# ---------------------------------------------------------------------------
+
+def rope_tables(T, d, base=10000.0, offset=0):
+    """Standard rotary tables: angle t * base^(-2c/d) for pair c at position t."""
+    half = d // 2
+    inv = base ** (-np.arange(half) * 2.0 / d)
+    ang = (np.arange(T) + offset)[:, None] * inv[None, :]
+    return np.cos(ang), np.sin(ang)
+
+
+def test_rotary_keeps_norms_and_zero_angle_is_identity():
+    r = rng(40)
+    x = r.standard_normal((2, 7, 3, 8))
+    ang = r.uniform(-10, 10, size=(7, 4))
+    y = orc.rotary(x, np.cos(ang), np.sin(ang))
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-13)
+    z = orc.rotary(x, np.ones((7, 4)), np.zeros((7, 4)))
+    assert np.array_equal(z, x)
+
+
+def test_rotary_quarter_turn_closed_form():
+    # angle pi/2 everywhere: y_c = x_{c+d/2}, y_{c+d/2} = -x_c (the reading's sign)
+    r = rng(41)
+    x = r.standard_normal((1, 5, 2, 6))
+    y = orc.rotary(x, np.zeros((5, 3)), np.ones((5, 3)))
+    np.testing.assert_array_equal(y[..., :3], x[..., 3:])
+    np.testing.assert_array_equal(y[..., 3:], -x[..., :3])
+
+
+def test_rotary_angles_add_and_backward_is_the_inverse_and_adjoint():
+    r = rng(42)
+    x = r.standard_normal((2, 6, 2, 8))
+    a = r.uniform(-3, 3, size=(6, 4))
+    b = r.uniform(-3, 3, size=(6, 4))
+    two = orc.rotary(orc.rotary(x, np.cos(a), np.sin(a)), np.cos(b), np.sin(b))
+    np.testing.assert_allclose(two, orc.rotary(x, np.cos(a + b), np.sin(a + b)), atol=1e-13)
+    y = orc.rotary(x, np.cos(a), np.sin(a))
+    np.testing.assert_allclose(orc.rotary_backward(y, np.cos(a), np.sin(a)), x, atol=1e-13)
+    w = r.standard_normal(x.shape)
+    np.testing.assert_allclose(np.sum(y * w), np.sum(x * orc.rotary_backward(w, np.cos(a), np.sin(a))),
+                               rtol=1e-12)
+
+
+def test_rotary_dot_products_depend_only_on_the_offset():
+    # the property rotary embeddings are built for: <R_t q, R_s k> is a
+    # function of t - s (standard tables), whatever the absolute positions
+    r = rng(43)
+    d = 16
+    qv, kv = r.standard_normal(d), r.standard_normal(d)
+    cos, sin = rope_tables(64, d)
+    x = np.zeros((64, 1, d))
+    x[:] = qv
+    y = np.zeros((64, 1, d))
+    y[:] = kv
+    rq = orc.rotary(x, cos, sin)[:, 0]
+    rk = orc.rotary(y, cos, sin)[:, 0]
+    for off in (0, 3, 17):
+        dots = [rq[t] @ rk[t - off] for t in range(off, 64)]
+        np.testing.assert_allclose(dots, dots[0], rtol=1e-11, atol=1e-11)
+
+
+def test_rotary_sampler_positions_select_table_rows():
+    r = rng(44)
+    x = r.standard_normal((1, 10, 2, 8))
+    cos, sin = rope_tables(10, 8)
+    full = orc.rotary(x, cos, sin)
+    rows = np.array([7, 2, 9])
+    part = orc.rotary(x[0, rows][None], cos, sin, positions=rows)
+    np.testing.assert_allclose(part[0], full[0, rows], atol=1e-15)
+
+
+def test_identity_rope_tables_change_nothing():
+    x = rand_problem(45, B=1, T=10, Hq=2, Hkv=1, d=8, with_ve=True)
+    ident = (np.ones((10, 4)), np.zeros((10, 4)))
+    o0, l0 = fwd(x, window=4)
+    o1, l1 = fwd(x, window=4, rope=ident)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+    g0, g1 = bwd(x, window=4), bwd(x, window=4, rope=ident)
+    for k in ("dq", "dk", "dv", "dgq", "dgk", "dve"):
+        np.testing.assert_allclose(g1[k], g0[k], rtol=0, atol=1e-15)
+
+
+def test_rope_is_undone_by_scale_free_rotation_of_both_sides():
+    # the same rotation at every position leaves all q.k products, hence the
+    # whole attention, unchanged (a global rotation is an isometry)
+    x = rand_problem(46, B=1, T=9, Hq=2, Hkv=1, d=8, with_gain=False)
+    ang = np.tile(np.array([[0.3, -1.1, 2.0, 0.7]]), (9, 1))
+    o0, _ = fwd(x, window=-1)
+    o1, _ = fwd(x, window=-1, rope=(np.cos(ang), np.sin(ang)))
+    np.testing.assert_allclose(o1, o0, atol=1e-12)
+
+
+@pytest.mark.parametrize("window,causal", [(-1, True), (3, True)])
+def test_backward_with_rope_matches_central_finite_differences(window, causal):
+    x = rand_problem(47, B=1, T=8, Hq=2, Hkv=1, d=6, with_ve=True, with_gate=True, vocab=5)
+    cos, sin = rope_tables(8, 6, base=3.0)
+    kw = dict(window=window, causal=causal, eps=1e-4, ve_scale=0.7, rope=(cos, sin))
+    g = bwd(x, **kw)
+    h = 1e-6
+    for name, gname in {"q": "dq", "k": "dk", "gq": "dgq", "gk": "dgk"}.items():
+        base = x[name]
+        num = np.zeros_like(base)
+        it = np.nditer(base, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = base[idx]
+            base[idx] = old + h
+            lp = loss(x, **kw)
+            base[idx] = old - h
+            lm = loss(x, **kw)
+            base[idx] = old
+            num[idx] = (lp - lm) / (2 * h)
+        err = np.linalg.norm(g[gname] - num) / max(np.linalg.norm(num), 1e-30)
+        assert err < 1e-6, (name, err)
+
+
+def test_rope_samplers_agree_with_full_backward():
+    x = rand_problem(48, B=2, T=16, Hq=4, Hkv=2, d=8, with_ve=True, with_gate=True)
+    cos, sin = rope_tables(16, 8)
+    kw = dict(window=5, eps=1e-5, ve_scale=0.5, rope=(cos, sin))
+    o, lse = fwd(x, **kw)
+    g = bwd(x, **kw)
+    rows = np.array([0, 6, 15])
+    for b in range(2):
+        for h in range(4):
+            ro, rl = orc.attention_forward_rows(x["q"], x["k"], x["v"], x["gq"], x["gk"], b=b, h=h,
+                                                rows=rows, ve=x["ve"], tok=x["tok"], gate=x["gate"],
+                                                **kw)
+            np.testing.assert_allclose(ro, o[b, rows, h], atol=1e-12)
+            dq = orc.attention_backward_rows(x["q"], x["k"], x["v"], x["gq"], x["gk"], x["dO"], b=b, h=h,
+                                             rows=rows, ve=x["ve"], tok=x["tok"], gate=x["gate"], **kw)
+            np.testing.assert_allclose(dq, g["dq"][b, rows, h], atol=1e-12)
+        for hk in range(2):
+            dk, dv = orc.attention_backward_cols(x["q"], x["k"], x["v"], x["gq"], x["gk"], x["dO"], b=b,
+                                                 hk=hk, cols=rows, ve=x["ve"], tok=x["tok"],
+                                                 gate=x["gate"], **kw)
+            np.testing.assert_allclose(dk, g["dk"][b, rows, hk], atol=1e-12)
+            np.testing.assert_allclose(dv, g["dv"][b, rows, hk], atol=1e-12)

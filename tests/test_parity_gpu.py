@@ -187,3 +187,41 @@ def test_forward_of_another_problem_in_between_keeps_the_backward_right(zeroing)
     got = _grads_bf16(X, gx, ox, lx, ws, ws_bytes=nbytes, flags=0)
     assert swa.swa_attn_check_status(ws) == swa.SWA_OK
     compare(got, run_oracle(X, xx), TOL["bf16"], keys=("dq", "dk", "dv", "dgq", "dgk"))
+
+
+# Rotary position embedding fused into the prologue (rotation, then the norm)
+# and into the backward (norm backward of the rotated rows, then the
+# transposed rotation). Tables with more rows than T; positions start at 0.
+ROPE_CASES = {
+    "ragged_gqa_ve": CASES["ragged_gqa_ve"],
+    "full_causal_d64": CASES["full_causal_d64"],
+    "noncausal_window": CASES["noncausal_window"],
+    "long_window_ragged": CASES["long_window_ragged"],
+}
+
+
+@pytest.mark.parametrize("kind", ["bf16", "fp32"])
+@pytest.mark.parametrize("name", list(ROPE_CASES))
+def test_parity_with_rope(kind, name):
+    from gpu_helpers import rope_tables
+    p = ROPE_CASES[name]
+    x = inputs(p, kind, layer=3, with_gate=True)
+    rope = rope_tables(p.T + 7, p.d)
+    got = run_library(p, x, rope=rope)
+    assert got["status"] == swa.SWA_OK
+    compare(got, run_oracle(p, x, rope=rope), TOL[kind])
+
+
+def test_rope_without_prologue_reuse_and_identity_tables():
+    from gpu_helpers import rope_tables
+    p = CASES["ragged_gqa_ve"]
+    x = inputs(p, "bf16", with_gate=True)
+    rope = rope_tables(p.T, p.d)
+    a = run_library(p, x, reuse_prologue=False, rope=rope)
+    compare(a, run_oracle(p, x, rope=rope), TOL["bf16"])
+    # identity tables (cos 1, sin 0) give exactly the result without rotary
+    ident = (torch.ones(p.T, p.d // 2), torch.zeros(p.T, p.d // 2))
+    b = run_library(p, x, rope=ident)
+    c = run_library(p, x)
+    for k in ("o", "lse"):
+        assert torch.equal(b[k], c[k]), k

@@ -106,7 +106,7 @@ def compare(got, ref, tol, keys=("o", "lse", "dq", "dk", "dv", "dgq", "dgk", "dv
     return errs
 
 
-def run_staged(p, x, dev=None):
+def run_staged(p, x, dev=None, rope=None):
     """Forward + backward through the C ABI exactly as the benchmark calls
     it: swa_attn_fwd with the ve gate left out, then the three backward
     stages one call at a time with the prologue outputs reused. Returns CPU
@@ -125,13 +125,15 @@ def run_staged(p, x, dev=None):
     dgk = torch.empty(p.d, device=dev) if g["gk"] is not None else None
     dve = torch.empty(g["ve"].shape, device=dev) if p.ve else None
     gate = g.get("gate")
-    st = swa.swa_attn_fwd(prm, g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"], g["tok"], gate,
-                          o, lse, ws, kind=kind)
+    rt = None if rope is None else tuple(t.to(dev).contiguous() for t in rope)
+    rp = None if rope is None else swa.make_rope(*rt)
+    st = swa.swa_attn_fwd_rope(prm, rp, g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"], g["tok"],
+                               gate, o, lse, ws, kind=kind)
     assert st == swa.SWA_OK, swa.swa_strerror(st)
     for stage in (swa.SWA_BWD_STAGE_PRE, swa.SWA_BWD_STAGE_MAIN, swa.SWA_BWD_STAGE_POST):
-        st = swa.swa_attn_bwd(prm, g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"], g["tok"],
-                              gate, o, lse, g["dO"], dq, dk, dv, dgq, dgk, dve, ws,
-                              flags=swa.SWA_REUSE_PROLOGUE | stage, kind=kind)
+        st = swa.swa_attn_bwd_rope(prm, rp, g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"],
+                                   g["tok"], gate, o, lse, g["dO"], dq, dk, dv, dgq, dgk, dve, ws,
+                                   flags=swa.SWA_REUSE_PROLOGUE | stage, kind=kind)
         assert st == swa.SWA_OK, swa.swa_strerror(st)
     status = swa.swa_attn_check_status(ws, kind=kind)
     torch.cuda.synchronize()

@@ -23,7 +23,7 @@ import oracle
 import sliding_window_gqa_qk_gb300 as swa
 from sliding_window_gqa_qk_gb300.inputs import (L_LAYER, LONG_L, LONG_S, S_LAYER, Problem,
                                                 as_f64, make_inputs)
-from gpu_helpers import TOL, batch_slice, compare, rel_err, run_oracle, run_staged
+from gpu_helpers import TOL, batch_slice, compare, rel_err, rope_tables, run_oracle, run_staged
 
 pytestmark = pytest.mark.gpu
 
@@ -42,9 +42,9 @@ T2048 = {
 }
 
 
-def _slice_checks(p, x, got, slices):
+def _slice_checks(p, x, got, slices, rope=None):
     for b in slices:
-        ref = run_oracle(p.replace(B=1), batch_slice(x, b))
+        ref = run_oracle(p.replace(B=1), batch_slice(x, b), rope=rope)
         compare({k: got[k][b:b + 1] for k in ("o", "dq", "dk", "dv")} | {"lse": got["lse"][b:b + 1]},
                 ref, TOL_BF16, keys=("o", "lse", "dq", "dk", "dv"))
 
@@ -198,3 +198,19 @@ def test_maximum_sequence_length_sampled():
     errs = {k: rel_err(np.concatenate(a), np.concatenate(r)) for k, (a, r) in acc.items()}
     bad = {k: e for k, e in errs.items() if not e <= TOL_BF16}
     assert not bad, f"relative errors above {TOL_BF16}: {bad} (all: {errs})"
+
+
+def test_full_size_value_embedding_s_layer_with_rope():
+    """Layer 1 of the stack (window 1024, value embedding) at B=16, T=2048
+    with standard rotary tables through the _rope calls: two whole batch
+    elements against the oracle, shared gradients by batch additivity."""
+    p, layer = T2048["stack_layer1_s_ve"]
+    x = make_inputs(p, layer=layer)
+    rope = rope_tables(p.T, p.d)
+    got = run_staged(p, x, rope=rope)
+    assert got["status"] == swa.SWA_OK
+    _slice_checks(p, x, got, (0, p.B - 1), rope=rope)
+    per = [run_staged(p.replace(B=1), batch_slice(x, b), rope=rope) for b in range(p.B)]
+    for k in ("dgq", "dgk", "dve"):
+        total = sum(r[k].double() for r in per)
+        assert rel_err(got[k], as_f64(total)) <= TOL_SUM, k

@@ -187,6 +187,7 @@ WORKLOADS = {
     "s_layer": "one S layer (B=16, T=2048, Hq=6, Hkv=3, d=128, window 1024, no VE)",
     "l_layer": "one L layer (B=16, T=2048, Hq=6, Hkv=3, d=128, full causal, no VE)",
     "stack_rope": WORKLOAD[:-1] + ", rotary tables (base 10000) fused before the QK-norm)",
+    "stack_full": WORKLOAD[:-1] + ", rotary tables, learned VE gate 2 sigmoid(W x[:32]) on the VE layers)",
 }
 
 
@@ -203,13 +204,14 @@ class Stack:
         self.swa = swa
         self.dev = dev
         self.rope = None
-        if workload == "stack_rope":
+        self.learned_gate = workload == "stack_full"
+        if workload in ("stack_rope", "stack_full"):
             # standard rotary tables: angle t * 10000^(-2c/d), positions 0..T-1
             inv = 10000.0 ** (-torch.arange(D // 2, dtype=torch.float64) * 2.0 / D)
             ang = torch.arange(T, dtype=torch.float64)[:, None] * inv[None, :]
             self.rope_t = (torch.cos(ang).float().to(dev).contiguous(),
                            torch.sin(ang).float().to(dev).contiguous())
-            self.rope = swa.make_rope(*self.rope_t)
+            self.rope = swa.make_extras(rope=self.rope_t)
         self.sched = schedule_for(workload, swa.swa_sssl_window, swa.swa_has_ve)
         self.layers = []
         for li, (W, ve) in enumerate(self.sched):
@@ -227,15 +229,26 @@ class Stack:
             L["dgq"] = torch.empty(D, dtype=torch.float32, device=dev)
             L["dgk"] = torch.empty(D, dtype=torch.float32, device=dev)
             L["dve"] = (torch.empty(g["ve"].shape, dtype=torch.float32, device=dev) if ve else None)
+            L["ex"] = self.rope
+            if self.learned_gate and ve:
+                # block input rows [B, T, 768] (the gate reads 32 channels) and
+                # gate weights [Hkv, 32], seeded per layer
+                gen = torch.Generator().manual_seed(1000 + li)
+                L["gx"] = torch.randn(B, T, 768, generator=gen).to(torch.bfloat16).to(dev)
+                L["gw"] = (0.1 * torch.randn(HKV, 32, generator=gen)).to(dev)
+                L["dgw"] = torch.empty(HKV, 32, dtype=torch.float32, device=dev)
+                L["dgx"] = torch.empty(B, T, 32, dtype=torch.float32, device=dev)
+                L["ex"] = swa.make_extras(rope=self.rope_t, gate_x=L["gx"], gate_w=L["gw"],
+                                          d_gate_w=L["dgw"], d_gate_x=L["dgx"])
             self.layers.append(L)
         self.flops_fwd = sum(flops(B, T, HQ, D, W)[0] for W, _ in self.sched)
         self.flops_bwd = sum(flops(B, T, HQ, D, W)[1] for W, _ in self.sched)
 
     def fwd(self, L):
         g = L["g"]
-        if self.rope is not None:
-            st = self.swa.swa_attn_fwd_rope(L["prm"], self.rope, g["q"], g["k"], g["v"], g["gq"], g["gk"],
-                                            g["ve"], g["tok"], None, L["o"], L["lse"], L["ws"])
+        if L["ex"] is not None:
+            st = self.swa.swa_attn_fwd_ex(L["prm"], L["ex"], g["q"], g["k"], g["v"], g["gq"], g["gk"],
+                                          g["ve"], g["tok"], None, L["o"], L["lse"], L["ws"])
         else:
             st = self.swa.swa_attn_fwd(L["prm"], g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"],
                                        g["tok"], None, L["o"], L["lse"], L["ws"])
@@ -246,9 +259,9 @@ class Stack:
         g = L["g"]
         args = (g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"], g["tok"], None, L["o"], L["lse"],
                 g["dO"], L["dq"], L["dk"], L["dv"], L["dgq"], L["dgk"], L["dve"], L["ws"])
-        if self.rope is not None:
-            st = self.swa.swa_attn_bwd_rope(L["prm"], self.rope, *args,
-                                            flags=self.swa.SWA_REUSE_PROLOGUE | stage)
+        if L["ex"] is not None:
+            st = self.swa.swa_attn_bwd_ex(L["prm"], L["ex"], *args,
+                                          flags=self.swa.SWA_REUSE_PROLOGUE | stage)
         else:
             st = self.swa.swa_attn_bwd(L["prm"], *args, flags=self.swa.SWA_REUSE_PROLOGUE | stage)
         if st != 0:
@@ -277,8 +290,13 @@ class Stack:
                     ev[name][-1][1].record()
 
     # launches of our kernels per layer and step: fwd = prologue + attention;
-    # bwd = pre + main + post + gain sum
+    # bwd = pre + main + post + gain sum (+ the learned gate's backward and
+    # its weight-gradient sum on VE layers)
     LAUNCHES_PER_LAYER = 2 + 4
+
+    def launches_per_step(self):
+        return sum(self.LAUNCHES_PER_LAYER + (2 if (self.learned_gate and ve) else 0)
+                   for _, ve in self.sched)
 
 
 def _ev_pair():
@@ -348,7 +366,7 @@ def run_ours(args, rank, world, dev):
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": NCU_TRAFFIC_BYTES,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops_sustained)"},
-        "gpu_launches": Stack.LAUNCHES_PER_LAYER * n_layer * args.steps,
+        "gpu_launches": stack.launches_per_step() * args.steps,
         "clocks": clocks.summary(t0, t1),
     }
     if not args.skip_e2e:

@@ -142,7 +142,8 @@ swa_status swa_attn_fwd(const swa_params* p, const void* q, const void* k, const
  *                    gradient with respect to it.
  *   dve              may be NULL; when non-NULL (and ve != NULL) it receives
  *                    the gradient of the VE table, zero in rows no token used.
- * The gradient of the VE gate is not produced (the gate is an input).
+ * The gradient of a given ve_gate is not produced (it is an input); the
+ * learned gate of swa_attn_bwd_ex produces its own gradients.
  * flags: SWA_REUSE_PROLOGUE and the SWA_BWD_STAGE_* bits.
  */
 swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const void* v,
@@ -152,40 +153,65 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
                         void* workspace, size_t ws_bytes, unsigned flags, void* stream);
 
 /*
- * Rotary position embedding fused into the QK-norm prologue (rotation first,
- * then the norm, so the norm comes right before the dot product, as in the
- * autoresearch train.py walkthrough post, model paragraph; the Administrator
- * & Developer Guide §8.2.1 model table, "Rotary embeddings" row, has the
- * cos / sin tables precomputed once by the caller). The pages print neither
- * the channel pairing nor the sign; this library pairs channel c with
- * c + d/2 and turns the pair of position t by the angle of row t, column c:
+ * Extras of the _ex entry points (each part optional; all-NULL extras, or a
+ * NULL pointer, make them identical to swa_attn_fwd / swa_attn_bwd).
+ *
+ * Rotary position embedding, fused into the QK-norm prologue (rotation
+ * first, then the norm, so the norm comes right before the dot product, as
+ * in the autoresearch train.py walkthrough post, model paragraph; the
+ * Administrator & Developer Guide §8.2.1 model table, "Rotary embeddings"
+ * row, has the cos / sin tables precomputed once by the caller). The pages
+ * print neither the channel pairing nor the sign; this library pairs channel
+ * c with c + d/2 and turns the pair of position t by the angle of row t,
+ * column c:
  *   y_c       =  x_c cos[t][c] + x_{c+d/2} sin[t][c]
  *   y_{c+d/2} = -x_c sin[t][c] + x_{c+d/2} cos[t][c]        (c < d/2)
- * Tables: fp32, row-major [rows][d/2], device pointers, 16-byte aligned,
- * rows >= T (row t is position t). cos and sin both NULL (or rope NULL):
- * no rotation, identical to swa_attn_fwd / swa_attn_bwd.
+ *   rope_cos, rope_sin  fp32 [rope_rows][d/2] row-major, 16-byte aligned,
+ *                       rope_rows >= T (row t is position t); both NULL: none.
+ *
+ * Learned value-embedding gate (Guide §8.2.1, the gate snippet): on VE
+ * calls, gate[b,t,h] = 2 * sigmoid(sum_c gate_w[h][c] * gate_x[b,t,c]), used
+ * in place of the ve_gate argument (which must then be NULL):
+ *   gate_x         elem (bf16 / fp32 per library) rows of the block input;
+ *                  channel c of position (b, t) at gate_x[(b*T + t)*gate_x_stride + c]
+ *   gate_x_stride  elements between consecutive (b, t) rows (>= gate_ch)
+ *   gate_w         fp32 [Hkv][gate_ch]; NULL: no learned gate
+ *   gate_ch        1 .. 32 channels (32 in the pages); Hkv <= 32
+ *   d_gate_w       backward output, fp32 [Hkv][gate_ch] (overwritten), or NULL
+ *   d_gate_x       backward output, fp32 [B, T, gate_ch] (overwritten): the
+ *                  gradient of the channels read (the caller adds it into
+ *                  its gradient of the block input), or NULL
+ * The forward keeps the gate values in the workspace for the backward.
  */
 typedef struct {
-  const float* cos;
-  const float* sin;
-  int rows;
-} swa_rope;
+  const float* rope_cos;
+  const float* rope_sin;
+  int rope_rows;
+  const void* gate_x;
+  long long gate_x_stride;
+  const float* gate_w;
+  int gate_ch;
+  float* d_gate_w;
+  float* d_gate_x;
+} swa_extras;
 
-/* swa_attn_fwd with the rotary tables (arguments otherwise identical). */
-swa_status swa_attn_fwd_rope(const swa_params* p, const swa_rope* rope, const void* q, const void* k,
-                             const void* v, const float* gq, const float* gk, const void* ve,
-                             const int32_t* tok, const float* ve_gate, void* o, float* lse,
-                             void* workspace, size_t ws_bytes, unsigned flags, void* stream);
+/* swa_attn_fwd with extras (arguments otherwise identical). */
+swa_status swa_attn_fwd_ex(const swa_params* p, const swa_extras* ex, const void* q, const void* k,
+                           const void* v, const float* gq, const float* gk, const void* ve,
+                           const int32_t* tok, const float* ve_gate, void* o, float* lse,
+                           void* workspace, size_t ws_bytes, unsigned flags, void* stream);
 
-/* swa_attn_bwd with the rotary tables: dq and dk are the gradients of the
- * unrotated q and k (the transposed rotation of the norm backward's result).
- * A backward with SWA_REUSE_PROLOGUE needs the same tables as its forward. */
-swa_status swa_attn_bwd_rope(const swa_params* p, const swa_rope* rope, const void* q, const void* k,
-                             const void* v, const float* gq, const float* gk, const void* ve,
-                             const int32_t* tok, const float* ve_gate, const void* o,
-                             const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                             float* dgq, float* dgk, float* dve, void* workspace, size_t ws_bytes,
-                             unsigned flags, void* stream);
+/* swa_attn_bwd with extras: with rotary, dq and dk are the gradients of the
+ * unrotated q and k (the transposed rotation of the norm backward's result);
+ * with the learned gate, d_gate_w and d_gate_x as above (written by the POST
+ * stage). A backward with SWA_REUSE_PROLOGUE needs the same extras as its
+ * forward. */
+swa_status swa_attn_bwd_ex(const swa_params* p, const swa_extras* ex, const void* q, const void* k,
+                           const void* v, const float* gq, const float* gk, const void* ve,
+                           const int32_t* tok, const float* ve_gate, const void* o,
+                           const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                           float* dgq, float* dgk, float* dve, void* workspace, size_t ws_bytes,
+                           unsigned flags, void* stream);
 
 /*
  * Forward without a caller-provided workspace: the same computation and

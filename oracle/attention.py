@@ -36,6 +36,9 @@ Readings where the pages are silent (each one is listed in the design doc):
     caller): applied to q and k before the norm, pairing channel c with
     c + d/2 and turning the pair by the angle of table entry [t, c]:
     y_c = x_c cos + x_{c+d/2} sin, y_{c+d/2} = -x_c sin + x_{c+d/2} cos.
+  * Learned VE gate (optional, ``gate_x`` [B, T, C] and ``gate_w`` [Hkv, C]):
+    gate[b, t, h] = 2 * sigmoid(<gate_w[h], gate_x[b, t]>), in place of a
+    given ``gate``; the backward then also returns its gradients.
 
 parity pinned: every function here is checked in ``tests/test_oracle.py``
 against the pages' worked examples, closed forms, invariants, brute force,
@@ -56,6 +59,7 @@ __all__ = [
     "rms_norm",
     "rms_norm_backward",
     "ve_mix",
+    "learned_gate",
     "band_mask",
     "attention_logits",
     "attention_forward",
@@ -191,6 +195,30 @@ def ve_mix(v: np.ndarray, ve, tok, gate, ve_scale: float) -> np.ndarray:
     return v + ve_scale * g[..., None] * rows
 
 
+def learned_gate(gate_x, gate_w) -> np.ndarray:
+    """The value-embedding gate of [Guide] §8.2.1 (the printed gate snippet):
+    2 * sigmoid of a bias-free linear map of the first C channels of the
+    block input, one output per kv head:
+      gate[b, t, h] = 2 / (1 + exp(-sum_c gate_w[h, c] * gate_x[b, t, c])).
+    With gate_w = 0 (its initialisation) the gate is 1 everywhere."""
+    z = np.asarray(gate_x, dtype=np.float64) @ np.asarray(gate_w, dtype=np.float64).T
+    return 2.0 / (1.0 + np.exp(-z))
+
+
+def learned_gate_backward(gate_x, gate_w, dgate):
+    """Gradients of ``learned_gate`` for an upstream dgate [B, T, Hkv]:
+    with s = sigmoid(z), d gate / dz = 2 s (1 - s), so
+      dz = dgate * 2 s (1 - s);  dgate_x = dz gate_w;  dgate_w = sum_{b,t} dz^T gate_x.
+    Returns (dgate_x [B, T, C], dgate_w [Hkv, C])."""
+    x = np.asarray(gate_x, dtype=np.float64)
+    w = np.asarray(gate_w, dtype=np.float64)
+    sg = 1.0 / (1.0 + np.exp(-(x @ w.T)))
+    dz = np.asarray(dgate, dtype=np.float64) * 2.0 * sg * (1.0 - sg)
+    dx = dz @ w
+    dw = dz.reshape(-1, w.shape[0]).T @ x.reshape(-1, x.shape[-1])
+    return dx, dw
+
+
 # ----------------------------------------------------------------------------
 # Mask and attention
 # ----------------------------------------------------------------------------
@@ -258,7 +286,8 @@ def _softmax_rows(S: np.ndarray, M: np.ndarray):
 
 def attention_forward(q, k, v, gq=None, gk=None, *, window: int, causal: bool = True,
                       scale=None, eps: float = 1e-6, ve=None, tok=None, gate=None,
-                      ve_scale: float = 0.5, row_chunk: int = 1024, rope=None):
+                      ve_scale: float = 0.5, row_chunk: int = 1024, rope=None,
+                      gate_x=None, gate_w=None):
     """Forward of the attention block: returns (o [B,T,Hq,d], lse [B,Hq,T]).
 
     Steps in the pages' order: rotary of q and k when ``rope`` is given
@@ -275,6 +304,8 @@ def attention_forward(q, k, v, gq=None, gk=None, *, window: int, causal: bool = 
         raise ValueError("Hq must be a multiple of Hkv")
     G = Hq // Hkv
     sc = _scale(d, scale)
+    if gate_w is not None:
+        gate = learned_gate(gate_x, gate_w)
     qn, kn, v_eff = _prep(q, k, v, gq, gk, eps, ve, tok, gate, ve_scale, rope)
     o = np.zeros((B, T, Hq, d))
     lse = np.zeros((B, Hq, T))
@@ -317,7 +348,7 @@ def attention_forward_rows(q, k, v, gq=None, gk=None, *, b: int, h: int, rows,
 def attention_backward(q, k, v, gq=None, gk=None, dO=None, *, window: int,
                        causal: bool = True, scale=None, eps: float = 1e-6, ve=None,
                        tok=None, gate=None, ve_scale: float = 0.5,
-                       row_chunk: int = 1024, rope=None):
+                       row_chunk: int = 1024, rope=None, gate_x=None, gate_w=None):
     """Analytic backward of ``attention_forward`` for the loss <O, dO>.
 
     Per (b, h), with A the masked softmax and kv head hk = h // G:
@@ -331,8 +362,12 @@ def attention_backward(q, k, v, gq=None, gk=None, dO=None, *, window: int,
     dv = dv_eff and dVE[tok] += ve_scale * gate * dv_eff ([Guide] §8.2.1 VE
     mix, differentiated).
 
-    Returns a dict with dq, dk, dv, dgq, dgk (None when the gain is None) and
-    dve ([vocab, Hkv*d], None without VE).
+    With the learned gate (``gate_w``), dgate[b, t, h] = ve_scale *
+    <dv_eff[b, t, h], VE[tok[b, t], h]> goes through ``learned_gate_backward``.
+
+    Returns a dict with dq, dk, dv, dgq, dgk (None when the gain is None),
+    dve ([vocab, Hkv*d], None without VE) and, with the learned gate,
+    dgate_x and dgate_w.
     """
     q = np.asarray(q, dtype=np.float64)
     dO = np.asarray(dO, dtype=np.float64)
@@ -340,6 +375,8 @@ def attention_backward(q, k, v, gq=None, gk=None, dO=None, *, window: int,
     Hkv = np.asarray(k).shape[2]
     G = Hq // Hkv
     sc = _scale(d, scale)
+    if gate_w is not None:
+        gate = learned_gate(gate_x, gate_w)
     qn, kn, v_eff = _prep(q, k, v, gq, gk, eps, ve, tok, gate, ve_scale, rope)
     dqn = np.zeros_like(qn)
     dkn = np.zeros_like(kn)
@@ -367,7 +404,12 @@ def attention_backward(q, k, v, gq=None, gk=None, dO=None, *, window: int,
         contrib = (ve_scale * g[..., None] * dveff).reshape(B * T, Hd)
         dve = np.zeros((np.asarray(ve).shape[0], Hd))
         np.add.at(dve, np.asarray(tok, dtype=np.int64).reshape(-1), contrib)
-    return {"dq": dq, "dk": dk, "dv": dveff, "dgq": dgq, "dgk": dgk, "dve": dve}
+    out = {"dq": dq, "dk": dk, "dv": dveff, "dgq": dgq, "dgk": dgk, "dve": dve}
+    if gate_w is not None:
+        rows = np.asarray(ve, dtype=np.float64).reshape(-1, Hkv, d)[np.asarray(tok, dtype=np.int64)]
+        dgate = ve_scale * np.sum(dveff * rows, axis=-1)          # [B, T, Hkv]
+        out["dgate_x"], out["dgate_w"] = learned_gate_backward(gate_x, gate_w, dgate)
+    return out
 
 
 def _one_batch(q, k, v, dO, tok, gate, b):

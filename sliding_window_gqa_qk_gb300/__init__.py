@@ -25,7 +25,7 @@ from . import build as _build
 __all__ = [
     "swa_params", "SwaError", "load",
     "swa_attn_workspace_size", "swa_attn_workspace_init", "swa_attn_fwd", "swa_attn_bwd",
-    "swa_attn_fwd_rope", "swa_attn_bwd_rope",
+    "swa_attn_fwd_ex", "swa_attn_bwd_ex",
     "swa_attn_fwd_noalloc",
     "swa_attn_check_status", "swa_sssl_window", "swa_has_ve", "swa_strerror",
     "swa_build_info", "attention_forward", "attention_backward", "make_params",
@@ -63,9 +63,13 @@ class SwaError(RuntimeError):
         self.status = status
 
 
-class swa_rope(ctypes.Structure):
-    """Rotary tables of the _rope entry points (see include/swa_attn.h)."""
-    _fields_ = [("cos", ctypes.c_void_p), ("sin", ctypes.c_void_p), ("rows", ctypes.c_int)]
+class swa_extras(ctypes.Structure):
+    """Extras of the _ex entry points: rotary tables and the learned
+    value-embedding gate (see include/swa_attn.h)."""
+    _fields_ = [("rope_cos", ctypes.c_void_p), ("rope_sin", ctypes.c_void_p), ("rope_rows", ctypes.c_int),
+                ("gate_x", ctypes.c_void_p), ("gate_x_stride", ctypes.c_longlong),
+                ("gate_w", ctypes.c_void_p), ("gate_ch", ctypes.c_int),
+                ("d_gate_w", ctypes.c_void_p), ("d_gate_x", ctypes.c_void_p)]
 
 
 _LIBS: dict = {}
@@ -90,11 +94,11 @@ def load(kind: str = "bf16") -> ctypes.CDLL:
     lib.swa_attn_fwd.restype = ctypes.c_int
     lib.swa_attn_bwd.argtypes = [P] + [_vp] * 18 + [ctypes.c_size_t, ctypes.c_uint, _vp]
     lib.swa_attn_bwd.restype = ctypes.c_int
-    R = ctypes.POINTER(swa_rope)
-    lib.swa_attn_fwd_rope.argtypes = [P, R] + [_vp] * 11 + [ctypes.c_size_t, ctypes.c_uint, _vp]
-    lib.swa_attn_fwd_rope.restype = ctypes.c_int
-    lib.swa_attn_bwd_rope.argtypes = [P, R] + [_vp] * 18 + [ctypes.c_size_t, ctypes.c_uint, _vp]
-    lib.swa_attn_bwd_rope.restype = ctypes.c_int
+    R = ctypes.POINTER(swa_extras)
+    lib.swa_attn_fwd_ex.argtypes = [P, R] + [_vp] * 11 + [ctypes.c_size_t, ctypes.c_uint, _vp]
+    lib.swa_attn_fwd_ex.restype = ctypes.c_int
+    lib.swa_attn_bwd_ex.argtypes = [P, R] + [_vp] * 18 + [ctypes.c_size_t, ctypes.c_uint, _vp]
+    lib.swa_attn_bwd_ex.restype = ctypes.c_int
     lib.swa_attn_fwd_noalloc.argtypes = [P] + [_vp] * 10 + [_vp]
     lib.swa_attn_fwd_noalloc.restype = ctypes.c_int
     lib.swa_attn_check_status.argtypes = [_vp, _vp]
@@ -173,30 +177,43 @@ def swa_attn_bwd(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, d
         _ptr(dgk), _ptr(dve), _ptr(ws), n, int(flags), _stream(stream)))
 
 
-def make_rope(cos, sin) -> swa_rope:
-    """swa_rope of two [rows, d/2] fp32 device tensors (None, None: no rotary)."""
-    if cos is None and sin is None:
-        return swa_rope(None, None, 0)
-    return swa_rope(_ptr(cos), _ptr(sin), int(cos.shape[0]))
+def make_extras(rope=None, gate_x=None, gate_w=None, d_gate_w=None, d_gate_x=None) -> swa_extras:
+    """swa_extras from device tensors: rope = (cos, sin) fp32 [rows, d/2] or
+    None; gate_x [B, T, >= C] rows (its row stride is taken from the tensor),
+    gate_w fp32 [Hkv, C] or None; backward outputs d_gate_w [Hkv, C],
+    d_gate_x [B, T, C] (fp32) or None."""
+    e = swa_extras()
+    if rope is not None:
+        e.rope_cos, e.rope_sin, e.rope_rows = _ptr(rope[0]), _ptr(rope[1]), int(rope[0].shape[0])
+    if gate_w is not None:
+        if gate_x.stride(-1) != 1 or gate_x.dim() != 3 or gate_x.stride(0) != gate_x.shape[1] * gate_x.stride(1):
+            raise ValueError("gate_x must be [B, T, *] with unit channel stride and packed rows")
+        e.gate_x = gate_x.data_ptr()
+        e.gate_x_stride = int(gate_x.stride(1))
+        e.gate_w = _ptr(gate_w)
+        e.gate_ch = int(gate_w.shape[1])
+        e.d_gate_w = _ptr(d_gate_w)
+        e.d_gate_x = _ptr(d_gate_x)
+    return e
 
 
-def swa_attn_fwd_rope(p, rope, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, ws, ws_bytes=None,
-                      flags=0, stream=None, kind=None) -> int:
+def swa_attn_fwd_ex(p, ex, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, ws, ws_bytes=None,
+                    flags=0, stream=None, kind=None) -> int:
     kind = kind or _kind_of(q)
     n = ws.numel() if ws_bytes is None else ws_bytes
-    rp = None if rope is None else ctypes.byref(rope)
-    return int(load(kind).swa_attn_fwd_rope(
-        ctypes.byref(p), rp, _ptr(q), _ptr(k), _ptr(v), _ptr(gq), _ptr(gk), _ptr(ve), _ptr(tok),
+    ep = None if ex is None else ctypes.byref(ex)
+    return int(load(kind).swa_attn_fwd_ex(
+        ctypes.byref(p), ep, _ptr(q), _ptr(k), _ptr(v), _ptr(gq), _ptr(gk), _ptr(ve), _ptr(tok),
         _ptr(ve_gate), _ptr(o), _ptr(lse), _ptr(ws), n, int(flags), _stream(stream)))
 
 
-def swa_attn_bwd_rope(p, rope, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, dgq, dgk,
-                      dve, ws, ws_bytes=None, flags=0, stream=None, kind=None) -> int:
+def swa_attn_bwd_ex(p, ex, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, dgq, dgk,
+                    dve, ws, ws_bytes=None, flags=0, stream=None, kind=None) -> int:
     kind = kind or _kind_of(q)
     n = ws.numel() if ws_bytes is None else ws_bytes
-    rp = None if rope is None else ctypes.byref(rope)
-    return int(load(kind).swa_attn_bwd_rope(
-        ctypes.byref(p), rp, _ptr(q), _ptr(k), _ptr(v), _ptr(gq), _ptr(gk), _ptr(ve), _ptr(tok),
+    ep = None if ex is None else ctypes.byref(ex)
+    return int(load(kind).swa_attn_bwd_ex(
+        ctypes.byref(p), ep, _ptr(q), _ptr(k), _ptr(v), _ptr(gq), _ptr(gk), _ptr(ve), _ptr(tok),
         _ptr(ve_gate), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgq),
         _ptr(dgk), _ptr(dve), _ptr(ws), n, int(flags), _stream(stream)))
 
@@ -255,11 +272,13 @@ def new_workspace(p: swa_params, for_backward: bool, device, kind: str, stream=N
 def attention_forward(q, k, v, gq=None, gk=None, *, window: int = -1, causal: bool = True,
                       softmax_scale: float = 0.0, eps: float = 1e-6, ve=None, tok=None,
                       ve_gate=None, ve_scale: float = 0.5, workspace=None, stream=None,
-                      rope=None):
+                      rope=None, gate_x=None, gate_w=None):
     """o, lse, workspace = attention_forward(q, k, v, ...). The workspace is
     allocated for the backward too, so it can be passed on to
     ``attention_backward`` with the prologue outputs kept. ``rope``: None or
-    (cos, sin) fp32 device tensors [rows >= T, d/2] (rotary before the norm)."""
+    (cos, sin) fp32 device tensors [rows >= T, d/2] (rotary before the norm).
+    ``gate_x`` [B, T, >= C] and ``gate_w`` fp32 [Hkv, C]: the learned
+    value-embedding gate 2 sigmoid(gate_w x[:C]) (then ve_gate must be None)."""
     B, T, Hq, d = q.shape
     Hkv = k.shape[2]
     kind = _kind_of(q)
@@ -268,20 +287,23 @@ def attention_forward(q, k, v, gq=None, gk=None, *, window: int = -1, causal: bo
     ws = workspace if workspace is not None else new_workspace(p, True, q.device, kind, stream)
     o = torch.empty_like(q)
     lse = torch.empty(B, Hq, T, dtype=torch.float32, device=q.device)
-    if rope is None:
+    if rope is None and gate_w is None:
         _check(swa_attn_fwd(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, ws, stream=stream),
                "swa_attn_fwd")
     else:
-        _check(swa_attn_fwd_rope(p, make_rope(*rope), q, k, v, gq, gk, ve, tok, ve_gate, o, lse, ws,
-                                 stream=stream), "swa_attn_fwd_rope")
+        ex = make_extras(rope, gate_x, gate_w)
+        _check(swa_attn_fwd_ex(p, ex, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, ws, stream=stream),
+               "swa_attn_fwd_ex")
     return o, lse, ws
 
 
 def attention_backward(q, k, v, gq, gk, o, lse, dO, *, window: int = -1, causal: bool = True,
                        softmax_scale: float = 0.0, eps: float = 1e-6, ve=None, tok=None,
                        ve_gate=None, ve_scale: float = 0.5, workspace=None,
-                       reuse_prologue: bool = False, stream=None, rope=None) -> dict:
-    """Gradients dq, dk, dv, dgq, dgk, dve (dve None without a VE table)."""
+                       reuse_prologue: bool = False, stream=None, rope=None, gate_x=None,
+                       gate_w=None) -> dict:
+    """Gradients dq, dk, dv, dgq, dgk, dve (dve None without a VE table) and,
+    with the learned gate, dgate_w [Hkv, C] and dgate_x [B, T, C]."""
     B, T, Hq, d = q.shape
     Hkv = k.shape[2]
     kind = _kind_of(q)
@@ -293,11 +315,17 @@ def attention_backward(q, k, v, gq, gk, o, lse, dO, *, window: int = -1, causal:
     dgk = torch.empty(d, dtype=torch.float32, device=q.device)
     dve = torch.empty(ve.shape, dtype=torch.float32, device=q.device) if ve is not None else None
     flags = SWA_REUSE_PROLOGUE if (reuse_prologue and workspace is not None) else 0
-    if rope is None:
+    out = {"dq": dq, "dk": dk, "dv": dv, "dgq": dgq, "dgk": dgk, "dve": dve, "workspace": ws}
+    if rope is None and gate_w is None:
         _check(swa_attn_bwd(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, dgq, dgk,
                             dve, ws, flags=flags, stream=stream), "swa_attn_bwd")
     else:
-        _check(swa_attn_bwd_rope(p, make_rope(*rope), q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq,
-                                 dk, dv, dgq, dgk, dve, ws, flags=flags, stream=stream),
-               "swa_attn_bwd_rope")
-    return {"dq": dq, "dk": dk, "dv": dv, "dgq": dgq, "dgk": dgk, "dve": dve, "workspace": ws}
+        dgw = dgx = None
+        if gate_w is not None:
+            dgw = torch.empty(gate_w.shape, dtype=torch.float32, device=q.device)
+            dgx = torch.empty(B, T, gate_w.shape[1], dtype=torch.float32, device=q.device)
+            out["dgate_w"], out["dgate_x"] = dgw, dgx
+        ex = make_extras(rope, gate_x, gate_w, dgw, dgx)
+        _check(swa_attn_bwd_ex(p, ex, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, dgq,
+                               dgk, dve, ws, flags=flags, stream=stream), "swa_attn_bwd_ex")
+    return out

@@ -175,6 +175,7 @@ struct WsLayout {
   size_t veff;      // elem [B, Hkv, T, d]
   size_t rstd_q;    // f32  [B, Hq, T]
   size_t rstd_k;    // f32  [B, Hkv, T]
+  size_t gate;      // f32  [B, T, Hkv]     learned value-embedding gate values
   size_t fwd_end;
   size_t lse2;      // f32  [B, Hq, Tpad]   LSE * log2(e)
   size_t dvec;      // f32  [B, Hq, Tpad]   D = rowsum(dO * O)
@@ -183,6 +184,7 @@ struct WsLayout {
   size_t dv_acc;    // f32  [B, Hkv, T, d]  gradient of v_eff
   size_t gpart;     // f32  [2, post_blocks, d] per-block partial gain gradients
   size_t gpart_k;   // f32  [B * Hkv * ceil(T / 128), d] per-key-tile partials of dgk
+  size_t gpart_w;   // f32  [post_blocks, 32 * 32] per-block partials of the gate weight gradient
   size_t bwd_end;
 };
 
@@ -209,6 +211,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int T, int Hq, int Hkv, int
   L.veff = o; o = align256(o + bt * Hkv * d * es);
   L.rstd_q = o; o = align256(o + bt * Hq * 4);
   L.rstd_k = o; o = align256(o + bt * Hkv * 4);
+  L.gate = o; o = align256(o + bt * Hkv * 4);
   L.fwd_end = o;
   const size_t btp = static_cast<size_t>(B) * static_cast<size_t>(t_pad(T));
   L.lse2 = o; o = align256(o + btp * Hq * 4);
@@ -218,6 +221,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int T, int Hq, int Hkv, int
   L.dv_acc = o; o = align256(o + bt * Hkv * d * 4);
   L.gpart = o; o = align256(o + size_t(2) * post_blocks(B, T, Hq) * d * 4);
   L.gpart_k = o; o = align256(o + static_cast<size_t>(B) * Hkv * ((T + 127) / 128) * d * 4);
+  L.gpart_w = o; o = align256(o + static_cast<size_t>(post_blocks(B, T, Hq)) * 32 * 32 * 4);
   L.bwd_end = o;
   return L;
 }
@@ -235,6 +239,10 @@ struct ProArgs {  // QK-norm + VE-mix prologue
   elem_t* qn; elem_t* kn; elem_t* veff;
   float* rstd_q; float* rstd_k;
   const float* rcos; const float* rsin;   // rotary tables [rows, d/2], NULL: none
+  // learned value-embedding gate (gw NULL: none): input rows, weights
+  // [Hkv][gch], and where the gate values go ([B, T, Hkv])
+  const elem_t* gx; long long gx_stride; const float* gw; int gch;
+  float* gate_out;
   uint32_t* status;
 };
 
@@ -269,10 +277,23 @@ struct PostArgs {  // backward post: RMSNorm backward, dv, dVE, gain partials
 };
 
 struct GainArgs {
-  int d;
+  int d;                          // partial row length (a multiple of 32)
   const float* part_q; int n_q;   // partials of dgq: [n_q][d]
   const float* part_k; int n_k;   // partials of dgk: [n_k][d]
   float* dgq; float* dgk;
+  int n_out;                      // columns written (<= d)
+};
+
+struct GateBwdArgs {  // backward of the learned value-embedding gate
+  int B, T, Hkv, vocab, gch;
+  long long gx_stride;
+  float ve_scale;
+  const elem_t* dv;    // [B, T, Hkv, d] gradient of v_eff (final dv)
+  const elem_t* ve; const int32_t* tok;
+  const float* gate;   // [B, T, Hkv] gate values of the forward
+  const elem_t* gx; const float* gw;
+  float* d_gx;         // [B, T, gch] or NULL
+  float* gpart_w;      // [gridDim.x][1024]: [h * gch + c] partials of the weight gradient
 };
 
 }  // namespace swa

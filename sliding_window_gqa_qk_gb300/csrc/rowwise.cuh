@@ -128,9 +128,10 @@ __device__ __forceinline__ long long grid_warps() {
 // then (nseg = 3: value-embedding layers, and every layer of the fp32 build,
 // which makes a head-major copy of v) the v rows. Inputs are [B, T, H, d];
 // outputs are written head-major [B, H, T, d]. ROPE: q and k rows are
-// rotated (rotate_row) before the norm.
-template <int D, bool ROPE>
-__global__ void __launch_bounds__(kRowWarps * 32, ROPE ? kProBlocksPerSm - 1 : kProBlocksPerSm)
+// rotated (rotate_row) before the norm. GATE: the v rows' gate is the
+// learned 2 sigmoid(<w_h, x[b, t, :C]>), also written to a.gate_out.
+template <int D, bool ROPE, bool GATE>
+__global__ void __launch_bounds__(kRowWarps * 32, (ROPE || GATE) ? kProBlocksPerSm - 1 : kProBlocksPerSm)
     prologue_kernel(ProArgs a) {
   using M = RowMap<D>;
   constexpr int EPL = M::EPL;
@@ -188,7 +189,24 @@ __global__ void __launch_bounds__(kRowWarps * 32, ROPE ? kProBlocksPerSm - 1 : k
       }
     } else {
       uint4 vr[kRowSlots], er[kRowSlots];
-      float sc[kRowSlots];
+      float sc[kRowSlots], lg[kRowSlots];
+      // Learned gate 2 sigmoid(<w_h, x[b, t, :C]>) of each row (all lanes
+      // of the row take part in the dot product).
+      if (GATE) {
+        const int cl = lane % M::LPR;
+#pragma unroll
+        for (int u = 0; u < kRowSlots; ++u) {
+          const int t = tg + u * M::RPI;
+          float z = 0.f;
+          if (t < a.T) {
+            const elem_t* xrow = a.gx + (static_cast<long long>(b) * a.T + t) * a.gx_stride;
+            for (int c = cl; c < a.gch; c += M::LPR) z = fmaf(a.gw[h * a.gch + c], to_f32(xrow[c]), z);
+          }
+          z = row_sum<M::LPR>(z);
+          lg[u] = 2.0f / (1.0f + expf(-z));
+          if (t < a.T && cl == 0) a.gate_out[(static_cast<long long>(b) * a.T + t) * a.Hkv + h] = lg[u];
+        }
+      }
 #pragma unroll
       for (int u = 0; u < kRowSlots; ++u) {
         const int t = tg + u * M::RPI;
@@ -201,7 +219,7 @@ __global__ void __launch_bounds__(kRowWarps * 32, ROPE ? kProBlocksPerSm - 1 : k
         const int tok = a.tok[bt];
         if (tok >= 0 && tok < a.vocab) {
           er[u] = ld16(a.ve + static_cast<long long>(tok) * Hd + h * D + c0);
-          sc[u] = a.ve_scale * (a.gate ? a.gate[bt * a.Hkv + h] : 1.0f);
+          sc[u] = a.ve_scale * (GATE ? lg[u] : (a.gate ? a.gate[bt * a.Hkv + h] : 1.0f));
         } else if (c0 == 0) {
           // An id outside the table contributes nothing and is reported.
           atomicOr(a.status, DEV_ERR_TOKEN);
@@ -403,6 +421,62 @@ __global__ void __launch_bounds__(kRowWarps * 32, kPostBlocksPerSm) bwd_post_ker
   }
 }
 
+// Backward of the learned value-embedding gate (autoresearch Administrator
+// & Developer Guide §8.2.1, gate snippet, differentiated), one warp per
+// position (b, t), persistent: for each kv head h
+//   dgate_h = ve_scale <dv[b, t, h], VE[tok, h]>      (0 for a token outside the table)
+//   dz_h    = dgate_h * gate_h (1 - gate_h / 2)       (d(2 sigmoid)/dz = 2 s (1 - s))
+// then d_gx[b, t, c] = sum_h dz_h w[h, c] (lane c) and the block's partial
+// of dW[h, c] = sum over its positions of dz_h x[b, t, c], reduced over the
+// warps in a fixed order into gpart_w[block][h * gch + c] (rows of 1024).
+template <int D>
+__global__ void __launch_bounds__(kRowWarps * 32) ve_gate_bwd_kernel(GateBwdArgs a) {
+  constexpr int CPL = D / 32;   // channels of d per lane
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long n_tok = static_cast<long long>(a.B) * a.T;
+  const int Hd = a.Hkv * D;
+  float wacc[32];
+#pragma unroll
+  for (int h = 0; h < 32; ++h) wacc[h] = 0.f;
+  for (long long bt = grid_warp(); bt < n_tok; bt += grid_warps()) {
+    const int tk = a.tok[bt];
+    const bool in_table = tk >= 0 && tk < a.vocab;
+    const float xc = lane < a.gch ? to_f32(a.gx[bt * a.gx_stride + lane]) : 0.f;
+    float dgx = 0.f;
+#pragma unroll
+    for (int h = 0; h < 32; ++h) {
+      if (h >= a.Hkv) break;
+      float dot = 0.f;
+      if (in_table) {
+        const elem_t* dvr = a.dv + (bt * a.Hkv + h) * D + lane * CPL;
+        const elem_t* ver = a.ve + static_cast<long long>(tk) * Hd + h * D + lane * CPL;
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) dot = fmaf(to_f32(dvr[e]), to_f32(ver[e]), dot);
+      }
+      dot = warp_sum(dot);
+      const float g = a.gate[bt * a.Hkv + h];
+      const float dz = a.ve_scale * dot * g * (1.f - 0.5f * g);
+      wacc[h] = fmaf(dz, xc, wacc[h]);
+      if (lane < a.gch) dgx = fmaf(dz, a.gw[h * a.gch + lane], dgx);
+    }
+    if (a.d_gx != nullptr && lane < a.gch) a.d_gx[bt * a.gch + lane] = dgx;
+  }
+  __shared__ float red[kRowWarps][32];
+#pragma unroll
+  for (int h = 0; h < 32; ++h) {
+    if (h >= a.Hkv) break;   // uniform over the block
+    red[warp][lane] = wacc[h];
+    __syncthreads();
+    if (warp == 0 && lane < a.gch) {
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < kRowWarps; ++w) s += red[w][lane];
+      a.gpart_w[static_cast<long long>(blockIdx.x) * 1024 + h * a.gch + lane] = s;
+    }
+    __syncthreads();
+  }
+}
+
 // Blocks of a persistent row-wise launch: `per_sm` per SM, no more than
 // there are row groups (nor than `cap`).
 inline int row_grid(long long groups, int per_sm, int cap) {
@@ -443,7 +517,7 @@ __global__ void __launch_bounds__(kGainWarps * 32) gain_sum_kernel(GainArgs a) {
     float tot = 0.f;
 #pragma unroll
     for (int w = 0; w < kGainWarps; ++w) tot += red[w][lane];
-    out[c] = tot;
+    if (c < a.n_out) out[c] = tot;
   }
 }
 

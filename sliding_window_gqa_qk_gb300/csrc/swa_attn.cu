@@ -41,17 +41,39 @@ struct Call {
   cudaStream_t stream;
   const float* rcos = nullptr;   // rotary tables [rows, d/2], NULL: none
   const float* rsin = nullptr;
+  const elem_t* gx = nullptr;    // learned VE gate: input rows, weights [Hkv][gch]
+  long long gx_stride = 0;
+  const float* gw = nullptr;
+  int gch = 0;
+  float* d_gw = nullptr;         // its gradients (backward outputs, NULL: skip)
+  float* d_gx = nullptr;
 };
 
-// Rotary tables of a call: none (NULL or NULL tables), or both tables,
-// 16-byte aligned, with at least T rows.
-swa_status set_rope(Call& c, const swa_rope* r) {
-  if (r == nullptr || (r->cos == nullptr && r->sin == nullptr)) return SWA_OK;
-  if (r->cos == nullptr || r->sin == nullptr || !aligned(r->cos, 16) || !aligned(r->sin, 16) ||
-      r->rows < c.p.T)
-    return SWA_ERR_INVALID_ARG;
-  c.rcos = r->cos;
-  c.rsin = r->sin;
+// Extras of a call. Rotary: none (both tables NULL), or both tables, 16-byte
+// aligned, with at least T rows. Learned gate: gate_w NULL (none), or
+// gate_x and gate_w set, 1 <= gate_ch <= 32, gate_x_stride >= gate_ch,
+// Hkv <= 32, and no ve_gate argument.
+constexpr int kMaxGateCh = 32, kMaxGateHeads = 32;
+swa_status set_extras(Call& c, const swa_extras* e, const float* ve_gate) {
+  if (e == nullptr) return SWA_OK;
+  if (e->rope_cos != nullptr || e->rope_sin != nullptr) {
+    if (e->rope_cos == nullptr || e->rope_sin == nullptr || !aligned(e->rope_cos, 16) ||
+        !aligned(e->rope_sin, 16) || e->rope_rows < c.p.T)
+      return SWA_ERR_INVALID_ARG;
+    c.rcos = e->rope_cos;
+    c.rsin = e->rope_sin;
+  }
+  if (e->gate_w != nullptr) {
+    if (e->gate_x == nullptr || e->gate_ch < 1 || e->gate_ch > kMaxGateCh ||
+        e->gate_x_stride < e->gate_ch || c.p.Hkv > kMaxGateHeads || ve_gate != nullptr)
+      return SWA_ERR_INVALID_ARG;
+    c.gx = static_cast<const elem_t*>(e->gate_x);
+    c.gx_stride = e->gate_x_stride;
+    c.gw = e->gate_w;
+    c.gch = e->gate_ch;
+    c.d_gw = e->d_gate_w;
+    c.d_gx = e->d_gate_x;
+  }
   return SWA_OK;
 }
 
@@ -121,19 +143,24 @@ swa_status run_prologue(const Call& c, const elem_t* q, const elem_t* k, const e
   a.qn = at<elem_t>(c, c.L.qn); a.kn = at<elem_t>(c, c.L.kn); a.veff = at<elem_t>(c, c.L.veff);
   a.rstd_q = at<float>(c, c.L.rstd_q); a.rstd_k = at<float>(c, c.L.rstd_k);
   a.rcos = c.rcos; a.rsin = c.rsin;
+  if (ve != nullptr && c.gw != nullptr) {
+    a.gx = c.gx; a.gx_stride = c.gx_stride; a.gw = c.gw; a.gch = c.gch;
+    a.gate_out = at<float>(c, c.L.gate);
+  }
   a.status = at<uint32_t>(c, c.L.status);
   a.nseg = (ve != nullptr || copy_v) ? 3 : 2;
   const int rg = p.d == 64 ? RowMap<64>::RG : RowMap<128>::RG;
   const long long ngt = (p.T + rg - 1) / rg;
   const long long groups = ngt * p.B * (p.Hq + p.Hkv * (a.nseg - 1));
-  const bool rope = a.rcos != nullptr;
-  const int grid = row_grid(groups, rope ? kProBlocksPerSm - 1 : kProBlocksPerSm, 0);
+  const bool rope = a.rcos != nullptr, learned = a.gw != nullptr;
+  const int grid = row_grid(groups, (rope || learned) ? kProBlocksPerSm - 1 : kProBlocksPerSm, 0);
+  auto launch = [&](auto kern) { kern<<<grid, kRowWarps * 32, 0, c.stream>>>(a); };
   if (p.d == 64) {
-    if (rope) prologue_kernel<64, true><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
-    else prologue_kernel<64, false><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
+    if (rope) learned ? launch(prologue_kernel<64, true, true>) : launch(prologue_kernel<64, true, false>);
+    else learned ? launch(prologue_kernel<64, false, true>) : launch(prologue_kernel<64, false, false>);
   } else {
-    if (rope) prologue_kernel<128, true><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
-    else prologue_kernel<128, false><<<grid, kRowWarps * 32, 0, c.stream>>>(a);
+    if (rope) learned ? launch(prologue_kernel<128, true, true>) : launch(prologue_kernel<128, true, false>);
+    else learned ? launch(prologue_kernel<128, false, true>) : launch(prologue_kernel<128, false, false>);
   }
   return launched();
 }
@@ -175,14 +202,14 @@ namespace {
 // The forward of swa_attn_fwd. prepare_bwd: a workspace sized for the
 // backward also gets its dQ accumulator zeroed by the forward kernel (the
 // no-allocation entry point passes false).
-swa_status fwd_impl(const swa_params* p, const swa_rope* rope, const void* q, const void* k,
+swa_status fwd_impl(const swa_params* p, const swa_extras* ex, const void* q, const void* k,
                     const void* v, const float* gq, const float* gk, const void* ve,
                     const int32_t* tok, const float* ve_gate, void* o, float* lse, void* workspace,
                     size_t ws_bytes, unsigned flags, void* stream, bool prepare_bwd) {
   Call c;
   swa_status s = begin(c, p, workspace, ws_bytes, false, stream);
   if (s != SWA_OK) return s;
-  if ((s = set_rope(c, rope)) != SWA_OK) return s;
+  if ((s = set_extras(c, ex, ve_gate)) != SWA_OK) return s;
   if ((flags & ~SWA_REUSE_PROLOGUE) != 0) return SWA_ERR_INVALID_ARG;
   if (!tensor_ok(q) || !tensor_ok(k) || !tensor_ok(v) || !tensor_ok(o) || lse == nullptr)
     return SWA_ERR_INVALID_ARG;
@@ -241,7 +268,7 @@ swa_status fwd_impl(const swa_params* p, const swa_rope* rope, const void* q, co
 #endif
 }
 
-swa_status bwd_impl(const swa_params* p, const swa_rope* rope, const void* q, const void* k,
+swa_status bwd_impl(const swa_params* p, const swa_extras* ex, const void* q, const void* k,
                     const void* v, const float* gq, const float* gk, const void* ve,
                     const int32_t* tok, const float* ve_gate, const void* o, const float* lse,
                     const void* dO, void* dq, void* dk, void* dv, float* dgq, float* dgk, float* dve,
@@ -249,7 +276,10 @@ swa_status bwd_impl(const swa_params* p, const swa_rope* rope, const void* q, co
   Call c;
   swa_status s = begin(c, p, workspace, ws_bytes, true, stream);
   if (s != SWA_OK) return s;
-  if ((s = set_rope(c, rope)) != SWA_OK) return s;
+  if ((s = set_extras(c, ex, ve_gate)) != SWA_OK) return s;
+  // with the learned gate, the gate values are the ones the forward (or the
+  // prologue below) left in the workspace
+  const float* gate_vals = (ve != nullptr && c.gw != nullptr) ? at<float>(c, c.L.gate) : ve_gate;
   const unsigned known = SWA_REUSE_PROLOGUE | SWA_BWD_STAGE_PRE | SWA_BWD_STAGE_MAIN | SWA_BWD_STAGE_POST;
   if ((flags & ~known) != 0) return SWA_ERR_INVALID_ARG;
   if (!tensor_ok(q) || !tensor_ok(k) || !tensor_ok(v) || !tensor_ok(o) || !tensor_ok(dO) ||
@@ -267,6 +297,9 @@ swa_status bwd_impl(const swa_params* p, const swa_rope* rope, const void* q, co
       if (dgq && cudaMemsetAsync(dgq, 0, sizeof(float) * P.d, st) != cudaSuccess) return SWA_ERR_CUDA;
       if (dgk && cudaMemsetAsync(dgk, 0, sizeof(float) * P.d, st) != cudaSuccess) return SWA_ERR_CUDA;
       if (dve && ve && cudaMemsetAsync(dve, 0, sizeof(float) * P.vocab * P.Hkv * P.d, st) != cudaSuccess)
+        return SWA_ERR_CUDA;
+      if (c.gw && c.d_gw &&
+          cudaMemsetAsync(c.d_gw, 0, sizeof(float) * P.Hkv * c.gch, st) != cudaSuccess)
         return SWA_ERR_CUDA;
     }
     return SWA_OK;
@@ -286,7 +319,7 @@ swa_status bwd_impl(const swa_params* p, const swa_rope* rope, const void* q, co
   constexpr bool kFp32Build = false;
 #endif
   if ((stages & SWA_BWD_STAGE_PRE) && !(flags & SWA_REUSE_PROLOGUE)) {
-    if ((s = run_prologue(c, qe, ke, vin, gq, gk, vee, tok, ve_gate, copy_v)) != SWA_OK) return s;
+    if ((s = run_prologue(c, qe, ke, vin, gq, gk, vee, tok, gate_vals, copy_v)) != SWA_OK) return s;
   }
   if (stages & SWA_BWD_STAGE_PRE) {
     PreArgs a{};
@@ -354,7 +387,7 @@ swa_status bwd_impl(const swa_params* p, const swa_rope* rope, const void* q, co
     b.lse2 = at<float>(c, c.L.lse2); b.dvec = at<float>(c, c.L.dvec); b.Tpad = t_pad(P.T);
     b.dq_acc = at<float>(c, c.L.dq_acc);
     // key-side gradients come out of the kernel's epilogue
-    b.k = ke; b.rstd_k = at<float>(c, c.L.rstd_k); b.gk = gk; b.tok = tok; b.gate = ve_gate;
+    b.k = ke; b.rstd_k = at<float>(c, c.L.rstd_k); b.gk = gk; b.tok = tok; b.gate = gate_vals;
     b.dve = (ve != nullptr) ? dve : nullptr; b.ve_scale = P.ve_scale; b.vocab = P.vocab;
     b.dk = static_cast<elem_t*>(dk); b.dv = static_cast<elem_t*>(dv);
     b.gpart_k = at<float>(c, c.L.gpart_k);
@@ -381,7 +414,7 @@ swa_status bwd_impl(const swa_params* p, const swa_rope* rope, const void* q, co
     PostArgs a{};
     a.B = P.B; a.T = P.T; a.Hq = P.Hq; a.Hkv = P.Hkv; a.d = P.d; a.vocab = P.vocab;
     a.ve_scale = P.ve_scale;
-    a.q = qe; a.k = ke; a.gq = gq; a.gk = gk; a.tok = tok; a.gate = ve_gate;
+    a.q = qe; a.k = ke; a.gq = gq; a.gk = gk; a.tok = tok; a.gate = gate_vals;
     a.rstd_q = at<float>(c, c.L.rstd_q); a.rstd_k = at<float>(c, c.L.rstd_k);
     a.dq_acc = at<float>(c, c.L.dq_acc); a.dk_acc = at<float>(c, c.L.dk_acc);
     a.dv_acc = at<float>(c, c.L.dv_acc);
@@ -409,9 +442,32 @@ swa_status bwd_impl(const swa_params* p, const swa_rope* rope, const void* q, co
                                    : at<float>(c, c.L.gpart_k);
       const int n_k = post_k ? nblk : P.B * P.Hkv * ((P.T + 127) / 128);
 #endif
-      GainArgs g{P.d, at<float>(c, c.L.gpart), nblk, part_k, n_k, dgq, dgk};
+      GainArgs g{P.d, at<float>(c, c.L.gpart), nblk, part_k, n_k, dgq, dgk, P.d};
       gain_sum_kernel<<<dim3(2, P.d / 32), kGainWarps * 32, 0, st>>>(g);
       if ((s = launched()) != SWA_OK) return s;
+    }
+    if (ve != nullptr && c.gw != nullptr && (c.d_gw != nullptr || c.d_gx != nullptr)) {
+      // learned gate: dgate from the final dv, then the gate's own backward
+      GateBwdArgs ga{};
+      ga.B = P.B; ga.T = P.T; ga.Hkv = P.Hkv; ga.vocab = P.vocab; ga.gch = c.gch;
+      ga.gx_stride = c.gx_stride; ga.ve_scale = P.ve_scale;
+      ga.dv = static_cast<const elem_t*>(dv); ga.ve = vee; ga.tok = tok;
+      ga.gate = at<float>(c, c.L.gate); ga.gx = c.gx; ga.gw = c.gw; ga.d_gx = c.d_gx;
+      ga.gpart_w = at<float>(c, c.L.gpart_w);
+      const int gblk = row_grid(static_cast<long long>(P.B) * P.T, kPreBlocksPerSm,
+                                post_blocks(P.B, P.T, P.Hq));
+      if (P.d == 64) ve_gate_bwd_kernel<64><<<gblk, kRowWarps * 32, 0, st>>>(ga);
+      else ve_gate_bwd_kernel<128><<<gblk, kRowWarps * 32, 0, st>>>(ga);
+      if ((s = launched()) != SWA_OK) return s;
+      if (c.d_gw != nullptr) {
+        const int width = P.Hkv * c.gch;
+        GainArgs gw{(width + 31) / 32 * 32, at<float>(c, c.L.gpart_w), gblk, nullptr, 0, c.d_gw,
+                    nullptr, width};
+        // partial rows are 1024 floats apart
+        gw.d = 1024;
+        gain_sum_kernel<<<dim3(1, (width + 31) / 32), kGainWarps * 32, 0, st>>>(gw);
+        if ((s = launched()) != SWA_OK) return s;
+      }
     }
   }
   return SWA_OK;
@@ -445,11 +501,11 @@ swa_status swa_attn_fwd(const swa_params* p, const void* q, const void* k, const
                   stream, true);
 }
 
-swa_status swa_attn_fwd_rope(const swa_params* p, const swa_rope* rope, const void* q, const void* k,
+swa_status swa_attn_fwd_ex(const swa_params* p, const swa_extras* ex, const void* q, const void* k,
                              const void* v, const float* gq, const float* gk, const void* ve,
                              const int32_t* tok, const float* ve_gate, void* o, float* lse,
                              void* workspace, size_t ws_bytes, unsigned flags, void* stream) {
-  return fwd_impl(p, rope, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, workspace, ws_bytes, flags,
+  return fwd_impl(p, ex, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, workspace, ws_bytes, flags,
                   stream, true);
 }
 
@@ -462,13 +518,13 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
                   workspace, ws_bytes, flags, stream);
 }
 
-swa_status swa_attn_bwd_rope(const swa_params* p, const swa_rope* rope, const void* q, const void* k,
+swa_status swa_attn_bwd_ex(const swa_params* p, const swa_extras* ex, const void* q, const void* k,
                              const void* v, const float* gq, const float* gk, const void* ve,
                              const int32_t* tok, const float* ve_gate, const void* o,
                              const float* lse, const void* dO, void* dq, void* dk, void* dv,
                              float* dgq, float* dgk, float* dve, void* workspace, size_t ws_bytes,
                              unsigned flags, void* stream) {
-  return bwd_impl(p, rope, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, dgq, dgk, dve,
+  return bwd_impl(p, ex, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, dgq, dgk, dve,
                   workspace, ws_bytes, flags, stream);
 }
 

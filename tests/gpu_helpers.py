@@ -32,29 +32,45 @@ def rope_tables(rows, d, base=10000.0):
     return (torch.tensor(np.cos(ang), dtype=torch.float32), torch.tensor(np.sin(ang), dtype=torch.float32))
 
 
-def run_library(p, x, reuse_prologue=True, rope=None):
+def gate_weights(p, kind, channels=32, width=48, seed=9):
+    """Inputs of the learned VE gate: block-input rows [B, T, width] (the gate
+    reads the first ``channels``) in the library's element type, and weights
+    [Hkv, channels] fp32 of a size that puts the gate well inside (0, 2)."""
+    g = torch.Generator().manual_seed(seed)
+    gx = torch.randn(p.B, p.T, width, generator=g).to(DTYPE[kind])
+    gw = 0.25 * torch.randn(p.Hkv, channels, generator=g)
+    return gx, gw
+
+
+def run_library(p, x, reuse_prologue=True, rope=None, gate=None):
     """Forward + backward through the C ABI on cuda:0. Returns CPU tensors.
-    rope: None or (cos, sin) CPU fp32 tensors."""
+    rope: None or (cos, sin) CPU fp32 tensors; gate: None or (gate_x, gate_w)
+    CPU tensors of the learned value-embedding gate."""
     dev = torch.device("cuda:0")
     g = {k: (t.to(dev).contiguous() if t is not None else None) for k, t in x.items()}
     rp = None if rope is None else tuple(t.to(dev).contiguous() for t in rope)
+    gx = gw = None
+    if gate is not None:
+        gx, gw = gate[0].to(dev).contiguous(), gate[1].to(dev).contiguous()
     o, lse, ws = swa.attention_forward(
         g["q"], g["k"], g["v"], g["gq"], g["gk"], window=p.window, causal=p.causal, eps=p.eps,
-        ve=g["ve"], tok=g["tok"], ve_gate=g["gate"], ve_scale=p.ve_scale, rope=rp)
+        ve=g["ve"], tok=g["tok"], ve_gate=None if gate is not None else g["gate"], ve_scale=p.ve_scale,
+        rope=rp, gate_x=gx, gate_w=gw)
     grads = swa.attention_backward(
         g["q"], g["k"], g["v"], g["gq"], g["gk"], o, lse, g["dO"], window=p.window,
-        causal=p.causal, eps=p.eps, ve=g["ve"], tok=g["tok"], ve_gate=g["gate"],
-        ve_scale=p.ve_scale, workspace=ws, reuse_prologue=reuse_prologue, rope=rp)
+        causal=p.causal, eps=p.eps, ve=g["ve"], tok=g["tok"],
+        ve_gate=None if gate is not None else g["gate"], ve_scale=p.ve_scale, workspace=ws,
+        reuse_prologue=reuse_prologue, rope=rp, gate_x=gx, gate_w=gw)
     kind = "fp32" if x["q"].dtype == torch.float32 else "bf16"
     status = swa.swa_attn_check_status(ws, kind=kind)
     torch.cuda.synchronize()
     out = {"o": o.cpu(), "lse": lse.cpu(), "status": status}
-    for k in ("dq", "dk", "dv", "dgq", "dgk", "dve"):
-        out[k] = grads[k].cpu() if grads[k] is not None else None
+    for k in ("dq", "dk", "dv", "dgq", "dgk", "dve", "dgate_x", "dgate_w"):
+        out[k] = grads[k].cpu() if grads.get(k) is not None else None
     return out
 
 
-def run_oracle(p, x, b_slice=None, rope=None):
+def run_oracle(p, x, b_slice=None, rope=None, learned=None):
     f = {k: as_f64(t) for k, t in x.items()}
     tok = x["tok"].numpy() if x["tok"] is not None else None
     gate = f.get("gate")
@@ -68,6 +84,11 @@ def run_oracle(p, x, b_slice=None, rope=None):
               ve_scale=p.ve_scale)
     if rope is not None:
         kw["rope"] = (rope[0].double().numpy(), rope[1].double().numpy())
+    if learned is not None:   # (gate_x, gate_w) of the learned VE gate
+        C = learned[1].shape[1]
+        kw["gate"] = None
+        kw["gate_x"] = as_f64(learned[0])[..., :C]
+        kw["gate_w"] = learned[1].double().numpy()
     o, lse = oracle.attention_forward(q, k, v, f["gq"], f["gk"], **kw)
     ref = oracle.attention_backward(q, k, v, f["gq"], f["gk"], dO, **kw)
     ref["o"], ref["lse"] = o, lse
@@ -83,17 +104,18 @@ def rel_err(a, r):
     return float(np.linalg.norm(a - r) / den) if den > 0 else float(np.linalg.norm(a))
 
 
-def compare(got, ref, tol, keys=("o", "lse", "dq", "dk", "dv", "dgq", "dgk", "dve"), sl=None):
+def compare(got, ref, tol, keys=("o", "lse", "dq", "dk", "dv", "dgq", "dgk", "dve", "dgate_x", "dgate_w"),
+            sl=None):
     """Relative error per tensor. Where the oracle's tensor is exactly zero (a
     degenerate case of the method, e.g. window 0 makes dS vanish, so dq, dk and
     the gain gradients are 0), the error is measured against the norm of the
     oracle's dv, the gradient the same terms are built from."""
     errs = {}
     for k in keys:
-        if ref.get(k) is None:
+        if ref.get(k) is None or got.get(k) is None:
             continue
         a = got[k]
-        if sl is not None and k not in ("dgq", "dgk", "dve"):
+        if sl is not None and k not in ("dgq", "dgk", "dve", "dgate_w"):
             a = a[sl]
         if np.linalg.norm(ref[k]) == 0.0 and ref.get("dv") is not None:
             a64 = as_f64(a)
@@ -126,12 +148,12 @@ def run_staged(p, x, dev=None, rope=None):
     dve = torch.empty(g["ve"].shape, device=dev) if p.ve else None
     gate = g.get("gate")
     rt = None if rope is None else tuple(t.to(dev).contiguous() for t in rope)
-    rp = None if rope is None else swa.make_rope(*rt)
-    st = swa.swa_attn_fwd_rope(prm, rp, g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"], g["tok"],
+    rp = None if rope is None else swa.make_extras(rope=rt)
+    st = swa.swa_attn_fwd_ex(prm, rp, g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"], g["tok"],
                                gate, o, lse, ws, kind=kind)
     assert st == swa.SWA_OK, swa.swa_strerror(st)
     for stage in (swa.SWA_BWD_STAGE_PRE, swa.SWA_BWD_STAGE_MAIN, swa.SWA_BWD_STAGE_POST):
-        st = swa.swa_attn_bwd_rope(prm, rp, g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"],
+        st = swa.swa_attn_bwd_ex(prm, rp, g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"],
                                    g["tok"], gate, o, lse, g["dO"], dq, dk, dv, dgq, dgk, dve, ws,
                                    flags=swa.SWA_REUSE_PROLOGUE | stage, kind=kind)
         assert st == swa.SWA_OK, swa.swa_strerror(st)

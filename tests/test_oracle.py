@@ -654,3 +654,77 @@ def test_rope_samplers_agree_with_full_backward():
                                                  gate=x["gate"], **kw)
             np.testing.assert_allclose(dk, g["dk"][b, rows, hk], atol=1e-12)
             np.testing.assert_allclose(dv, g["dv"][b, rows, hk], atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Learned value-embedding gate: gate = 2 sigmoid(W x[:C]) per kv head
+# ---------------------------------------------------------------------------
+
+def gate_inputs(seed, B, T, Hkv, C=5, scale=0.7):
+    r = rng(seed)
+    return r.standard_normal((B, T, C)), scale * r.standard_normal((Hkv, C))
+
+
+def test_learned_gate_at_initialisation_is_one():
+    # the Guide: the gate weight starts at zero, so 2 * sigmoid(0) = 1 and the
+    # value-embedding path starts as the identity mix
+    x = rand_problem(50, B=2, T=7, Hq=2, Hkv=1, d=8, with_ve=True)
+    gx, _ = gate_inputs(51, 2, 7, 1)
+    w0 = np.zeros((1, gx.shape[-1]))
+    assert np.array_equal(orc.learned_gate(gx, w0), np.ones((2, 7, 1)))
+    o0, l0 = fwd(x, window=3)
+    o1, l1 = fwd(x, window=3, gate_x=gx, gate_w=w0)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+
+
+def test_learned_gate_range_and_saturation():
+    gx, w = gate_inputs(52, 1, 9, 2, scale=3.0)
+    g = orc.learned_gate(gx, w)
+    assert np.all(g > 0) and np.all(g < 2)
+    # symmetry of the sigmoid: gate(-z) = 2 - gate(z)
+    np.testing.assert_allclose(orc.learned_gate(-gx, w), 2.0 - g, rtol=0, atol=1e-15)
+    # far in the tails the gate is 0 or 2 and its gradient vanishes
+    big = np.array([[[200.0]]]), np.array([[1.0]])
+    assert orc.learned_gate(*big)[0, 0, 0] == 2.0
+    dx, dw = orc.learned_gate_backward(big[0], big[1], np.ones((1, 1, 1)))
+    assert dx[0, 0, 0] == 0.0 and dw[0, 0] == 0.0
+    # at z = 0 the slope of 2 sigmoid is 1/2
+    dx, dw = orc.learned_gate_backward(np.array([[[0.0]]]), np.array([[0.3]]), np.ones((1, 1, 1)))
+    assert dx[0, 0, 0] == 0.5 * 0.3 and dw[0, 0] == 0.0
+
+
+def test_learned_gate_equals_the_same_gate_given_as_input():
+    x = rand_problem(53, B=2, T=8, Hq=4, Hkv=2, d=8, with_ve=True)
+    gx, w = gate_inputs(54, 2, 8, 2)
+    kw = dict(window=4, eps=1e-5, ve_scale=0.6)
+    o0, _ = orc.attention_forward(x["q"], x["k"], x["v"], x["gq"], x["gk"], ve=x["ve"], tok=x["tok"],
+                                  gate=orc.learned_gate(gx, w), **kw)
+    o1, _ = fwd(x, gate_x=gx, gate_w=w, **kw)
+    assert np.array_equal(o0, o1)
+
+
+def test_backward_with_learned_gate_matches_central_finite_differences():
+    x = rand_problem(55, B=1, T=7, Hq=2, Hkv=2, d=4, with_ve=True, vocab=5)
+    gx, w = gate_inputs(56, 1, 7, 2, C=3)
+    kw = dict(window=3, causal=True, eps=1e-4, ve_scale=0.8)
+    g = bwd(x, gate_x=gx, gate_w=w, **kw)
+    h = 1e-6
+
+    def lossf():
+        o, _ = fwd(x, gate_x=gx, gate_w=w, **kw)
+        return float(np.sum(o * x["dO"]))
+
+    for arr, gname in ((gx, "dgate_x"), (w, "dgate_w"), (x["v"], "dv"), (x["ve"], "dve")):
+        num = np.zeros_like(arr)
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = arr[idx]
+            arr[idx] = old + h
+            lp = lossf()
+            arr[idx] = old - h
+            lm = lossf()
+            arr[idx] = old
+            num[idx] = (lp - lm) / (2 * h)
+        err = np.linalg.norm(g[gname] - num) / max(np.linalg.norm(num), 1e-30)
+        assert err < 1e-6, (gname, err)

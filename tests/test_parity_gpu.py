@@ -225,3 +225,46 @@ def test_rope_without_prologue_reuse_and_identity_tables():
     c = run_library(p, x)
     for k in ("o", "lse"):
         assert torch.equal(b[k], c[k]), k
+
+
+# Learned value-embedding gate 2 sigmoid(w x[:C]) computed in the prologue,
+# with its gradients (dgate_w, dgate_x) from the backward's post stage.
+GATE_CASES = {
+    "ragged_gqa_ve": CASES["ragged_gqa_ve"],
+    "group4_short": CASES["group4_short"],
+    "long_window_ragged": CASES["long_window_ragged"],
+}
+
+
+@pytest.mark.parametrize("kind", ["bf16", "fp32"])
+@pytest.mark.parametrize("name", list(GATE_CASES))
+def test_parity_with_learned_gate(kind, name):
+    from gpu_helpers import gate_weights
+    p = GATE_CASES[name]
+    x = inputs(p, kind, layer=5)
+    gate = gate_weights(p, kind)
+    got = run_library(p, x, gate=gate)
+    assert got["status"] == swa.SWA_OK
+    assert got["dgate_x"] is not None and got["dgate_w"] is not None
+    compare(got, run_oracle(p, x, learned=gate), TOL[kind])
+
+
+def test_learned_gate_with_rope_and_without_prologue_reuse():
+    from gpu_helpers import gate_weights, rope_tables
+    p = CASES["ragged_gqa_ve"]
+    x = inputs(p, "bf16", layer=6)
+    gate = gate_weights(p, "bf16", channels=20, width=20)
+    rope = rope_tables(p.T, p.d)
+    got = run_library(p, x, reuse_prologue=False, rope=rope, gate=gate)
+    compare(got, run_oracle(p, x, rope=rope, learned=gate), TOL["bf16"])
+
+
+def test_learned_gate_at_zero_weights_equals_unit_gate():
+    # the Guide: the gate weight starts at zero, 2 sigmoid(0) = 1
+    p = CASES["ragged_gqa_ve"]
+    x = inputs(p, "bf16", layer=7)
+    gx, gw = (torch.randn(p.B, p.T, 32).to(torch.bfloat16), torch.zeros(p.Hkv, 32))
+    a = run_library(p, x, gate=(gx, gw))
+    b = run_library(p, dict(x, gate=None))
+    for k in ("o", "lse"):
+        assert torch.equal(a[k], b[k]), k

@@ -174,3 +174,62 @@ def test_empty_forward_is_a_no_op(kind):
 def test_binding_names_mirror_the_c_abi():
     for name in declared_functions():
         assert hasattr(swa, name), name
+
+
+def fwd_ex_call(p, ex, kind="bf16", **over):
+    args = dict(q=A, k=A, v=A, gq=None, gk=None, ve=None, tok=None, gate=None, o=A, lse=A, ws=A)
+    args.update(over)
+    lib = swa.load(kind)
+    ep = None if ex is None else ctypes.byref(ex)
+    return lib.swa_attn_fwd_ex(ctypes.byref(p), ep, args["q"], args["k"], args["v"], args["gq"],
+                               args["gk"], args["ve"], args["tok"], args["gate"], args["o"],
+                               args["lse"], args["ws"], 1 << 40, 0, None)
+
+
+def bwd_ex_call(p, ex, kind="bf16", **over):
+    args = dict(q=A, k=A, v=A, gq=None, gk=None, ve=None, tok=None, gate=None, o=A, lse=A,
+                dO=A, dq=A, dk=A, dv=A, dgq=None, dgk=None, dve=None, ws=A)
+    args.update(over)
+    lib = swa.load(kind)
+    ep = None if ex is None else ctypes.byref(ex)
+    return lib.swa_attn_bwd_ex(ctypes.byref(p), ep, args["q"], args["k"], args["v"], args["gq"],
+                               args["gk"], args["ve"], args["tok"], args["gate"], args["o"],
+                               args["lse"], args["dO"], args["dq"], args["dk"], args["dv"],
+                               args["dgq"], args["dgk"], args["dve"], args["ws"], 1 << 40, 0, None)
+
+
+def extras(**kw):
+    e = swa.swa_extras()
+    for k, v in kw.items():
+        setattr(e, k, v)
+    return e
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("bad", [
+    dict(rope_cos=A, rope_rows=1 << 20),                       # one table only
+    dict(rope_cos=A, rope_sin=A, rope_rows=63),                # fewer rows than T
+    dict(rope_cos=MIS, rope_sin=A, rope_rows=1 << 20),         # not 16-byte aligned
+    dict(gate_w=A, gate_x=None, gate_ch=32, gate_x_stride=32), # no gate input
+    dict(gate_w=A, gate_x=A, gate_ch=0, gate_x_stride=32),
+    dict(gate_w=A, gate_x=A, gate_ch=33, gate_x_stride=33),
+    dict(gate_w=A, gate_x=A, gate_ch=32, gate_x_stride=16),    # rows shorter than the channels
+])
+def test_bad_extras_are_rejected(kind, bad):
+    p = params(T=64)
+    assert fwd_ex_call(p, extras(**bad), kind) == swa.SWA_ERR_INVALID_ARG
+    assert bwd_ex_call(p, extras(**bad), kind) == swa.SWA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_learned_gate_excludes_a_given_gate_and_large_head_counts(kind):
+    gate = dict(gate_w=A, gate_x=A, gate_ch=32, gate_x_stride=32)
+    assert fwd_ex_call(params(T=64), extras(**gate), kind, gate=A) == swa.SWA_ERR_INVALID_ARG
+    assert fwd_ex_call(params(T=64, Hq=33, Hkv=33), extras(**gate), kind) == swa.SWA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_null_extras_behave_like_the_plain_calls(kind):
+    assert fwd_ex_call(params(B=0), None, kind) == swa.SWA_OK
+    assert fwd_ex_call(params(B=0), extras(), kind) == swa.SWA_OK
+    assert fwd_ex_call(params(), None, kind, q=None) == swa.SWA_ERR_INVALID_ARG

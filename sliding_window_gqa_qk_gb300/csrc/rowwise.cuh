@@ -448,10 +448,11 @@ __global__ void __launch_bounds__(kRowWarps * 32) ve_gate_bwd_kernel(GateBwdArgs
       if (h >= a.Hkv) break;
       float dot = 0.f;
       if (in_table) {
-        const elem_t* dvr = a.dv + (bt * a.Hkv + h) * D + lane * CPL;
-        const elem_t* ver = a.ve + static_cast<long long>(tk) * Hd + h * D + lane * CPL;
+        float dvv[CPL], vev[CPL];
+        load_vec<CPL>(a.dv + (bt * a.Hkv + h) * D + lane * CPL, dvv);
+        load_vec<CPL>(a.ve + static_cast<long long>(tk) * Hd + h * D + lane * CPL, vev);
 #pragma unroll
-        for (int e = 0; e < CPL; ++e) dot = fmaf(to_f32(dvr[e]), to_f32(ver[e]), dot);
+        for (int e = 0; e < CPL; ++e) dot = fmaf(dvv[e], vev[e], dot);
       }
       dot = warp_sum(dot);
       const float g = a.gate[bt * a.Hkv + h];

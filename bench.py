@@ -188,6 +188,7 @@ WORKLOADS = {
     "l_layer": "one L layer (B=16, T=2048, Hq=6, Hkv=3, d=128, full causal, no VE)",
     "stack_rope": WORKLOAD[:-1] + ", rotary tables (base 10000) fused before the QK-norm)",
     "stack_full": WORKLOAD[:-1] + ", rotary tables, learned VE gate 2 sigmoid(W x[:32]) on the VE layers)",
+    "stack_mha": WORKLOAD.replace("Hkv=3", "Hkv=6") + " with Hkv = Hq (the Guide's default n_kv_head = n_head)",
 }
 
 
@@ -203,6 +204,8 @@ class Stack:
     def __init__(self, swa, dev, workload="stack"):
         self.swa = swa
         self.dev = dev
+        hkv = HQ if workload == "stack_mha" else HKV
+        self.hkv = hkv
         self.rope = None
         self.learned_gate = workload == "stack_full"
         if workload in ("stack_rope", "stack_full"):
@@ -215,10 +218,10 @@ class Stack:
         self.sched = schedule_for(workload, swa.swa_sssl_window, swa.swa_has_ve)
         self.layers = []
         for li, (W, ve) in enumerate(self.sched):
-            p = Problem(B=B, T=T, Hq=HQ, Hkv=HKV, d=D, window=W, gain_std=0.1, ve=ve, vocab=VOCAB)
+            p = Problem(B=B, T=T, Hq=HQ, Hkv=hkv, d=D, window=W, gain_std=0.1, ve=ve, vocab=VOCAB)
             x = make_inputs(p, layer=li)
             g = {k: (t.to(dev) if t is not None else None) for k, t in x.items()}
-            prm = swa.make_params(B, T, HQ, HKV, D, W, True, 0.0, p.eps, VE_SCALE,
+            prm = swa.make_params(B, T, HQ, hkv, D, W, True, 0.0, p.eps, VE_SCALE,
                                   VOCAB if ve else 0)
             ws = swa.new_workspace(prm, True, dev, "bf16")
             L = dict(p=p, prm=prm, x=x, g=g, ws=ws)

@@ -124,7 +124,8 @@ __global__ void __launch_bounds__(kB2Threads, 1)
     bwd_tc128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                      const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmDK,
-                     const __grid_constant__ CUtensorMap tmDV, const BwdParams prm) {
+                     const __grid_constant__ CUtensorMap tmDV, const __grid_constant__ CUtensorMap tmKr,
+                     const BwdParams prm) {
   using C = B2Cfg;
   constexpr int D = C::D, BQ = C::BQ;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -226,6 +227,18 @@ __global__ void __launch_bounds__(kB2Threads, 1)
         const long long row = (static_cast<long long>(b) * prm.Hq + h) * prm.Tpad + q0;
         bulk_load(sbase + C::oL + s * BQ * 4, prm.lse2 + row, BQ * 4, bar(B2_QFULL + s));
         bulk_load(sbase + C::oD + s * BQ * 4, prm.dvec + row, BQ * 4, bar(B2_QFULL + s));
+        if (it == n_it - 1 && prm.dkn_out == nullptr) {
+          // the epilogue's raw k rows and their inverse RMS into L2, a couple
+          // of steps ahead of their use
+          for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tmKr, 64 * c, k0, hk, b);
+          const float* rs = prm.rstd_k + (static_cast<long long>(b) * prm.Hkv + hk) * prm.T + k0;
+          const uint32_t nrs = static_cast<uint32_t>(prm.T - k0 < kBK ? prm.T - k0 : kBK) * 4;
+          // whole 16-byte units inside the row only (a bulk prefetch needs
+          // a 16-byte aligned start and size)
+          const uintptr_t a0 = (reinterpret_cast<uintptr_t>(rs) + 15) & ~uintptr_t(15);
+          const uintptr_t a1 = (reinterpret_cast<uintptr_t>(rs) + nrs) & ~uintptr_t(15);
+          if (a1 > a0) bulk_prefetch_l2(reinterpret_cast<const void*>(a0), static_cast<uint32_t>(a1 - a0));
+        }
       }
       mbar_wait_drain(bar(B2_KV), 0, prm.wait_limit_ns);
       for (int s = 0; s < 2; ++s)
@@ -540,13 +553,14 @@ inline bool map_dq_acc_rows(CUtensorMap* m, float* base, int BH, int T, int rows
 
 inline swa_status launch_bwd128(const BwdLaunch& f, cudaStream_t st) {
   using C = B2Cfg;
-  CUtensorMap mq, mk, mv, mg, mdq, mdk, mdv;
+  CUtensorMap mq, mk, mv, mg, mdq, mdk, mdv, mkr;
   if (!map_token_major(&mdk, f.dk, f.B, f.Hkv, f.T, 128) ||
       !map_token_major(&mdv, f.dv, f.B, f.Hkv, f.T, 128) ||
       !map_head_major(&mq, f.qn, f.B, f.Hq, f.T, 128) ||
       !map_token_major(&mg, f.dO, f.B, f.Hq, f.T, 128) ||
       !map_head_major(&mk, f.kn, f.B, f.Hkv, f.T, 128) ||
-      !map_dq_acc_rows(&mdq, f.dq_acc, f.B * f.Hq, f.T, 32))
+      !map_dq_acc_rows(&mdq, f.dq_acc, f.B * f.Hq, f.T, 32) ||
+      !map_token_major(&mkr, f.k, f.B, f.Hkv, f.T, 128))
     return SWA_ERR_CUDA;
   const bool okv = f.v_head_major ? map_head_major(&mv, f.v, f.B, f.Hkv, f.T, 128)
                                   : map_token_major(&mv, f.v, f.B, f.Hkv, f.T, 128);
@@ -576,7 +590,7 @@ inline swa_status launch_bwd128(const BwdLaunch& f, cudaStream_t st) {
   const long long n_cta = static_cast<long long>(p.n_ktiles) * p.n_bhk;
   if (n_cta > 0x7fffffffLL) return SWA_ERR_UNSUPPORTED;
   bwd_tc128_kernel<<<static_cast<unsigned>(n_cta), kB2Threads, C::kBytes, st>>>(mq, mk, mv, mg, mdq, mdk,
-                                                                                mdv, p);
+                                                                                mdv, mkr, p);
   return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 

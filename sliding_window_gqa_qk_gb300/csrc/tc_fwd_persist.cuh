@@ -1,7 +1,9 @@
 // Forward attention core, persistent: one CTA per SM loops over work items,
-// each item the same 128-row query tile of the two query heads 2p, 2p + 1 of
-// a GQA group (they read the same kv head and have the same band) against
-// one stream of K/V tiles (sm_103a tcgen05).
+// each item two 128-row query tiles A and B that read the same kv head,
+// against one stream of K/V tiles (sm_103a tcgen05): with an even GQA group
+// the same query tile of the query heads 2p, 2p + 1 (same band); with an odd
+// group (plain multi-head attention included) the query tiles 2m + 1 and 2m
+// of one head, against the union of their bands.
 //   warp 8      TMA producer: per item Q_A, Q_B, then the item's K_j, V_j
 //               (two stages each, shared with the next item's tiles);
 //   warp 9      MMA issuer (lane 0 of the converged warp issues):
@@ -73,6 +75,7 @@ enum {
 
 struct FwdPerParams {
   int B, T, Hq, Hkv, window, causal, n_qtiles, n_items;
+  int pair_heads;    // 1: items pair two query heads (even GQA group); 0: two query tiles of one head
   float scale_log2;  // softmax scale * log2(e)
   float* lse;
   uint32_t* status;
@@ -93,23 +96,49 @@ __device__ __forceinline__ int per_item(int k, int c, int G, int n_items) {
   return idx < n_items ? idx : -1;
 }
 
+// One work item: the query tiles A and B (128 rows each, heads hA / hB,
+// first rows q0A / q0B) that run against one stream of K/V tiles
+// [kt_lo, kt_lo + n_tiles) of kv head hA / (Hq / Hkv).
 struct PerItem {
-  int b, pair, q0, kt_lo, n_tiles;
+  int b, hA, hB, q0A, q0B, kt_lo, n_tiles;
 };
 
-// Item index -> (query tile, batch, head pair): query tiles from the last
-// (the most key tiles) to the first.
+// Item index -> item, the heaviest first (query tiles from the end of the
+// sequence, where the band holds the most key tiles).
+//   Even GQA group: A and B are the same query tile of the two query heads
+//   2p, 2p + 1 of a group (same kv head, same band).
+//   Odd group (e.g. plain multi-head attention): A and B are the adjacent
+//   query tiles 2m + 1 and 2m of one head; they share the kv head, and the K/V
+//   stream is the union of their bands (a tile outside one of them is fully
+//   masked for that tile's rows; A may lie past the end of the sequence).
 __device__ __forceinline__ PerItem per_decode(int w, const FwdPerParams& p, const Band& band) {
-  const int npair = p.Hq / 2;
-  const int per_q = p.B * npair;
-  const int qt = p.n_qtiles - 1 - w / per_q;
-  const int rest = w % per_q;
   PerItem it;
-  it.b = rest / npair;
-  it.pair = rest % npair;
-  it.q0 = qt * kBM;
   int lo = 0, hi = -1;
-  kv_tile_range(band, it.q0, kBM, kBN, lo, hi);
+  if (p.pair_heads) {
+    const int npair = p.Hq / 2;
+    const int per_q = p.B * npair;
+    const int qt = p.n_qtiles - 1 - w / per_q;
+    const int rest = w % per_q;
+    it.b = rest / npair;
+    it.hA = 2 * (rest % npair);
+    it.hB = it.hA + 1;
+    it.q0A = it.q0B = qt * kBM;
+    kv_tile_range(band, it.q0A, kBM, kBN, lo, hi);
+  } else {
+    const int per_q = p.B * p.Hq;
+    const int m = (p.n_qtiles + 1) / 2 - 1 - w / per_q;
+    const int rest = w % per_q;
+    it.b = rest / p.Hq;
+    it.hA = it.hB = rest % p.Hq;
+    it.q0B = 2 * m * kBM;
+    it.q0A = it.q0B + kBM;
+    int lo2 = 0, hi2 = -1;
+    kv_tile_range(band, it.q0B, kBM, kBN, lo, hi);
+    if (it.q0A < p.T && kv_tile_range(band, it.q0A, kBM, kBN, lo2, hi2)) {
+      if (lo2 < lo) lo = lo2;
+      if (hi2 > hi) hi = hi2;
+    }
+  }
   it.kt_lo = lo;
   it.n_tiles = hi - lo + 1;
   return it;
@@ -185,13 +214,13 @@ __global__ void __launch_bounds__(kPerThreads, 1)
         if (w < 0) break;
         const PerItem I = per_decode(w, prm, band);
         if (I.n_tiles <= 0) continue;
-        const int hA = 2 * I.pair, hk = hA / Gq;
+        const int hk = I.hA / Gq;
         // Q of this item: the previous item's S products have completed
         if (it > 0 && !(ok = mbar_wait_warp(bar(QP_QEMPTY), (it - 1) & 1, ctl))) break;
         mbar_arrive_expect_tx_w(bar(QP_QFULL), 2 * L::kTile, one);
         for (int c = 0; c < KCH; ++c) {
-          tma_load_4d_w(sbase + L::kQA + c * L::kHalf, &tmQ, bar(QP_QFULL), 64 * c, I.q0, hA, I.b, one);
-          tma_load_4d_w(sbase + L::kQB + c * L::kHalf, &tmQ, bar(QP_QFULL), 64 * c, I.q0, hA + 1, I.b, one);
+          tma_load_4d_w(sbase + L::kQA + c * L::kHalf, &tmQ, bar(QP_QFULL), 64 * c, I.q0A, I.hA, I.b, one);
+          tma_load_4d_w(sbase + L::kQB + c * L::kHalf, &tmQ, bar(QP_QFULL), 64 * c, I.q0B, I.hB, I.b, one);
         }
         for (int j = 0; j < I.n_tiles && ok; ++j, ++g) {
           const int s = g & 1;
@@ -214,17 +243,25 @@ __global__ void __launch_bounds__(kPerThreads, 1)
             // A share of the item's rows of the backward's dQ accumulator
             // (per head one contiguous run of up to 128 rows of D floats),
             // spread over its key tiles, as bulk copies of the zero block.
-            const int nrows = prm.T - I.q0 < kBM ? prm.T - I.q0 : kBM;
-            const uint32_t run = static_cast<uint32_t>(nrows) * D * 4;
-            const int per_head = static_cast<int>((run + L::kZeroBytes - 1) / L::kZeroBytes);
-            const int total = 2 * per_head;
+            int nr[2];
+            uint32_t run[2];
+            int per[2];
+            for (int x = 0; x < 2; ++x) {
+              const int q0x = x ? I.q0B : I.q0A;
+              nr[x] = prm.T - q0x < kBM ? prm.T - q0x : kBM;
+              if (nr[x] < 0) nr[x] = 0;
+              run[x] = static_cast<uint32_t>(nr[x]) * D * 4;
+              per[x] = static_cast<int>((run[x] + L::kZeroBytes - 1) / L::kZeroBytes);
+            }
+            const int total = per[0] + per[1];
             const int c1 = (j + 1) * total / I.n_tiles;
             for (int cpy = j * total / I.n_tiles; cpy < c1; ++cpy) {
-              const int hx = cpy / per_head;
-              const uint32_t off = static_cast<uint32_t>(cpy - hx * per_head) * L::kZeroBytes;
-              const uint32_t bytes = run - off < static_cast<uint32_t>(L::kZeroBytes) ? run - off
-                                                                                     : L::kZeroBytes;
-              float* dst = prm.dq_acc + ((static_cast<long long>(I.b) * prm.Hq + hA + hx) * prm.T + I.q0) * D;
+              const int x = cpy < per[0] ? 0 : 1;
+              const uint32_t off = static_cast<uint32_t>(cpy - (x ? per[0] : 0)) * L::kZeroBytes;
+              const uint32_t bytes = run[x] - off < static_cast<uint32_t>(L::kZeroBytes) ? run[x] - off
+                                                                                         : L::kZeroBytes;
+              const int hx = x ? I.hB : I.hA, q0x = x ? I.q0B : I.q0A;
+              float* dst = prm.dq_acc + ((static_cast<long long>(I.b) * prm.Hq + hx) * prm.T + q0x) * D;
               bulk_store(reinterpret_cast<uint8_t*>(dst) + off, sbase + L::kZero, bytes);
             }
             bulk_commit_group();
@@ -344,8 +381,8 @@ __global__ void __launch_bounds__(kPerThreads, 1)
       const PerItem I = per_decode(w, prm, band);
       const int n = I.n_tiles;
       if (n <= 0) continue;
-      const int h = 2 * I.pair + X;
-      const int q0 = I.q0;
+      const int h = X ? I.hB : I.hA;
+      const int q0 = X ? I.q0B : I.q0A;
       const int i = q0 + row;                 // query position
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < n && ok; ++j) {
@@ -475,9 +512,9 @@ __global__ void __launch_bounds__(kPerThreads, 1)
             empty ? -INFINITY : (m + log2f(l)) * 0.69314718055994531f;
       }
       // bf16 O through this warpgroup's 64-column staging half, one TMA store
-      // of 128 rows x 64 columns per round.
+      // of 128 rows x 64 columns per round (none for a tile past the end).
 #pragma unroll
-      for (int r = 0; r < KCH; ++r) {
+      for (int r = 0; r < KCH && q0 < prm.T; ++r) {
         if (leader) bulk_wait_group_read<0>();   // the previous store has read the half
         named_bar_sync(1 + X, 128);
 #pragma unroll
@@ -527,7 +564,8 @@ inline swa_status launch_fwd_persist_d(const FwdLaunch& f, cudaStream_t st) {
   FwdPerParams p{};
   p.B = f.B; p.T = f.T; p.Hq = f.Hq; p.Hkv = f.Hkv; p.window = f.window; p.causal = f.causal;
   p.n_qtiles = (f.T + kBM - 1) / kBM;
-  p.n_items = f.B * (f.Hq / 2) * p.n_qtiles;
+  p.pair_heads = (f.Hq / f.Hkv) % 2 == 0;
+  p.n_items = p.pair_heads ? f.B * (f.Hq / 2) * p.n_qtiles : f.B * f.Hq * ((p.n_qtiles + 1) / 2);
   p.scale_log2 = f.scale * 1.4426950408889634f;
   p.lse = f.lse; p.status = f.status; p.wait_limit_ns = f.wait_limit_ns;
   p.dq_acc = f.dq_acc; p.acc_flag = f.acc_flag;
@@ -540,15 +578,10 @@ inline swa_status launch_fwd_persist_d(const FwdLaunch& f, cudaStream_t st) {
   return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 
-// Forward dispatch: the persistent two-heads-per-item kernel when the GQA
-// group size is even, one head per CTA otherwise.
+// Forward dispatch: the persistent kernel for every group size (even groups
+// pair two query heads per item, odd groups two query tiles of one head).
 inline swa_status launch_fwd_any2(const FwdLaunch& f, cudaStream_t st) {
-  if ((f.Hq / f.Hkv) % 2 == 0)
-    return f.d == 64 ? launch_fwd_persist_d<64>(f, st) : launch_fwd_persist_d<128>(f, st);
-  // This kernel leaves the dQ accumulator alone: drop any record of it.
-  if (f.acc_flag != nullptr && cudaMemsetAsync(f.acc_flag, 0, 2 * sizeof(unsigned long long), st) != cudaSuccess)
-    return SWA_ERR_CUDA;
-  return launch_fwd(f, st);
+  return f.d == 64 ? launch_fwd_persist_d<64>(f, st) : launch_fwd_persist_d<128>(f, st);
 }
 
 }  // namespace tc

@@ -61,6 +61,19 @@ def test_layer_schedule_helpers_reject_bad_arguments():
     assert swa.swa_sssl_window(4, 6, "S", 101) == 50
 
 
+@pytest.mark.parametrize("pattern", ["L", "S", "SL", "SSL", "SSSL", "SSSSL", "LSSS", "SLSL"])
+@pytest.mark.parametrize("n_layer", [1, 2, 5, 8, 12])
+def test_layer_schedule_agrees_with_the_oracle_for_other_window_patterns(pattern, n_layer):
+    # WINDOW_PATTERN is the script's main tuning lever (the Guide, §3.4 and the
+    # techniques table): the library's schedule helpers and the oracle's,
+    # written independently, agree on every layer of every pattern
+    import oracle
+    for T in (2048, 777):
+        for layer in range(n_layer):
+            assert swa.swa_sssl_window(layer, n_layer, pattern, T) == oracle.sssl_window(layer, n_layer, pattern, T)
+            assert swa.swa_has_ve(layer, n_layer) == int(oracle.has_ve(layer, n_layer))
+
+
 def test_strerror_covers_every_status():
     texts = {swa.swa_strerror(s) for s in range(7)}
     assert len(texts) == 7

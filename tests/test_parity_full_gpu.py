@@ -39,6 +39,9 @@ T2048 = {
     "l_layer": (L_LAYER, 0),
     "stack_layer1_s_ve": (S_LAYER.replace(ve=True), 1),
     "stack_layer3_l_ve": (L_LAYER.replace(ve=True), 3),
+    # the Guide's default n_kv_head = n_head (plain multi-head attention),
+    # window 1024 with value embeddings, on 4 sequences
+    "mha_s_layer_ve": (S_LAYER.replace(B=4, Hkv=6, ve=True), 1),
 }
 
 

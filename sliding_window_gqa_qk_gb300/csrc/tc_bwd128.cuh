@@ -27,9 +27,9 @@
 // dP^T(i+1) waits for that drain (it reuses the columns).
 // dQ^T(i) goes from TMEM to shared memory in four [32 queries][128] fp32
 // boxes, two in the dedicated staging buffer (free once the previous step's
-// boxes there were read) and two in the step's Q stage (free once dK(i) has
-// read it), and from there into the fp32 dQ accumulator by TMA bulk
-// reductions. Those run at the rate the L2 accepts fp32 adds (about 6.6 TB/s
+// boxes there were read) and two in the dS^T buffer (free once dK(i) has read
+// it; dS^T(i+1) waits for the reducer), and from there into the fp32 dQ
+// accumulator by TMA bulk reductions. Those run at the rate the L2 accepts fp32 adds (about 6.6 TB/s
 // over the whole GPU, about 21 bytes per clock per SM), 64 KB per step.
 // Registers (setmaxnreg; 512 x 128 at launch): element-wise warpgroups 176
 // per thread, drain warpgroup 96, the four single-role warps 56.
@@ -75,7 +75,7 @@ struct B2Cfg {
 enum {
   B2_KV = 0,
   B2_QFULL = 1,      // +stage: Q, LSE, D of a step landed
-  B2_QEMPTY = 3,     // +stage: the dQ boxes staged in the Q stage were read (Q stage reusable)
+  B2_QEMPTY = 3,     // +stage: the dK product of the step completed (Q stage reusable)
   B2_GFULL = 5,      // dO landed
   B2_GFREE = 7,      // the dV product of the step completed (dO stage reusable)
   B2_SFULL = 9,      // S^T in TMEM
@@ -86,6 +86,7 @@ enum {
   B2_DQFREE = 14,    // dQ^T read out of TMEM (8 warps)
   B2_STAGED = 15,    // the step's four dQ boxes are in shared memory (8 warps)
   B2_XFREE = 16,     // the dQ boxes in the staging buffer were read
+  B2_DSFREE = 17,    // the dQ boxes staged in the dS^T buffer were read
   B2_FINAL = 18,
   B2_DKDONE = 19,    // the dK product of the step completed (dQ-first order)
   B2_COUNT = 20
@@ -185,6 +186,7 @@ __global__ void __launch_bounds__(kB2Threads, 1)
     mbar_init(bar(B2_DQFREE), 4);
     mbar_init(bar(B2_STAGED), 4);
     mbar_init(bar(B2_XFREE), 1);
+    mbar_init(bar(B2_DSFREE), 1);
     mbar_init(bar(B2_FINAL), 1);
     mbar_init(bar(B2_DKDONE), 1);
     fence_mbar_init();
@@ -272,14 +274,14 @@ __global__ void __launch_bounds__(kB2Threads, 1)
         const int h = hk * G + m / nq;
         const int q0 = (qlo + m % nq) * BQ;
         for (int X = 0; X < 2; ++X)
-          tma_reduce_add_3d(&tmDQ, sbase + C::oQ + (m & 1) * C::kTile + X * C::kHalf, 0, q0 + 64 * X,
+          tma_reduce_add_3d(&tmDQ, sbase + C::oS + X * C::kHalf, 0, q0 + 64 * X,
                             b * prm.Hq + h);
         bulk_commit_group();
         for (int X = 0; X < 2; ++X)
           tma_reduce_add_3d(&tmDQ, sbase + C::oX + X * C::kHalf, 0, q0 + 64 * X + 32, b * prm.Hq + h);
         bulk_commit_group();
         bulk_wait_group_read<1>();
-        mbar_arrive(bar(B2_QEMPTY + (m & 1)));
+        mbar_arrive(bar(B2_DSFREE));
         bulk_wait_group_read<0>();
         mbar_arrive(bar(B2_XFREE));
       }
@@ -340,6 +342,7 @@ __global__ void __launch_bounds__(kB2Threads, 1)
           umma_ss_imm<idKV, aoff, kk * 128>(tmem + cDK, dSk, qd, (i > 0 || kk > 0), 1u);
         });
         umma_commit(bar(B2_DKDONE));
+        umma_commit(bar(B2_QEMPTY + (i & 1)));   // the last reader of the Q stage
       };
       bool ok = mbar_wait(bar(B2_KV), 0, ctl) && mbar_wait(bar(B2_QFULL), 0, ctl);
       if (ok) {
@@ -380,15 +383,16 @@ __global__ void __launch_bounds__(kB2Threads, 1)
   } else if (warp >= 8) {
     // --------- drain warpgroup: dQ^T(i) (lane = head-dim index) -> staged boxes ---------
     // Boxes [32 queries][128] fp32: queries 64X .. 64X + 31 in half X of the
-    // step's Q stage (free once dK(i) has read it), 64X + 32 .. 64X + 63 in
-    // half X of the staging buffer (free once the reducer read the previous
-    // step's boxes there). TMEM is handed back (DQFREE) as soon as every
-    // column has been read.
+    // dS^T buffer (free once dK(i), its last reader, completed; the next dS^T
+    // waits until the reducer has read them), 64X + 32 .. 64X + 63 in half X
+    // of the staging buffer (free once the reducer read the previous step's
+    // boxes there). TMEM is handed back (DQFREE) as soon as every column has
+    // been read. The Q stages hold no dQ, so a Q stage is reloaded as soon as
+    // dK of its step completed.
     setmaxnreg_dec<kB2RegsDrain>();
     const int t = threadIdx.x & 127;
     const uint32_t tDQ = tmem + cDP + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     for (int i = 0; i < n_it; ++i) {
-      const int s = i & 1;
       if (!mbar_wait_warp(bar(B2_DQFULL), i & 1, ctl)) break;
       tc_fence_after();
       uint32_t a[2][32];
@@ -414,7 +418,7 @@ __global__ void __launch_bounds__(kB2Threads, 1)
       for (int X = 0; X < 2; ++X)
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-          st_shared_f32(sbase + C::oQ + s * C::kTile + X * C::kHalf + e * 512 + t * 4,
+          st_shared_f32(sbase + C::oS + X * C::kHalf + e * 512 + t * 4,
                         __uint_as_float(a[X][e]));
       fence_async_smem();
       __syncwarp();
@@ -507,6 +511,7 @@ __global__ void __launch_bounds__(kB2Threads, 1)
       pack64(dp, pk);
       // MN-major B operand of dQ^T, in this warpgroup's half of the dS^T
       // buffer, once the dQ box of step i - 1 staged there has been read
+      if (i > 0 && !mbar_wait_warp(bar(B2_DSFREE), (i - 1) & 1, ctl)) return false;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch)
         st_sw128_chunk(sSx, kBK, t, ch, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
@@ -518,13 +523,13 @@ __global__ void __launch_bounds__(kB2Threads, 1)
     };
     bool ok = n_it > 0;
     for (int i = 0; i < n_it && ok; ++i) ok = p_phase(i) && ds_phase(i);
-    // Once every product has completed, K, V and the dS^T buffer are free:
-    // the epilogue stages dk and dv there (and its scratch in the dS^T
-    // buffer) while the reducer may still be reading the last dQ boxes out
-    // of the Q stage and the staging buffer.
+    // Once every product has completed, K, V and the Q stages are free: the
+    // epilogue stages dk and dv in K and V and keeps its scratch in a Q
+    // stage, while the reducer may still be reading the last dQ boxes out of
+    // the dS^T buffer and the staging buffer.
     const bool final_ok = ok && n_it > 0 && mbar_wait_warp(bar(B2_FINAL), 0, ctl);
     tc_fence_after();
-    float* scratch = reinterpret_cast<float*>(smem + C::oS);
+    float* scratch = reinterpret_cast<float*>(smem + C::oQ);
     const uint32_t sdk = sbase + C::oK, sdv = sbase + C::oV;
     kv_epilogue<D>(prm, tmem + cDK + lane_off + X * 64, tmem + cDV + lane_off + X * 64, final_ok, X,
                    t, b, hk, kt, scratch, scratch + 256, sdk, sdv, &tmDK, &tmDV);

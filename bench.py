@@ -48,7 +48,7 @@ WORKLOAD = "8-layer SSSL stack (B=16, T=2048, Hq=6, Hkv=3, d=128, W=1024 on S la
 # kernel (bwd_tc128_kernel) from one ncu capture, summarised in profiles/:
 # the mean over the stack's 6 S-layer and 2 L-layer launches (None whenever
 # the kernel has changed since the capture).
-NCU_TRAFFIC_BYTES = 467_308_256
+NCU_TRAFFIC_BYTES = 469_915_392
 
 
 def layer_schedule(window_fn, ve_fn):
@@ -324,15 +324,30 @@ def run_ours(args, rank, world, dev):
             st = swa.swa_attn_check_status(L["ws"])
             if st != swa.SWA_OK:
                 raise swa.SwaError(st, "device status after warm-up")
+        graph = None
+        if not args.no_graph:
+            # one step's launches captured once, replayed per timed step
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                stack.step()
+            graph.replay()
         torch.cuda.synchronize()
         _barrier(world)
         t0 = clocks.mark()
         start.record()
         for _ in range(args.steps):
-            stack.step(ev)
+            if graph is not None:
+                graph.replay()
+            else:
+                stack.step(ev)
         stop.record()
         torch.cuda.synchronize()
         t1 = clocks.mark()
+        if graph is not None:
+            # per-stage split from eager steps bracketed by events
+            for _ in range(args.steps):
+                stack.step(ev)
+            torch.cuda.synchronize()
     _barrier(world)
     for L in stack.layers:
         st = swa.swa_attn_check_status(L["ws"])
@@ -362,7 +377,10 @@ def run_ours(args, rank, world, dev):
                    "flops_per_step": flops_step,
                    "pct_of_peak": round(100 * value / world / peak, 2),
                    "peak_tflops": peak, "peak_source": f"{peak_kind} bf16_tflops_sustained",
+                   "launch": ("one step's launches captured in a CUDA graph, replayed per step"
+                              if graph is not None else "eager launches"),
                    "stage_ms_per_step": {k: round(v, 4) for k, v in stage_ms.items()},
+                   "stage_split": "CUDA events around each stage of eager steps",
                    "fwd_tflops": round(fwd_launch_tflops, 1)},
         "roofline": {"kernel": "bwd_tc128_kernel (backward main, d=128; one launch per layer)",
                      "bound": "tensor",
@@ -504,6 +522,8 @@ def main():
     ap.add_argument("--workload", choices=list(WORKLOADS), default="stack",
                     help="stack (the headline) or one S / L layer (profiling)")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager launches instead of replaying a CUDA graph of one step")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--quick-cpu", action="store_true", help="oracle sample of 2 layers only")
     args = ap.parse_args()

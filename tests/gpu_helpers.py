@@ -128,12 +128,13 @@ def compare(got, ref, tol, keys=("o", "lse", "dq", "dk", "dv", "dgq", "dgk", "dv
     return errs
 
 
-def run_staged(p, x, dev=None, rope=None):
+def run_staged(p, x, dev=None, rope=None, graph=False):
     """Forward + backward through the C ABI exactly as the benchmark calls
     it: swa_attn_fwd with the ve gate left out, then the three backward
     stages one call at a time with the prologue outputs reused. Returns CPU
     tensors (bf16 outputs as stored, fp32 gradients of the shared
-    parameters)."""
+    parameters). graph=True captures the four calls in a CUDA graph, fills
+    every output with NaN and replays the graph twice."""
     dev = dev or torch.device("cuda:0")
     g = {k: (t.to(dev).contiguous() if t is not None else None) for k, t in x.items()}
     kind = "fp32" if x["q"].dtype == torch.float32 else "bf16"
@@ -149,14 +150,27 @@ def run_staged(p, x, dev=None, rope=None):
     gate = g.get("gate")
     rt = None if rope is None else tuple(t.to(dev).contiguous() for t in rope)
     rp = None if rope is None else swa.make_extras(rope=rt)
-    st = swa.swa_attn_fwd_ex(prm, rp, g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"], g["tok"],
-                               gate, o, lse, ws, kind=kind)
-    assert st == swa.SWA_OK, swa.swa_strerror(st)
-    for stage in (swa.SWA_BWD_STAGE_PRE, swa.SWA_BWD_STAGE_MAIN, swa.SWA_BWD_STAGE_POST):
-        st = swa.swa_attn_bwd_ex(prm, rp, g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"],
-                                   g["tok"], gate, o, lse, g["dO"], dq, dk, dv, dgq, dgk, dve, ws,
-                                   flags=swa.SWA_REUSE_PROLOGUE | stage, kind=kind)
+    def calls():
+        st = swa.swa_attn_fwd_ex(prm, rp, g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"],
+                                 g["tok"], gate, o, lse, ws, kind=kind)
         assert st == swa.SWA_OK, swa.swa_strerror(st)
+        for stage in (swa.SWA_BWD_STAGE_PRE, swa.SWA_BWD_STAGE_MAIN, swa.SWA_BWD_STAGE_POST):
+            st = swa.swa_attn_bwd_ex(prm, rp, g["q"], g["k"], g["v"], g["gq"], g["gk"], g["ve"],
+                                     g["tok"], gate, o, lse, g["dO"], dq, dk, dv, dgq, dgk, dve, ws,
+                                     flags=swa.SWA_REUSE_PROLOGUE | stage, kind=kind)
+            assert st == swa.SWA_OK, swa.swa_strerror(st)
+
+    if graph:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            calls()
+        for t in (o, lse, dq, dk, dv, dgq, dgk, dve):
+            if t is not None:
+                t.fill_(float("nan"))
+        gr.replay()
+        gr.replay()
+    else:
+        calls()
     status = swa.swa_attn_check_status(ws, kind=kind)
     torch.cuda.synchronize()
     out = {"o": o.cpu(), "lse": lse.cpu(), "dq": dq.cpu(), "dk": dk.cpu(), "dv": dv.cpu(),

@@ -9,7 +9,7 @@ import torch
 
 from sliding_window_gqa_qk_gb300.inputs import TINY, Problem
 import sliding_window_gqa_qk_gb300 as swa
-from gpu_helpers import TOL, compare, inputs, run_library, run_oracle
+from gpu_helpers import TOL, compare, inputs, run_library, run_oracle, run_staged
 
 pytestmark = pytest.mark.gpu
 
@@ -268,3 +268,15 @@ def test_learned_gate_at_zero_weights_equals_unit_gate():
     b = run_library(p, dict(x, gate=None))
     for k in ("o", "lse"):
         assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("kind", ["bf16", "fp32"])
+def test_cuda_graph_of_forward_and_backward_replays_correctly(kind):
+    # The entry points make no synchronous calls, so a caller can capture a
+    # whole step; replays recompute every output (they start from NaN) and
+    # the second replay finds the workspace as the first left it.
+    p = CASES["ragged_gqa_ve"]
+    x = inputs(p, kind, layer=1, with_gate=True)
+    got = run_staged(p, x, graph=True)
+    assert got["status"] == swa.SWA_OK
+    compare(got, run_oracle(p, x), TOL[kind])

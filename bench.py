@@ -189,7 +189,18 @@ WORKLOADS = {
     "stack_rope": WORKLOAD[:-1] + ", rotary tables (base 10000) fused before the QK-norm)",
     "stack_full": WORKLOAD[:-1] + ", rotary tables, learned VE gate 2 sigmoid(W x[:32]) on the VE layers)",
     "stack_mha": WORKLOAD.replace("Hkv=3", "Hkv=6") + " with Hkv = Hq (the Guide's default n_kv_head = n_head)",
+    "long": ("long context: one S layer (window 8192) and one L layer (full causal), B=2, T=16384, "
+             "Hq=16, Hkv=4, d=128, QK-RMSNorm gains 1+0.1N, no VE"),
 }
+
+# (B, T, Hq, Hkv) of each workload; d = 128 throughout
+LONG_SHAPE = (2, 16384, 16, 4)
+
+
+def shape_for(workload):
+    if workload == "long":
+        return LONG_SHAPE
+    return (B, T, HQ, HQ if workload == "stack_mha" else HKV)
 
 
 def schedule_for(workload, window_fn, ve_fn):
@@ -197,6 +208,11 @@ def schedule_for(workload, window_fn, ve_fn):
         return [(T // 2, False)]
     if workload == "l_layer":
         return [(-1, False)]
+    if workload == "long":
+        # one layer of each kind of the SSSL pattern at T = 16384
+        t_long = LONG_SHAPE[1]
+        return [(window_fn(0, N_LAYER, PATTERN, t_long), False),
+                (window_fn(N_LAYER - 1, N_LAYER, PATTERN, t_long), False)]
     return layer_schedule(window_fn, ve_fn)
 
 
@@ -204,8 +220,8 @@ class Stack:
     def __init__(self, swa, dev, workload="stack"):
         self.swa = swa
         self.dev = dev
-        hkv = HQ if workload == "stack_mha" else HKV
-        self.hkv = hkv
+        Bn, Tn, hq, hkv = shape_for(workload)
+        self.B, self.T, self.hq, self.hkv = Bn, Tn, hq, hkv
         self.rope = None
         self.learned_gate = workload == "stack_full"
         if workload in ("stack_rope", "stack_full"):
@@ -218,15 +234,15 @@ class Stack:
         self.sched = schedule_for(workload, swa.swa_sssl_window, swa.swa_has_ve)
         self.layers = []
         for li, (W, ve) in enumerate(self.sched):
-            p = Problem(B=B, T=T, Hq=HQ, Hkv=hkv, d=D, window=W, gain_std=0.1, ve=ve, vocab=VOCAB)
+            p = Problem(B=Bn, T=Tn, Hq=hq, Hkv=hkv, d=D, window=W, gain_std=0.1, ve=ve, vocab=VOCAB)
             x = make_inputs(p, layer=li)
             g = {k: (t.to(dev) if t is not None else None) for k, t in x.items()}
-            prm = swa.make_params(B, T, HQ, hkv, D, W, True, 0.0, p.eps, VE_SCALE,
+            prm = swa.make_params(Bn, Tn, hq, hkv, D, W, True, 0.0, p.eps, VE_SCALE,
                                   VOCAB if ve else 0)
             ws = swa.new_workspace(prm, True, dev, "bf16")
             L = dict(p=p, prm=prm, x=x, g=g, ws=ws)
             L["o"] = torch.empty_like(g["q"])
-            L["lse"] = torch.empty(B, HQ, T, dtype=torch.float32, device=dev)
+            L["lse"] = torch.empty(Bn, hq, Tn, dtype=torch.float32, device=dev)
             L["dq"], L["dk"], L["dv"] = (torch.empty_like(g["q"]), torch.empty_like(g["k"]),
                                          torch.empty_like(g["v"]))
             L["dgq"] = torch.empty(D, dtype=torch.float32, device=dev)
@@ -238,14 +254,26 @@ class Stack:
                 # gate weights [Hkv, 32], seeded per layer
                 gen = torch.Generator().manual_seed(1000 + li)
                 L["gx"] = torch.randn(B, T, 768, generator=gen).to(torch.bfloat16).to(dev)
-                L["gw"] = (0.1 * torch.randn(HKV, 32, generator=gen)).to(dev)
-                L["dgw"] = torch.empty(HKV, 32, dtype=torch.float32, device=dev)
+                L["gw"] = (0.1 * torch.randn(hkv, 32, generator=gen)).to(dev)
+                L["dgw"] = torch.empty(hkv, 32, dtype=torch.float32, device=dev)
                 L["dgx"] = torch.empty(B, T, 32, dtype=torch.float32, device=dev)
                 L["ex"] = swa.make_extras(rope=self.rope_t, gate_x=L["gx"], gate_w=L["gw"],
                                           d_gate_w=L["dgw"], d_gate_x=L["dgx"])
             self.layers.append(L)
-        self.flops_fwd = sum(flops(B, T, HQ, D, W)[0] for W, _ in self.sched)
-        self.flops_bwd = sum(flops(B, T, HQ, D, W)[1] for W, _ in self.sched)
+        self.flops_fwd = sum(flops(Bn, Tn, hq, D, W)[0] for W, _ in self.sched)
+        self.flops_bwd = sum(flops(Bn, Tn, hq, D, W)[1] for W, _ in self.sched)
+
+    def layer_gb(self):
+        """Device bytes of one layer's tensors (inputs, outputs, gradients,
+        workspace), in GB."""
+        L = self.layers[0]
+        n = L["ws"].numel() * L["ws"].element_size()
+        for k in ("o", "lse", "dq", "dk", "dv"):
+            n += L[k].numel() * L[k].element_size()
+        for t in L["g"].values():
+            if t is not None:
+                n += t.numel() * t.element_size()
+        return n / 1e9
 
     def fwd(self, L):
         g = L["g"]
@@ -371,9 +399,11 @@ def run_ours(args, rank, world, dev):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q/k/v/dO, gains 1+0.1N, VE N(0,0.02), tokens U[0,8192))",
-        "config": {"workload": WORKLOADS[args.workload], "global_batch": B * world, "seq_len": T,
+        "config": {"workload": WORKLOADS[args.workload], "global_batch": stack.B * world,
+                   "seq_len": stack.T,
                    "parallelism": f"replicas over batch x{world}" if world > 1 else "single GPU",
-                   "l2": f"inputs larger than L2: {n_layer} layer(s) x ~0.4 GB of tensors per step",
+                   "l2": f"inputs larger than L2: {n_layer} layer(s) x {stack.layer_gb():.1f} GB of "
+                         "tensors per step",
                    "flops_per_step": flops_step,
                    "pct_of_peak": round(100 * value / world / peak, 2),
                    "peak_tflops": peak, "peak_source": f"{peak_kind} bf16_tflops_sustained",
@@ -385,7 +415,8 @@ def run_ours(args, rank, world, dev):
         "roofline": {"kernel": "bwd_tc128_kernel (backward main, d=128; one launch per layer)",
                      "bound": "tensor",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": NCU_TRAFFIC_BYTES,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": NCU_TRAFFIC_BYTES if args.workload == "stack" else None,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops_sustained)"},
         "gpu_launches": stack.launches_per_step() * args.steps,
         "clocks": clocks.summary(t0, t1),
@@ -406,7 +437,12 @@ def run_ours(args, rank, world, dev):
 def run_e2e(args, stack, world):
     """Same metric through the public API with host buffers: every step copies
     the inputs of all layers from pinned host memory to the device, runs the
-    stack, and reads o and every gradient back."""
+    stack, and reads o and every gradient back. The copies run on two side
+    streams: layer i's inputs go up while earlier layers compute, and its
+    outputs come down as soon as its backward is done. Events keep each
+    layer's buffers safe across steps: the next step's upload of layer i waits
+    for this step's backward of layer i, and its forward of layer i waits for
+    this step's download of layer i."""
     host_in, host_out = [], []
     h2d = d2h = 0
     for L in stack.layers:
@@ -425,29 +461,64 @@ def run_e2e(args, stack, world):
                 d2h += t.numel() * t.element_size()
         host_out.append(hout)
 
+    n = len(stack.layers)
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(n)]
+    bwd_done = [torch.cuda.Event() for _ in range(n)]
+    out_read = [torch.cuda.Event() for _ in range(n)]
+    for ev in bwd_done + out_read:
+        ev.record(comp)
+    swa = stack.swa
+    stages = (swa.SWA_BWD_STAGE_PRE, swa.SWA_BWD_STAGE_MAIN, swa.SWA_BWD_STAGE_POST)
+
     def step():
-        for L, hin in zip(stack.layers, host_in):
-            for k, t in hin.items():
-                L["g"][k].copy_(t, non_blocking=True)
-        stack.step()
-        for L, hout in zip(stack.layers, host_out):
-            for k, t in hout.items():
-                t.copy_(L[k], non_blocking=True)
+        for i, (L, hin) in enumerate(zip(stack.layers, host_in)):
+            up.wait_event(bwd_done[i])
+            with torch.cuda.stream(up):
+                for k, t in hin.items():
+                    L["g"][k].copy_(t, non_blocking=True)
+            in_ready[i].record(up)
+        for i, L in enumerate(stack.layers):
+            comp.wait_event(in_ready[i])
+            comp.wait_event(out_read[i])
+            stack.fwd(L)
+        for i in reversed(range(n)):
+            L = stack.layers[i]
+            for stage in stages:
+                stack.bwd(L, stage)
+            bwd_done[i].record(comp)
+            down.wait_event(bwd_done[i])
+            with torch.cuda.stream(down):
+                for k, t in host_out[i].items():
+                    t.copy_(L[k], non_blocking=True)
+            out_read[i].record(down)
+
+    def drain():
+        # the step's downloads are part of it: the compute stream waits for them
+        for ev in out_read:
+            comp.wait_event(ev)
 
     for _ in range(max(1, args.warmup)):
         step()
+    drain()
     torch.cuda.synchronize()
     _barrier(world)
     a, b = _ev_pair()
     a.record()
+    up.wait_stream(comp)
+    down.wait_stream(comp)
     for _ in range(args.steps):
         step()
+    drain()
     b.record()
     torch.cuda.synchronize()
     ms = _max_over_ranks(a.elapsed_time(b), world) / args.steps
     value = _aggregate(stack.flops_fwd + stack.flops_bwd, world, ms)
     return {"value": round(value, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "copies": "pinned host buffers; uploads and downloads on two side streams, "
+                      "overlapping the compute of other layers"}
 
 
 def run_reference(args, rank, world):
@@ -520,7 +591,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="stack",
-                    help="stack (the headline) or one S / L layer (profiling)")
+                    help="stack (the headline); one S / L layer (profiling); the stack with "
+                         "rotary, learned gate or Hkv = Hq; long context")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches instead of replaying a CUDA graph of one step")

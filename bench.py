@@ -191,6 +191,9 @@ WORKLOADS = {
     "stack_mha": WORKLOAD.replace("Hkv=3", "Hkv=6") + " with Hkv = Hq (the Guide's default n_kv_head = n_head)",
     "long": ("long context: one S layer (window 8192) and one L layer (full causal), B=2, T=16384, "
              "Hq=16, Hkv=4, d=128, QK-RMSNorm gains 1+0.1N, no VE"),
+    "block_stack": ("8 whole attention blocks (pre-norm, c_q / c_k / c_v, attention, c_proj, "
+                    "residual) at C=768: B=16, T=2048, Hq=6, Hkv=3, d=128, SSSL windows, rotary "
+                    "tables, VE with the learned gate on odd layers"),
 }
 
 # (B, T, Hq, Hkv) of each workload; d = 128 throughout
@@ -328,6 +331,144 @@ class Stack:
     def launches_per_step(self):
         return sum(self.LAUNCHES_PER_LAYER + (2 if (self.learned_gate and ve) else 0)
                    for _, ve in self.sched)
+
+
+class BlockStack:
+    """The stack of whole attention blocks: per layer the block forward
+    (pre-norm, projections, attention, output projection, residual), then
+    the block backwards in reverse layer order, through swa_block_fwd /
+    swa_block_bwd."""
+
+    C = 768
+
+    def __init__(self, swa, dev):
+        from sliding_window_gqa_qk_gb300.inputs import make_block_inputs
+        self.swa = swa
+        C = self.C
+        self.sched = layer_schedule(swa.swa_sssl_window, swa.swa_has_ve)
+        inv = 10000.0 ** (-torch.arange(D // 2, dtype=torch.float64) * 2.0 / D)
+        ang = torch.arange(T, dtype=torch.float64)[:, None] * inv[None, :]
+        self.rope = (torch.cos(ang).float().to(dev).contiguous(),
+                     torch.sin(ang).float().to(dev).contiguous())
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.layers = []
+        for li, (W, ve) in enumerate(self.sched):
+            p = Problem(B=B, T=T, Hq=HQ, Hkv=HKV, d=D, window=W, gain_std=0.1, ve=ve, vocab=VOCAB)
+            x = make_block_inputs(p, C, layer=li, gate_ch=32 if ve else None)
+            g = {k: (t.to(dev) if t is not None else None) for k, t in x.items()}
+            prm = swa.make_params(B, T, HQ, HKV, D, W, True, 0.0, p.eps, VE_SCALE, VOCAB if ve else 0)
+            n = swa.swa_block_workspace_size(prm, C, 1)
+            ws = torch.empty(n, dtype=torch.uint8, device=dev)
+            if swa.swa_attn_workspace_init(ws, n) != 0:
+                raise RuntimeError("workspace init")
+            L = dict(prm=prm, g=g, ws=ws, out=torch.empty_like(g["x"]), dx=torch.empty_like(g["x"]))
+            for k in ("wq", "wk", "wv", "wo"):
+                L["d" + k] = torch.empty(g[k].shape, **f32)
+            L["dgq"], L["dgk"] = torch.empty(D, **f32), torch.empty(D, **f32)
+            L["dve"] = torch.empty(g["ve"].shape, **f32) if ve else None
+            L["dgate_w"] = torch.empty(g["gate_w"].shape, **f32) if ve else None
+            L["ex"] = swa.make_block_extras(rope=self.rope, gate_w=g["gate_w"], d_gate_w=L["dgate_w"])
+            L["w"] = swa.make_block_weights(g["wq"], g["wk"], g["wv"], g["wo"])
+            self.layers.append(L)
+        rows, nq, nkv = B * T, HQ * D, HKV * D
+        gemm_fwd = 2 * rows * C * (nq + 2 * nkv) + 2 * rows * nq * C
+        self.flops_attn = sum(sum(flops(B, T, HQ, D, W)) for W, _ in self.sched)
+        self.flops_gemm = len(self.sched) * 3 * gemm_fwd    # forward + 2x in the backward
+        self.flops = self.flops_attn + self.flops_gemm
+
+    def fwd(self, L):
+        g = L["g"]
+        st = self.swa.swa_block_fwd(L["prm"], L["ex"], L["w"], g["x"], g["gq"], g["gk"], g["ve"],
+                                    g["tok"], L["out"], L["ws"])
+        if st != 0:
+            raise self.swa.SwaError(st, "swa_block_fwd")
+
+    def bwd(self, L):
+        g = L["g"]
+        st = self.swa.swa_block_bwd(L["prm"], L["ex"], L["w"], g["x"], g["gq"], g["gk"], g["ve"],
+                                    g["tok"], g["dout"], L["dx"], L["dwq"], L["dwk"], L["dwv"],
+                                    L["dwo"], L["dgq"], L["dgk"], L["dve"], L["ws"])
+        if st != 0:
+            raise self.swa.SwaError(st, "swa_block_bwd")
+
+    def step(self, ev=None):
+        for L in self.layers:
+            if ev is not None:
+                ev["fwd"].append(_ev_pair())
+                ev["fwd"][-1][0].record()
+            self.fwd(L)
+            if ev is not None:
+                ev["fwd"][-1][1].record()
+        for L in reversed(self.layers):
+            if ev is not None:
+                ev["bwd"].append(_ev_pair())
+                ev["bwd"][-1][0].record()
+            self.bwd(L)
+            if ev is not None:
+                ev["bwd"][-1][1].record()
+
+
+def run_block_stack(args, rank, world, dev):
+    """Times the block stack: one step's launches (our kernels and the
+    cuBLASLt projections) captured in a CUDA graph and replayed."""
+    import sliding_window_gqa_qk_gb300 as swa
+    swa.load("bf16")
+    stack = BlockStack(swa, dev)
+    start, stop = _ev_pair()
+    ev = {"fwd": [], "bwd": []}
+    with ClockSampler(_physical_index(torch.cuda.current_device())) as clocks:
+        for _ in range(args.warmup):
+            stack.step()
+        for L in stack.layers:
+            st = swa.swa_attn_check_status(L["ws"])
+            if st != swa.SWA_OK:
+                raise swa.SwaError(st, "device status after warm-up")
+        graph = None
+        if not args.no_graph:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                stack.step()
+            graph.replay()
+        torch.cuda.synchronize()
+        _barrier(world)
+        t0 = clocks.mark()
+        start.record()
+        for _ in range(args.steps):
+            if graph is not None:
+                graph.replay()
+            else:
+                stack.step()
+        stop.record()
+        torch.cuda.synchronize()
+        t1 = clocks.mark()
+        for _ in range(args.steps):
+            stack.step(ev)
+        torch.cuda.synchronize()
+    _barrier(world)
+    ms = _max_over_ranks(start.elapsed_time(stop), world) / args.steps
+    stage_ms = {k: sum(a.elapsed_time(b) for a, b in v) / args.steps for k, v in ev.items()}
+    value = _aggregate(stack.flops, world, ms)
+    peaks, peak_kind = load_peaks()
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    return {
+        "metric": "TFLOP/s fwd+bwd of the whole attention block (masked attention + projections)",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOADS["block_stack"], "global_batch": B * world, "seq_len": T,
+                   "parallelism": "single GPU" if world == 1 else f"replicas over batch x{world}",
+                   "l2": "inputs larger than L2", "flops_per_step": stack.flops,
+                   "attention_flops_per_step": stack.flops_attn,
+                   "projection_flops_per_step": stack.flops_gemm,
+                   "attention_only_tflops": round(stack.flops_attn * world / (ms * 1e-3) / 1e12, 2),
+                   "pct_of_peak": round(100 * value / world / peak, 2), "peak_tflops": peak,
+                   "peak_source": f"{peak_kind} bf16_tflops_sustained",
+                   "launch": ("one step's launches captured in a CUDA graph, replayed per step"
+                              if graph is not None else "eager launches"),
+                   "stage_ms_per_step": {k: round(v, 4) for k, v in stage_ms.items()},
+                   "projections": "cuBLASLt (bf16 operands, fp32 accumulation)"},
+        "clocks": clocks.summary(t0, t1),
+    }
 
 
 def _ev_pair():
@@ -592,7 +733,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="stack",
                     help="stack (the headline); one S / L layer (profiling); the stack with "
-                         "rotary, learned gate or Hkv = Hq; long context")
+                         "rotary, learned gate or Hkv = Hq; long context; the stack of whole "
+                         "blocks (projections included)")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches instead of replaying a CUDA graph of one step")
@@ -613,7 +755,10 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    out = run_ours(args, rank, world, dev)
+    if args.workload == "block_stack":
+        out = run_block_stack(args, rank, world, dev)
+    else:
+        out = run_ours(args, rank, world, dev)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

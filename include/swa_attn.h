@@ -26,7 +26,8 @@
  * Conventions common to every call:
  *   - All tensor pointers are DEVICE pointers of the current CUDA device; the
  *     caller owns every buffer, including the workspace. The library never
- *     allocates or frees memory.
+ *     allocates or frees device memory (the block calls below give cuBLASLt
+ *     a slice of the workspace as its scratch).
  *   - Layouts are dense row-major:
  *       q, o, dO, dq       [B, T, Hq,  d]   elem
  *       k, v, dk, dv       [B, T, Hkv, d]   elem
@@ -244,6 +245,60 @@ swa_status swa_attn_fwd_noalloc(const swa_params* p, const void* q, const void* 
                                 const void* v, const float* gq, const float* gk, const void* ve,
                                 const int32_t* tok, const float* ve_gate, void* o, float* lse,
                                 void* stream);
+
+/*
+ * The whole attention block around the core: the block's pre-norm, the four
+ * bias-free projections c_q, c_k, c_v, c_proj and the residual
+ * (autoresearch Administrator & Developer Guide §8.2.1 model table,
+ * "Pre-norm + residual": x = x + attn(norm(x)); train.py walkthrough post,
+ * model paragraph: RMSNorm on the block inputs):
+ *   xn  = x / sqrt(mean_c(x^2) + eps)               (no gain; eps of swa_params)
+ *   q   = xn wq^T, k = xn wk^T, v = xn wv^T         (viewed as [B, T, H, d])
+ *   o   = the attention of swa_attn_fwd_ex on (q, k, v), with the learned
+ *         gate (if any) reading the first gate_ch channels of xn
+ *   out = x + o wo^T                                (o viewed as [B, T, Hq*d])
+ * Weights use the torch.nn.Linear layout [out_features][in_features], elem:
+ *   wq [Hq*d][C], wk and wv [Hkv*d][C], wo [C][Hq*d];  x, out, dout, dx
+ *   [B, T, C] elem;  weight gradients dwq, dwk, dwv, dwo fp32, same shapes
+ *   as the weights (overwritten; NULL skips one).
+ * C (the model width) is a multiple of 8, at most 65536; B*T < 2^31.
+ * Extras: rotary tables and gate_w / gate_ch / d_gate_w as for the _ex
+ * calls; gate_x and d_gate_x must be NULL (the block supplies the gate's
+ * input and adds the gradient of the channels it read into dx); gate_ch <= C.
+ * The projections run on cuBLASLt, opened at run time (dlopen of
+ * libcublasLt.so.13): where it cannot be opened the block calls return
+ * SWA_ERR_UNSUPPORTED. Its handle is created on the first block call made
+ * on each device; it gets a slice of the workspace as its only device
+ * scratch. The workspace (swa_block_workspace_size) holds the attention's
+ * workspace first (so swa_attn_check_status reads the block workspace too),
+ * then the forward's saved tensors (xn, q, k, v, o, lse); swa_block_bwd
+ * needs the workspace that swa_block_fwd filled for the same inputs.
+ */
+typedef struct {
+  int C;              /* model width: channels of x                         */
+  const void* wq;     /* [Hq*d][C]  elem                                     */
+  const void* wk;     /* [Hkv*d][C] elem                                     */
+  const void* wv;     /* [Hkv*d][C] elem                                     */
+  const void* wo;     /* [C][Hq*d]  elem                                     */
+} swa_block_weights;
+
+/* Bytes of workspace for swa_block_fwd (for_backward = 0) or for the pair
+ * swa_block_fwd + swa_block_bwd (for_backward = 1); 0 for invalid arguments. */
+size_t swa_block_workspace_size(const swa_params* p, int C, int for_backward);
+
+/* out = x + c_proj(attention(c_q, c_k, c_v of the normed x)). */
+swa_status swa_block_fwd(const swa_params* p, const swa_extras* ex, const swa_block_weights* w,
+                         const void* x, const float* gq, const float* gk, const void* ve,
+                         const int32_t* tok, void* out, void* workspace, size_t ws_bytes, void* stream);
+
+/* Gradients of <out, dout>: dx (elem, including the residual's dout), the
+ * weight gradients, and the attention's dgq, dgk, dve, d_gate_w as in
+ * swa_attn_bwd_ex. */
+swa_status swa_block_bwd(const swa_params* p, const swa_extras* ex, const swa_block_weights* w,
+                         const void* x, const float* gq, const float* gk, const void* ve,
+                         const int32_t* tok, const void* dout, void* dx, float* dwq, float* dwk,
+                         float* dwv, float* dwo, float* dgq, float* dgk, float* dve, void* workspace,
+                         size_t ws_bytes, void* stream);
 
 /*
  * Synchronises `stream`, reads the workspace status word, clears it, and

@@ -27,6 +27,8 @@ __all__ = [
     "swa_attn_workspace_size", "swa_attn_workspace_init", "swa_attn_fwd", "swa_attn_bwd",
     "swa_attn_fwd_ex", "swa_attn_bwd_ex",
     "swa_attn_fwd_noalloc",
+    "swa_block_weights", "swa_block_workspace_size", "swa_block_fwd", "swa_block_bwd",
+    "make_block_weights", "make_block_extras",
     "swa_attn_check_status", "swa_sssl_window", "swa_has_ve", "swa_strerror",
     "swa_build_info", "attention_forward", "attention_backward", "make_params",
     "SWA_OK", "SWA_ERR_INVALID_ARG", "SWA_ERR_UNSUPPORTED", "SWA_ERR_CUDA", "SWA_ERR_TIMEOUT",
@@ -72,6 +74,13 @@ class swa_extras(ctypes.Structure):
                 ("d_gate_w", ctypes.c_void_p), ("d_gate_x", ctypes.c_void_p)]
 
 
+class swa_block_weights(ctypes.Structure):
+    """Weights of the block calls: model width C and the four projection
+    matrices in the torch.nn.Linear layout (see include/swa_attn.h)."""
+    _fields_ = [("C", ctypes.c_int), ("wq", ctypes.c_void_p), ("wk", ctypes.c_void_p),
+                ("wv", ctypes.c_void_p), ("wo", ctypes.c_void_p)]
+
+
 _LIBS: dict = {}
 _vp = ctypes.c_void_p
 
@@ -101,6 +110,13 @@ def load(kind: str = "bf16") -> ctypes.CDLL:
     lib.swa_attn_bwd_ex.restype = ctypes.c_int
     lib.swa_attn_fwd_noalloc.argtypes = [P] + [_vp] * 10 + [_vp]
     lib.swa_attn_fwd_noalloc.restype = ctypes.c_int
+    W = ctypes.POINTER(swa_block_weights)
+    lib.swa_block_workspace_size.argtypes = [P, ctypes.c_int, ctypes.c_int]
+    lib.swa_block_workspace_size.restype = ctypes.c_size_t
+    lib.swa_block_fwd.argtypes = [P, R, W] + [_vp] * 7 + [ctypes.c_size_t, _vp]
+    lib.swa_block_fwd.restype = ctypes.c_int
+    lib.swa_block_bwd.argtypes = [P, R, W] + [_vp] * 15 + [ctypes.c_size_t, _vp]
+    lib.swa_block_bwd.restype = ctypes.c_int
     lib.swa_attn_check_status.argtypes = [_vp, _vp]
     lib.swa_attn_check_status.restype = ctypes.c_int
     lib.swa_sssl_window.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_char_p, ctypes.c_int]
@@ -226,6 +242,48 @@ def swa_attn_fwd_noalloc(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, stream=No
     return int(load(kind).swa_attn_fwd_noalloc(
         ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(gq), _ptr(gk), _ptr(ve), _ptr(tok),
         _ptr(ve_gate), _ptr(o), _ptr(lse), _stream(stream)))
+
+
+def make_block_weights(wq, wk, wv, wo) -> swa_block_weights:
+    """swa_block_weights from device tensors wq [Hq*d, C], wk, wv [Hkv*d, C],
+    wo [C, Hq*d] (the model width C is taken from wq)."""
+    return swa_block_weights(int(wq.shape[1]), _ptr(wq), _ptr(wk), _ptr(wv), _ptr(wo))
+
+
+def make_block_extras(rope=None, gate_w=None, d_gate_w=None) -> swa_extras:
+    """swa_extras of the block calls: rope = (cos, sin) fp32 [rows, d/2] or
+    None; gate_w fp32 [Hkv, C] (the block feeds the gate its normed input);
+    d_gate_w fp32 [Hkv, C] backward output or None."""
+    e = make_extras(rope)
+    if gate_w is not None:
+        e.gate_w = _ptr(gate_w)
+        e.gate_ch = int(gate_w.shape[1])
+        e.d_gate_w = _ptr(d_gate_w)
+    return e
+
+
+def swa_block_workspace_size(p: swa_params, C: int, for_backward: int, kind: str = "bf16") -> int:
+    return int(load(kind).swa_block_workspace_size(ctypes.byref(p), int(C), int(for_backward)))
+
+
+def swa_block_fwd(p, ex, w, x, gq, gk, ve, tok, out, ws, ws_bytes=None, stream=None, kind=None) -> int:
+    kind = kind or _kind_of(x)
+    n = ws.numel() if ws_bytes is None else ws_bytes
+    ep = None if ex is None else ctypes.byref(ex)
+    return int(load(kind).swa_block_fwd(
+        ctypes.byref(p), ep, ctypes.byref(w), _ptr(x), _ptr(gq), _ptr(gk), _ptr(ve), _ptr(tok),
+        _ptr(out), _ptr(ws), n, _stream(stream)))
+
+
+def swa_block_bwd(p, ex, w, x, gq, gk, ve, tok, dout, dx, dwq, dwk, dwv, dwo, dgq, dgk, dve, ws,
+                  ws_bytes=None, stream=None, kind=None) -> int:
+    kind = kind or _kind_of(x)
+    n = ws.numel() if ws_bytes is None else ws_bytes
+    ep = None if ex is None else ctypes.byref(ex)
+    return int(load(kind).swa_block_bwd(
+        ctypes.byref(p), ep, ctypes.byref(w), _ptr(x), _ptr(gq), _ptr(gk), _ptr(ve), _ptr(tok),
+        _ptr(dout), _ptr(dx), _ptr(dwq), _ptr(dwk), _ptr(dwv), _ptr(dwo), _ptr(dgq), _ptr(dgk),
+        _ptr(dve), _ptr(ws), n, _stream(stream)))
 
 
 def swa_attn_check_status(ws, stream=None, kind: str = "bf16") -> int:

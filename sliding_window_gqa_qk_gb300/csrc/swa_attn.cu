@@ -11,6 +11,7 @@
 #include "../../include/swa_attn.h"
 #include "common.cuh"
 #include "rowwise.cuh"
+#include "block.cuh"
 
 #if defined(SWA_ELEM_FP32)
 #include "simt.cuh"
@@ -473,6 +474,161 @@ swa_status bwd_impl(const swa_params* p, const swa_extras* ex, const void* q, co
   return SWA_OK;
 }
 
+// ---------------------------------------------------------------------------
+// The block around the attention core: pre-norm, c_q / c_k / c_v, attention,
+// c_proj and the residual (block.cuh).
+// ---------------------------------------------------------------------------
+struct BlockCall {
+  int B, T, Hq, Hkv, d, C;
+  long long rows;                // B * T
+  blk::BlockLayout L;
+  uint8_t* ws;
+  cudaStream_t st;
+  swa_extras ex{};               // the caller's extras with the gate's input set to the normed x
+  const swa_extras* exp = nullptr;
+};
+
+swa_status block_begin(BlockCall& b, const swa_params* p, const swa_extras* ex, const swa_block_weights* w,
+                       const void* x, void* workspace, size_t ws_bytes, bool bwd, void* stream) {
+  swa_status s = check_params(p);
+  if (s != SWA_OK) return s;
+  if (w == nullptr || x == nullptr || !aligned(x, 16)) return SWA_ERR_INVALID_ARG;
+  if (w->C < 8 || w->C % 8 != 0 || w->C > (1 << 16)) return SWA_ERR_INVALID_ARG;
+  for (const void* m : {w->wq, w->wk, w->wv, w->wo})
+    if (!tensor_ok(m)) return SWA_ERR_INVALID_ARG;
+  b.B = p->B; b.T = p->T; b.Hq = p->Hq; b.Hkv = p->Hkv; b.d = p->d; b.C = w->C;
+  b.rows = static_cast<long long>(p->B) * p->T;
+  if (b.rows > 0x7fffffffLL) return SWA_ERR_UNSUPPORTED;   // GEMM dimensions are 32-bit
+  b.L = blk::block_layout(p->B, p->T, p->Hq, p->Hkv, p->d, w->C);
+  if (workspace == nullptr || !aligned(workspace, 256)) return SWA_ERR_INVALID_ARG;
+  if (ws_bytes < (bwd ? b.L.bwd_end : b.L.fwd_end)) return SWA_ERR_WORKSPACE;
+  b.ws = static_cast<uint8_t*>(workspace);
+  b.st = static_cast<cudaStream_t>(stream);
+  if (ex != nullptr) {
+    // the block gives the learned gate its input (the normed x) and takes
+    // the gradient of the channels it read
+    if (ex->gate_x != nullptr || ex->d_gate_x != nullptr) return SWA_ERR_INVALID_ARG;
+    b.ex = *ex;
+    if (ex->gate_w != nullptr) {
+      if (ex->gate_ch < 1 || ex->gate_ch > blk::kMaxBlockGateCh || ex->gate_ch > w->C)
+        return SWA_ERR_INVALID_ARG;
+      b.ex.gate_x = b.ws + b.L.xn;
+      b.ex.gate_x_stride = w->C;
+      if (bwd) b.ex.d_gate_x = reinterpret_cast<float*>(b.ws + b.L.dgx);
+    }
+    b.exp = &b.ex;
+  }
+  return SWA_OK;
+}
+
+swa_status block_fwd_impl(const swa_params* p, const swa_extras* ex, const swa_block_weights* w,
+                          const void* x, const float* gq, const float* gk, const void* ve,
+                          const int32_t* tok, void* out, void* workspace, size_t ws_bytes, void* stream) {
+  BlockCall b;
+  swa_status s = block_begin(b, p, ex, w, x, workspace, ws_bytes, false, stream);
+  if (s != SWA_OK) return s;
+  if (!tensor_ok(out)) return SWA_ERR_INVALID_ARG;
+  if (b.rows == 0) return SWA_OK;
+  if ((s = check_device()) != SWA_OK) return s;
+  uint8_t* ws = b.ws;
+  const int C = b.C, nq = b.Hq * b.d, nkv = b.Hkv * b.d, rows = static_cast<int>(b.rows);
+  elem_t* xn = reinterpret_cast<elem_t*>(ws + b.L.xn);
+  blk::prenorm_fwd_kernel<<<blk::prenorm_grid(b.rows), blk::kPnWarps * 32, 0, b.st>>>(
+      static_cast<const elem_t*>(x), xn, reinterpret_cast<float*>(ws + b.L.rstd), b.rows, C, p->eps);
+  if ((s = launched()) != SWA_OK) return s;
+  void* lt = ws + b.L.lt;
+  // q / k / v rows = xn rows times w^T: column-major D[n_out x rows] = W^T-stored (C x n_out)^T xn
+  const void* wmat[3] = {w->wq, w->wk, w->wv};
+  const size_t dst[3] = {b.L.q, b.L.k, b.L.v};
+  const int nout[3] = {nq, nkv, nkv};
+  for (int i = 0; i < 3; ++i) {
+    blk::Gemm g;
+    g.ta = true; g.tb = false; g.m = nout[i]; g.n = rows; g.k = C;
+    g.A = wmat[i]; g.lda = C; g.B = xn; g.ldb = C; g.D = ws + dst[i]; g.ldd = nout[i];
+    if ((s = blk::gemm(g, lt, blk::kLtWsBytes, b.st)) != SWA_OK) return s;
+  }
+  s = fwd_impl(p, b.exp, ws + b.L.q, ws + b.L.k, ws + b.L.v, gq, gk, ve, tok, nullptr, ws + b.L.o,
+               reinterpret_cast<float*>(ws + b.L.lse), ws, b.L.attn_bytes, 0, stream, true);
+  if (s != SWA_OK) return s;
+  // out = x + o wo^T
+  blk::Gemm g;
+  g.ta = true; g.tb = false; g.m = C; g.n = rows; g.k = nq;
+  g.A = w->wo; g.lda = nq; g.B = ws + b.L.o; g.ldb = nq;
+  g.beta = 1.f; g.C = x; g.D = out; g.ldd = C;
+  return blk::gemm(g, lt, blk::kLtWsBytes, b.st);
+}
+
+swa_status block_bwd_impl(const swa_params* p, const swa_extras* ex, const swa_block_weights* w,
+                          const void* x, const float* gq, const float* gk, const void* ve,
+                          const int32_t* tok, const void* dout, void* dx, float* dwq, float* dwk,
+                          float* dwv, float* dwo, float* dgq, float* dgk, float* dve, void* workspace,
+                          size_t ws_bytes, void* stream) {
+  BlockCall b;
+  swa_status s = block_begin(b, p, ex, w, x, workspace, ws_bytes, true, stream);
+  if (s != SWA_OK) return s;
+  if (!tensor_ok(dout) || !tensor_ok(dx)) return SWA_ERR_INVALID_ARG;
+  uint8_t* ws = b.ws;
+  const int C = b.C, nq = b.Hq * b.d, nkv = b.Hkv * b.d, rows = static_cast<int>(b.rows);
+  if (b.rows == 0) {
+    // nothing to differentiate: every weight gradient is zero
+    const size_t n[4] = {static_cast<size_t>(nq) * C, static_cast<size_t>(nkv) * C,
+                         static_cast<size_t>(nkv) * C, static_cast<size_t>(C) * nq};
+    float* dw[4] = {dwq, dwk, dwv, dwo};
+    for (int i = 0; i < 4; ++i)
+      if (dw[i] && cudaMemsetAsync(dw[i], 0, n[i] * sizeof(float), b.st) != cudaSuccess) return SWA_ERR_CUDA;
+    return bwd_impl(p, b.exp, ws + b.L.q, ws + b.L.k, ws + b.L.v, gq, gk, ve, tok, nullptr, ws + b.L.o,
+                    reinterpret_cast<const float*>(ws + b.L.lse), ws + b.L.dO, ws + b.L.dq, ws + b.L.dk,
+                    ws + b.L.dv, dgq, dgk, dve, ws, b.L.attn_bytes, 0, stream);
+  }
+  if ((s = check_device()) != SWA_OK) return s;
+  void* lt = ws + b.L.lt;
+  const elem_t* xn = reinterpret_cast<const elem_t*>(ws + b.L.xn);
+  // dwo [C][nq] = dout^T o: column-major (nq x C) = o (nq x rows) dout^T
+  if (dwo != nullptr) {
+    blk::Gemm g;
+    g.ta = false; g.tb = true; g.m = nq; g.n = C; g.k = rows;
+    g.A = ws + b.L.o; g.lda = nq; g.B = dout; g.ldb = C; g.D = dwo; g.dt = CUDA_R_32F; g.ldd = nq;
+    if ((s = blk::gemm(g, lt, blk::kLtWsBytes, b.st)) != SWA_OK) return s;
+  }
+  // gradient of the attention output: dO rows = dout rows times wo
+  {
+    blk::Gemm g;
+    g.ta = false; g.tb = false; g.m = nq; g.n = rows; g.k = C;
+    g.A = w->wo; g.lda = nq; g.B = dout; g.ldb = C; g.D = ws + b.L.dO; g.ldd = nq;
+    if ((s = blk::gemm(g, lt, blk::kLtWsBytes, b.st)) != SWA_OK) return s;
+  }
+  s = bwd_impl(p, b.exp, ws + b.L.q, ws + b.L.k, ws + b.L.v, gq, gk, ve, tok, nullptr, ws + b.L.o,
+               reinterpret_cast<const float*>(ws + b.L.lse), ws + b.L.dO, ws + b.L.dq, ws + b.L.dk,
+               ws + b.L.dv, dgq, dgk, dve, ws, b.L.attn_bytes, SWA_REUSE_PROLOGUE, stream);
+  if (s != SWA_OK) return s;
+  const void* wmat[3] = {w->wq, w->wk, w->wv};
+  const size_t grad[3] = {b.L.dq, b.L.dk, b.L.dv};
+  const int nout[3] = {nq, nkv, nkv};
+  float* dw[3] = {dwq, dwk, dwv};
+  float* dxn = reinterpret_cast<float*>(ws + b.L.dxn);
+  for (int i = 0; i < 3; ++i) {
+    // dw [n_out][C] = grad^T xn: column-major (C x n_out) = xn (C x rows) grad^T
+    if (dw[i] != nullptr) {
+      blk::Gemm g;
+      g.ta = false; g.tb = true; g.m = C; g.n = nout[i]; g.k = rows;
+      g.A = xn; g.lda = C; g.B = ws + grad[i]; g.ldb = nout[i]; g.D = dw[i]; g.dt = CUDA_R_32F; g.ldd = C;
+      if ((s = blk::gemm(g, lt, blk::kLtWsBytes, b.st)) != SWA_OK) return s;
+    }
+    // dxn rows += grad rows times w
+    blk::Gemm g;
+    g.ta = false; g.tb = false; g.m = C; g.n = rows; g.k = nout[i];
+    g.A = wmat[i]; g.lda = C; g.B = ws + grad[i]; g.ldb = nout[i];
+    g.beta = i == 0 ? 0.f : 1.f; g.D = dxn; g.dt = CUDA_R_32F; g.ldd = C;
+    if ((s = blk::gemm(g, lt, blk::kLtWsBytes, b.st)) != SWA_OK) return s;
+  }
+  const bool gate = b.exp != nullptr && b.ex.gate_w != nullptr;
+  blk::prenorm_bwd_kernel<<<blk::prenorm_grid(b.rows), blk::kPnWarps * 32, 0, b.st>>>(
+      static_cast<const elem_t*>(x), reinterpret_cast<const float*>(ws + b.L.rstd), dxn,
+      gate ? reinterpret_cast<const float*>(ws + b.L.dgx) : nullptr, gate ? b.ex.gate_ch : 0,
+      static_cast<const elem_t*>(dout), static_cast<elem_t*>(dx), b.rows, C);
+  return launched();
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -557,6 +713,27 @@ swa_status swa_attn_fwd_noalloc(const swa_params* p, const void* q, const void* 
   if (ss != SWA_OK) return ss;
   return fwd_impl(p, nullptr, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, scratch,
                   SWA_NOALLOC_SCRATCH_BYTES, 0, stream, false);
+}
+
+size_t swa_block_workspace_size(const swa_params* p, int C, int for_backward) {
+  if (check_params(p) != SWA_OK || C < 8 || C % 8 != 0 || C > (1 << 16)) return 0;
+  const blk::BlockLayout L = blk::block_layout(p->B, p->T, p->Hq, p->Hkv, p->d, C);
+  return for_backward ? L.bwd_end : L.fwd_end;
+}
+
+swa_status swa_block_fwd(const swa_params* p, const swa_extras* ex, const swa_block_weights* w,
+                         const void* x, const float* gq, const float* gk, const void* ve,
+                         const int32_t* tok, void* out, void* workspace, size_t ws_bytes, void* stream) {
+  return block_fwd_impl(p, ex, w, x, gq, gk, ve, tok, out, workspace, ws_bytes, stream);
+}
+
+swa_status swa_block_bwd(const swa_params* p, const swa_extras* ex, const swa_block_weights* w,
+                         const void* x, const float* gq, const float* gk, const void* ve,
+                         const int32_t* tok, const void* dout, void* dx, float* dwq, float* dwk,
+                         float* dwv, float* dwo, float* dgq, float* dgk, float* dve, void* workspace,
+                         size_t ws_bytes, void* stream) {
+  return block_bwd_impl(p, ex, w, x, gq, gk, ve, tok, dout, dx, dwq, dwk, dwv, dwo, dgq, dgk, dve,
+                        workspace, ws_bytes, stream);
 }
 
 int swa_sssl_window(int layer, int n_layer, const char* pattern, int T) {

@@ -95,6 +95,40 @@ def make_inputs(p: Problem, layer: int = 0, dtype: torch.dtype = torch.bfloat16,
     return out
 
 
+def make_block_inputs(p: Problem, C: int, layer: int = 0, dtype: torch.dtype = torch.bfloat16,
+                      gate_ch: Optional[int] = None, seed: int = BASE_SEED, device="cpu") -> dict:
+    """Draw the inputs of one whole attention block (pre-norm, projections,
+    residual around the attention) of model width C.
+
+    Recipe: seeds base + 100 * layer + 10.. in the order x, wq, wk, wv, wo,
+    dout, gate_w; x, dout ~ N(0, 1) [B, T, C]; the projection weights in the
+    torch.nn.Linear layout, uniform with variance 1 / fan_in (wq, wk, wv:
+    [H*d, C], fan_in C; wo: [C, Hq*d], fan_in Hq*d; the pages' initialisation
+    zeroes c_proj, which would hide the attention from the output, so wo is
+    drawn like the others); gate_w ~ 0.25 N(0, 1) fp32 [Hkv, gate_ch] when
+    gate_ch is given. Gains, VE table and token ids come from make_inputs
+    (same seeds). All elem tensors are rounded to ``dtype``."""
+    s = seed + 100 * layer + 10
+    B, T, Hq, Hkv, d = p.B, p.T, p.Hq, p.Hkv, p.d
+    kw = dict(device=device)
+
+    def uniform(shape, fan_in, i):
+        a = (3.0 / fan_in) ** 0.5
+        return ((2.0 * torch.rand(*shape, generator=_gen(s + i, device), **kw) - 1.0) * a).to(dtype)
+
+    base = make_inputs(p, layer=layer, dtype=dtype, seed=seed, device=device)
+    out = {k: base[k] for k in ("gq", "gk", "ve", "tok")}
+    out["x"] = torch.randn(B, T, C, generator=_gen(s + 0, device), **kw).to(dtype)
+    out["wq"] = uniform((Hq * d, C), C, 1)
+    out["wk"] = uniform((Hkv * d, C), C, 2)
+    out["wv"] = uniform((Hkv * d, C), C, 3)
+    out["wo"] = uniform((C, Hq * d), Hq * d, 4)
+    out["dout"] = torch.randn(B, T, C, generator=_gen(s + 5, device), **kw).to(dtype)
+    out["gate_w"] = (None if gate_ch is None else
+                     0.25 * torch.randn(Hkv, gate_ch, generator=_gen(s + 6, device), **kw))
+    return out
+
+
 def as_f64(t):
     """The exact float64 value of a tensor (or None), as a NumPy array."""
     if t is None:

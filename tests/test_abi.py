@@ -246,3 +246,79 @@ def test_null_extras_behave_like_the_plain_calls(kind):
     assert fwd_ex_call(params(B=0), None, kind) == swa.SWA_OK
     assert fwd_ex_call(params(B=0), extras(), kind) == swa.SWA_OK
     assert fwd_ex_call(params(), None, kind, q=None) == swa.SWA_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------------------
+# Block calls (pre-norm, projections, residual around the attention)
+# ---------------------------------------------------------------------------
+
+def block_weights(C=512, wq=A, wk=A, wv=A, wo=A):
+    return swa.swa_block_weights(C, wq, wk, wv, wo)
+
+
+def block_fwd_call(p, w, ex=None, kind="bf16", ws_bytes=1 << 40, x=A, out=A, ws=A):
+    lib = swa.load(kind)
+    ep = None if ex is None else ctypes.byref(ex)
+    wp = None if w is None else ctypes.byref(w)
+    return lib.swa_block_fwd(ctypes.byref(p), ep, wp, x, None, None, None, None, out, ws, ws_bytes,
+                             None)
+
+
+def block_bwd_call(p, w, ex=None, kind="bf16", ws_bytes=1 << 40, x=A, dout=A, dx=A, ws=A):
+    lib = swa.load(kind)
+    ep = None if ex is None else ctypes.byref(ex)
+    wp = None if w is None else ctypes.byref(w)
+    return lib.swa_block_bwd(ctypes.byref(p), ep, wp, x, None, None, None, None, dout, dx, None,
+                             None, None, None, None, None, None, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_block_workspace_size(kind):
+    p = params()
+    attn = swa.swa_attn_workspace_size(p, 1, kind)
+    fwd = swa.swa_block_workspace_size(p, 512, 0, kind)
+    bwd = swa.swa_block_workspace_size(p, 512, 1, kind)
+    es = 2 if kind == "bf16" else 4
+    B, T, Hq, Hkv, d, C = 2, 300, 4, 2, 128, 512
+    # the attention's backward workspace, xn, q, k, v, o, lse, rstd, cuBLASLt scratch
+    assert fwd >= attn + B * T * (C + 2 * Hq * d + 2 * Hkv * d) * es + 4 * B * T * (Hq + 1) + (32 << 20)
+    # + dO, dq, dk, dv, dxn (fp32), the gate's channel gradients (fp32)
+    assert bwd >= fwd + B * T * (2 * Hq * d + 2 * Hkv * d) * es + 4 * B * T * (C + 32)
+    for C_bad in (0, 4, 12, 1 << 17):
+        assert swa.swa_block_workspace_size(p, C_bad, 0, kind) == 0
+    assert swa.swa_block_workspace_size(params(d=96), 512, 0, kind) == 0
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_block_calls_reject_bad_arguments(kind):
+    p = params()
+    for call in (block_fwd_call, block_bwd_call):
+        assert call(p, None, kind=kind) == swa.SWA_ERR_INVALID_ARG
+        assert call(p, block_weights(C=12), kind=kind) == swa.SWA_ERR_INVALID_ARG
+        for name in ("wq", "wk", "wv", "wo"):
+            assert call(p, block_weights(**{name: None}), kind=kind) == swa.SWA_ERR_INVALID_ARG
+            assert call(p, block_weights(**{name: MIS}), kind=kind) == swa.SWA_ERR_INVALID_ARG
+        assert call(p, block_weights(), kind=kind, x=MIS) == swa.SWA_ERR_INVALID_ARG
+        assert call(p, block_weights(), kind=kind, ws=A + 16) == swa.SWA_ERR_INVALID_ARG
+        assert call(params(d=96), block_weights(), kind=kind) == swa.SWA_ERR_UNSUPPORTED
+        # the block gives the gate its input itself
+        assert call(p, block_weights(), extras(gate_w=A, gate_x=A, gate_ch=8, gate_x_stride=8),
+                    kind=kind) == swa.SWA_ERR_INVALID_ARG
+        assert call(p, block_weights(C=16), extras(gate_w=A, gate_ch=32), kind=kind) == \
+            swa.SWA_ERR_INVALID_ARG
+    assert block_fwd_call(p, block_weights(), kind=kind, out=None) == swa.SWA_ERR_INVALID_ARG
+    assert block_bwd_call(p, block_weights(), kind=kind, dx=MIS) == swa.SWA_ERR_INVALID_ARG
+    assert block_bwd_call(p, block_weights(), extras(d_gate_x=A), kind=kind) == swa.SWA_ERR_INVALID_ARG
+    need = swa.swa_block_workspace_size(p, 512, 0, kind)
+    need_b = swa.swa_block_workspace_size(p, 512, 1, kind)
+    assert block_fwd_call(p, block_weights(), kind=kind, ws_bytes=need - 1) == swa.SWA_ERR_WORKSPACE
+    assert block_bwd_call(p, block_weights(), kind=kind, ws_bytes=need) == swa.SWA_ERR_WORKSPACE
+    assert block_bwd_call(p, block_weights(), kind=kind, ws_bytes=need_b - 1) == swa.SWA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_empty_block_forward_is_a_no_op(kind):
+    assert block_fwd_call(params(B=0), block_weights(), kind=kind) == swa.SWA_OK
+    assert block_fwd_call(params(T=0), block_weights(), kind=kind) == swa.SWA_OK
+    # nothing to zero when every gradient output is NULL
+    assert block_bwd_call(params(B=0), block_weights(), kind=kind) == swa.SWA_OK

@@ -1,0 +1,138 @@
+"""GPU parity of the whole attention block (pre-norm, c_q / c_k / c_v, the
+attention, c_proj and the residual) through the C ABI, against the float64
+block oracle on the same seeded inputs, for both builds (relative error per
+tensor, 2e-2 for bf16 tensors and fp32 accumulation, 1e-5 for the fp32 debug
+build). The output and the input gradient are also compared without the
+residual's exact pass-through (out - x, dx - dout), so the attention branch
+is held to the same bound."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sliding_window_gqa_qk_gb300 as swa
+from sliding_window_gqa_qk_gb300.inputs import S_LAYER, Problem, as_f64, make_block_inputs
+from gpu_helpers import DTYPE, TOL, rope_tables
+
+pytestmark = pytest.mark.gpu
+
+# (problem, model width C, learned-gate channels or None, rotary tables)
+CASES = {
+    "gqa_ve_gate_rope_d64": (Problem(B=2, T=200, Hq=4, Hkv=2, d=64, window=100, gain_std=0.1,
+                                     ve=True, vocab=97), 192, 32, True),
+    "mha_full_causal_d128": (Problem(B=1, T=300, Hq=2, Hkv=2, d=128, window=-1, gain_std=0.1),
+                             256, None, False),
+    "group3_ragged_unit_gains": (Problem(B=1, T=131, Hq=3, Hkv=1, d=128, window=40, ve=True,
+                                         vocab=50), 136, 8, False),
+}
+
+
+def run_block_library(p, C, x, rope=False):
+    dev = torch.device("cuda:0")
+    g = {k: (t.to(dev).contiguous() if t is not None else None) for k, t in x.items()}
+    kind = "fp32" if x["x"].dtype == torch.float32 else "bf16"
+    prm = swa.make_params(p.B, p.T, p.Hq, p.Hkv, p.d, p.window, p.causal, 0.0, p.eps, p.ve_scale,
+                          p.vocab if p.ve else 0)
+    rp = None
+    if rope:
+        rp = tuple(t.to(dev).contiguous() for t in rope_tables(p.T, p.d))
+    dgw = torch.zeros_like(g["gate_w"]) if g["gate_w"] is not None else None
+    ex = swa.make_block_extras(rope=rp, gate_w=g["gate_w"], d_gate_w=dgw)
+    w = swa.make_block_weights(g["wq"], g["wk"], g["wv"], g["wo"])
+    n = swa.swa_block_workspace_size(prm, C, 1, kind)
+    assert n > 0
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+    assert swa.swa_attn_workspace_init(ws, n, kind=kind) == swa.SWA_OK
+    out = torch.empty_like(g["x"])
+    assert swa.swa_block_fwd(prm, ex, w, g["x"], g["gq"], g["gk"], g["ve"], g["tok"], out, ws) == swa.SWA_OK
+    f32 = dict(dtype=torch.float32, device=dev)
+    dx = torch.empty_like(g["x"])
+    dwq, dwk, dwv, dwo = (torch.empty(g[k].shape, **f32) for k in ("wq", "wk", "wv", "wo"))
+    dgq = torch.empty(p.d, **f32) if g["gq"] is not None else None
+    dgk = torch.empty(p.d, **f32) if g["gk"] is not None else None
+    dve = torch.empty(g["ve"].shape, **f32) if g["ve"] is not None else None
+    assert swa.swa_block_bwd(prm, ex, w, g["x"], g["gq"], g["gk"], g["ve"], g["tok"], g["dout"], dx,
+                             dwq, dwk, dwv, dwo, dgq, dgk, dve, ws) == swa.SWA_OK
+    status = swa.swa_attn_check_status(ws, kind=kind)
+    torch.cuda.synchronize()
+    res = {"out": out, "dx": dx, "dwq": dwq, "dwk": dwk, "dwv": dwv, "dwo": dwo, "dgq": dgq,
+           "dgk": dgk, "dve": dve, "dgate_w": dgw}
+    res = {k: (v.cpu() if v is not None else None) for k, v in res.items()}
+    res["status"] = status
+    return res
+
+
+def run_block_oracle(p, x, rope=False, b_slice=None):
+    f = {k: as_f64(t) for k, t in x.items()}
+    kw = dict(Hq=p.Hq, Hkv=p.Hkv, window=p.window, causal=p.causal, eps=p.eps, gq=f["gq"],
+              gk=f["gk"], ve=f["ve"], tok=x["tok"].numpy() if x["tok"] is not None else None,
+              ve_scale=p.ve_scale, gate_w=f["gate_w"])
+    if rope:
+        kw["rope"] = tuple(t.double().numpy() for t in rope_tables(p.T, p.d))
+    xs, dout = f["x"], f["dout"]
+    if b_slice is not None:
+        xs, dout = xs[b_slice:b_slice + 1], dout[b_slice:b_slice + 1]
+        kw["tok"] = None if kw["tok"] is None else kw["tok"][b_slice:b_slice + 1]
+    out, _ = oracle.block_forward(xs, f["wq"], f["wk"], f["wv"], f["wo"], **kw)
+    g = oracle.block_backward(xs, f["wq"], f["wk"], f["wv"], f["wo"], dout, **kw)
+    g["out"] = out
+    return g
+
+
+def rel(a, r):
+    a = np.asarray(a, dtype=np.float64)
+    return np.linalg.norm(a - r) / max(np.linalg.norm(r), 1e-30)
+
+
+def compare_block(got, ref, x, tol, keys):
+    xs, dout = as_f64(x["x"]), as_f64(x["dout"])
+    errs = {}
+    for k in keys:
+        if ref.get(k) is None:
+            assert got.get(k) is None or k == "dgate_w", k
+            continue
+        errs[k] = rel(got[k].double().numpy(), ref[k])
+    errs["out - x"] = rel(got["out"].double().numpy() - xs, ref["out"] - xs)
+    errs["dx - dout"] = rel(got["dx"].double().numpy() - dout, ref["dx"] - dout)
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, (bad, errs)
+
+
+ALL = ("out", "dx", "dwq", "dwk", "dwv", "dwo", "dgq", "dgk", "dve", "dgate_w")
+
+
+@pytest.mark.parametrize("kind", ["bf16", "fp32"])
+@pytest.mark.parametrize("name", list(CASES))
+def test_block_parity_small(kind, name):
+    p, C, gate_ch, rope = CASES[name]
+    x = make_block_inputs(p, C, layer=1, dtype=DTYPE[kind], gate_ch=gate_ch)
+    got = run_block_library(p, C, x, rope)
+    assert got["status"] == swa.SWA_OK
+    compare_block(got, run_block_oracle(p, x, rope), x, TOL[kind], ALL)
+
+
+def test_block_at_zero_output_projection_is_the_identity():
+    """The pages' initialisation (c_proj = 0): the block returns its input
+    bit for bit and passes dout through to dx."""
+    p, C, gate_ch, rope = CASES["gqa_ve_gate_rope_d64"]
+    x = make_block_inputs(p, C, dtype=torch.bfloat16, gate_ch=gate_ch)
+    x["wo"] = torch.zeros_like(x["wo"])
+    got = run_block_library(p, C, x, rope)
+    assert torch.equal(got["out"], x["x"])
+    assert torch.equal(got["dx"], x["dout"])
+    assert not torch.any(got["dwq"]) and not torch.any(got["dgate_w"])
+
+
+def test_block_full_size_s_layer():
+    """The S layer's shapes inside the block at the model width of the pages'
+    default (C = 768 = Hq * d), with the value embedding, its learned gate and
+    rotary tables: every output and gradient over the whole batch (B = 16,
+    T = 2048), the weight gradients summed over all 32768 positions."""
+    p = S_LAYER.replace(ve=True, vocab=8192)
+    C = 768
+    x = make_block_inputs(p, C, layer=1, dtype=torch.bfloat16, gate_ch=32)
+    got = run_block_library(p, C, x, rope=True)
+    assert got["status"] == swa.SWA_OK
+    ref = run_block_oracle(p, x, rope=True)
+    compare_block(got, ref, x, TOL["bf16"], ALL)

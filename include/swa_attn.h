@@ -268,8 +268,8 @@ swa_status swa_attn_fwd_noalloc(const swa_params* p, const void* q, const void* 
  * The projections run on cuBLASLt, opened at run time (dlopen of
  * libcublasLt.so.13): where it cannot be opened the block calls return
  * SWA_ERR_UNSUPPORTED. Its handle is created on the first block call made
- * on each device; it gets a slice of the workspace as its only device
- * scratch. The workspace (swa_block_workspace_size) holds the attention's
+ * on each device, so make that first call outside stream capture; cuBLASLt
+ * gets a slice of the workspace as its only device scratch. The workspace (swa_block_workspace_size) holds the attention's
  * workspace first (so swa_attn_check_status reads the block workspace too),
  * then the forward's saved tensors (xn, q, k, v, o, lse); swa_block_bwd
  * needs the workspace that swa_block_fwd filled for the same inputs.

@@ -68,6 +68,15 @@ def flops(Bn, Tn, Hq, d, W):
     return 4 * d * P * Bn * Hq, 10 * d * P * Bn * Hq
 
 
+def block_gemm_flops(rows, C, nq, nkv):
+    """FLOPs of one block layer's projections, forward and backward: the
+    forward's q, k, v and output projections (2 rows C (nq + 2 nkv) and
+    2 rows nq C), twice that in the backward (each weight's gradient and
+    each input's gradient)."""
+    fwd = 2 * rows * C * (nq + 2 * nkv) + 2 * rows * nq * C
+    return 3 * fwd
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -370,10 +379,8 @@ class BlockStack:
             L["ex"] = swa.make_block_extras(rope=self.rope, gate_w=g["gate_w"], d_gate_w=L["dgate_w"])
             L["w"] = swa.make_block_weights(g["wq"], g["wk"], g["wv"], g["wo"])
             self.layers.append(L)
-        rows, nq, nkv = B * T, HQ * D, HKV * D
-        gemm_fwd = 2 * rows * C * (nq + 2 * nkv) + 2 * rows * nq * C
         self.flops_attn = sum(sum(flops(B, T, HQ, D, W)) for W, _ in self.sched)
-        self.flops_gemm = len(self.sched) * 3 * gemm_fwd    # forward + 2x in the backward
+        self.flops_gemm = len(self.sched) * block_gemm_flops(B * T, C, HQ * D, HKV * D)
         self.flops = self.flops_attn + self.flops_gemm
 
     def fwd(self, L):

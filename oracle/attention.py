@@ -23,7 +23,7 @@ Sources (the pages this follows):
           value embeddings ``Embedding(vocab_size, kv_dim)`` and the gated mix
           ``v = v + gate * ve``; ``has_ve``: alternating layers, last included).
 
-Readings where the pages are silent (each one is listed in the design doc):
+Readings where the pages are silent (the CUDA library takes the same ones):
   * window: key j is visible to query i iff 0 <= i - j <= W (W + 1 keys,
     self included); W < 0 means no window. Non-causal: |i - j| <= W.
   * softmax scale 1/sqrt(d) unless given; RMSNorm epsilon is a parameter.

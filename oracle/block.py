@@ -18,7 +18,7 @@ Sources:
           matrices and zeroes ``c_proj`` (the output projection), so at
           initialisation the block returns its input.
 
-Readings where the pages are silent (each one is listed in the design doc):
+Readings where the pages are silent (the CUDA library takes the same ones):
   * weights in the ``nn.Linear`` layout [out_features, in_features]:
     wq [Hq*d, C], wk and wv [Hkv*d, C], wo [C, Hq*d]; a projection is
     y = x @ w^T; no biases.

@@ -5,7 +5,7 @@ This module holds no arithmetic of the method: it only draws random tensors
 with a fixed seed recipe and rounds them to the dtypes the library consumes,
 so that the CUDA path and the float64 oracle see identical bits.
 
-Recipe (stated once here and in the design doc):
+Recipe:
   * base seed 42 (the training script's fixed seed, autoresearch Administrator
     & Developer Guide §3.4), plus ``100 * layer``; one ``torch.Generator`` per
     tensor, seeded base + i in the order q, k, v, gq, gk, dO, VE, tok.

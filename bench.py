@@ -200,6 +200,8 @@ WORKLOADS = {
     "stack_mha": WORKLOAD.replace("Hkv=3", "Hkv=6") + " with Hkv = Hq (the Guide's default n_kv_head = n_head)",
     "long": ("long context: one S layer (window 8192) and one L layer (full causal), B=2, T=16384, "
              "Hq=16, Hkv=4, d=128, QK-RMSNorm gains 1+0.1N, no VE"),
+    "tiny": ("tiny: one layer B=1, T=256, Hq=2, Hkv=1, d=64, window 128, unit gains, no VE "
+             "(latency-bound: 3 query tiles)"),
     "block_stack": ("8 whole attention blocks (pre-norm, c_q / c_k / c_v, attention, c_proj, "
                     "residual) at C=768: B=16, T=2048, Hq=6, Hkv=3, d=128, SSSL windows, rotary "
                     "tables, VE with the learned gate on odd layers"),
@@ -212,7 +214,14 @@ LONG_SHAPE = (2, 16384, 16, 4)
 def shape_for(workload):
     if workload == "long":
         return LONG_SHAPE
+    if workload == "tiny":
+        return (1, 256, 2, 1)
     return (B, T, HQ, HQ if workload == "stack_mha" else HKV)
+
+
+def head_dim_for(workload):
+    """(head dim, gain std: None for unit gains) of a workload."""
+    return (64, None) if workload == "tiny" else (D, 0.1)
 
 
 def schedule_for(workload, window_fn, ve_fn):
@@ -220,6 +229,8 @@ def schedule_for(workload, window_fn, ve_fn):
         return [(T // 2, False)]
     if workload == "l_layer":
         return [(-1, False)]
+    if workload == "tiny":
+        return [(128, False)]
     if workload == "long":
         # one layer of each kind of the SSSL pattern at T = 16384
         t_long = LONG_SHAPE[1]
@@ -234,6 +245,10 @@ class Stack:
         self.dev = dev
         Bn, Tn, hq, hkv = shape_for(workload)
         self.B, self.T, self.hq, self.hkv = Bn, Tn, hq, hkv
+        d, gain_std = head_dim_for(workload)
+        self.d = d
+        # inputs smaller than L2: flush it before every timed step
+        self.small = workload == "tiny"
         self.rope = None
         self.learned_gate = workload == "stack_full"
         if workload in ("stack_rope", "stack_full"):
@@ -246,10 +261,11 @@ class Stack:
         self.sched = schedule_for(workload, swa.swa_sssl_window, swa.swa_has_ve)
         self.layers = []
         for li, (W, ve) in enumerate(self.sched):
-            p = Problem(B=Bn, T=Tn, Hq=hq, Hkv=hkv, d=D, window=W, gain_std=0.1, ve=ve, vocab=VOCAB)
+            p = Problem(B=Bn, T=Tn, Hq=hq, Hkv=hkv, d=d, window=W, gain_std=gain_std, ve=ve,
+                        vocab=VOCAB)
             x = make_inputs(p, layer=li)
             g = {k: (t.to(dev) if t is not None else None) for k, t in x.items()}
-            prm = swa.make_params(Bn, Tn, hq, hkv, D, W, True, 0.0, p.eps, VE_SCALE,
+            prm = swa.make_params(Bn, Tn, hq, hkv, d, W, True, 0.0, p.eps, VE_SCALE,
                                   VOCAB if ve else 0)
             ws = swa.new_workspace(prm, True, dev, "bf16")
             L = dict(p=p, prm=prm, x=x, g=g, ws=ws)
@@ -257,8 +273,8 @@ class Stack:
             L["lse"] = torch.empty(Bn, hq, Tn, dtype=torch.float32, device=dev)
             L["dq"], L["dk"], L["dv"] = (torch.empty_like(g["q"]), torch.empty_like(g["k"]),
                                          torch.empty_like(g["v"]))
-            L["dgq"] = torch.empty(D, dtype=torch.float32, device=dev)
-            L["dgk"] = torch.empty(D, dtype=torch.float32, device=dev)
+            L["dgq"] = torch.empty(d, dtype=torch.float32, device=dev)
+            L["dgk"] = torch.empty(d, dtype=torch.float32, device=dev)
             L["dve"] = (torch.empty(g["ve"].shape, dtype=torch.float32, device=dev) if ve else None)
             L["ex"] = self.rope
             if self.learned_gate and ve:
@@ -272,8 +288,8 @@ class Stack:
                 L["ex"] = swa.make_extras(rope=self.rope_t, gate_x=L["gx"], gate_w=L["gw"],
                                           d_gate_w=L["dgw"], d_gate_x=L["dgx"])
             self.layers.append(L)
-        self.flops_fwd = sum(flops(Bn, Tn, hq, D, W)[0] for W, _ in self.sched)
-        self.flops_bwd = sum(flops(Bn, Tn, hq, D, W)[1] for W, _ in self.sched)
+        self.flops_fwd = sum(flops(Bn, Tn, hq, d, W)[0] for W, _ in self.sched)
+        self.flops_bwd = sum(flops(Bn, Tn, hq, d, W)[1] for W, _ in self.sched)
 
     def layer_gb(self):
         """Device bytes of one layer's tensors (inputs, outputs, gradients,
@@ -507,15 +523,25 @@ def run_ours(args, rank, world, dev):
             with torch.cuda.graph(graph):
                 stack.step()
             graph.replay()
+        # inputs smaller than L2: a 256 MB write before each step, outside
+        # the events, and the steps timed one by one
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if stack.small else None
+        per_step = []
         torch.cuda.synchronize()
         _barrier(world)
         t0 = clocks.mark()
         start.record()
-        for _ in range(args.steps):
+        for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(i & 255)
+                per_step.append(_ev_pair())
+                per_step[-1][0].record()
             if graph is not None:
                 graph.replay()
             else:
                 stack.step(ev)
+            if flush is not None:
+                per_step[-1][1].record()
         stop.record()
         torch.cuda.synchronize()
         t1 = clocks.mark()
@@ -529,7 +555,8 @@ def run_ours(args, rank, world, dev):
         st = swa.swa_attn_check_status(L["ws"])
         if st != swa.SWA_OK:
             raise swa.SwaError(st, "device status after the timed steps")
-    ms_total = start.elapsed_time(stop)
+    ms_total = (sum(a.elapsed_time(b) for a, b in per_step) if per_step
+                else start.elapsed_time(stop))
     ms = _max_over_ranks(ms_total, world) / args.steps
     stage_ms = {k: sum(a.elapsed_time(b) for a, b in v) / args.steps for k, v in ev.items()}
     flops_step = stack.flops_fwd + stack.flops_bwd
@@ -548,10 +575,13 @@ def run_ours(args, rank, world, dev):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q/k/v/dO, gains 1+0.1N, VE N(0,0.02), tokens U[0,8192))",
         "config": {"workload": WORKLOADS[args.workload], "global_batch": stack.B * world,
+                   "head_dim": stack.d,
                    "seq_len": stack.T,
                    "parallelism": f"replicas over batch x{world}" if world > 1 else "single GPU",
-                   "l2": f"inputs larger than L2: {n_layer} layer(s) x {stack.layer_gb():.1f} GB of "
-                         "tensors per step",
+                   "l2": (f"inputs larger than L2: {n_layer} layer(s) x {stack.layer_gb():.1f} GB of "
+                          "tensors per step" if flush is None else
+                          "inputs smaller than L2: L2 flushed by a 256 MB write before every "
+                          "timed step, steps timed one by one with CUDA events"),
                    "flops_per_step": flops_step,
                    "pct_of_peak": round(100 * value / world / peak, 2),
                    "peak_tflops": peak, "peak_source": f"{peak_kind} bf16_tflops_sustained",
@@ -560,7 +590,9 @@ def run_ours(args, rank, world, dev):
                    "stage_ms_per_step": {k: round(v, 4) for k, v in stage_ms.items()},
                    "stage_split": "CUDA events around each stage of eager steps",
                    "fwd_tflops": round(fwd_launch_tflops, 1)},
-        "roofline": {"kernel": "bwd_tc128_kernel (backward main, d=128; one launch per layer)",
+        "roofline": {"kernel": ("bwd_tc128_kernel (backward main, d=128; one launch per layer)"
+                                if stack.d == 128 else
+                                "bwd_tc_kernel<64> (backward main, d=64; one launch per layer)"),
                      "bound": "tensor",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),

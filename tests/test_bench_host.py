@@ -52,3 +52,11 @@ def test_block_projection_flops_match_the_gemms_the_block_runs():
              (nq, C, rows), (nkv, C, rows), (nkv, C, rows),                    # dwq, dwk, dwv
              (rows, C, nq), (rows, C, nkv), (rows, C, nkv)]                    # dxn
     assert bench.block_gemm_flops(rows, C, nq, nkv) == sum(2 * m * n * k for m, n, k in gemms)
+
+
+def test_tiny_workload_shape_schedule_and_flops():
+    assert bench.shape_for("tiny") == (1, 256, 2, 1)
+    assert bench.head_dim_for("tiny") == (64, None)
+    assert bench.schedule_for("tiny", oracle.sssl_window, oracle.has_ve) == [(128, False)]
+    fwd, bwd = bench.flops(1, 256, 2, 64, 128)
+    assert (fwd, bwd) == (12_681_216, 31_703_040)

@@ -265,6 +265,8 @@ swa_status swa_attn_fwd_noalloc(const swa_params* p, const void* q, const void* 
  * Extras: rotary tables and gate_w / gate_ch / d_gate_w as for the _ex
  * calls; gate_x and d_gate_x must be NULL (the block supplies the gate's
  * input and adds the gradient of the channels it read into dx); gate_ch <= C.
+ * As in the attention calls, the gate applies on value-embedding calls only
+ * (ve != NULL); without a VE table it is ignored and d_gate_w is not written.
  * The projections run on cuBLASLt, opened at run time (dlopen of
  * libcublasLt.so.13): where it cannot be opened the block calls return
  * SWA_ERR_UNSUPPORTED. Its handle is created on the first block call made

@@ -621,7 +621,8 @@ swa_status block_bwd_impl(const swa_params* p, const swa_extras* ex, const swa_b
     g.beta = i == 0 ? 0.f : 1.f; g.D = dxn; g.dt = CUDA_R_32F; g.ldd = C;
     if ((s = blk::gemm(g, lt, blk::kLtWsBytes, b.st)) != SWA_OK) return s;
   }
-  const bool gate = b.exp != nullptr && b.ex.gate_w != nullptr;
+  // the gate applies on value-embedding calls only (as in the attention calls)
+  const bool gate = b.exp != nullptr && b.ex.gate_w != nullptr && ve != nullptr;
   blk::prenorm_bwd_kernel<<<blk::prenorm_grid(b.rows), blk::kPnWarps * 32, 0, b.st>>>(
       static_cast<const elem_t*>(x), reinterpret_cast<const float*>(ws + b.L.rstd), dxn,
       gate ? reinterpret_cast<const float*>(ws + b.L.dgx) : nullptr, gate ? b.ex.gate_ch : 0,

@@ -136,3 +136,16 @@ def test_block_full_size_s_layer():
     assert got["status"] == swa.SWA_OK
     ref = run_block_oracle(p, x, rope=True)
     compare_block(got, ref, x, TOL["bf16"], ALL)
+
+
+@pytest.mark.parametrize("kind", ["bf16", "fp32"])
+def test_block_ignores_the_gate_without_a_value_embedding(kind):
+    """gate_w given on a layer without a VE table: the gate does not apply (as
+    in the attention calls), so the block equals the block without a gate."""
+    p, C, _, rope = CASES["mha_full_causal_d128"]
+    x = make_block_inputs(p, C, layer=2, dtype=DTYPE[kind], gate_ch=16)
+    got = run_block_library(p, C, x, rope)
+    assert got["status"] == swa.SWA_OK
+    ref = run_block_oracle(p, dict(x, gate_w=None), rope)
+    keys = tuple(k for k in ALL if k != "dgate_w")
+    compare_block(got, ref, x, TOL[kind], keys)

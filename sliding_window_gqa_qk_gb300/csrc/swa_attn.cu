@@ -489,7 +489,8 @@ struct BlockCall {
 };
 
 swa_status block_begin(BlockCall& b, const swa_params* p, const swa_extras* ex, const swa_block_weights* w,
-                       const void* x, void* workspace, size_t ws_bytes, bool bwd, void* stream) {
+                       const void* x, const void* ve, const int32_t* tok, void* workspace, size_t ws_bytes,
+                       bool bwd, void* stream) {
   swa_status s = check_params(p);
   if (s != SWA_OK) return s;
   if (w == nullptr || x == nullptr || !aligned(x, 16)) return SWA_ERR_INVALID_ARG;
@@ -518,6 +519,12 @@ swa_status block_begin(BlockCall& b, const swa_params* p, const swa_extras* ex, 
     }
     b.exp = &b.ex;
   }
+  // Everything the attention calls check, checked here before the first
+  // launch, so that a non-OK return launched nothing.
+  Call c;
+  c.p = *p;
+  if ((s = set_extras(c, b.exp, nullptr)) != SWA_OK) return s;
+  if (ve != nullptr && (!aligned(ve, 16) || tok == nullptr || p->vocab < 1)) return SWA_ERR_INVALID_ARG;
   return SWA_OK;
 }
 
@@ -525,7 +532,7 @@ swa_status block_fwd_impl(const swa_params* p, const swa_extras* ex, const swa_b
                           const void* x, const float* gq, const float* gk, const void* ve,
                           const int32_t* tok, void* out, void* workspace, size_t ws_bytes, void* stream) {
   BlockCall b;
-  swa_status s = block_begin(b, p, ex, w, x, workspace, ws_bytes, false, stream);
+  swa_status s = block_begin(b, p, ex, w, x, ve, tok, workspace, ws_bytes, false, stream);
   if (s != SWA_OK) return s;
   if (!tensor_ok(out)) return SWA_ERR_INVALID_ARG;
   if (b.rows == 0) return SWA_OK;
@@ -564,7 +571,7 @@ swa_status block_bwd_impl(const swa_params* p, const swa_extras* ex, const swa_b
                           float* dwv, float* dwo, float* dgq, float* dgk, float* dve, void* workspace,
                           size_t ws_bytes, void* stream) {
   BlockCall b;
-  swa_status s = block_begin(b, p, ex, w, x, workspace, ws_bytes, true, stream);
+  swa_status s = block_begin(b, p, ex, w, x, ve, tok, workspace, ws_bytes, true, stream);
   if (s != SWA_OK) return s;
   if (!tensor_ok(dout) || !tensor_ok(dx)) return SWA_ERR_INVALID_ARG;
   uint8_t* ws = b.ws;

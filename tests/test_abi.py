@@ -256,19 +256,21 @@ def block_weights(C=512, wq=A, wk=A, wv=A, wo=A):
     return swa.swa_block_weights(C, wq, wk, wv, wo)
 
 
-def block_fwd_call(p, w, ex=None, kind="bf16", ws_bytes=1 << 40, x=A, out=A, ws=A):
+def block_fwd_call(p, w, ex=None, kind="bf16", ws_bytes=1 << 40, x=A, out=A, ws=A, ve=None,
+                   tok=None):
     lib = swa.load(kind)
     ep = None if ex is None else ctypes.byref(ex)
     wp = None if w is None else ctypes.byref(w)
-    return lib.swa_block_fwd(ctypes.byref(p), ep, wp, x, None, None, None, None, out, ws, ws_bytes,
+    return lib.swa_block_fwd(ctypes.byref(p), ep, wp, x, None, None, ve, tok, out, ws, ws_bytes,
                              None)
 
 
-def block_bwd_call(p, w, ex=None, kind="bf16", ws_bytes=1 << 40, x=A, dout=A, dx=A, ws=A):
+def block_bwd_call(p, w, ex=None, kind="bf16", ws_bytes=1 << 40, x=A, dout=A, dx=A, ws=A, ve=None,
+                   tok=None):
     lib = swa.load(kind)
     ep = None if ex is None else ctypes.byref(ex)
     wp = None if w is None else ctypes.byref(w)
-    return lib.swa_block_bwd(ctypes.byref(p), ep, wp, x, None, None, None, None, dout, dx, None,
+    return lib.swa_block_bwd(ctypes.byref(p), ep, wp, x, None, None, ve, tok, dout, dx, None,
                              None, None, None, None, None, None, ws, ws_bytes, None)
 
 
@@ -306,6 +308,17 @@ def test_block_calls_reject_bad_arguments(kind):
                     kind=kind) == swa.SWA_ERR_INVALID_ARG
         assert call(p, block_weights(C=16), extras(gate_w=A, gate_ch=32), kind=kind) == \
             swa.SWA_ERR_INVALID_ARG
+    # the attention's own argument checks run before the block launches anything
+    for call in (block_fwd_call, block_bwd_call):
+        assert call(params(T=64), block_weights(), extras(rope_cos=A, rope_sin=A, rope_rows=63),
+                    kind=kind) == swa.SWA_ERR_INVALID_ARG
+        assert call(params(T=64), block_weights(), extras(rope_cos=A, rope_rows=64),
+                    kind=kind) == swa.SWA_ERR_INVALID_ARG
+        assert call(params(vocab=8), block_weights(), kind=kind, ve=A) == swa.SWA_ERR_INVALID_ARG
+        assert call(params(vocab=0), block_weights(), kind=kind, ve=A, tok=A) == \
+            swa.SWA_ERR_INVALID_ARG
+        assert call(params(Hq=66, Hkv=33), block_weights(), extras(gate_w=A, gate_ch=8),
+                    kind=kind) == swa.SWA_ERR_INVALID_ARG
     assert block_fwd_call(p, block_weights(), kind=kind, out=None) == swa.SWA_ERR_INVALID_ARG
     assert block_bwd_call(p, block_weights(), kind=kind, dx=MIS) == swa.SWA_ERR_INVALID_ARG
     assert block_bwd_call(p, block_weights(), extras(d_gate_x=A), kind=kind) == swa.SWA_ERR_INVALID_ARG

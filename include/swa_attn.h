@@ -39,8 +39,12 @@
  *       ve_gate            [B, T, Hkv]      fp32
  *   - Tensor pointers must be 16-byte aligned; the workspace 256-byte aligned.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
- *     stream). A status other than SWA_OK returned by the host call means that
- *     nothing was launched. Errors found on the device (a bounded wait that ran
+ *     stream). SWA_ERR_INVALID_ARG, SWA_ERR_WORKSPACE and the unsupported-
+ *     size checks come before the first launch: nothing was launched. A
+ *     failing CUDA or cuBLASLt call inside a call (SWA_ERR_CUDA, or
+ *     SWA_ERR_UNSUPPORTED when cuBLASLt has no algorithm for a projection)
+ *     can come after earlier launches of that call; its outputs are then
+ *     undefined. Errors found on the device (a bounded wait that ran
  *     out, a token id outside [0, vocab)) are OR-ed into a status word in the
  *     workspace header and read back by swa_attn_check_status().
  *   - B == 0 or T == 0 is a valid empty problem: nothing is computed; the

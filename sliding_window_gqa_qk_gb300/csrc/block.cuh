@@ -200,6 +200,16 @@ struct Gemm {
   int ldd = 0;
 };
 
+// Largest power of two (at most 256) that divides the address: cuBLASLt's
+// algorithm choice assumes 256-byte aligned operands unless told otherwise,
+// and callers' tensors need only be 16-byte aligned.
+inline uint32_t ptr_alignment(const void* p) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  uint32_t al = 256;
+  while (al > 1 && (a & (al - 1)) != 0) al >>= 1;
+  return al;
+}
+
 inline swa_status gemm(const Gemm& g, void* lt_ws, size_t lt_ws_bytes, cudaStream_t st) {
   if (g.m == 0 || g.n == 0) return SWA_OK;
   cublasLtHandle_t h = nullptr;
@@ -213,6 +223,16 @@ inline swa_status gemm(const Gemm& g, void* lt_ws, size_t lt_ws_bytes, cudaStrea
   const cublasOperation_t opa = g.ta ? CUBLAS_OP_T : CUBLAS_OP_N;
   const cublasOperation_t opb = g.tb ? CUBLAS_OP_T : CUBLAS_OP_N;
   const uint64_t wsb = lt_ws_bytes;
+  const void* cptr = g.C != nullptr ? g.C : g.D;
+  const uint32_t al[4] = {ptr_alignment(g.A), ptr_alignment(g.B), ptr_alignment(cptr), ptr_alignment(g.D)};
+  const cublasLtMatmulPreferenceAttributes_t al_attr[4] = {
+      CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_A_BYTES, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_B_BYTES,
+      CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_C_BYTES, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_D_BYTES};
+  auto set_alignments = [&]() {
+    for (int i = 0; i < 4; ++i)
+      if (L.pref_set(pref, al_attr[i], &al[i], sizeof(al[i])) != CUBLAS_STATUS_SUCCESS) return false;
+    return true;
+  };
   cublasLtMatmulHeuristicResult_t res{};
   int found = 0;
   const float alpha = 1.f;
@@ -224,11 +244,12 @@ inline swa_status gemm(const Gemm& g, void* lt_ws, size_t lt_ws_bytes, cudaStrea
       L.layout_create(&lc, g.dt, g.m, g.n, g.ldd) == CUBLAS_STATUS_SUCCESS &&
       L.pref_create(&pref) == CUBLAS_STATUS_SUCCESS &&
       L.pref_set(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &wsb, sizeof(wsb)) ==
-          CUBLAS_STATUS_SUCCESS) {
+          CUBLAS_STATUS_SUCCESS &&
+      set_alignments()) {
     if (L.heuristic(h, desc, la, lb, lc, lc, pref, 1, &res, &found) != CUBLAS_STATUS_SUCCESS || found < 1) {
       s = SWA_ERR_UNSUPPORTED;
-    } else if (L.matmul(h, desc, &alpha, g.A, la, g.B, lb, &g.beta, g.C != nullptr ? g.C : g.D, lc, g.D,
-                        lc, &res.algo, lt_ws, lt_ws_bytes, st) == CUBLAS_STATUS_SUCCESS) {
+    } else if (L.matmul(h, desc, &alpha, g.A, la, g.B, lb, &g.beta, cptr, lc, g.D, lc, &res.algo, lt_ws,
+                        lt_ws_bytes, st) == CUBLAS_STATUS_SUCCESS) {
       s = SWA_OK;
     }
   }

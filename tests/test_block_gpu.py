@@ -28,9 +28,21 @@ CASES = {
 }
 
 
-def run_block_library(p, C, x, rope=False):
+def offset_copy(t, dev, elems):
+    """A contiguous device copy of t that starts `elems` elements into a
+    larger buffer (a tensor that is 16-byte but not 256-byte aligned)."""
+    flat = torch.empty(t.numel() + elems, dtype=t.dtype, device=dev)
+    view = flat[elems:].view(t.shape)
+    view.copy_(t)
+    return view
+
+
+def run_block_library(p, C, x, rope=False, offset=None):
     dev = torch.device("cuda:0")
     g = {k: (t.to(dev).contiguous() if t is not None else None) for k, t in x.items()}
+    if offset is not None:
+        for k in ("x", "dout", "wo"):
+            g[k] = offset_copy(x[k], dev, offset)
     kind = "fp32" if x["x"].dtype == torch.float32 else "bf16"
     prm = swa.make_params(p.B, p.T, p.Hq, p.Hkv, p.d, p.window, p.causal, 0.0, p.eps, p.ve_scale,
                           p.vocab if p.ve else 0)
@@ -44,10 +56,10 @@ def run_block_library(p, C, x, rope=False):
     assert n > 0
     ws = torch.empty(n, dtype=torch.uint8, device=dev)
     assert swa.swa_attn_workspace_init(ws, n, kind=kind) == swa.SWA_OK
-    out = torch.empty_like(g["x"])
+    out = torch.empty_like(g["x"]) if offset is None else offset_copy(torch.zeros_like(x["x"]), dev, offset)
     assert swa.swa_block_fwd(prm, ex, w, g["x"], g["gq"], g["gk"], g["ve"], g["tok"], out, ws) == swa.SWA_OK
     f32 = dict(dtype=torch.float32, device=dev)
-    dx = torch.empty_like(g["x"])
+    dx = torch.empty_like(g["x"]) if offset is None else offset_copy(torch.zeros_like(x["x"]), dev, offset)
     dwq, dwk, dwv, dwo = (torch.empty(g[k].shape, **f32) for k in ("wq", "wk", "wv", "wo"))
     dgq = torch.empty(p.d, **f32) if g["gq"] is not None else None
     dgk = torch.empty(p.d, **f32) if g["gk"] is not None else None
@@ -149,3 +161,15 @@ def test_block_ignores_the_gate_without_a_value_embedding(kind):
     ref = run_block_oracle(p, dict(x, gate_w=None), rope)
     keys = tuple(k for k in ALL if k != "dgate_w")
     compare_block(got, ref, x, TOL[kind], keys)
+
+
+@pytest.mark.parametrize("kind", ["bf16", "fp32"])
+def test_block_with_16_byte_aligned_tensors(kind):
+    """x, dout, out, dx and wo start 16 bytes past a 256-byte boundary (the
+    library asks for 16-byte alignment only)."""
+    p, C, gate_ch, rope = CASES["gqa_ve_gate_rope_d64"]
+    x = make_block_inputs(p, C, layer=3, dtype=DTYPE[kind], gate_ch=gate_ch)
+    elems = 16 // (2 if kind == "bf16" else 4)
+    got = run_block_library(p, C, x, rope, offset=elems)
+    assert got["status"] == swa.SWA_OK
+    compare_block(got, run_block_oracle(p, x, rope), x, TOL[kind], ALL)

@@ -60,3 +60,17 @@ def test_tiny_workload_shape_schedule_and_flops():
     assert bench.schedule_for("tiny", oracle.sssl_window, oracle.has_ve) == [(128, False)]
     fwd, bwd = bench.flops(1, 256, 2, 64, 128)
     assert (fwd, bwd) == (12_681_216, 31_703_040)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """bench.py --impl reference: the oracle timed on the host cores on a
+    bounded sample, one JSON object with the keys the driver reads."""
+    import argparse
+    args = argparse.Namespace(steps=1, warmup=1, gpus=1, impl="reference", workload="stack")
+    out = bench.run_reference(args, 0, 1)
+    assert out["impl"] == "reference" and out["metric"] == bench.METRIC
+    assert out["unit"] == "TFLOP/s" and out["higher_is_better"] is True and out["value"] > 0
+    assert out["cpu_baseline"]["kind"] == "oracle" and out["cpu_baseline"]["cores"] >= 1
+    assert out["cpu_baseline"]["value"] == out["value"]
+    assert out["e2e"] == {"value": out["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0}

@@ -152,3 +152,38 @@ def test_block_against_float64_torch_autograd():
     for name, gname in pairs.items():
         np.testing.assert_allclose(t[name].grad.numpy(), g[gname], rtol=1e-10, atol=1e-12,
                                    err_msg=name)
+
+
+def test_grouped_query_block_equals_the_block_with_repeated_kv_projections():
+    """GQA inside the block: query head h reads kv head h // G, so the block
+    with Hkv kv heads equals the block with one kv head per query head whose
+    k / v projection rows, VE-table columns and gate rows are the group's,
+    repeated; the gradients of the shared rows are the sums over the group."""
+    B, T, C, Hq, Hkv, d, G = 1, 7, 12, 4, 2, 4, 2
+    x, _ = block_problem(106, B=B, T=T, C=C, Hq=Hq, Hkv=Hkv, d=d, vocab=6, gate_ch=3)
+    kw = dict(window=3, causal=True, eps=1e-5, ve_scale=0.6)
+
+    def rep_rows(w):       # [Hkv*d, ...] -> [Hq*d, ...], kv head h // G for query head h
+        return np.concatenate([w[(h // G) * d:(h // G + 1) * d] for h in range(Hq)], axis=0)
+
+    mha = dict(x)
+    mha["wk"], mha["wv"] = rep_rows(x["wk"]), rep_rows(x["wv"])
+    mha["ve"] = rep_rows(x["ve"].T).T
+    mha["gate_w"] = np.repeat(x["gate_w"], G, axis=0)
+    out_g = run_fwd(x, dict(Hq=Hq, Hkv=Hkv), **kw)
+    out_m = run_fwd(mha, dict(Hq=Hq, Hkv=Hq), **kw)
+    np.testing.assert_allclose(out_g, out_m, rtol=1e-12, atol=1e-12)
+    g_g = run_bwd(x, dict(Hq=Hq, Hkv=Hkv), **kw)
+    g_m = run_bwd(mha, dict(Hq=Hq, Hkv=Hq), **kw)
+    for name in ("dx", "dwq", "dwo", "dgq", "dgk"):
+        np.testing.assert_allclose(g_g[name], g_m[name], rtol=1e-10, atol=1e-12, err_msg=name)
+
+    def group_sum(dw):     # [Hq*d, ...] -> [Hkv*d, ...]
+        return np.concatenate([sum(dw[h * d:(h + 1) * d] for h in range(k * G, (k + 1) * G))
+                               for k in range(Hkv)], axis=0)
+
+    for name in ("dwk", "dwv"):
+        np.testing.assert_allclose(g_g[name], group_sum(g_m[name]), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g_g["dve"], group_sum(g_m["dve"].T).T, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g_g["dgate_w"], g_m["dgate_w"].reshape(Hkv, G, -1).sum(axis=1),
+                               rtol=1e-10, atol=1e-12)

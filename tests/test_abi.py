@@ -335,3 +335,17 @@ def test_empty_block_forward_is_a_no_op(kind):
     assert block_fwd_call(params(T=0), block_weights(), kind=kind) == swa.SWA_OK
     # nothing to zero when every gradient output is NULL
     assert block_bwd_call(params(B=0), block_weights(), kind=kind) == swa.SWA_OK
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the compiled library the binding raises: there is no fallback
+    path that would compute anything elsewhere."""
+    import torch
+    monkeypatch.setattr(swa, "_LIBS", {})
+    monkeypatch.setattr(swa._build, "lib_path", lambda kind: str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        swa.load("bf16")
+    q = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)
+    with pytest.raises(RuntimeError, match="not built"):
+        swa.attention_forward(q, k, k, window=4)

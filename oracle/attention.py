@@ -58,6 +58,7 @@ __all__ = [
     "rotary_backward",
     "rms_norm",
     "rms_norm_backward",
+    "rms_norm_backward_scale",
     "ve_mix",
     "learned_gate",
     "band_mask",
@@ -175,6 +176,21 @@ def rms_norm_backward(x: np.ndarray, g, eps: float, dy: np.ndarray):
     if g is not None:
         dg = (dy * xh).reshape(-1, x.shape[-1]).sum(axis=0)
     return dx, dg
+
+
+def rms_norm_backward_scale(x: np.ndarray, g, eps: float, dy: np.ndarray) -> np.ndarray:
+    """Row norms of r * (g * dy): the gradient of ``rms_norm_backward`` before
+    its last step removes the component along xh (dx = r * (dxh - xh *
+    mean(dxh * xh)) with dxh = g * dy, and that step is an orthogonal
+    projection, so |dx_row| <= this norm, with equality when dxh is
+    orthogonal to xh). Returns an array of shape x.shape[:-1]. It is the
+    scale of a row of dx that carries errors of dy through the projection:
+    where most of dxh lies along xh, dx is small and the error is not."""
+    x = np.asarray(x, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    _, r = rms_norm(x, None, eps)
+    dxh = dy if g is None else dy * np.asarray(g, dtype=np.float64)
+    return r * np.linalg.norm(dxh, axis=-1)
 
 
 def ve_mix(v: np.ndarray, ve, tok, gate, ve_scale: float) -> np.ndarray:
@@ -348,7 +364,8 @@ def attention_forward_rows(q, k, v, gq=None, gk=None, *, b: int, h: int, rows,
 def attention_backward(q, k, v, gq=None, gk=None, dO=None, *, window: int,
                        causal: bool = True, scale=None, eps: float = 1e-6, ve=None,
                        tok=None, gate=None, ve_scale: float = 0.5,
-                       row_chunk: int = 1024, rope=None, gate_x=None, gate_w=None):
+                       row_chunk: int = 1024, rope=None, gate_x=None, gate_w=None,
+                       scales: bool = False):
     """Analytic backward of ``attention_forward`` for the loss <O, dO>.
 
     Per (b, h), with A the masked softmax and kv head hk = h // G:
@@ -367,7 +384,8 @@ def attention_backward(q, k, v, gq=None, gk=None, dO=None, *, window: int,
 
     Returns a dict with dq, dk, dv, dgq, dgk (None when the gain is None),
     dve ([vocab, Hkv*d], None without VE) and, with the learned gate,
-    dgate_x and dgate_w.
+    dgate_x and dgate_w. With ``scales``, also dq_scale [B, T, Hq] and
+    dk_scale [B, T, Hkv]: ``rms_norm_backward_scale`` of each row of dq and dk.
     """
     q = np.asarray(q, dtype=np.float64)
     dO = np.asarray(dO, dtype=np.float64)
@@ -394,8 +412,9 @@ def attention_backward(q, k, v, gq=None, gk=None, dO=None, *, window: int,
                 dqn[b, rows, h, :] += sc * (dS @ kn[b, :, hk, :])
                 dkn[b, :, hk, :] += sc * (dS.T @ qn[b, rows, h, :])
                 dveff[b, :, hk, :] += A.T @ dOr
-    dq, dgq = rms_norm_backward(_rot(q, rope), gq, eps, dqn)
-    dk, dgk = rms_norm_backward(_rot(np.asarray(k, dtype=np.float64), rope), gk, eps, dkn)
+    qr, kr = _rot(q, rope), _rot(np.asarray(k, dtype=np.float64), rope)
+    dq, dgq = rms_norm_backward(qr, gq, eps, dqn)
+    dk, dgk = rms_norm_backward(kr, gk, eps, dkn)
     dq, dk = _unrot(dq, rope), _unrot(dk, rope)
     dve = None
     if ve is not None:
@@ -405,6 +424,9 @@ def attention_backward(q, k, v, gq=None, gk=None, dO=None, *, window: int,
         dve = np.zeros((np.asarray(ve).shape[0], Hd))
         np.add.at(dve, np.asarray(tok, dtype=np.int64).reshape(-1), contrib)
     out = {"dq": dq, "dk": dk, "dv": dveff, "dgq": dgq, "dgk": dgk, "dve": dve}
+    if scales:
+        out["dq_scale"] = rms_norm_backward_scale(qr, gq, eps, dqn)
+        out["dk_scale"] = rms_norm_backward_scale(kr, gk, eps, dkn)
     if gate_w is not None:
         rows = np.asarray(ve, dtype=np.float64).reshape(-1, Hkv, d)[np.asarray(tok, dtype=np.int64)]
         dgate = ve_scale * np.sum(dveff * rows, axis=-1)          # [B, T, Hkv]
@@ -422,13 +444,15 @@ def _one_batch(q, k, v, dO, tok, gate, b):
 
 def attention_backward_rows(q, k, v, gq=None, gk=None, dO=None, *, b: int, h: int, rows,
                             window: int, causal: bool = True, scale=None, eps: float = 1e-6,
-                            ve=None, tok=None, gate=None, ve_scale: float = 0.5, rope=None):
+                            ve=None, tok=None, gate=None, ve_scale: float = 0.5, rope=None,
+                            with_scale: bool = False):
     """dq of ``attention_backward`` at the query rows ``rows`` of one (b, h).
 
     Row i of dq depends only on row i of the softmax: dA_i = dO_i v_eff^T,
     dS_i = A_i * (dA_i - <dA_i, A_i>), dqn_i = scale * dS_i kn, then the
-    RMSNorm backward of that row. Returns dq [len(rows), d]. Used to sample
-    the gradient of full-size problems one row at a time.
+    RMSNorm backward of that row. Returns dq [len(rows), d] (and, with
+    ``with_scale``, its rows' ``rms_norm_backward_scale``). Used to sample the
+    gradient of full-size problems one row at a time.
     """
     q, k, v, dO, tk, gt = _one_batch(q, k, v, dO, tok, gate, b)
     T, d = q.shape[1], q.shape[3]
@@ -443,14 +467,16 @@ def attention_backward_rows(q, k, v, gq=None, gk=None, dO=None, *, b: int, h: in
     A, _ = _softmax_rows(sc * (qn @ kn.T), band_mask(rows, T, window, causal))
     dA = dO[0, rows, h, :] @ v_eff.T
     dS = A * (dA - np.sum(dA * A, axis=1, keepdims=True))
-    dq, _ = rms_norm_backward(qr, gq, eps, sc * (dS @ kn))
-    return _unrot(dq[:, None, :], rope, rows)[:, 0, :]
+    dqn = sc * (dS @ kn)
+    dq, _ = rms_norm_backward(qr, gq, eps, dqn)
+    dq = _unrot(dq[:, None, :], rope, rows)[:, 0, :]
+    return (dq, rms_norm_backward_scale(qr, gq, eps, dqn)) if with_scale else dq
 
 
 def attention_backward_cols(q, k, v, gq=None, gk=None, dO=None, *, b: int, hk: int, cols,
                             window: int, causal: bool = True, scale=None, eps: float = 1e-6,
                             ve=None, tok=None, gate=None, ve_scale: float = 0.5,
-                            row_chunk: int = 512, rope=None):
+                            row_chunk: int = 512, rope=None, with_scale: bool = False):
     """dk and dv of ``attention_backward`` at the key positions ``cols`` of one
     (b, kv head hk).
 
@@ -459,7 +485,8 @@ def attention_backward_cols(q, k, v, gq=None, gk=None, dO=None, *, b: int, hk: i
     the full rows of the softmax and its backward (a row must be seen whole
     to be normalised). Only rows whose band holds one of ``cols`` are
     visited; the others add exact zeros. Then the RMSNorm backward of the k
-    rows. Returns (dk [len(cols), d], dv [len(cols), d]).
+    rows. Returns (dk [len(cols), d], dv [len(cols), d]), and with
+    ``with_scale`` the dk rows' ``rms_norm_backward_scale`` third.
     """
     q, k, v, dO, tk, gt = _one_batch(q, k, v, dO, tok, gate, b)
     T, Hq, d = q.shape[1], q.shape[2], q.shape[3]
@@ -487,4 +514,7 @@ def attention_backward_cols(q, k, v, gq=None, gk=None, dO=None, *, b: int, hk: i
             dv += A[:, cols].T @ dOr
             dkn += sc * (dS[:, cols].T @ qn)
     dk, _ = rms_norm_backward(kr[cols], gk, eps, dkn)
-    return _unrot(dk[:, None, :], rope, cols)[:, 0, :], dv
+    dk = _unrot(dk[:, None, :], rope, cols)[:, 0, :]
+    if with_scale:
+        return dk, dv, rms_norm_backward_scale(kr[cols], gk, eps, dkn)
+    return dk, dv

@@ -1,6 +1,8 @@
 """Shared helpers of the GPU parity tests: run the library through its C ABI
 and the float64 oracle on the same seeded inputs, and compare."""
 
+import os
+
 import numpy as np
 import torch
 
@@ -90,7 +92,7 @@ def run_oracle(p, x, b_slice=None, rope=None, learned=None):
         kw["gate_x"] = as_f64(learned[0])[..., :C]
         kw["gate_w"] = learned[1].double().numpy()
     o, lse = oracle.attention_forward(q, k, v, f["gq"], f["gk"], **kw)
-    ref = oracle.attention_backward(q, k, v, f["gq"], f["gk"], dO, **kw)
+    ref = oracle.attention_backward(q, k, v, f["gq"], f["gk"], dO, scales=True, **kw)
     ref["o"], ref["lse"] = o, lse
     return ref
 
@@ -104,27 +106,132 @@ def rel_err(a, r):
     return float(np.linalg.norm(a - r) / den) if den > 0 else float(np.linalg.norm(a))
 
 
+# Keys compared element by element (every element its own "row"); the others
+# row by row along their last axis (a head row of d channels, a VE-table row).
+ELEMENTWISE = ("lse", "dgq", "dgk")
+# Floor of a row's reference norm in the per-row bound, as a multiple of the
+# root mean square of all rows' reference norms. The library's rounding
+# errors in a row are absolute, at the scale of a typical row, not relative
+# to the row's own size. Rows that see only a few keys show it most: there
+# dS = P (dP - D) is a difference of nearly equal numbers of size |dO| |v|
+# formed from bf16 operands (on value-embedding layers v_eff itself is
+# rounded to bf16), so a row whose exact gradient is small keeps an error of
+# 2-3 % of a typical row (measured worst: 2.9 %, the second query row of a
+# value-embedding layer; 1.9 % on layers without value embeddings); the fp32
+# build shows the same at its own precision. So every row is held to tol
+# times the larger of its own norm and twice the rows' root mean square norm:
+# relative for rows of twice the typical size and above, absolute below. A
+# wrong row, or a wrong element of lse or of the gain gradients, is off by
+# about its own size and exceeds the bound many times over.
+ROW_FLOOR = 2.0
+FLOOR = {}
+# (test, tensor, Frobenius error, worst row error, max abs error) of every
+# comparison of this session, printed at its end by conftest.py.
+REPORT = []
+
+
+def _rows(x, elementwise):
+    return x.reshape(-1, 1) if (elementwise or x.ndim < 2) else x.reshape(-1, x.shape[-1])
+
+
+def errors(a, r, elementwise=False, zero_ref_scale=None, floor=ROW_FLOOR, row_scale=None):
+    """Errors of the library's tensor a against the oracle's r (same shape):
+      frob   ||a - r|| / ||r|| over the whole tensor;
+      row    max over rows of ||a_row - r_row|| / max(||r_row||, floor * rms_row),
+             rms_row the root mean square of the reference rows' norms (rows =
+             last axis, or single elements when ``elementwise``);
+      maxabs max |a - r| over all elements.
+    ``row_scale`` (one value per row, e.g. the oracle's
+    rms_norm_backward_scale of a dq or dk row) raises a row's reference norm
+    to the natural scale of its errors where that is larger.
+    Where r is exactly zero (a degenerate case of the method) the scale comes
+    from another tensor: ``zero_ref_scale`` = (its norm, the root mean square
+    of its rows' norms), giving frob = ||a|| / norm and row = max ||a_row|| /
+    rms."""
+    a = as_f64(a) if isinstance(a, torch.Tensor) else np.asarray(a, dtype=np.float64)
+    r = np.asarray(r, dtype=np.float64)
+    assert a.shape == r.shape, (a.shape, r.shape)
+    assert np.all(np.isfinite(a)), "non-finite values"
+    diff = a - r
+    maxabs = float(np.max(np.abs(diff))) if diff.size else 0.0
+    dn = np.linalg.norm(_rows(diff, elementwise), axis=1)
+    if zero_ref_scale is not None:
+        norm, rms = zero_ref_scale
+        frob = float(np.linalg.norm(diff) / norm)
+        row = float(np.max(dn) / rms) if dn.size else 0.0
+        return frob, row, maxabs
+    den = np.linalg.norm(r)
+    frob = float(np.linalg.norm(diff) / den) if den > 0 else float(np.linalg.norm(diff))
+    sn = np.linalg.norm(_rows(r, elementwise), axis=1)
+    rms = float(np.sqrt(np.mean(sn ** 2))) if sn.size else 0.0
+    if dn.size == 0:
+        row = 0.0
+    elif rms > 0:
+        den = np.maximum(sn, floor * rms)
+        if row_scale is not None:
+            den = np.maximum(den, np.asarray(row_scale, dtype=np.float64).reshape(-1))
+        row = float(np.max(dn / den))
+    else:
+        row = 0.0 if np.all(dn == 0) else float("inf")
+    return frob, row, maxabs
+
+
+def _record(key, frob, row, maxabs):
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    REPORT.append((test, key, frob, row, maxabs))
+
+
+def check(key, a, r, tol, row_scale=None):
+    """Asserts the Frobenius and the per-row (per-element for ELEMENTWISE keys)
+    bounds of ``errors`` at ``tol``; records the errors. Returns (frob, row,
+    maxabs)."""
+    e = errors(a, r, elementwise=key in ELEMENTWISE, floor=FLOOR.get(key, ROW_FLOOR),
+               row_scale=row_scale)
+    _record(key, *e)
+    frob, row, maxabs = e
+    assert frob <= tol and row <= tol, (
+        f"{key}: relative error {frob:.3e}, worst row {row:.3e} (tolerance {tol}), "
+        f"max abs error {maxabs:.3e}")
+    return e
+
+
 def compare(got, ref, tol, keys=("o", "lse", "dq", "dk", "dv", "dgq", "dgk", "dve", "dgate_x", "dgate_w"),
             sl=None):
-    """Relative error per tensor. Where the oracle's tensor is exactly zero (a
+    """Errors per tensor (``errors``), each bounded by ``tol`` both over the
+    whole tensor and row by row. Where the oracle's tensor is exactly zero (a
     degenerate case of the method, e.g. window 0 makes dS vanish, so dq, dk and
-    the gain gradients are 0), the error is measured against the norm of the
-    oracle's dv, the gradient the same terms are built from."""
+    the gain gradients are 0), the library's values are measured against the
+    oracle's dv, the gradient the same terms are built from: its norm for the
+    whole tensor, the root mean square of its row norms for each row. Rows of
+    dq and dk are the output of the QK-norm's backward, a projection that
+    removes the component of the gradient along the normed row: their scale
+    is at least the oracle's dq_scale / dk_scale (the row norm before that
+    projection), where the errors they carry come from."""
     errs = {}
+    bad = {}
     for k in keys:
         if ref.get(k) is None or got.get(k) is None:
             continue
         a = got[k]
         if sl is not None and k not in ("dgq", "dgk", "dve", "dgate_w"):
             a = a[sl]
+        zs = None
         if np.linalg.norm(ref[k]) == 0.0 and ref.get("dv") is not None:
-            a64 = as_f64(a)
-            assert np.all(np.isfinite(a64)), "non-finite values"
-            errs[k] = float(np.linalg.norm(a64) / np.linalg.norm(ref["dv"]))
-            continue
-        errs[k] = rel_err(a, ref[k])
-    bad = {k: e for k, e in errs.items() if not e <= tol}
-    assert not bad, f"relative errors above {tol}: {bad} (all: {errs})"
+            dv = np.asarray(ref["dv"], dtype=np.float64)
+            dvn = np.linalg.norm(_rows(dv, False), axis=1)
+            zs = (float(np.linalg.norm(dv)), float(np.sqrt(np.mean(dvn ** 2))))
+        rs = ref.get(k + "_scale") if k in ("dq", "dk") else None
+        if rs is not None and sl is not None:
+            rs = rs[sl]
+        e = errors(a, ref[k], elementwise=k in ELEMENTWISE, zero_ref_scale=zs,
+                   floor=FLOOR.get(k, ROW_FLOOR), row_scale=rs)
+        _record(k, *e)
+        errs[k] = e[0]
+        errs[k + "_row"] = e[1]
+        errs[k + "_maxabs"] = e[2]
+        if not (e[0] <= tol and e[1] <= tol):
+            bad[k] = e
+    assert not bad, f"errors above {tol} (frob, worst row, max abs): {bad} (all: {errs})"
     return errs
 
 

@@ -390,6 +390,41 @@ def test_rms_norm_backward_identities():
     np.testing.assert_allclose(dg, np.sum(dy * xh, axis=0), rtol=1e-13)
 
 
+def test_rms_norm_backward_scale_bounds_the_gradient_and_is_reached_orthogonally():
+    """The row scale of the RMSNorm backward: |dx_row| <= r |g * dy_row| (the
+    last step is an orthogonal projection), with equality when g * dy is
+    orthogonal to the normed row, and a ratio near zero when g * dy lies
+    along it (the cancellation the scale is for)."""
+    r = rng(41)
+    x = r.standard_normal((7, 12))
+    g = 1.0 + 0.3 * r.standard_normal(12)
+    eps = 0.05
+    dy = r.standard_normal((7, 12))
+    dx, _ = orc.rms_norm_backward(x, g, eps, dy)
+    sc = orc.rms_norm_backward_scale(x, g, eps, dy)
+    assert sc.shape == (7,)
+    assert np.all(np.linalg.norm(dx, axis=1) <= sc * (1 + 1e-12))
+    xh = x / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + eps)
+    # g * dy orthogonal to xh row by row: no cancellation, equality
+    w = r.standard_normal((7, 12))
+    w -= xh * (np.sum(w * xh, axis=1, keepdims=True) / np.sum(xh * xh, axis=1, keepdims=True))
+    dy_perp = w / g
+    dx, _ = orc.rms_norm_backward(x, g, eps, dy_perp)
+    np.testing.assert_allclose(np.linalg.norm(dx, axis=1), orc.rms_norm_backward_scale(x, g, eps, dy_perp),
+                               rtol=1e-12)
+    # g * dy along xh (eps = 0): dx vanishes while the scale does not
+    dy_par = 3.0 * xh / g
+    dx, _ = orc.rms_norm_backward(x, g, 0.0, dy_par)
+    assert np.max(np.linalg.norm(dx, axis=1)) < 1e-12 * np.min(orc.rms_norm_backward_scale(x, g, 0.0, dy_par))
+    # the scales the attention backward returns belong to its dq and dk rows
+    p = rand_problem(42, B=1, T=9, Hq=2, Hkv=1, d=8, with_ve=False, with_gate=False)
+    out = bwd(p, window=3, eps=1e-6, scales=True)
+    for key in ("dq", "dk"):
+        rows = np.linalg.norm(out[key], axis=-1)
+        assert out[key + "_scale"].shape == rows.shape
+        assert np.all(rows <= out[key + "_scale"] * (1 + 1e-12))
+
+
 def test_against_float64_torch_autograd():
     """Independent library check: torch float64 autograd through
     F.scaled_dot_product_attention with an explicit boolean mask."""

@@ -11,8 +11,13 @@ over every batch element for the S layer, and elsewhere with the oracle on
 single batch elements plus the identity "gradient of the batch = sum of the
 gradients of its elements", which holds at any size.
 
-Tolerance: relative error (Frobenius norm of the difference over that of the
-oracle) of 2e-2 for the bf16 library, per tensor, over the compared set.
+Tolerance, 2e-2 for the bf16 library, on three measures of every compared
+tensor (gpu_helpers.errors): the Frobenius norm of the difference over that
+of the oracle over the compared set; the same ratio for every row (a head row
+of d channels of o, dq, dk, dv, against the larger of its own norm and twice
+the rows' root mean square norm, gpu_helpers.ROW_FLOOR); and every element of
+lse and of the gain gradients, in the same way. The largest absolute error of each tensor is
+recorded and printed at the end of the session.
 """
 
 import numpy as np
@@ -23,7 +28,8 @@ import oracle
 import sliding_window_gqa_qk_gb300 as swa
 from sliding_window_gqa_qk_gb300.inputs import (L_LAYER, LONG_L, LONG_S, S_LAYER, Problem,
                                                 as_f64, make_inputs)
-from gpu_helpers import TOL, batch_slice, compare, rel_err, rope_tables, run_oracle, run_staged
+from gpu_helpers import (TOL, batch_slice, check, compare, rel_err, rope_tables, run_oracle,
+                         run_staged)
 
 pytestmark = pytest.mark.gpu
 
@@ -92,7 +98,7 @@ def test_full_size_s_layer_gain_gradients_over_the_whole_batch():
         for k in sums:
             sums[k] = sums[k] + ref[k]
     for k, r in sums.items():
-        assert rel_err(got[k], r) <= TOL_BF16, k
+        check(k, got[k], r, TOL_BF16)
 
 
 def _rows(T, seed):
@@ -109,27 +115,32 @@ def _sampled(p, x, got, heads, kv_heads, cols, row_chunk=512):
     args = (f["q"], f["k"], f["v"], f["gq"], f["gk"], f["dO"])
     rows = _rows(p.T, 5)
     acc = {k: ([], []) for k in ("o", "lse", "dq", "dk", "dv")}
+    scale = {"dq": [], "dk": []}
     for b in range(p.B):
         for h in heads:
             o_r, l_r = oracle.attention_forward_rows(*args[:5], b=b, h=h, rows=rows, **kw)
-            dq_r = oracle.attention_backward_rows(*args, b=b, h=h, rows=rows, **kw)
+            dq_r, dq_s = oracle.attention_backward_rows(*args, b=b, h=h, rows=rows, with_scale=True,
+                                                        **kw)
+            scale["dq"].append(dq_s)
             for k, mine, ref in (("o", got["o"][b, rows, h], o_r),
                                  ("lse", got["lse"][b, h, rows], l_r),
                                  ("dq", got["dq"][b, rows, h], dq_r)):
                 assert tuple(mine.shape) == np.shape(ref), (k, tuple(mine.shape), np.shape(ref))
-                acc[k][0].append(as_f64(mine).ravel())
-                acc[k][1].append(np.ravel(ref))
+                acc[k][0].append(as_f64(mine))
+                acc[k][1].append(np.asarray(ref))
         for hk in kv_heads:
-            dk_c, dv_c = oracle.attention_backward_cols(*args, b=b, hk=hk, cols=cols,
-                                                        row_chunk=row_chunk, **kw)
+            dk_c, dv_c, dk_s = oracle.attention_backward_cols(*args, b=b, hk=hk, cols=cols,
+                                                              row_chunk=row_chunk, with_scale=True,
+                                                              **kw)
+            scale["dk"].append(dk_s)
             for k, mine, ref in (("dk", got["dk"][b, cols, hk], dk_c),
                                  ("dv", got["dv"][b, cols, hk], dv_c)):
                 assert tuple(mine.shape) == np.shape(ref), (k, tuple(mine.shape), np.shape(ref))
-                acc[k][0].append(as_f64(mine).ravel())
-                acc[k][1].append(np.ravel(ref))
-    errs = {k: rel_err(np.concatenate(a), np.concatenate(r)) for k, (a, r) in acc.items()}
-    bad = {k: e for k, e in errs.items() if not e <= TOL_BF16}
-    assert not bad, f"sampled relative errors above {TOL_BF16}: {bad} (all: {errs})"
+                acc[k][0].append(as_f64(mine))
+                acc[k][1].append(np.asarray(ref))
+    for k, (a, r) in acc.items():
+        rs = np.concatenate(scale[k]) if k in scale else None
+        check(k, np.concatenate(a), np.concatenate(r), TOL_BF16, row_scale=rs)
 
 
 LONG = {"long_context_s": (LONG_S, 0), "long_context_l": (LONG_L, 3)}
@@ -181,11 +192,14 @@ def test_maximum_sequence_length_sampled():
     got = run_staged(p, x, dev)
     assert got["status"] == swa.SWA_OK
     acc = {k: ([], []) for k in ("o", "lse", "dq", "dk", "dv")}
+    scale = {"dq": [], "dk": []}
     for s0 in (0, T // 2 - L // 2, T - L):
         sl = slice(s0, s0 + L)
         xs = {k: (None if t is None else (t[:, sl] if k in ("q", "k", "v", "dO") else t).cpu())
               for k, t in x.items()}
         ref = run_oracle(p.replace(T=L), xs)
+        ref["dq_scale"] = ref["dq_scale"][0]        # [L, Hq]
+        ref["dk_scale"] = ref["dk_scale"][0]        # [L, Hkv]
         lo = 0 if s0 == 0 else W                       # rows with their whole band inside
         rows = np.arange(lo, L)
         c_hi = L if s0 + L == T else L - W             # columns with all their rows inside
@@ -196,11 +210,15 @@ def test_maximum_sequence_length_sampled():
                            ("dk", got["dk"][0, s0 + cols], ref["dk"][0, cols]),
                            ("dv", got["dv"][0, s0 + cols], ref["dv"][0, cols])):
             assert tuple(mine.shape) == np.shape(r), (k, tuple(mine.shape), np.shape(r))
-            acc[k][0].append(as_f64(mine).ravel())
-            acc[k][1].append(np.ravel(r))
-    errs = {k: rel_err(np.concatenate(a), np.concatenate(r)) for k, (a, r) in acc.items()}
-    bad = {k: e for k, e in errs.items() if not e <= TOL_BF16}
-    assert not bad, f"relative errors above {TOL_BF16}: {bad} (all: {errs})"
+            # rows of d channels (o, dq: [rows, Hq, d]; dk, dv: [cols, Hkv, d]);
+            # lse [Hq, rows] element by element
+            acc[k][0].append(as_f64(mine).reshape(-1) if k == "lse" else as_f64(mine).reshape(-1, p.d))
+            acc[k][1].append(np.reshape(r, -1) if k == "lse" else np.reshape(r, (-1, p.d)))
+        scale["dq"].append(ref["dq_scale"][rows].reshape(-1))
+        scale["dk"].append(ref["dk_scale"][cols].reshape(-1))
+    for k, (a, r) in acc.items():
+        rs = np.concatenate(scale[k]) if k in scale else None
+        check(k, np.concatenate(a), np.concatenate(r), TOL_BF16, row_scale=rs)
 
 
 def test_full_size_value_embedding_s_layer_with_rope():

@@ -187,6 +187,22 @@ swa_status swa_attn_bwd(const swa_params* p, const void* q, const void* k, const
  *                  gradient of the channels read (the caller adds it into
  *                  its gradient of the block input), or NULL
  * The forward keeps the gate values in the workspace for the backward.
+ *
+ * Time limit of the kernels' pipeline waits (not from the pages: a property
+ * of this library's kernels, whose warps hand work to each other through
+ * shared-memory barriers):
+ *   wait_limit_ns  0: the default, 2 s per wait. Else the limit of every
+ *                  pipeline wait of this call's tensor-core kernels. A wait
+ *                  that runs out makes its CTA give up: it records
+ *                  SWA_ERR_TIMEOUT in the workspace status word, lets the
+ *                  copies and MMAs it issued land (those waits keep their
+ *                  own 2 s limit), and returns; the call's outputs are then
+ *                  undefined. A short limit is how a caller (or a test) can
+ *                  make this path run. Limits below 1 ms are kept by polling
+ *                  the barrier without suspending; longer ones by the
+ *                  barrier's suspending wait, with the clock read every 64
+ *                  polls. The fp32 debug build has no such waits and ignores
+ *                  the field.
  */
 typedef struct {
   const float* rope_cos;
@@ -198,6 +214,7 @@ typedef struct {
   int gate_ch;
   float* d_gate_w;
   float* d_gate_x;
+  unsigned long long wait_limit_ns;
 } swa_extras;
 
 /* swa_attn_fwd with extras (arguments otherwise identical). */
@@ -232,8 +249,11 @@ swa_status swa_attn_bwd_ex(const swa_params* p, const swa_extras* ex, const void
  *     routine. The array is part of the library's device code, so every GPU
  *     that loads the library holds it until the process exits.
  *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before any
- *     stream capture begins.
+ *     per device, with that device current), and a call looks it up again
+ *     when the calling thread's current CUDA context is not the one of that
+ *     lookup (after cudaDeviceReset, or under a context the caller made
+ *     current); make the first call on a device, and the first after such a
+ *     change, before any stream capture begins.
  *   - Problems whose forward workspace (swa_attn_workspace_size(p, 0)) is
  *     larger than the array are rejected with SWA_ERR_WORKSPACE, launching
  *     nothing.
@@ -241,8 +261,11 @@ swa_status swa_attn_bwd_ex(const swa_params* p, const swa_extras* ex, const void
  *     keeps the last call's contents: calls that overlap on the GPU race and
  *     corrupt each other's results; order them (same stream or events).
  *     Nothing in it has to start at zero (the prologue writes every value the
- *     forward reads). Device-side checks are not reported: use swa_attn_fwd
- *     with a workspace and swa_attn_check_status to see them.
+ *     forward reads).
+ *   - Device-side checks are not reported: when one fires (a token id outside
+ *     [0, vocab), a pipeline wait that ran out) this call still returns
+ *     SWA_OK, and o and lse are undefined. Callers that need to see those
+ *     checks use swa_attn_fwd with a workspace and swa_attn_check_status.
  */
 #define SWA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 swa_status swa_attn_fwd_noalloc(const swa_params* p, const void* q, const void* k,
@@ -309,6 +332,9 @@ swa_status swa_block_bwd(const swa_params* p, const swa_extras* ex, const swa_bl
 /*
  * Synchronises `stream`, reads the workspace status word, clears it, and
  * returns SWA_OK, SWA_ERR_TIMEOUT or SWA_ERR_DEVICE_CHECK (timeout wins).
+ * After a timeout it also drops the record of a zeroed dQ accumulator (a
+ * forward that gave up may not have zeroed it), so the next backward clears
+ * the accumulator itself.
  */
 swa_status swa_attn_check_status(void* workspace, void* stream);
 

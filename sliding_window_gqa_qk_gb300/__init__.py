@@ -66,12 +66,13 @@ class SwaError(RuntimeError):
 
 
 class swa_extras(ctypes.Structure):
-    """Extras of the _ex entry points: rotary tables and the learned
-    value-embedding gate (see include/swa_attn.h)."""
+    """Extras of the _ex entry points: rotary tables, the learned
+    value-embedding gate and the pipeline-wait limit (see include/swa_attn.h)."""
     _fields_ = [("rope_cos", ctypes.c_void_p), ("rope_sin", ctypes.c_void_p), ("rope_rows", ctypes.c_int),
                 ("gate_x", ctypes.c_void_p), ("gate_x_stride", ctypes.c_longlong),
                 ("gate_w", ctypes.c_void_p), ("gate_ch", ctypes.c_int),
-                ("d_gate_w", ctypes.c_void_p), ("d_gate_x", ctypes.c_void_p)]
+                ("d_gate_w", ctypes.c_void_p), ("d_gate_x", ctypes.c_void_p),
+                ("wait_limit_ns", ctypes.c_ulonglong)]
 
 
 class swa_block_weights(ctypes.Structure):
@@ -193,12 +194,15 @@ def swa_attn_bwd(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk, dv, d
         _ptr(dgk), _ptr(dve), _ptr(ws), n, int(flags), _stream(stream)))
 
 
-def make_extras(rope=None, gate_x=None, gate_w=None, d_gate_w=None, d_gate_x=None) -> swa_extras:
+def make_extras(rope=None, gate_x=None, gate_w=None, d_gate_w=None, d_gate_x=None,
+                wait_limit_ns: int = 0) -> swa_extras:
     """swa_extras from device tensors: rope = (cos, sin) fp32 [rows, d/2] or
     None; gate_x [B, T, >= C] rows (its row stride is taken from the tensor),
     gate_w fp32 [Hkv, C] or None; backward outputs d_gate_w [Hkv, C],
-    d_gate_x [B, T, C] (fp32) or None."""
+    d_gate_x [B, T, C] (fp32) or None; wait_limit_ns the time limit of one
+    pipeline wait of the kernels (0: the library's default)."""
     e = swa_extras()
+    e.wait_limit_ns = int(wait_limit_ns)
     if rope is not None:
         e.rope_cos, e.rope_sin, e.rope_rows = _ptr(rope[0]), _ptr(rope[1]), int(rope[0].shape[0])
     if gate_w is not None:

@@ -255,6 +255,7 @@ struct PreArgs {  // backward preprocess: D = rowsum(dO * O), LSE2, clear dQ acc
   // the clear is skipped when it names exactly this call's accumulator.
   const unsigned long long* acc_flag;
   unsigned long long acc_off, acc_len;
+  const uint32_t* status;   // device status word: the record does not count after a timeout
   // dvec = d_mul * D, lse2 = lse2_mul * LSE + lse2_add (the forms the
   // attention backward kernels consume)
   float d_mul, lse2_mul, lse2_add;

@@ -67,24 +67,59 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
 // Shared state of the bounded waits of one CTA: an abort flag in shared memory
 // (set by the first wait that times out, so that every other wait of the CTA
 // gives up at once) and the global status word the host reads back.
+// kPolled selects how the limit is kept: false (limits of 1 ms and more,
+// the default 2 s among them), with the barrier's suspending try_wait and
+// the clock read every 64 polls; true (shorter limits), by polling the
+// barrier without suspending and reading the clock on every poll, since a
+// suspending try_wait can sleep until the phase completes, longer than a
+// short limit. The kernels are compiled for both and the host picks one per
+// call, so that the default waits are not slowed by the other form (a
+// run-time branch in every wait measured 22 % slower on the backward).
+template <bool kPolled = false>
 struct WaitCtl {
   volatile uint32_t* abort_flag;  // shared memory
   uint32_t* status;               // global memory (workspace header)
   uint64_t limit_ns;              // time limit of one wait
 };
 
+// Limits below this are kept by the polled form (WaitCtl<true>).
+constexpr uint64_t kPollBelowNs = 1000000ull;
+
+// Non-suspending test of the phase with the given parity.
+__device__ __forceinline__ uint32_t mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done;
+}
+
 // Waits until the phase with the given parity of the barrier has completed.
 // Returns false (and never blocks for longer than ctl.limit_ns, nor for more
 // than 2^31 polls) when the wait gives up: on timeout it records
 // DEV_ERR_TIMEOUT in the status word and raises the CTA's abort flag.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1; it < (1u << 31); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+template <bool kPolled>
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl<kPolled>& ctl) {
+  if constexpr (kPolled) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0; it < (1u << 31); ++it) {
+      if (mbar_test_wait(bar, parity)) return true;
       if (*ctl.abort_flag) return false;
       if (global_timer_ns() - t0 > ctl.limit_ns) break;
+    }
+  } else {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1; it < (1u << 31); ++it) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if ((it & 63u) == 0) {
+        if (*ctl.abort_flag) return false;
+        if (global_timer_ns() - t0 > ctl.limit_ns) break;
+      }
     }
   }
   *ctl.abort_flag = 1u;
@@ -115,10 +150,16 @@ __device__ __forceinline__ uint32_t mbar_test3(uint32_t b0, uint32_t p0, uint32_
 
 // mbar_wait whose outcome is the same for every lane of the warp (so that the
 // warp stays converged for the warp-collective tcgen05 loads that follow).
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
+template <bool kPolled>
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtl<kPolled>& ctl) {
   const bool ok = mbar_wait(bar, parity, ctl);
   return __all_sync(0xffffffffu, ok);
 }
+
+// Time limit of the waits on the way out of a CTA (mbar_wait_drain). It is
+// fixed, not the caller's pipeline-wait limit, so that a CTA whose pipeline
+// waits gave up early still lets every copy and MMA it issued land.
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 // Wait used on the way out of a CTA for its own asynchronous operations (TMA
 // copies, MMAs) to land before shared or tensor memory is released. It ignores

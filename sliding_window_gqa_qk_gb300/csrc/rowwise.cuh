@@ -250,9 +250,13 @@ __global__ void __launch_bounds__(kRowWarps * 32, kPreBlocksPerSm) bwd_pre_kerne
   constexpr int EPL = M::EPL;
   const int lane = threadIdx.x & 31;
   const int slot = lane / M::LPR, c0 = (lane % M::LPR) * EPL;
-  // the forward may already have zeroed exactly this accumulator
+  // the forward may already have zeroed exactly this accumulator (a record
+  // that counts only while no wait has run out: a forward CTA that gave up
+  // may not have zeroed its rows)
+  const bool timed_out = a.status != nullptr && (*a.status & DEV_ERR_TIMEOUT) != 0u;
   const bool clear = a.clear_acc &&
-                     !(a.acc_flag != nullptr && a.acc_flag[0] == a.acc_off && a.acc_flag[1] == a.acc_len);
+                     !(a.acc_flag != nullptr && !timed_out && a.acc_flag[0] == a.acc_off &&
+                       a.acc_flag[1] == a.acc_len);
   const int ngt = (a.T + M::RG - 1) / M::RG;
   const long long n_all = static_cast<long long>(a.B) * a.Hq * ngt;
   const long long in_stride = static_cast<long long>(a.Hq) * D;

@@ -26,7 +26,7 @@ using namespace swa;
 
 namespace {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait (default)
 
 inline bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
@@ -48,6 +48,7 @@ struct Call {
   int gch = 0;
   float* d_gw = nullptr;         // its gradients (backward outputs, NULL: skip)
   float* d_gx = nullptr;
+  uint64_t wait_ns = kWaitLimitNs;   // time limit of one pipeline wait
 };
 
 // Extras of a call. Rotary: none (both tables NULL), or both tables, 16-byte
@@ -57,6 +58,7 @@ struct Call {
 constexpr int kMaxGateCh = 32, kMaxGateHeads = 32;
 swa_status set_extras(Call& c, const swa_extras* e, const float* ve_gate) {
   if (e == nullptr) return SWA_OK;
+  if (e->wait_limit_ns != 0) c.wait_ns = e->wait_limit_ns;
   if (e->rope_cos != nullptr || e->rope_sin != nullptr) {
     if (e->rope_cos == nullptr || e->rope_sin == nullptr || !aligned(e->rope_cos, 16) ||
         !aligned(e->rope_sin, 16) || e->rope_rows < c.p.T)
@@ -177,22 +179,53 @@ namespace {
 
 constexpr int kMaxDevices = 256;
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices] = {};
+struct NoallocAddr {
+  CUcontext ctx;   // context current when the address was looked up
+  void* addr;
+};
+NoallocAddr g_noalloc[kMaxDevices] = {};
 
-// Device address of swa_noalloc_scratch on the current device, looked up once
-// per device with that device current.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// cuCtxGetCurrent from the driver (through the runtime's entry-point query,
+// so the library does not link against the driver library).
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  }
+  return fn;
+}
+
+// Device address of swa_noalloc_scratch on the current device. Looked up once
+// per device (with that device current), and again when the calling thread's
+// current context is not the one of that lookup: after cudaDeviceReset, or
+// under a context the caller made current, the module can sit elsewhere.
 swa_status noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SWA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return SWA_ERR_UNSUPPORTED;
+  CtxGetCurrentFn get = ctx_get_current();
+  if (get == nullptr) return SWA_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return SWA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_addr[dev] == nullptr) {
+  NoallocAddr& e = g_noalloc[dev];
+  if (ctx == nullptr || e.addr == nullptr || e.ctx != ctx) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, swa_noalloc_scratch) != cudaSuccess || ptr == nullptr)
       return SWA_ERR_CUDA;
-    g_noalloc_addr[dev] = ptr;
+    // the lookup makes the device's primary context current if none was
+    if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return SWA_ERR_CUDA;
+    e.ctx = ctx;
+    e.addr = ptr;
   }
-  *out = g_noalloc_addr[dev];
+  *out = e.addr;
   return SWA_OK;
 }
 
@@ -256,7 +289,7 @@ swa_status fwd_impl(const swa_params* p, const swa_extras* ex, const void* q, co
   f.v_head_major = (ve != nullptr);
   f.o = static_cast<elem_t*>(o); f.lse = lse;
   f.status = at<uint32_t>(c, c.L.status);
-  f.wait_limit_ns = kWaitLimitNs;
+  f.wait_limit_ns = c.wait_ns;
   // The forward is compute-bound, so it can zero the backward's dQ
   // accumulator at little cost; the backward's preprocess then skips it.
   f.acc_flag = at<unsigned long long>(c, c.L.status + 8);
@@ -332,6 +365,7 @@ swa_status bwd_impl(const swa_params* p, const swa_extras* ex, const void* q, co
     a.acc_flag = at<unsigned long long>(c, c.L.status + 8);
     a.acc_off = c.L.dq_acc;
     a.acc_len = static_cast<unsigned long long>(P.B) * P.T * P.Hq * P.d * sizeof(float);
+    a.status = at<uint32_t>(c, c.L.status);
     // The d = 128 tensor-core backward takes -D and log2(scale) - LSE log2(e)
     // (its P carries the softmax scale); the others take D and LSE log2(e).
     const bool scaled_p = !kFp32Build && P.d == 128;
@@ -393,7 +427,7 @@ swa_status bwd_impl(const swa_params* p, const swa_extras* ex, const void* q, co
     b.dk = static_cast<elem_t*>(dk); b.dv = static_cast<elem_t*>(dv);
     b.gpart_k = at<float>(c, c.L.gpart_k);
     b.status = at<uint32_t>(c, c.L.status);
-    b.wait_limit_ns = kWaitLimitNs;
+    b.wait_limit_ns = c.wait_ns;
     b.acc_flag = at<unsigned long long>(c, c.L.status + 8);
     // with rotary the k-side norm backward moves to the post kernel
     b.dkn_out = c.rcos != nullptr ? at<float>(c, c.L.dk_acc) : nullptr;
@@ -701,6 +735,11 @@ swa_status swa_attn_check_status(void* workspace, void* stream) {
   if (cudaStreamSynchronize(st) != cudaSuccess) return SWA_ERR_CUDA;
   if (word != 0) {
     if (cudaMemsetAsync(workspace, 0, sizeof(word), st) != cudaSuccess) return SWA_ERR_CUDA;
+    // After a wait ran out, a forward may not have zeroed all of the dQ
+    // accumulator it recorded as zeroed: drop the record (its length word).
+    if ((word & DEV_ERR_TIMEOUT) &&
+        cudaMemsetAsync(static_cast<uint8_t*>(workspace) + 16, 0, 8, st) != cudaSuccess)
+      return SWA_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return SWA_ERR_CUDA;
   }
   if (word & DEV_ERR_TIMEOUT) return SWA_ERR_TIMEOUT;

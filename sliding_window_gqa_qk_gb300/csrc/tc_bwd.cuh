@@ -346,7 +346,7 @@ __device__ __forceinline__ void st_sw128_chunk(uint32_t tile, int rows, int r, i
   st_shared_v4(addr, a, b, c, d);
 }
 
-template <int D>
+template <int D, bool kPolled>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   q_tile_range(band, k0, kBK, BQ, qlo, qhi);
   const int nq = qhi - qlo + 1;
   const int n_it = nq > 0 ? nq * G : 0;
-  const WaitCtl ctl{&abort_flag, prm.status, prm.wait_limit_ns};
+  const WaitCtl<kPolled> ctl{&abort_flag, prm.status, prm.wait_limit_ns};
   const uint32_t sbase = smem_u32(smem);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
@@ -436,9 +436,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bulk_load(sbase + C::oD + st * BQ * 4, prm.dvec + row, BQ * 4, bar(BB_QFULL + st));
       }
       // Let every copy this thread started land before the CTA can exit.
-      mbar_wait_drain(bar(BB_KV), 0, prm.wait_limit_ns);
+      mbar_wait_drain(bar(BB_KV), 0, kDrainLimitNs);
       for (int s = 0; s < 2; ++s)
-        if (last[s] >= 0) mbar_wait_drain(bar(BB_QFULL + s), (last[s] >> 1) & 1, prm.wait_limit_ns);
+        if (last[s] >= 0) mbar_wait_drain(bar(BB_QFULL + s), (last[s] >> 1) & 1, kDrainLimitNs);
     }
   } else if (warp == kBwdMmaWarp) {
     // ---------------- MMA issuer ----------------
@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         umma_commit(bar(BB_QEMPTY + st));
       }
       umma_commit(bar(BB_FINAL));
-      mbar_wait_drain(bar(BB_FINAL), 0, prm.wait_limit_ns);
+      mbar_wait_drain(bar(BB_FINAL), 0, kDrainLimitNs);
     }
   } else {
     // ------------- softmax-backward warpgroups (warps 0-3 and 4-7) -------------
@@ -737,12 +737,14 @@ inline swa_status launch_bwd_d(const BwdLaunch& f, cudaStream_t st) {
   p.status = f.status; p.wait_limit_ns = f.wait_limit_ns;
   p.acc_flag = f.acc_flag;
   p.dkn_out = f.dkn_out;
-  if (cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::kAlloc) != cudaSuccess)
-    return SWA_ERR_CUDA;
   dim3 grid(f.B * f.Hkv, p.n_ktiles);
-  bwd_tc_kernel<D><<<grid, kBwdThreads, C::kAlloc, st>>>(mq, mk, mv, mg, mdq, mdk, mdv, p);
-  return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+  auto launch = [&](auto kern) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc) != cudaSuccess)
+      return SWA_ERR_CUDA;
+    kern<<<grid, kBwdThreads, C::kAlloc, st>>>(mq, mk, mv, mg, mdq, mdk, mdv, p);
+    return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+  };
+  return p.wait_limit_ns < kPollBelowNs ? launch(bwd_tc_kernel<D, true>) : launch(bwd_tc_kernel<D, false>);
 }
 
 // d = 64 (d = 128 has its own kernel, tc_bwd128.cuh).

@@ -121,6 +121,7 @@ __device__ __forceinline__ void pack64(const uint32_t (&v)[2][32], uint32_t (&pk
                         __uint_as_float(v[w >> 4][(w & 15) * 2 + 1]));
 }
 
+template <bool kPolled>
 __global__ void __launch_bounds__(kB2Threads, 1)
     bwd_tc128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
@@ -164,7 +165,7 @@ __global__ void __launch_bounds__(kB2Threads, 1)
   q_tile_range(band, k0, kBK, BQ, qlo, qhi);
   const int nq = qhi - qlo + 1;
   const int n_it = nq > 0 ? nq * G : 0;
-  const WaitCtl ctl{abort_flag, prm.status, prm.wait_limit_ns};
+  const WaitCtl<kPolled> ctl{abort_flag, prm.status, prm.wait_limit_ns};
   auto bar = [&](int i) { return sbase + C::oBar + 8u * static_cast<uint32_t>(i); };
 
   if (threadIdx.x == 0) {
@@ -242,9 +243,9 @@ __global__ void __launch_bounds__(kB2Threads, 1)
           if (a1 > a0) bulk_prefetch_l2(reinterpret_cast<const void*>(a0), static_cast<uint32_t>(a1 - a0));
         }
       }
-      mbar_wait_drain(bar(B2_KV), 0, prm.wait_limit_ns);
+      mbar_wait_drain(bar(B2_KV), 0, kDrainLimitNs);
       for (int s = 0; s < 2; ++s)
-        if (last[s] >= 0) mbar_wait_drain(bar(B2_QFULL + s), (last[s] >> 1) & 1, prm.wait_limit_ns);
+        if (last[s] >= 0) mbar_wait_drain(bar(B2_QFULL + s), (last[s] >> 1) & 1, kDrainLimitNs);
     } else if (warp == kB2GWarp && lane == 0 && n_it > 0) {
       // ---------------- TMA producer of dO (one stage) ----------------
       tma_prefetch_desc(&tmG);
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(kB2Threads, 1)
         for (int c = 0; c < 2; ++c)
           tma_load_4d(sbase + C::oG + c * C::kHalf, &tmG, bar(B2_GFULL), 64 * c, q0, h, b);
       }
-      if (last >= 0) mbar_wait_drain(bar(B2_GFULL), last & 1, prm.wait_limit_ns);
+      if (last >= 0) mbar_wait_drain(bar(B2_GFULL), last & 1, kDrainLimitNs);
     } else if (warp == kB2RedWarp && lane == 0 && n_it > 0) {
       // ---------------- dQ reducer ----------------
       // Step m's dQ boxes, for each warpgroup X: queries qb.. in half X of the
@@ -378,7 +379,7 @@ __global__ void __launch_bounds__(kB2Threads, 1)
         }
       }
       umma_commit(bar(B2_FINAL));
-      mbar_wait_drain(bar(B2_FINAL), 0, prm.wait_limit_ns);
+      mbar_wait_drain(bar(B2_FINAL), 0, kDrainLimitNs);
     }
   } else if (warp >= 8) {
     // --------- drain warpgroup: dQ^T(i) (lane = head-dim index) -> staged boxes ---------
@@ -583,9 +584,7 @@ inline swa_status launch_bwd128(const BwdLaunch& f, cudaStream_t st) {
   p.k = f.k; p.rstd_k = f.rstd_k; p.gk = f.gk; p.tok = f.tok; p.gate = f.gate; p.dve = f.dve;
   p.ve_scale = f.ve_scale; p.vocab = f.vocab; p.dk = f.dk; p.dv = f.dv; p.gpart_k = f.gpart_k;
   p.status = f.status; p.wait_limit_ns = f.wait_limit_ns;
-  if (cudaFuncSetAttribute(bwd_tc128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::kBytes) != cudaSuccess)
-    return SWA_ERR_CUDA;
+
   // chunks of about 2.5 waves of CTAs
   p.n_bhk = f.B * f.Hkv;
   const int want = (5 * num_sms() + 2 * p.n_ktiles - 1) / (2 * p.n_ktiles);
@@ -594,9 +593,13 @@ inline swa_status launch_bwd128(const BwdLaunch& f, cudaStream_t st) {
   p.dkn_out = f.dkn_out;
   const long long n_cta = static_cast<long long>(p.n_ktiles) * p.n_bhk;
   if (n_cta > 0x7fffffffLL) return SWA_ERR_UNSUPPORTED;
-  bwd_tc128_kernel<<<static_cast<unsigned>(n_cta), kB2Threads, C::kBytes, st>>>(mq, mk, mv, mg, mdq, mdk,
-                                                                                mdv, mkr, p);
-  return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+  auto launch = [&](auto kern) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes) != cudaSuccess)
+      return SWA_ERR_CUDA;
+    kern<<<static_cast<unsigned>(n_cta), kB2Threads, C::kBytes, st>>>(mq, mk, mv, mg, mdq, mdk, mdv, mkr, p);
+    return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+  };
+  return p.wait_limit_ns < kPollBelowNs ? launch(bwd_tc128_kernel<true>) : launch(bwd_tc128_kernel<false>);
 }
 
 }  // namespace tc

@@ -144,7 +144,7 @@ __device__ __forceinline__ PerItem per_decode(int w, const FwdPerParams& p, cons
   return it;
 }
 
-template <int D>
+template <int D, bool kPolled>
 __global__ void __launch_bounds__(kPerThreads, 1)
     fwd_tc_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kPerThreads, 1)
   const int cta = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
   const int Gq = prm.Hq / prm.Hkv;
   const Band band{prm.T, prm.window, prm.causal};
-  const WaitCtl ctl{abort_flag, prm.status, prm.wait_limit_ns};
+  const WaitCtl<kPolled> ctl{abort_flag, prm.status, prm.wait_limit_ns};
   auto bar = [&](int i) { return sbase + L::kBar + 8u * static_cast<uint32_t>(i); };
 
   if (threadIdx.x == 0) {
@@ -269,10 +269,10 @@ __global__ void __launch_bounds__(kPerThreads, 1)
         }
         ++it;
       }
-      if (it > 0) mbar_wait_drain(bar(QP_QFULL), (it - 1) & 1, prm.wait_limit_ns);
+      if (it > 0) mbar_wait_drain(bar(QP_QFULL), (it - 1) & 1, kDrainLimitNs);
       for (int s = 0; s < 2; ++s) {
-        if (last_k[s] >= 0) mbar_wait_drain(bar(QP_KFULL + s), (last_k[s] >> 1) & 1, prm.wait_limit_ns);
-        if (last_v[s] >= 0) mbar_wait_drain(bar(QP_VFULL + s), (last_v[s] >> 1) & 1, prm.wait_limit_ns);
+        if (last_k[s] >= 0) mbar_wait_drain(bar(QP_KFULL + s), (last_k[s] >> 1) & 1, kDrainLimitNs);
+        if (last_v[s] >= 0) mbar_wait_drain(bar(QP_VFULL + s), (last_v[s] >> 1) & 1, kDrainLimitNs);
       }
       if (one) bulk_wait_group_all();   // the zero-block copies have finished
     } else if (warp == 9) {
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kPerThreads, 1)
         ++it;
       }
       umma_commit_w(bar(QP_FINAL), one);
-      mbar_wait_drain(bar(QP_FINAL), 0, prm.wait_limit_ns);
+      mbar_wait_drain(bar(QP_FINAL), 0, kDrainLimitNs);
     }
   } else {
     // ---------------- softmax warpgroups (A: warps 0-3, B: warps 4-7) ----------------
@@ -570,12 +570,15 @@ inline swa_status launch_fwd_persist_d(const FwdLaunch& f, cudaStream_t st) {
   p.lse = f.lse; p.status = f.status; p.wait_limit_ns = f.wait_limit_ns;
   p.dq_acc = f.dq_acc; p.acc_flag = f.acc_flag;
   p.acc_off = f.acc_off; p.acc_len = f.acc_len;
-  if (cudaFuncSetAttribute(fwd_tc_persist_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           L::kBytes) != cudaSuccess)
-    return SWA_ERR_CUDA;
   const int grid = p.n_items < num_sms() ? p.n_items : num_sms();
-  fwd_tc_persist_kernel<D><<<grid, kPerThreads, L::kBytes, st>>>(mq, mk, mv, mo, p);
-  return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+  auto launch = [&](auto kern) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes) != cudaSuccess)
+      return SWA_ERR_CUDA;
+    kern<<<grid, kPerThreads, L::kBytes, st>>>(mq, mk, mv, mo, p);
+    return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+  };
+  return p.wait_limit_ns < kPollBelowNs ? launch(fwd_tc_persist_kernel<D, true>)
+                                        : launch(fwd_tc_persist_kernel<D, false>);
 }
 
 // Forward dispatch: the persistent kernel for every group size (even groups

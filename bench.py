@@ -235,6 +235,8 @@ WORKLOADS = {
     "block_stack": ("8 whole attention blocks (pre-norm, c_q / c_k / c_v, attention, c_proj, "
                     "residual) at C=768: B=16, T=2048, Hq=6, Hkv=3, d=128, SSSL windows, rotary "
                     "tables, VE with the learned gate on odd layers"),
+    "block_layer": ("one whole attention block (layer 1 of the block stack: window 1024, rotary, "
+                    "VE with the learned gate) at C=768, B=16, T=2048, Hq=6, Hkv=3, d=128 (profiling)"),
 }
 
 # (B, T, Hq, Hkv) of each workload; d = 128 throughout
@@ -396,11 +398,13 @@ class BlockStack:
 
     C = 768
 
-    def __init__(self, swa, dev):
+    def __init__(self, swa, dev, only_layer=None):
         from sliding_window_gqa_qk_gb300.inputs import make_block_inputs
         self.swa = swa
         C = self.C
         self.sched = layer_schedule(swa.swa_sssl_window, swa.swa_has_ve)
+        if only_layer is not None:
+            self.sched = [self.sched[only_layer]]
         inv = 10000.0 ** (-torch.arange(D // 2, dtype=torch.float64) * 2.0 / D)
         ang = torch.arange(T, dtype=torch.float64)[:, None] * inv[None, :]
         self.rope = (torch.cos(ang).float().to(dev).contiguous(),
@@ -409,7 +413,8 @@ class BlockStack:
         self.layers = []
         for li, (W, ve) in enumerate(self.sched):
             p = Problem(B=B, T=T, Hq=HQ, Hkv=HKV, d=D, window=W, gain_std=0.1, ve=ve, vocab=VOCAB)
-            x = make_block_inputs(p, C, layer=li, gate_ch=32 if ve else None)
+            x = make_block_inputs(p, C, layer=li if only_layer is None else only_layer,
+                                  gate_ch=32 if ve else None)
             g = {k: (t.to(dev) if t is not None else None) for k, t in x.items()}
             prm = swa.make_params(B, T, HQ, HKV, D, W, True, 0.0, p.eps, VE_SCALE, VOCAB if ve else 0)
             n = swa.swa_block_workspace_size(prm, C, 1)
@@ -462,11 +467,11 @@ class BlockStack:
 
 
 def run_block_stack(args, rank, world, dev):
-    """Times the block stack: one step's launches (our kernels and the
-    cuBLASLt projections) captured in a CUDA graph and replayed."""
+    """Times the block stack (or one block layer): one step's launches
+    captured in a CUDA graph and replayed."""
     import sliding_window_gqa_qk_gb300 as swa
     swa.load("bf16")
-    stack = BlockStack(swa, dev)
+    stack = BlockStack(swa, dev, only_layer=1 if args.workload == "block_layer" else None)
     start, stop = _ev_pair()
     ev = {"fwd": [], "bwd": []}
     with ClockSampler(_physical_index(torch.cuda.current_device())) as clocks:
@@ -508,7 +513,7 @@ def run_block_stack(args, rank, world, dev):
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOADS["block_stack"], "global_batch": B * world, "seq_len": T,
+        "config": {"workload": WORKLOADS[args.workload], "global_batch": B * world, "seq_len": T,
                    "parallelism": "single GPU" if world == 1 else f"replicas over batch x{world}",
                    "l2": "inputs larger than L2", "flops_per_step": stack.flops,
                    "attention_flops_per_step": stack.flops_attn,
@@ -519,7 +524,7 @@ def run_block_stack(args, rank, world, dev):
                    "launch": ("one step's launches captured in a CUDA graph, replayed per step"
                               if graph is not None else "eager launches"),
                    "stage_ms_per_step": {k: round(v, 4) for k, v in stage_ms.items()},
-                   "projections": "cuBLASLt (bf16 operands, fp32 accumulation)"},
+                   "projections": "the library's tcgen05 GEMM (bf16 operands, fp32 accumulation)"},
         "clocks": clocks.summary(t0, t1),
     }
 
@@ -838,7 +843,7 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    if args.workload == "block_stack":
+    if args.workload in ("block_stack", "block_layer"):
         out = run_block_stack(args, rank, world, dev)
     else:
         out = run_ours(args, rank, world, dev)

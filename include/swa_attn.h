@@ -26,8 +26,7 @@
  * Conventions common to every call:
  *   - All tensor pointers are DEVICE pointers of the current CUDA device; the
  *     caller owns every buffer, including the workspace. The library never
- *     allocates or frees device memory (the block calls below give cuBLASLt
- *     a slice of the workspace as its scratch).
+ *     allocates or frees device memory.
  *   - Layouts are dense row-major:
  *       q, o, dO, dq       [B, T, Hq,  d]   elem
  *       k, v, dk, dv       [B, T, Hkv, d]   elem
@@ -41,10 +40,8 @@
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream). SWA_ERR_INVALID_ARG, SWA_ERR_WORKSPACE and the unsupported-
  *     size checks come before the first launch: nothing was launched. A
- *     failing CUDA or cuBLASLt call inside a call (SWA_ERR_CUDA, or
- *     SWA_ERR_UNSUPPORTED when cuBLASLt has no algorithm for a projection)
- *     can come after earlier launches of that call; its outputs are then
- *     undefined. Errors found on the device (a bounded wait that ran
+ *     failing CUDA call inside a call (SWA_ERR_CUDA) can come after earlier
+ *     launches of that call; its outputs are then undefined. Errors found on the device (a bounded wait that ran
  *     out, a token id outside [0, vocab)) are OR-ed into a status word in the
  *     workspace header and read back by swa_attn_check_status().
  *   - B == 0 or T == 0 is a valid empty problem: nothing is computed; the
@@ -294,12 +291,13 @@ swa_status swa_attn_fwd_noalloc(const swa_params* p, const void* q, const void* 
  * input and adds the gradient of the channels it read into dx); gate_ch <= C.
  * As in the attention calls, the gate applies on value-embedding calls only
  * (ve != NULL); without a VE table it is ignored and d_gate_w is not written.
- * The projections run on cuBLASLt, opened at run time (dlopen of
- * libcublasLt.so.13): where it cannot be opened the block calls return
- * SWA_ERR_UNSUPPORTED. Its handle is created on the first block call made
- * on each device, so make that first call outside stream capture; cuBLASLt
- * gets a slice of the workspace as its only device scratch. The workspace (swa_block_workspace_size) holds the attention's
- * workspace first (so swa_attn_check_status reads the block workspace too),
+ * The projections run on this library's own GEMM kernels (tcgen05 tensor
+ * cores with bf16 operands and fp32 accumulation in the bf16 library, fp32
+ * SIMT in the fp32 debug library); the weight gradients split B*T over
+ * several CTAs and add their fp32 partial sums into dwq, dwk, dwv and dwo,
+ * so their last bits can differ from run to run. The workspace
+ * (swa_block_workspace_size) holds the attention's workspace first (so
+ * swa_attn_check_status reads the block workspace too),
  * then the forward's saved tensors (xn, q, k, v, o, lse); swa_block_bwd
  * needs the workspace that swa_block_fwd filled for the same inputs.
  */

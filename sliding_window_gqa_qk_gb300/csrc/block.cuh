@@ -5,20 +5,15 @@
 // paragraph: RMSNorm on the block inputs).
 //
 // The pre-norm and its backward are row-wise kernels here. The projections
-// are plain GEMMs and go to cuBLASLt (bf16 operands with fp32 accumulation in
-// the bf16 library, fp32 throughout in the fp32 debug library). cuBLASLt is
-// opened at run time with dlopen, so the library neither links against it
-// nor fails to load where it is missing; the block entry points then return
-// SWA_ERR_UNSUPPORTED. cuBLASLt gets a slice of the caller's workspace as its
-// only device scratch.
+// are GEMMs of this library: the tcgen05 kernel of tc_gemm.cuh in the bf16
+// library (bf16 operands, fp32 accumulation), a plain fp32 SIMT kernel in the
+// fp32 debug library.
 #pragma once
 
-#include <cublasLt.h>
-#include <dlfcn.h>
-
-#include <mutex>
-
 #include "rowwise.cuh"
+#if !defined(SWA_ELEM_FP32)
+#include "tc_gemm.cuh"
+#endif
 
 namespace swa {
 namespace blk {
@@ -111,161 +106,72 @@ inline int prenorm_grid(long long rows) {
   return static_cast<int>(per < cap ? (per < 1 ? 1 : per) : cap);
 }
 
-// ---------------------------------------------------------------------------
-// cuBLASLt, opened at run time.
-// ---------------------------------------------------------------------------
-struct LtApi {
-  decltype(&cublasLtCreate) create = nullptr;
-  decltype(&cublasLtMatmulDescCreate) desc_create = nullptr;
-  decltype(&cublasLtMatmulDescDestroy) desc_destroy = nullptr;
-  decltype(&cublasLtMatmulDescSetAttribute) desc_set = nullptr;
-  decltype(&cublasLtMatrixLayoutCreate) layout_create = nullptr;
-  decltype(&cublasLtMatrixLayoutDestroy) layout_destroy = nullptr;
-  decltype(&cublasLtMatmulPreferenceCreate) pref_create = nullptr;
-  decltype(&cublasLtMatmulPreferenceDestroy) pref_destroy = nullptr;
-  decltype(&cublasLtMatmulPreferenceSetAttribute) pref_set = nullptr;
-  decltype(&cublasLtMatmulAlgoGetHeuristic) heuristic = nullptr;
-  decltype(&cublasLtMatmul) matmul = nullptr;
-  bool ok = false;
-};
-
-inline const LtApi& lt_api() {
-  static const LtApi api = [] {
-    LtApi a;
-    void* h = dlopen("libcublasLt.so.13", RTLD_NOW | RTLD_LOCAL);
-    if (h == nullptr) h = dlopen("libcublasLt.so", RTLD_NOW | RTLD_LOCAL);
-    if (h == nullptr) return a;
-    bool all = true;
-    auto get = [&](auto& fn, const char* name) {
-      fn = reinterpret_cast<std::remove_reference_t<decltype(fn)>>(dlsym(h, name));
-      all = all && fn != nullptr;
-    };
-    get(a.create, "cublasLtCreate");
-    get(a.desc_create, "cublasLtMatmulDescCreate");
-    get(a.desc_destroy, "cublasLtMatmulDescDestroy");
-    get(a.desc_set, "cublasLtMatmulDescSetAttribute");
-    get(a.layout_create, "cublasLtMatrixLayoutCreate");
-    get(a.layout_destroy, "cublasLtMatrixLayoutDestroy");
-    get(a.pref_create, "cublasLtMatmulPreferenceCreate");
-    get(a.pref_destroy, "cublasLtMatmulPreferenceDestroy");
-    get(a.pref_set, "cublasLtMatmulPreferenceSetAttribute");
-    get(a.heuristic, "cublasLtMatmulAlgoGetHeuristic");
-    get(a.matmul, "cublasLtMatmul");
-    a.ok = all;
-    return a;
-  }();
-  return api;
-}
-
-// One cuBLASLt handle per device, created on the first block call made with
-// that device current (host-side state of cuBLASLt).
-inline swa_status lt_handle(cublasLtHandle_t* out) {
-  const LtApi& L = lt_api();
-  if (!L.ok) return SWA_ERR_UNSUPPORTED;
-  constexpr int kMaxDev = 64;
-  static std::mutex mu;
-  static cublasLtHandle_t handles[kMaxDev] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return SWA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(mu);
-  if (handles[dev] == nullptr && L.create(&handles[dev]) != CUBLAS_STATUS_SUCCESS) {
-    handles[dev] = nullptr;
-    return SWA_ERR_CUDA;
-  }
-  *out = handles[dev];
-  return SWA_OK;
-}
-
 #if defined(SWA_ELEM_FP32)
-constexpr cudaDataType_t kElemType = CUDA_R_32F;
-#else
-constexpr cudaDataType_t kElemType = CUDA_R_16BF;
-#endif
-
-// Column-major GEMM D[m x n] = op(A) op(B) + beta C, with C = D unless given:
-// A is stored k x m (lda) when ta, else m x k; B is stored n x k (ldb) when
-// tb, else k x n; C and D are m x n (ldd). A and B are elem_t; C and D are
-// dt (elem_t or fp32). Accumulation and alpha / beta in fp32.
-struct Gemm {
-  bool ta = false, tb = false;
-  int m = 0, n = 0, k = 0;
-  const void* A = nullptr;
-  int lda = 0;
-  const void* B = nullptr;
-  int ldb = 0;
-  float beta = 0.f;
-  const void* C = nullptr;
-  void* D = nullptr;
-  cudaDataType_t dt = kElemType;
-  int ldd = 0;
+// ---------------------------------------------------------------------------
+// fp32 debug GEMM: one thread per output element, fp32 accumulation over the
+// K segments in order (the same GemmCall as the tensor-core kernel).
+// ---------------------------------------------------------------------------
+struct SimtGemmArgs {
+  int M, N, n_kseg;
+  bool a_mn, b_mn;
+  const float* A[3];
+  long long lda[3];
+  int K[3];
+  const float* B[3];
+  long long ldb[3];
+  float* D;
+  long long ldd;
+  const float* C;
+  long long ldc;
+  float beta;
 };
 
-// Largest power of two (at most 256) that divides the address: cuBLASLt's
-// algorithm choice assumes 256-byte aligned operands unless told otherwise,
-// and callers' tensors need only be 16-byte aligned.
-inline uint32_t ptr_alignment(const void* p) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  uint32_t al = 256;
-  while (al > 1 && (a & (al - 1)) != 0) al >>= 1;
-  return al;
-}
-
-inline swa_status gemm(const Gemm& g, void* lt_ws, size_t lt_ws_bytes, cudaStream_t st) {
-  if (g.m == 0 || g.n == 0) return SWA_OK;
-  cublasLtHandle_t h = nullptr;
-  swa_status s = lt_handle(&h);
-  if (s != SWA_OK) return s;
-  const LtApi& L = lt_api();
-  cublasLtMatmulDesc_t desc = nullptr;
-  cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
-  cublasLtMatmulPreference_t pref = nullptr;
-  s = SWA_ERR_CUDA;
-  const cublasOperation_t opa = g.ta ? CUBLAS_OP_T : CUBLAS_OP_N;
-  const cublasOperation_t opb = g.tb ? CUBLAS_OP_T : CUBLAS_OP_N;
-  const uint64_t wsb = lt_ws_bytes;
-  const void* cptr = g.C != nullptr ? g.C : g.D;
-  const uint32_t al[4] = {ptr_alignment(g.A), ptr_alignment(g.B), ptr_alignment(cptr), ptr_alignment(g.D)};
-  const cublasLtMatmulPreferenceAttributes_t al_attr[4] = {
-      CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_A_BYTES, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_B_BYTES,
-      CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_C_BYTES, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_D_BYTES};
-  auto set_alignments = [&]() {
-    for (int i = 0; i < 4; ++i)
-      if (L.pref_set(pref, al_attr[i], &al[i], sizeof(al[i])) != CUBLAS_STATUS_SUCCESS) return false;
-    return true;
-  };
-  cublasLtMatmulHeuristicResult_t res{};
-  int found = 0;
-  const float alpha = 1.f;
-  if (L.desc_create(&desc, CUBLAS_COMPUTE_32F, CUDA_R_32F) == CUBLAS_STATUS_SUCCESS &&
-      L.desc_set(desc, CUBLASLT_MATMUL_DESC_TRANSA, &opa, sizeof(opa)) == CUBLAS_STATUS_SUCCESS &&
-      L.desc_set(desc, CUBLASLT_MATMUL_DESC_TRANSB, &opb, sizeof(opb)) == CUBLAS_STATUS_SUCCESS &&
-      L.layout_create(&la, kElemType, g.ta ? g.k : g.m, g.ta ? g.m : g.k, g.lda) == CUBLAS_STATUS_SUCCESS &&
-      L.layout_create(&lb, kElemType, g.tb ? g.n : g.k, g.tb ? g.k : g.n, g.ldb) == CUBLAS_STATUS_SUCCESS &&
-      L.layout_create(&lc, g.dt, g.m, g.n, g.ldd) == CUBLAS_STATUS_SUCCESS &&
-      L.pref_create(&pref) == CUBLAS_STATUS_SUCCESS &&
-      L.pref_set(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &wsb, sizeof(wsb)) ==
-          CUBLAS_STATUS_SUCCESS &&
-      set_alignments()) {
-    if (L.heuristic(h, desc, la, lb, lc, lc, pref, 1, &res, &found) != CUBLAS_STATUS_SUCCESS || found < 1) {
-      s = SWA_ERR_UNSUPPORTED;
-    } else if (L.matmul(h, desc, &alpha, g.A, la, g.B, lb, &g.beta, cptr, lc, g.D, lc, &res.algo, lt_ws,
-                        lt_ws_bytes, st) == CUBLAS_STATUS_SUCCESS) {
-      s = SWA_OK;
+__global__ void __launch_bounds__(256) gemm_simt_kernel(const SimtGemmArgs a) {
+  const int n = blockIdx.x * 32 + threadIdx.x;
+  const int m = blockIdx.y * 8 + threadIdx.y;
+  if (m >= a.M || n >= a.N) return;
+  float acc = 0.f;
+  for (int s = 0; s < a.n_kseg; ++s) {
+    const float* A = a.A[s];
+    const float* B = a.B[s];
+    for (int k = 0; k < a.K[s]; ++k) {
+      const float av = a.a_mn ? A[static_cast<long long>(k) * a.lda[s] + m] : A[static_cast<long long>(m) * a.lda[s] + k];
+      const float bv = a.b_mn ? B[static_cast<long long>(k) * a.ldb[s] + n] : B[static_cast<long long>(n) * a.ldb[s] + k];
+      acc = fmaf(av, bv, acc);
     }
   }
-  if (pref) L.pref_destroy(pref);
-  if (lc) L.layout_destroy(lc);
-  if (lb) L.layout_destroy(lb);
-  if (la) L.layout_destroy(la);
-  if (desc) L.desc_destroy(desc);
-  return s;
+  if (a.C != nullptr && a.beta != 0.f) acc = fmaf(a.beta, a.C[static_cast<long long>(m) * a.ldc + n], acc);
+  a.D[static_cast<long long>(m) * a.ldd + n] = acc;
 }
+
+inline swa_status run_gemm(const GemmCall& g, cudaStream_t st) {
+  if (g.M == 0) return SWA_OK;
+  for (int j = 0; j < g.n_nseg; ++j) {
+    const auto& o = g.nseg[j];
+    if (o.N == 0) continue;
+    SimtGemmArgs a{};
+    a.M = g.M; a.N = o.N; a.n_kseg = g.n_kseg; a.a_mn = g.a_mn; a.b_mn = g.b_mn;
+    for (int s = 0; s < g.n_kseg; ++s) {
+      a.A[s] = static_cast<const float*>(g.kseg[s].A); a.lda[s] = g.kseg[s].lda; a.K[s] = g.kseg[s].K;
+      const auto& b = g.bseg[g.n_kseg > 1 ? s : j];
+      a.B[s] = static_cast<const float*>(b.B); a.ldb[s] = b.ldb;
+    }
+    a.D = static_cast<float*>(o.D); a.ldd = o.ldd;
+    a.C = static_cast<const float*>(o.C); a.ldc = o.ldc; a.beta = g.beta;
+    dim3 grid((o.N + 31) / 32, (g.M + 7) / 8);
+    gemm_simt_kernel<<<grid, dim3(32, 8), 0, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return SWA_ERR_CUDA;
+  }
+  return SWA_OK;
+}
+#else
+inline swa_status run_gemm(const GemmCall& g, cudaStream_t st) { return tc::launch_gemm(g, st); }
+#endif
 
 // ---------------------------------------------------------------------------
 // Workspace of the block calls. The attention's own workspace (sized for its
 // backward) comes first, so its status word is the block workspace's header.
 // ---------------------------------------------------------------------------
-constexpr size_t kLtWsBytes = 32ull << 20;   // cuBLASLt scratch
 constexpr int kMaxBlockGateCh = 32;
 
 struct BlockLayout {
@@ -274,7 +180,6 @@ struct BlockLayout {
   size_t rstd;         // f32  [B*T]
   size_t q, k, v, o;   // elem [B*T, Hq*d], [B*T, Hkv*d] x 2, [B*T, Hq*d]
   size_t lse;          // f32  [B, Hq, T]
-  size_t lt;           // cuBLASLt scratch
   size_t fwd_end;
   size_t dO;           // elem [B*T, Hq*d]  gradient of the attention output
   size_t dq, dk, dv;   // elem
@@ -296,7 +201,6 @@ inline BlockLayout block_layout(int B, int T, int Hq, int Hkv, int d, int C) {
   L.v = o; o = align256(o + bt * Hkv * d * es);
   L.o = o; o = align256(o + bt * Hq * d * es);
   L.lse = o; o = align256(o + bt * Hq * sizeof(float));
-  L.lt = o; o += kLtWsBytes;
   L.fwd_end = o;
   L.dO = o; o = align256(o + bt * Hq * d * es);
   L.dq = o; o = align256(o + bt * Hq * d * es);

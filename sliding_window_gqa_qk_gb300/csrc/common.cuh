@@ -297,4 +297,37 @@ struct GateBwdArgs {  // backward of the learned value-embedding gate
   float* gpart_w;      // [gridDim.x][1024]: [h * gch + c] partials of the weight gradient
 };
 
+// ---------------------------------------------------------------------------
+// Projection GEMMs of the block (tc_gemm.cuh in the bf16 library, a SIMT
+// kernel in the fp32 debug library)
+// ---------------------------------------------------------------------------
+enum GemmOut : int {
+  GEMM_OUT_ELEM = 0,      // elem stores (D = A B + beta C, C elem or none)
+  GEMM_OUT_F32 = 1,       // fp32 stores
+  GEMM_OUT_F32_ADD = 2    // fp32 additions into D (K split over CTAs; D zeroed first)
+};
+
+// One GEMM, in row-major terms:
+//   D_j[M][N_j] = sum over K segments s of A_s B_s  (+ beta C_j)
+// A_s: [M][K_s] (a_mn false, row stride lda) or [K_s][M] (a_mn true).
+// B:   [N][K] (b_mn false) or [K][N] (b_mn true), one tensor per K segment
+//      (n_kseg > 1) or per N segment (n_kseg == 1).
+// N segments (outputs) other than the last are multiples of 128 long, all
+// multiples of 8; K segments other than the last multiples of 64. A, B and
+// C are elem; D is elem (GEMM_OUT_ELEM) or fp32.
+struct GemmCall {
+  int M = 0;
+  bool a_mn = false, b_mn = false;
+  int n_kseg = 1;
+  struct { const void* A; long long lda; int K; } kseg[3] = {};
+  struct { const void* B; long long ldb; } bseg[3] = {};
+  int n_nseg = 1;
+  struct { int N; void* D; long long ldd; const void* C; long long ldc; } nseg[3] = {};
+  int out = GEMM_OUT_ELEM;
+  float beta = 0.f;
+  int split = 1;           // requested K splits (fp32 outputs)
+  uint32_t* status = nullptr;
+  uint64_t wait_limit_ns = 2000000000ull;
+};
+
 }  // namespace swa

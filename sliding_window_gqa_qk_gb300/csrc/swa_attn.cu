@@ -125,6 +125,9 @@ swa_status begin(Call& c, const swa_params* p, void* workspace, size_t ws_bytes,
 
 bool tensor_ok(const void* ptr) { return ptr != nullptr && aligned(ptr, 16); }
 
+// Device status word in a workspace header.
+uint32_t* at_status(uint8_t* ws) { return reinterpret_cast<uint32_t*>(ws); }
+
 swa_status launched() {
   return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
@@ -577,26 +580,37 @@ swa_status block_fwd_impl(const swa_params* p, const swa_extras* ex, const swa_b
   blk::prenorm_fwd_kernel<<<blk::prenorm_grid(b.rows), blk::kPnWarps * 32, 0, b.st>>>(
       static_cast<const elem_t*>(x), xn, reinterpret_cast<float*>(ws + b.L.rstd), b.rows, C, p->eps);
   if ((s = launched()) != SWA_OK) return s;
-  void* lt = ws + b.L.lt;
-  // q / k / v rows = xn rows times w^T: column-major D[n_out x rows] = W^T-stored (C x n_out)^T xn
+  uint32_t* status = at_status(ws);
+  // q, k, v = xn w^T: A = xn [rows][C], B = the weights [out][C] (K-major),
+  // one launch with an output per projection where every head block of the
+  // kv projections is a multiple of 128 columns long, else one per projection
   const void* wmat[3] = {w->wq, w->wk, w->wv};
   const size_t dst[3] = {b.L.q, b.L.k, b.L.v};
   const int nout[3] = {nq, nkv, nkv};
-  for (int i = 0; i < 3; ++i) {
-    blk::Gemm g;
-    g.ta = true; g.tb = false; g.m = nout[i]; g.n = rows; g.k = C;
-    g.A = wmat[i]; g.lda = C; g.B = xn; g.ldb = C; g.D = ws + dst[i]; g.ldd = nout[i];
-    if ((s = blk::gemm(g, lt, blk::kLtWsBytes, b.st)) != SWA_OK) return s;
+  const bool fused = nq % 128 == 0 && nkv % 128 == 0;
+  for (int i = 0; i < (fused ? 1 : 3); ++i) {
+    GemmCall g;
+    g.M = rows; g.status = status;
+    g.kseg[0] = {xn, C, C};
+    g.n_nseg = fused ? 3 : 1;
+    for (int j = 0; j < g.n_nseg; ++j) {
+      const int t = fused ? j : i;
+      g.bseg[j] = {wmat[t], C};
+      g.nseg[j] = {nout[t], ws + dst[t], nout[t], nullptr, 0};
+    }
+    if ((s = blk::run_gemm(g, b.st)) != SWA_OK) return s;
   }
   s = fwd_impl(p, b.exp, ws + b.L.q, ws + b.L.k, ws + b.L.v, gq, gk, ve, tok, nullptr, ws + b.L.o,
                reinterpret_cast<float*>(ws + b.L.lse), ws, b.L.attn_bytes, 0, stream, true);
   if (s != SWA_OK) return s;
-  // out = x + o wo^T
-  blk::Gemm g;
-  g.ta = true; g.tb = false; g.m = C; g.n = rows; g.k = nq;
-  g.A = w->wo; g.lda = nq; g.B = ws + b.L.o; g.ldb = nq;
-  g.beta = 1.f; g.C = x; g.D = out; g.ldd = C;
-  return blk::gemm(g, lt, blk::kLtWsBytes, b.st);
+  // out = x + o wo^T: A = o [rows][nq], B = wo [C][nq] (K-major), C = x
+  GemmCall g;
+  g.M = rows; g.status = status;
+  g.kseg[0] = {ws + b.L.o, nq, nq};
+  g.bseg[0] = {w->wo, nq};
+  g.nseg[0] = {C, out, C, x, C};
+  g.beta = 1.f;
+  return blk::run_gemm(g, b.st);
 }
 
 swa_status block_bwd_impl(const swa_params* p, const swa_extras* ex, const swa_block_weights* w,
@@ -622,21 +636,32 @@ swa_status block_bwd_impl(const swa_params* p, const swa_extras* ex, const swa_b
                     ws + b.L.dv, dgq, dgk, dve, ws, b.L.attn_bytes, 0, stream);
   }
   if ((s = check_device()) != SWA_OK) return s;
-  void* lt = ws + b.L.lt;
+  uint32_t* status = at_status(ws);
   const elem_t* xn = reinterpret_cast<const elem_t*>(ws + b.L.xn);
-  // dwo [C][nq] = dout^T o: column-major (nq x C) = o (nq x rows) dout^T
+  // K = B*T GEMMs (the weight gradients) split K over about one wave of CTAs
+  auto splits = [&](int m, int n) {
+    const int tiles = ((m + 127) / 128) * ((n + 255) / 256);
+    const int k = num_sms() / tiles;
+    return k < 1 ? 1 : k;
+  };
+  // dwo [C][nq] = dout^T o: A = dout as [rows][C] (M-major), B = o [rows][nq] (N-major)
   if (dwo != nullptr) {
-    blk::Gemm g;
-    g.ta = false; g.tb = true; g.m = nq; g.n = C; g.k = rows;
-    g.A = ws + b.L.o; g.lda = nq; g.B = dout; g.ldb = C; g.D = dwo; g.dt = CUDA_R_32F; g.ldd = nq;
-    if ((s = blk::gemm(g, lt, blk::kLtWsBytes, b.st)) != SWA_OK) return s;
+    GemmCall g;
+    g.M = C; g.a_mn = true; g.b_mn = true; g.status = status;
+    g.kseg[0] = {dout, C, rows};
+    g.bseg[0] = {ws + b.L.o, nq};
+    g.nseg[0] = {nq, dwo, nq, nullptr, 0};
+    g.out = GEMM_OUT_F32; g.split = splits(C, nq);
+    if ((s = blk::run_gemm(g, b.st)) != SWA_OK) return s;
   }
-  // gradient of the attention output: dO rows = dout rows times wo
+  // gradient of the attention output: dO = dout wo, B = wo [C][nq] (N-major)
   {
-    blk::Gemm g;
-    g.ta = false; g.tb = false; g.m = nq; g.n = rows; g.k = C;
-    g.A = w->wo; g.lda = nq; g.B = dout; g.ldb = C; g.D = ws + b.L.dO; g.ldd = nq;
-    if ((s = blk::gemm(g, lt, blk::kLtWsBytes, b.st)) != SWA_OK) return s;
+    GemmCall g;
+    g.M = rows; g.b_mn = true; g.status = status;
+    g.kseg[0] = {dout, C, C};
+    g.bseg[0] = {w->wo, nq};
+    g.nseg[0] = {nq, ws + b.L.dO, nq, nullptr, 0};
+    if ((s = blk::run_gemm(g, b.st)) != SWA_OK) return s;
   }
   s = bwd_impl(p, b.exp, ws + b.L.q, ws + b.L.k, ws + b.L.v, gq, gk, ve, tok, nullptr, ws + b.L.o,
                reinterpret_cast<const float*>(ws + b.L.lse), ws + b.L.dO, ws + b.L.dq, ws + b.L.dk,
@@ -646,21 +671,30 @@ swa_status block_bwd_impl(const swa_params* p, const swa_extras* ex, const swa_b
   const size_t grad[3] = {b.L.dq, b.L.dk, b.L.dv};
   const int nout[3] = {nq, nkv, nkv};
   float* dw[3] = {dwq, dwk, dwv};
-  float* dxn = reinterpret_cast<float*>(ws + b.L.dxn);
   for (int i = 0; i < 3; ++i) {
-    // dw [n_out][C] = grad^T xn: column-major (C x n_out) = xn (C x rows) grad^T
-    if (dw[i] != nullptr) {
-      blk::Gemm g;
-      g.ta = false; g.tb = true; g.m = C; g.n = nout[i]; g.k = rows;
-      g.A = xn; g.lda = C; g.B = ws + grad[i]; g.ldb = nout[i]; g.D = dw[i]; g.dt = CUDA_R_32F; g.ldd = C;
-      if ((s = blk::gemm(g, lt, blk::kLtWsBytes, b.st)) != SWA_OK) return s;
+    // dw [n_out][C] = grad^T xn: A = grad as [rows][n_out] (M-major), B = xn [rows][C] (N-major)
+    if (dw[i] == nullptr) continue;
+    GemmCall g;
+    g.M = nout[i]; g.a_mn = true; g.b_mn = true; g.status = status;
+    g.kseg[0] = {ws + grad[i], nout[i], rows};
+    g.bseg[0] = {xn, C};
+    g.nseg[0] = {C, dw[i], C, nullptr, 0};
+    g.out = GEMM_OUT_F32; g.split = splits(nout[i], C);
+    if ((s = blk::run_gemm(g, b.st)) != SWA_OK) return s;
+  }
+  // dxn = dq wq + dk wk + dv wv: three K segments, B = the weights [n_out][C] (N-major)
+  float* dxn = reinterpret_cast<float*>(ws + b.L.dxn);
+  {
+    GemmCall g;
+    g.M = rows; g.b_mn = true; g.status = status;
+    g.n_kseg = 3;
+    for (int i = 0; i < 3; ++i) {
+      g.kseg[i] = {ws + grad[i], nout[i], nout[i]};
+      g.bseg[i] = {wmat[i], C};
     }
-    // dxn rows += grad rows times w
-    blk::Gemm g;
-    g.ta = false; g.tb = false; g.m = C; g.n = rows; g.k = nout[i];
-    g.A = wmat[i]; g.lda = C; g.B = ws + grad[i]; g.ldb = nout[i];
-    g.beta = i == 0 ? 0.f : 1.f; g.D = dxn; g.dt = CUDA_R_32F; g.ldd = C;
-    if ((s = blk::gemm(g, lt, blk::kLtWsBytes, b.st)) != SWA_OK) return s;
+    g.nseg[0] = {C, dxn, C, nullptr, 0};
+    g.out = GEMM_OUT_F32;
+    if ((s = blk::run_gemm(g, b.st)) != SWA_OK) return s;
   }
   // the gate applies on value-embedding calls only (as in the attention calls)
   const bool gate = b.exp != nullptr && b.ex.gate_w != nullptr && ve != nullptr;

@@ -27,10 +27,16 @@ constexpr int kPnEpl = 16 / static_cast<int>(sizeof(elem_t));  // elements per 1
 constexpr int kPnWarps = 8;
 constexpr int kPnBlocksPerSm = 4;
 
+// With gate_w (the learned value-embedding gate, on the fused projection
+// path) it also writes gate[r, h] = 2 sigmoid(<gate_w[h], xn[r, :gch]>) for
+// the Hkv kv heads, from the stored (rounded) xn: the value the prologue
+// kernel computes otherwise. gch <= 32.
 __global__ void __launch_bounds__(kPnWarps * 32) prenorm_fwd_kernel(const elem_t* __restrict__ x,
                                                                     elem_t* __restrict__ xn,
                                                                     float* __restrict__ rstd,
-                                                                    long long rows, int C, float eps) {
+                                                                    long long rows, int C, float eps,
+                                                                    const float* __restrict__ gate_w, int gch,
+                                                                    int Hkv, float* __restrict__ gate_out) {
   const int lane = threadIdx.x & 31;
   for (long long r = grid_warp(); r < rows; r += grid_warps()) {
     const elem_t* xr = x + r * C;
@@ -44,14 +50,31 @@ __global__ void __launch_bounds__(kPnWarps * 32) prenorm_fwd_kernel(const elem_t
     ss = row_sum<32>(ss);
     const float rs = rsqrtf(ss / C + eps);
     elem_t* yr = xn + r * C;
+    float g0[kPnEpl];   // this lane's first stored values (the gate reads channels < gch)
+#pragma unroll
+    for (int i = 0; i < kPnEpl; ++i) g0[i] = 0.f;
     for (int c = lane * kPnEpl; c < C; c += 32 * kPnEpl) {
       float f[kPnEpl];
       unpack16(ld16(xr + c), f);
 #pragma unroll
       for (int i = 0; i < kPnEpl; ++i) f[i] *= rs;
-      st16(yr + c, pack16(f));
+      const uint4 u = pack16(f);
+      st16(yr + c, u);
+      if (c < 32) unpack16(u, g0);
     }
     if (lane == 0) rstd[r] = rs;
+    if (gate_w != nullptr) {
+      for (int h = 0; h < Hkv; ++h) {
+        float z = 0.f;
+#pragma unroll
+        for (int i = 0; i < kPnEpl; ++i) {
+          const int c = lane * kPnEpl + i;
+          if (c < gch) z = fmaf(gate_w[h * gch + c], g0[i], z);
+        }
+        z = row_sum<32>(z);
+        if (lane == 0) gate_out[r * Hkv + h] = 2.0f / (1.0f + expf(-z));
+      }
+    }
   }
 }
 

@@ -328,6 +328,23 @@ struct GemmCall {
   int split = 1;           // requested K splits (fp32 outputs)
   uint32_t* status = nullptr;
   uint64_t wait_limit_ns = 2000000000ull;
+  // The q, k, v projection with the attention's prologue in its epilogue
+  // (bf16 library, head dim 128, T a multiple of 32, three N segments q, k,
+  // v): besides the projections (D of the segments), qn and kn = the
+  // QK-norm of the (rotated) q and k rows and their inverse RMS, head-major,
+  // and on value-embedding layers v_eff = v + ve_scale * gate * VE[tok],
+  // head-major, exactly as the prologue kernel writes them.
+  struct {
+    bool on;
+    int T, Hq, Hkv, vocab;
+    float eps, ve_scale;
+    const float* gq; const float* gk;        // [128] or NULL (unit)
+    const float* rcos; const float* rsin;    // [>= T][64] or NULL (no rotary)
+    void* qn; void* kn; void* veff;          // [B, H, T, 128]
+    float* rstd_q; float* rstd_k;            // [B, H, T]
+    const void* ve; const int32_t* tok;      // VE table [vocab][Hkv * 128] or NULL
+    const float* gate;                       // [B, T, Hkv] or NULL (1)
+  } qkv = {};
 };
 
 }  // namespace swa

@@ -577,10 +577,22 @@ swa_status block_fwd_impl(const swa_params* p, const swa_extras* ex, const swa_b
   uint8_t* ws = b.ws;
   const int C = b.C, nq = b.Hq * b.d, nkv = b.Hkv * b.d, rows = static_cast<int>(b.rows);
   elem_t* xn = reinterpret_cast<elem_t*>(ws + b.L.xn);
-  blk::prenorm_fwd_kernel<<<blk::prenorm_grid(b.rows), blk::kPnWarps * 32, 0, b.st>>>(
-      static_cast<const elem_t*>(x), xn, reinterpret_cast<float*>(ws + b.L.rstd), b.rows, C, p->eps);
-  if ((s = launched()) != SWA_OK) return s;
   uint32_t* status = at_status(ws);
+  const WsLayout A = ws_layout(b.B, b.T, b.Hq, b.Hkv, b.d);   // the attention's workspace, first in the block's
+  // The q, k, v projection with the attention's prologue (QK-norm, rotary,
+  // value-embedding mix) in its epilogue: bf16 library, head dim 128, T a
+  // multiple of 32. Elsewhere the projection, then the prologue kernel.
+#if defined(SWA_ELEM_FP32)
+  const bool fold = false;
+#else
+  const bool fold = b.d == 128 && b.T % 32 == 0;
+#endif
+  const bool learned = b.exp != nullptr && b.ex.gate_w != nullptr && ve != nullptr;
+  float* gate_vals = reinterpret_cast<float*>(ws + A.gate);
+  blk::prenorm_fwd_kernel<<<blk::prenorm_grid(b.rows), blk::kPnWarps * 32, 0, b.st>>>(
+      static_cast<const elem_t*>(x), xn, reinterpret_cast<float*>(ws + b.L.rstd), b.rows, C, p->eps,
+      fold && learned ? b.ex.gate_w : nullptr, b.ex.gate_ch, b.Hkv, gate_vals);
+  if ((s = launched()) != SWA_OK) return s;
   // q, k, v = xn w^T: A = xn [rows][C], B = the weights [out][C] (K-major),
   // one launch with an output per projection where every head block of the
   // kv projections is a multiple of 128 columns long, else one per projection
@@ -598,10 +610,22 @@ swa_status block_fwd_impl(const swa_params* p, const swa_extras* ex, const swa_b
       g.bseg[j] = {wmat[t], C};
       g.nseg[j] = {nout[t], ws + dst[t], nout[t], nullptr, 0};
     }
+    if (fold) {
+      auto& e = g.qkv;
+      e.on = true;
+      e.T = b.T; e.Hq = b.Hq; e.Hkv = b.Hkv; e.vocab = p->vocab; e.eps = p->eps; e.ve_scale = p->ve_scale;
+      e.gq = gq; e.gk = gk;
+      e.rcos = b.exp != nullptr ? b.ex.rope_cos : nullptr;
+      e.rsin = b.exp != nullptr ? b.ex.rope_sin : nullptr;
+      e.qn = ws + A.qn; e.kn = ws + A.kn; e.veff = ws + A.veff;
+      e.rstd_q = reinterpret_cast<float*>(ws + A.rstd_q); e.rstd_k = reinterpret_cast<float*>(ws + A.rstd_k);
+      e.ve = ve; e.tok = tok; e.gate = learned ? gate_vals : nullptr;
+    }
     if ((s = blk::run_gemm(g, b.st)) != SWA_OK) return s;
   }
   s = fwd_impl(p, b.exp, ws + b.L.q, ws + b.L.k, ws + b.L.v, gq, gk, ve, tok, nullptr, ws + b.L.o,
-               reinterpret_cast<float*>(ws + b.L.lse), ws, b.L.attn_bytes, 0, stream, true);
+               reinterpret_cast<float*>(ws + b.L.lse), ws, b.L.attn_bytes, fold ? SWA_REUSE_PROLOGUE : 0, stream,
+               true);
   if (s != SWA_OK) return s;
   // out = x + o wo^T: A = o [rows][nq], B = wo [C][nq] (K-major), C = x
   GemmCall g;

@@ -69,6 +69,16 @@ struct GmNSeg {
   int n0, n;
 };
 
+// The q, k, v projection's fused prologue (GemmCall::qkv).
+struct GmQkv {
+  int T, Hq, Hkv, vocab;
+  float eps, ve_scale;
+  const float* gq; const float* gk;
+  const float* rcos; const float* rsin;
+  float* rstd_q; float* rstd_k;
+  const elem_t* ve; const int32_t* tok; const float* gate;
+};
+
 struct GmParams {
   int M, N;
   int n_kseg;               // 1..3; segment s has kt_end[s] - kt_begin[s] K steps (A map s, B map s)
@@ -81,6 +91,7 @@ struct GmParams {
   int n_mt, n_nt, n_split, kt_per_split;
   uint32_t* status;
   uint64_t wait_limit_ns;
+  GmQkv qkv;
 };
 
 // N segment holding product column n (-1: none; segments are 128-aligned
@@ -92,14 +103,15 @@ __device__ __forceinline__ int gm_nseg_of(const GmParams& p, int n) {
   return s;
 }
 
-template <bool AMN, bool BMN>
+template <bool AMN, bool BMN, bool QKV>
 __global__ void __launch_bounds__(kGmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
                    const __grid_constant__ CUtensorMap tmD0, const __grid_constant__ CUtensorMap tmD1,
                    const __grid_constant__ CUtensorMap tmD2, const __grid_constant__ CUtensorMap tmC,
-                   const GmParams prm) {
+                   const __grid_constant__ CUtensorMap tmE0, const __grid_constant__ CUtensorMap tmE1,
+                   const __grid_constant__ CUtensorMap tmE2, const GmParams prm) {
   using S = GmSmem;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -244,7 +256,165 @@ __global__ void __launch_bounds__(kGmThreads, 1)
       umma_commit(bar(GM_FINAL));
       mbar_wait_drain(bar(GM_FINAL), 0, kDrainLimitNs);
     }
-  } else if (warp >= kGmEpiWarp0) {
+  } else if (QKV && warp >= kGmEpiWarp0) {
+    // -------- q, k, v epilogue: thread = row; one 128-column half = one head --------
+    // Per head row: the projection rounded to bf16 (stored as the raw q, k
+    // or v the backward reads); for q and k the rotary turn (pairs c, c + 64)
+    // and the QK-norm of the rounded values, for v on value-embedding layers
+    // v + ve_scale * gate * VE[tok]: the prologue kernel's arithmetic.
+    const GmQkv& e = prm.qkv;
+    const int q = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const CUtensorMap* mD[3] = {&tmD0, &tmD1, &tmD2};
+    const CUtensorMap* mE[3] = {&tmE0, &tmE1, &tmE2};
+    if (lane == 0)
+      for (int i = 0; i < 3; ++i) {
+        tma_prefetch_desc(mD[i]);
+        tma_prefetch_desc(mE[i]);
+      }
+    int cnt = 0;
+    // 32 rows x 128 bytes (32 words per row) through a staging buffer and
+    // one TMA store
+    auto stage_store = [&](const uint32_t* w32, const CUtensorMap* map, int x, int y) {
+      const int b = cnt & 1;
+      const uint32_t stg = sbase + S::oStg + static_cast<uint32_t>((q * 2 + b) * S::kStg);
+      if (lane == 0 && cnt >= 2) bulk_wait_group_read<1>();
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        st_shared_v4(stg + lane * 128 + ((j ^ (lane & 7)) << 4), w32[4 * j], w32[4 * j + 1], w32[4 * j + 2],
+                     w32[4 * j + 3]);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(map, stg, x, y);
+        bulk_commit_group();
+      }
+      ++cnt;
+    };
+    auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
+    auto hi = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
+    const bool rope = e.rcos != nullptr;
+    int tcount = 0;
+    for (int w = static_cast<int>(blockIdx.x); w < n_items; w += static_cast<int>(gridDim.x), ++tcount) {
+      int mt, nt, kb, ke;
+      decode(w, mt, nt, kb, ke);
+      const int buf = tcount & 1;
+      const int row0 = mt * kGmM + q * 32;     // the warp's 32 rows: one batch element (T % 32 == 0)
+      const int m = row0 + lane;
+      const bool valid = m < prm.M;
+      const int bb = row0 / e.T, t0 = row0 - bb * e.T, t = t0 + lane;
+      const int n0 = nt * kGmN;
+      if (!mbar_wait_warp(bar(GM_ACCFULL + buf), (tcount >> 1) & 1, ctl)) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const int n = n0 + 128 * h;
+        const int sg = gm_nseg_of(prm, n);
+        if (sg < 0) break;   // uniform
+        const int nl = n - prm.nseg[sg].n0;
+        const int head = nl >> 7;
+        // the VE-table row of a v head, loaded before the accumulator is read
+        uint4 er[16];
+        int tok = -1;
+        bool tok_ok = false;
+        if (sg == 2 && e.ve != nullptr) {
+          tok = valid ? e.tok[m] : -1;
+          tok_ok = tok >= 0 && tok < e.vocab;
+          const elem_t* vrow = e.ve + (static_cast<long long>(tok_ok ? tok : 0) * e.Hkv + head) * 128;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) er[j] = tok_ok ? ld16(vrow + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        uint32_t pk[64];     // the row's 128 values rounded to bf16, in pairs
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t v[32];
+          tmem_ld32(tmem + static_cast<uint32_t>(buf * kGmN + 128 * h + 32 * j) + lane_off, v);
+          tmem_wait_ld(v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[16 * j + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        }
+        if (h == 1 || gm_nseg_of(prm, n0 + 128) < 0) {
+          // every column of the tile is in registers: the accumulator is free
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(GM_ACCEMPTY + buf));
+        }
+        stage_store(pk, mD[sg], nl, row0);
+        stage_store(pk + 32, mD[sg], nl + 64, row0);
+        if (sg < 2) {
+          const float* g = sg == 0 ? e.gq : e.gk;
+          const int H = sg == 0 ? e.Hq : e.Hkv;
+          // the rotated row (pairs c, c + 64) in fp32, from the rounded values;
+          // the angles 16 columns at a time
+          float r[128];
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            r[c] = (c & 1) ? hi(pk[c / 2]) : lo(pk[c / 2]);
+            r[64 + c] = (c & 1) ? hi(pk[32 + c / 2]) : lo(pk[32 + c / 2]);
+          }
+          if (rope) {
+            const float* cs = e.rcos + static_cast<long long>(valid ? t : 0) * 64;
+            const float* sn = e.rsin + static_cast<long long>(valid ? t : 0) * 64;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float4 c4[4], s4[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                c4[j] = reinterpret_cast<const float4*>(cs + 16 * k)[j];
+                s4[j] = reinterpret_cast<const float4*>(sn + 16 * k)[j];
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int c = 16 * k + j;
+                const float co = j % 4 == 0 ? c4[j / 4].x : j % 4 == 1 ? c4[j / 4].y : j % 4 == 2 ? c4[j / 4].z : c4[j / 4].w;
+                const float si = j % 4 == 0 ? s4[j / 4].x : j % 4 == 1 ? s4[j / 4].y : j % 4 == 2 ? s4[j / 4].z : s4[j / 4].w;
+                const float x = r[c], y = r[64 + c];
+                r[c] = fmaf(x, co, y * si);
+                r[64 + c] = fmaf(y, co, -x * si);
+              }
+            }
+          }
+          float ss = 0.f;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) ss = fmaf(r[c], r[c], ss);
+          const float rstd = rsqrtf(ss / 128.f + e.eps);
+          if (valid) (sg == 0 ? e.rstd_q : e.rstd_k)[(static_cast<long long>(bb) * H + head) * e.T + t] = rstd;
+          const int yrow = (bb * H + head) * e.T + t0;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t o[32];   // channels 64 half .. 64 half + 63 of the normed row
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+              const float2 gg = g ? *reinterpret_cast<const float2*>(g + 64 * half + c) : make_float2(1.f, 1.f);
+              o[c / 2] = pack_bf16x2(r[64 * half + c] * rstd * gg.x, r[64 * half + c + 1] * rstd * gg.y);
+            }
+            stage_store(o, mE[sg], 64 * half, yrow);
+          }
+        } else if (e.ve != nullptr) {
+          if (valid && !tok_ok) atomicOr(prm.status, DEV_ERR_TOKEN);   // contributes nothing, reported
+          const float sc = tok_ok ? e.ve_scale * (e.gate ? e.gate[static_cast<long long>(m) * e.Hkv + head] : 1.f) : 0.f;
+          const int yrow = (bb * e.Hkv + head) * e.T + t0;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t o[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float ev[8];
+              unpack16(er[8 * half + j], ev);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint32_t w = pk[32 * half + 4 * j + i];
+                o[4 * j + i] = pack_bf16x2(fmaf(sc, ev[2 * i], lo(w)), fmaf(sc, ev[2 * i + 1], hi(w)));
+              }
+            }
+            stage_store(o, mE[2], 64 * half, yrow);
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_group_all();   // every store has completed
+  } else if (!QKV && warp >= kGmEpiWarp0) {
     // ---------------- epilogue: thread = row (TMEM lane) ----------------
     const int q = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
@@ -442,19 +612,33 @@ inline swa_status launch_gemm(const GemmCall& g, cudaStream_t st) {
   } else {
     mc = md[0];
   }
+  // the fused prologue's head-major outputs: [B * H * T][128] row views
+  CUtensorMap me[3] = {md[0], md[0], md[0]};
+  const auto& e = g.qkv;
+  if (e.on) {
+    if (g.n_nseg != 3 || g.n_kseg != 1 || g.a_mn || g.b_mn || p.out != GEMM_OUT_ELEM || p.has_c || e.T % 32 != 0 ||
+        g.M % e.T != 0 || g.nseg[0].N != e.Hq * 128 || g.nseg[1].N != e.Hkv * 128 || g.nseg[2].N != e.Hkv * 128)
+      return SWA_ERR_INVALID_ARG;
+    const long long rq = static_cast<long long>(g.M) * e.Hq, rk = static_cast<long long>(g.M) * e.Hkv;
+    if (!map_2d(&me[0], e.qn, 128, rq, 128, 32) || !map_2d(&me[1], e.kn, 128, rk, 128, 32)) return SWA_ERR_CUDA;
+    if (e.ve != nullptr && !map_2d(&me[2], e.veff, 128, rk, 128, 32)) return SWA_ERR_CUDA;
+    p.qkv = GmQkv{e.T, e.Hq, e.Hkv, e.vocab, e.eps, e.ve_scale, e.gq, e.gk, e.rcos, e.rsin, e.rstd_q, e.rstd_k,
+                  static_cast<const elem_t*>(e.ve), e.tok, e.gate};
+  }
   const int items = p.n_mt * p.n_nt * p.n_split;
   const int grid = items < num_sms() ? items : num_sms();
   auto launch = [&](auto kern) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes) != cudaSuccess)
       return SWA_ERR_CUDA;
     kern<<<grid, kGmThreads, S::kBytes, st>>>(ma[0], ma[1], ma[2], mb[0], mb[1], mb[2], md[0], md[1], md[2],
-                                              mc, p);
+                                              mc, me[0], me[1], me[2], p);
     return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
   };
-  if (!g.a_mn && !g.b_mn) return launch(gemm_tc_kernel<false, false>);
-  if (!g.a_mn && g.b_mn) return launch(gemm_tc_kernel<false, true>);
-  if (g.a_mn && g.b_mn) return launch(gemm_tc_kernel<true, true>);
-  return launch(gemm_tc_kernel<true, false>);
+  if (e.on) return launch(gemm_tc_kernel<false, false, true>);
+  if (!g.a_mn && !g.b_mn) return launch(gemm_tc_kernel<false, false, false>);
+  if (!g.a_mn && g.b_mn) return launch(gemm_tc_kernel<false, true, false>);
+  if (g.a_mn && g.b_mn) return launch(gemm_tc_kernel<true, true, false>);
+  return launch(gemm_tc_kernel<true, false, false>);
 }
 
 }  // namespace tc

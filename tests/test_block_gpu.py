@@ -27,6 +27,11 @@ CASES = {
                              256, None, False),
     "group3_ragged_unit_gains": (Problem(B=1, T=131, Hq=3, Hkv=1, d=128, window=40, ve=True,
                                          vocab=50), 136, 8, False),
+    # head dim 128 and T a multiple of 32: the bf16 library folds the
+    # attention's prologue into the q, k, v projection (rows 288 = 2.25 tiles)
+    "fold_gqa_ve_gate_rope": (Problem(B=3, T=96, Hq=4, Hkv=2, d=128, window=40, gain_std=0.1, ve=True,
+                                      vocab=61), 200, 32, True),
+    "fold_mha_plain": (Problem(B=2, T=64, Hq=2, Hkv=2, d=128, window=-1, gain_std=0.1), 256, None, False),
 }
 
 

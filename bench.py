@@ -53,10 +53,10 @@ WORKLOAD = "8-layer SSSL stack (B=16, T=2048, Hq=6, Hkv=3, d=128, W=1024 on S la
 # the kernel's sources have changed since, the bench line reports these as
 # null.
 NCU_CAPTURE = {
-    "source_sha": "84243b23cd7d401b",
-    "traffic_bytes": 432_097_024,
-    "tensor_pipe_pct": 36.7,
-    "dram_gbs": 1775.8,
+    "source_sha": "89e502e3067b5c27",
+    "traffic_bytes": 431_332_864,
+    "tensor_pipe_pct": 38.0,
+    "dram_gbs": 1815.1,
     "summary": "profiles/bwd_tc128_s_layer.md (S-layer launch)",
 }
 KERNEL_SOURCES = ("tc_bwd128.cuh", "tc_bwd.cuh", "tc_fwd.cuh", "ptx.cuh", "common.cuh")

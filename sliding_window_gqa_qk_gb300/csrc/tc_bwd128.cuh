@@ -9,8 +9,8 @@
 //   P^T  = scale exp2(S^T c - LSE log2 e)     -> bf16 into S^T's columns
 //   dS^T = P^T (dP^T - D)                     -> bf16 to shared memory
 //   dV  += P^T dO_i           (A operand from TMEM)
-//   dQ_i^T = K^T dS^T         (into dP^T's columns)
-//   dK  += dS^T Q_i           (A operand dS^T from shared memory)
+//   dQ_i^T = K^T dS^T         (into dP^T's columns; B operand dS^T from shared memory)
+//   dK  += dS^T Q_i           (A operand dS^T from TMEM, beside P^T)
 // P^T and dS^T carry the softmax scale, so dK and dQ come out final and dV
 // is divided by it in the epilogue.
 //
@@ -27,8 +27,8 @@
 // dP^T(i+1) waits for that drain (it reuses the columns).
 // dQ^T(i) goes from TMEM to shared memory in four [32 queries][128] fp32
 // boxes, two in the dedicated staging buffer (free once the previous step's
-// boxes there were read) and two in the dS^T buffer (free once dK(i) has read
-// it; dS^T(i+1) waits for the reducer), and from there into the fp32 dQ
+// boxes there were read) and two in the dS^T buffer (free once dQ^T(i), its
+// only reader, completed; dS^T(i+1) waits for the reducer), and from there into the fp32 dQ
 // accumulator by TMA bulk reductions. Those run at the rate the L2 accepts fp32 adds (about 6.6 TB/s
 // over the whole GPU, about 21 bytes per clock per SM), 64 KB per step.
 // Registers (setmaxnreg; 512 x 128 at launch): element-wise warpgroups 176
@@ -88,8 +88,7 @@ enum {
   B2_XFREE = 16,     // the dQ boxes in the staging buffer were read
   B2_DSFREE = 17,    // the dQ boxes staged in the dS^T buffer were read
   B2_FINAL = 18,
-  B2_DKDONE = 19,    // the dK product of the step completed (dQ-first order)
-  B2_COUNT = 20
+  B2_COUNT = 19
 };
 
 // Visible query columns [clo, chi] of key row j among the 64 queries
@@ -189,7 +188,6 @@ __global__ void __launch_bounds__(kB2Threads, 1)
     mbar_init(bar(B2_XFREE), 1);
     mbar_init(bar(B2_DSFREE), 1);
     mbar_init(bar(B2_FINAL), 1);
-    mbar_init(bar(B2_DKDONE), 1);
     fence_mbar_init();
   }
   if (warp == kB2MmaWarp) {
@@ -300,7 +298,6 @@ __global__ void __launch_bounds__(kB2Threads, 1)
       const uint64_t dQmn0 = sdesc_sw128(sbase + C::oQ, C::kHalf, 1024);
       const uint64_t dGmn = sdesc_sw128(sbase + C::oG, C::kHalf, 1024);
       const uint64_t dSmn = sdesc_sw128(sbase + C::oS, C::kHalf, 1024);
-      const uint64_t dSk = sdesc_sw128(sbase + C::oS, 16, 1024);
       // K-major operands: K step kk is 32 bytes into a row of its 64-column region.
       auto issue_S = [&](int i) {    // S^T = K Q_i^T
         const uint64_t qd = sdesc_add(dQk0, (i & 1) * C::kTile);
@@ -337,12 +334,12 @@ __global__ void __launch_bounds__(kB2Threads, 1)
         });
         umma_commit(bar(B2_DQFULL));
         const uint64_t qd = sdesc_add(dQmn0, (i & 1) * C::kTile);
+        // A = dS^T from TMEM (columns 32-63 of each warpgroup's 64 in S^T's region)
         static_for<0, 8>([&](auto kc) {
           constexpr int kk = decltype(kc)::value;
-          constexpr uint32_t aoff = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;
-          umma_ss_imm<idKV, aoff, kk * 128>(tmem + cDK, dSk, qd, (i > 0 || kk > 0), 1u);
+          umma_ts_imm<idKV, 32 + (kk >> 2) * 64 + (kk & 3) * 8, kk * 128>(tmem + cDK, tmem + cS, qd,
+                                                                            (i > 0 || kk > 0), 1u);
         });
-        umma_commit(bar(B2_DKDONE));
         umma_commit(bar(B2_QEMPTY + (i & 1)));   // the last reader of the Q stage
       };
       bool ok = mbar_wait(bar(B2_KV), 0, ctl) && mbar_wait(bar(B2_QFULL), 0, ctl);
@@ -384,8 +381,8 @@ __global__ void __launch_bounds__(kB2Threads, 1)
   } else if (warp >= 8) {
     // --------- drain warpgroup: dQ^T(i) (lane = head-dim index) -> staged boxes ---------
     // Boxes [32 queries][128] fp32: queries 64X .. 64X + 31 in half X of the
-    // dS^T buffer (free once dK(i), its last reader, completed; the next dS^T
-    // waits until the reducer has read them), 64X + 32 .. 64X + 63 in half X
+    // dS^T buffer (free once dQ^T(i), its only reader, completed: DQFULL; the
+    // next dS^T waits until the reducer has read them), 64X + 32 .. 64X + 63 in half X
     // of the staging buffer (free once the reducer read the previous step's
     // boxes there). TMEM is handed back (DQFREE) as soon as every column has
     // been read. The Q stages hold no dQ, so a Q stage is reloaded as soon as
@@ -414,7 +411,6 @@ __global__ void __launch_bounds__(kB2Threads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B2_DQFREE));
-      if (!mbar_wait_warp(bar(B2_DKDONE), i & 1, ctl)) break;
 #pragma unroll
       for (int X = 0; X < 2; ++X)
 #pragma unroll
@@ -516,6 +512,9 @@ __global__ void __launch_bounds__(kB2Threads, 1)
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch)
         st_sw128_chunk(sSx, kBK, t, ch, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+      // and into TMEM beside P^T: the A operand of dK
+      tmem_st32(tS + 32, pk);
+      tmem_wait_st();
       fence_async_smem();
       tc_fence_before();
       __syncwarp();

@@ -182,19 +182,19 @@ class ClockSampler:
 # Oracle leg (CPU baseline and --impl reference)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(schedule, layers=None, batch=1, kv_heads=1):
-    """Runs the float64 oracle on a slice of the stack's layers: `batch`
-    sequences of T=2048 and `kv_heads` kv heads (2 query heads each).
+def oracle_sample(schedule, layers=None, batch=1, kv_heads=1, Tn=T, G=HQ // HKV, d=D, gain_std=0.1):
+    """Runs the float64 oracle on a slice of a workload's layers: `batch`
+    sequences of Tn positions and `kv_heads` kv heads (G query heads each).
     Returns (seconds, masked FLOPs of the sample, description)."""
     import numpy as np  # noqa: F401
     import oracle
     from sliding_window_gqa_qk_gb300.inputs import as_f64
-    layers = list(range(N_LAYER)) if layers is None else layers
+    layers = list(range(len(schedule))) if layers is None else layers
     total_t, total_f = 0.0, 0
     for li in layers:
         W, ve = schedule[li]
-        p = Problem(B=batch, T=T, Hq=kv_heads * (HQ // HKV), Hkv=kv_heads, d=D, window=W,
-                    gain_std=0.1, ve=ve, vocab=VOCAB)
+        p = Problem(B=batch, T=Tn, Hq=kv_heads * G, Hkv=kv_heads, d=d, window=W,
+                    gain_std=gain_std, ve=ve, vocab=VOCAB)
         x = make_inputs(p, layer=li, seed=4242)
         f = {k: as_f64(t) for k, t in x.items()}
         tok = x["tok"].numpy() if x["tok"] is not None else None
@@ -203,10 +203,10 @@ def oracle_sample(schedule, layers=None, batch=1, kv_heads=1):
         oracle.attention_forward(f["q"], f["k"], f["v"], f["gq"], f["gk"], **kw)
         oracle.attention_backward(f["q"], f["k"], f["v"], f["gq"], f["gk"], f["dO"], **kw)
         total_t += time.perf_counter() - t0
-        ff, fb = flops(batch, T, kv_heads * (HQ // HKV), D, W)
+        ff, fb = flops(batch, Tn, kv_heads * G, d, W)
         total_f += ff + fb
-    desc = (f"float64 oracle fwd+bwd of layers {layers} of the stack on a slice of "
-            f"B={batch}, T={T}, Hq={kv_heads * (HQ // HKV)}, Hkv={kv_heads}, d={D}")
+    desc = (f"float64 oracle fwd+bwd of layers {layers} of the workload on a slice of "
+            f"B={batch}, T={Tn}, Hq={kv_heads * G}, Hkv={kv_heads}, d={d}")
     return total_t, total_f, desc
 
 
@@ -652,11 +652,25 @@ def run_ours(args, rank, world, dev):
     }
     if not args.skip_e2e:
         out["e2e"] = run_e2e(args, stack, world)
-    if rank == 0 and world == 1 and not args.skip_cpu and args.workload == "stack":
-        if args.quick_cpu:
-            t, f, desc = oracle_sample(stack.sched, layers=[0, 3])
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        if args.workload == "stack":
+            if args.quick_cpu:
+                t, f, desc = oracle_sample(stack.sched, layers=[0, 3])
+            else:
+                t, f, desc = oracle_sample(stack.sched, batch=2, kv_heads=HKV)
         else:
-            t, f, desc = oracle_sample(stack.sched, batch=2, kv_heads=HKV)
+            # one sequence and one kv-head group of the workload (the whole
+            # problem for tiny); at T = 16384 its first layer only (the oracle
+            # forms the full T x T logits of every head)
+            g = stack.hq // stack.hkv
+            layers = [0] if stack.T > 4096 else None
+            t = f = 0
+            reps = 0
+            while t < 5.0:   # repeated to at least 5 s for a stable rate
+                dt, df, desc = oracle_sample(stack.sched, layers=layers, Tn=stack.T, G=g, d=stack.d,
+                                             gain_std=head_dim_for(args.workload)[1])
+                t, f, reps = t + dt, f + df, reps + 1
+            desc += f", {reps} time(s)"
         out["cpu_baseline"] = {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s",
                                "cores": cores(), "kind": "oracle", "sample": desc,
                                "seconds": round(t, 2)}

@@ -298,8 +298,9 @@ swa_status swa_attn_fwd_noalloc(const swa_params* p, const void* q, const void* 
  * so their last bits can differ from run to run. The workspace
  * (swa_block_workspace_size) holds the attention's workspace first (so
  * swa_attn_check_status reads the block workspace too),
- * then the forward's saved tensors (xn, q, k, v, o, lse); swa_block_bwd
- * needs the workspace that swa_block_fwd filled for the same inputs.
+ * then the forward's saved tensors (xn, q, k, v, o, lse) and a transposed
+ * copy of the rotary tables; swa_block_bwd needs the workspace that
+ * swa_block_fwd filled for the same inputs.
  */
 typedef struct {
   int C;              /* model width: channels of x                         */

@@ -123,6 +123,31 @@ __global__ void __launch_bounds__(kPnWarps * 32) prenorm_bwd_kernel(
   }
 }
 
+// The rotary tables transposed for the fused q / k epilogue: out[0][c][t] =
+// cos[t][c], out[1][c][t] = sin[t][c] (t < T, c < 64, head dim 128), so that
+// the 32 lanes of a warp (32 consecutive positions) read one column in one
+// 128-byte line. Block (32 positions, table blockIdx.y), 256 threads.
+constexpr int kRtT = 32, kRtHalf = 64;
+__global__ void __launch_bounds__(256) rope_transpose_kernel(const float* __restrict__ rcos,
+                                                             const float* __restrict__ rsin,
+                                                             float* __restrict__ out, int T) {
+  __shared__ float tile[kRtT][kRtHalf + 1];
+  const int t0 = blockIdx.x * kRtT;
+  const float* src = blockIdx.y ? rsin : rcos;
+#pragma unroll
+  for (int r = 0; r < kRtT * kRtHalf / 256; ++r) {
+    const int i = threadIdx.x + 256 * r, tt = i / kRtHalf, c = i % kRtHalf;
+    tile[tt][c] = t0 + tt < T ? src[static_cast<long long>(t0 + tt) * kRtHalf + c] : 0.f;
+  }
+  __syncthreads();
+  float* dst = out + static_cast<long long>(blockIdx.y) * kRtHalf * T;
+#pragma unroll
+  for (int r = 0; r < kRtT * kRtHalf / 256; ++r) {
+    const int i = threadIdx.x + 256 * r, c = i / kRtT, tt = i % kRtT;
+    if (t0 + tt < T) dst[static_cast<long long>(c) * T + t0 + tt] = tile[tt][c];
+  }
+}
+
 inline int prenorm_grid(long long rows) {
   const long long per = (rows + kPnWarps - 1) / kPnWarps;
   const long long cap = static_cast<long long>(num_sms()) * kPnBlocksPerSm;
@@ -203,6 +228,7 @@ struct BlockLayout {
   size_t rstd;         // f32  [B*T]
   size_t q, k, v, o;   // elem [B*T, Hq*d], [B*T, Hkv*d] x 2, [B*T, Hq*d]
   size_t lse;          // f32  [B, Hq, T]
+  size_t rope_t;       // f32  [2][d/2][T]  rotary tables transposed (fused q / k epilogue)
   size_t fwd_end;
   size_t dO;           // elem [B*T, Hq*d]  gradient of the attention output
   size_t dq, dk, dv;   // elem
@@ -224,6 +250,7 @@ inline BlockLayout block_layout(int B, int T, int Hq, int Hkv, int d, int C) {
   L.v = o; o = align256(o + bt * Hkv * d * es);
   L.o = o; o = align256(o + bt * Hq * d * es);
   L.lse = o; o = align256(o + bt * Hq * sizeof(float));
+  L.rope_t = o; o = align256(o + static_cast<size_t>(T) * d * sizeof(float));
   L.fwd_end = o;
   L.dO = o; o = align256(o + bt * Hq * d * es);
   L.dq = o; o = align256(o + bt * Hq * d * es);

@@ -339,7 +339,7 @@ struct GemmCall {
     int T, Hq, Hkv, vocab;
     float eps, ve_scale;
     const float* gq; const float* gk;        // [128] or NULL (unit)
-    const float* rcos; const float* rsin;    // [>= T][64] or NULL (no rotary)
+    const float* rope_t;                     // [2][64][T]: cos, sin transposed (position fastest), or NULL
     void* qn; void* kn; void* veff;          // [B, H, T, 128]
     float* rstd_q; float* rstd_k;            // [B, H, T]
     const void* ve; const int32_t* tok;      // VE table [vocab][Hkv * 128] or NULL

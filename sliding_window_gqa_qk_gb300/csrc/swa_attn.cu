@@ -596,6 +596,13 @@ swa_status block_fwd_impl(const swa_params* p, const swa_extras* ex, const swa_b
   // q, k, v = xn w^T: A = xn [rows][C], B = the weights [out][C] (K-major),
   // one launch with an output per projection where every head block of the
   // kv projections is a multiple of 128 columns long, else one per projection
+  const float* rcos = b.exp != nullptr ? b.ex.rope_cos : nullptr;
+  float* rope_t = reinterpret_cast<float*>(ws + b.L.rope_t);
+  if (fold && rcos != nullptr) {
+    const dim3 grid(static_cast<unsigned>((b.T + blk::kRtT - 1) / blk::kRtT), 2);
+    blk::rope_transpose_kernel<<<grid, 256, 0, b.st>>>(rcos, b.ex.rope_sin, rope_t, b.T);
+    if ((s = launched()) != SWA_OK) return s;
+  }
   const void* wmat[3] = {w->wq, w->wk, w->wv};
   const size_t dst[3] = {b.L.q, b.L.k, b.L.v};
   const int nout[3] = {nq, nkv, nkv};
@@ -615,8 +622,7 @@ swa_status block_fwd_impl(const swa_params* p, const swa_extras* ex, const swa_b
       e.on = true;
       e.T = b.T; e.Hq = b.Hq; e.Hkv = b.Hkv; e.vocab = p->vocab; e.eps = p->eps; e.ve_scale = p->ve_scale;
       e.gq = gq; e.gk = gk;
-      e.rcos = b.exp != nullptr ? b.ex.rope_cos : nullptr;
-      e.rsin = b.exp != nullptr ? b.ex.rope_sin : nullptr;
+      e.rope_t = rcos != nullptr ? rope_t : nullptr;
       e.qn = ws + A.qn; e.kn = ws + A.kn; e.veff = ws + A.veff;
       e.rstd_q = reinterpret_cast<float*>(ws + A.rstd_q); e.rstd_k = reinterpret_cast<float*>(ws + A.rstd_k);
       e.ve = ve; e.tok = tok; e.gate = learned ? gate_vals : nullptr;

@@ -28,6 +28,13 @@
 //               the same buffer, added), into a 128-byte-swizzled staging
 //               buffer of 4 KB, and out by one TMA store (or, for split K,
 //               one TMA fp32 reduce-add); two buffers per warp.
+// The q, k, v projection with the attention's prologue in its epilogue runs
+// three stages and two epilogue warpgroups (warps 4-11, one head of the
+// tile each): per head row the projection rounded to bf16 (the raw q, k, v
+// the backward reads), then for q and k the rotary turn and the QK-norm in
+// two passes over the row (sum of squares; scaled rows), the rotary tables
+// read transposed (position fastest, one 128-byte line per warp and column)
+// and the gains from shared memory; for v the value-embedding mix.
 // Ragged M, N and K: TMA reads zeros past the ends and clips its stores at
 // them.
 #pragma once
@@ -38,18 +45,26 @@
 namespace swa {
 namespace tc {
 
-constexpr int kGmM = 128, kGmN = 256, kGmK = 64, kGmStages = 4;
-constexpr int kGmThreads = 256;
+constexpr int kGmM = 128, kGmN = 256, kGmK = 64;
 constexpr int kGmProdWarp = 0, kGmMmaWarp = 1, kGmEpiWarp0 = 4;
 
-struct GmSmem {
+// Shape of a launch: the plain GEMM runs four K stages and one epilogue
+// warpgroup; the q, k, v projection with the fused prologue three stages and
+// two epilogue warpgroups (one head of the tile each: its epilogue does the
+// prologue's work), their staging buffers in the stage it gives up.
+template <bool QKV>
+struct GmShape {
+  static constexpr int kStages = QKV ? 3 : 4;
+  static constexpr int kEpiWarps = QKV ? 8 : 4;
+  static constexpr int kThreads = 128 + 32 * kEpiWarps;
   static constexpr int kA = kGmM * kGmK * 2;        // 16 KB
   static constexpr int kB = kGmN * kGmK * 2;        // 32 KB
   static constexpr int kStage = kA + kB;
   static constexpr int kStg = 32 * 128;             // epilogue staging: 32 rows x 128 bytes
-  static constexpr int oStg = kGmStages * kStage;   // [4 warps][2 buffers]
-  static constexpr int oBar = oStg + 8 * kStg;      // barriers, TMEM base, abort flag
-  static constexpr int kBytes = oBar + 256;
+  static constexpr int oStg = kStages * kStage;     // [epilogue warps][2 buffers]
+  static constexpr int oBar = oStg + 2 * kEpiWarps * kStg;   // barriers, TMEM base, abort flag
+  static constexpr int oGain = oBar + 256;                    // QK-norm gains gq, gk: fp32 [2][128]
+  static constexpr int kBytes = oGain + (QKV ? 1024 : 0);
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
@@ -57,7 +72,7 @@ enum {
   GM_FULL = 0,        // +stage: the stage's boxes landed
   GM_EMPTY = 4,       // +stage: the products that read the stage completed
   GM_ACCFULL = 8,     // +buffer: a tile's accumulator is complete
-  GM_ACCEMPTY = 10,   // +buffer: the epilogue read the accumulator (4 warps)
+  GM_ACCEMPTY = 10,   // +buffer: the epilogue read the accumulator (every epilogue warp)
   GM_FINAL = 12,      // every product the MMA thread issued completed
   GM_CLOAD = 13,      // +2 warp + buffer: the residual's box landed in a staging buffer
   GM_COUNT = 21
@@ -74,7 +89,7 @@ struct GmQkv {
   int T, Hq, Hkv, vocab;
   float eps, ve_scale;
   const float* gq; const float* gk;
-  const float* rcos; const float* rsin;
+  const float* rope_t;      // [2][64][T] cos, sin with the position fastest
   float* rstd_q; float* rstd_k;
   const elem_t* ve; const int32_t* tok; const float* gate;
 };
@@ -104,7 +119,7 @@ __device__ __forceinline__ int gm_nseg_of(const GmParams& p, int n) {
 }
 
 template <bool AMN, bool BMN, bool QKV>
-__global__ void __launch_bounds__(kGmThreads, 1)
+__global__ void __launch_bounds__(GmShape<QKV>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
@@ -112,7 +127,8 @@ __global__ void __launch_bounds__(kGmThreads, 1)
                    const __grid_constant__ CUtensorMap tmD2, const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ CUtensorMap tmE0, const __grid_constant__ CUtensorMap tmE1,
                    const __grid_constant__ CUtensorMap tmE2, const GmParams prm) {
-  using S = GmSmem;
+  using S = GmShape<QKV>;
+  constexpr int kGmStages = S::kStages;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {   // swizzle atoms need 1024-byte aligned tiles (uniform over the CTA)
@@ -135,11 +151,18 @@ __global__ void __launch_bounds__(kGmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(GM_ACCFULL + b), 1);
-      mbar_init(bar(GM_ACCEMPTY + b), 4);
+      mbar_init(bar(GM_ACCEMPTY + b), S::kEpiWarps);
     }
     mbar_init(bar(GM_FINAL), 1);
     for (int i = 0; i < 8; ++i) mbar_init(bar(GM_CLOAD + i), 1);
     fence_mbar_init();
+  }
+  if constexpr (QKV) {   // the gains (1 where absent), read by every row of every q / k head
+    float* gs = reinterpret_cast<float*>(smem + S::oGain);
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+      const float* g = i < 128 ? prm.qkv.gq : prm.qkv.gk;
+      gs[i] = g ? g[i & 127] : 1.f;
+    }
   }
   if (warp == kGmMmaWarp) {
     tmem_alloc(smem_u32(tmem_base_sh), 512);
@@ -169,7 +192,8 @@ __global__ void __launch_bounds__(kGmThreads, 1)
         tma_prefetch_desc(mB[i]);
       }
       uint32_t it = 0;
-      int last[kGmStages] = {-1, -1, -1, -1};
+      int last[kGmStages];
+      for (int s2 = 0; s2 < kGmStages; ++s2) last[s2] = -1;
       bool ok = true;
       for (int w = static_cast<int>(blockIdx.x); w < n_items && ok; w += static_cast<int>(gridDim.x)) {
         int mt, nt, kb, ke;
@@ -264,6 +288,8 @@ __global__ void __launch_bounds__(kGmThreads, 1)
     // v + ve_scale * gate * VE[tok]: the prologue kernel's arithmetic.
     const GmQkv& e = prm.qkv;
     const int q = warp & 3;
+    const int ew = warp - kGmEpiWarp0;          // epilogue warp 0..7
+    const int hsel = ew >> 2;                   // the half (head) of the tile this warpgroup takes
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const CUtensorMap* mD[3] = {&tmD0, &tmD1, &tmD2};
     const CUtensorMap* mE[3] = {&tmE0, &tmE1, &tmE2};
@@ -275,15 +301,18 @@ __global__ void __launch_bounds__(kGmThreads, 1)
     int cnt = 0;
     // 32 rows x 128 bytes (32 words per row) through a staging buffer and
     // one TMA store
-    auto stage_store = [&](const uint32_t* w32, const CUtensorMap* map, int x, int y) {
+    // (stage_open: the next buffer, once its previous store has read it;
+    // stage_put: 16 bytes of the lane's row; stage_close: the store)
+    auto stage_open = [&]() {
       const int b = cnt & 1;
-      const uint32_t stg = sbase + S::oStg + static_cast<uint32_t>((q * 2 + b) * S::kStg);
       if (lane == 0 && cnt >= 2) bulk_wait_group_read<1>();
       __syncwarp();
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        st_shared_v4(stg + lane * 128 + ((j ^ (lane & 7)) << 4), w32[4 * j], w32[4 * j + 1], w32[4 * j + 2],
-                     w32[4 * j + 3]);
+      return sbase + S::oStg + static_cast<uint32_t>((ew * 2 + b) * S::kStg);
+    };
+    auto stage_put = [&](uint32_t stg, int j, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+      st_shared_v4(stg + lane * 128 + ((j ^ (lane & 7)) << 4), a, b, c, d);
+    };
+    auto stage_close = [&](uint32_t stg, const CUtensorMap* map, int x, int y) {
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -292,9 +321,15 @@ __global__ void __launch_bounds__(kGmThreads, 1)
       }
       ++cnt;
     };
+    auto stage_store = [&](const uint32_t* w32, const CUtensorMap* map, int x, int y) {
+      const uint32_t stg = stage_open();
+#pragma unroll
+      for (int j = 0; j < 8; ++j) stage_put(stg, j, w32[4 * j], w32[4 * j + 1], w32[4 * j + 2], w32[4 * j + 3]);
+      stage_close(stg, map, x, y);
+    };
     auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
     auto hi = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
-    const bool rope = e.rcos != nullptr;
+    const bool rope = e.rope_t != nullptr;
     int tcount = 0;
     for (int w = static_cast<int>(blockIdx.x); w < n_items; w += static_cast<int>(gridDim.x), ++tcount) {
       int mt, nt, kb, ke;
@@ -307,23 +342,28 @@ __global__ void __launch_bounds__(kGmThreads, 1)
       const int n0 = nt * kGmN;
       if (!mbar_wait_warp(bar(GM_ACCFULL + buf), (tcount >> 1) & 1, ctl)) break;
       tc_fence_after();
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
+      {
+        const int h = hsel;
         const int n = n0 + 128 * h;
         const int sg = gm_nseg_of(prm, n);
-        if (sg < 0) break;   // uniform
+        if (sg < 0) {   // uniform: this half is past N; the accumulator's share is free
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(GM_ACCEMPTY + buf));
+          continue;
+        }
         const int nl = n - prm.nseg[sg].n0;
         const int head = nl >> 7;
-        // the VE-table row of a v head, loaded before the accumulator is read
-        uint4 er[16];
+        // the VE-table row of a v head: into L2 before the accumulator is
+        // read, into registers (a half at a time) once the raw row is stored
         int tok = -1;
         bool tok_ok = false;
+        const elem_t* vrow = e.ve;
         if (sg == 2 && e.ve != nullptr) {
           tok = valid ? e.tok[m] : -1;
           tok_ok = tok >= 0 && tok < e.vocab;
-          const elem_t* vrow = e.ve + (static_cast<long long>(tok_ok ? tok : 0) * e.Hkv + head) * 128;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) er[j] = tok_ok ? ld16(vrow + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
+          vrow = e.ve + (static_cast<long long>(tok_ok ? tok : 0) * e.Hkv + head) * 128;
+          if (tok_ok) bulk_prefetch_l2(vrow, 256);
         }
         uint32_t pk[64];     // the row's 128 values rounded to bf16, in pairs
 #pragma unroll
@@ -334,81 +374,99 @@ __global__ void __launch_bounds__(kGmThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) pk[16 * j + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
         }
-        if (h == 1 || gm_nseg_of(prm, n0 + 128) < 0) {
-          // every column of the tile is in registers: the accumulator is free
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(GM_ACCEMPTY + buf));
-        }
+        // this warp's columns are in registers: its share of the accumulator is free
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(GM_ACCEMPTY + buf));
         stage_store(pk, mD[sg], nl, row0);
         stage_store(pk + 32, mD[sg], nl + 64, row0);
         if (sg < 2) {
-          const float* g = sg == 0 ? e.gq : e.gk;
+          const float* gsm = reinterpret_cast<const float*>(smem + S::oGain) + (sg == 0 ? 0 : 128);
           const int H = sg == 0 ? e.Hq : e.Hkv;
-          // the rotated row (pairs c, c + 64) in fp32, from the rounded values;
-          // the angles 16 columns at a time
-          float r[128];
+          // column c of the tables for the lane's position: one 128-byte
+          // line per warp
+          const float* cs = rope ? e.rope_t + (valid ? t : 0) : nullptr;
+          const float* sn = rope ? cs + 64LL * e.T : nullptr;
+          // the rotated pairs (c, c + 64), c = 8 k .. 8 k + 7, in fp32 from
+          // the rounded values; recomputed in the second pass rather than
+          // kept (a row of 128 fp32 values does not fit beside the rest)
+          auto rotated = [&](int k, float (&xr)[8], float (&yr)[8]) {
+            float co[8], si[8];
+            if (rope) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            r[c] = (c & 1) ? hi(pk[c / 2]) : lo(pk[c / 2]);
-            r[64 + c] = (c & 1) ? hi(pk[32 + c / 2]) : lo(pk[32 + c / 2]);
-          }
-          if (rope) {
-            const float* cs = e.rcos + static_cast<long long>(valid ? t : 0) * 64;
-            const float* sn = e.rsin + static_cast<long long>(valid ? t : 0) * 64;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              float4 c4[4], s4[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                c4[j] = reinterpret_cast<const float4*>(cs + 16 * k)[j];
-                s4[j] = reinterpret_cast<const float4*>(sn + 16 * k)[j];
-              }
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const int c = 16 * k + j;
-                const float co = j % 4 == 0 ? c4[j / 4].x : j % 4 == 1 ? c4[j / 4].y : j % 4 == 2 ? c4[j / 4].z : c4[j / 4].w;
-                const float si = j % 4 == 0 ? s4[j / 4].x : j % 4 == 1 ? s4[j / 4].y : j % 4 == 2 ? s4[j / 4].z : s4[j / 4].w;
-                const float x = r[c], y = r[64 + c];
-                r[c] = fmaf(x, co, y * si);
-                r[64 + c] = fmaf(y, co, -x * si);
+              for (int j = 0; j < 8; ++j) {
+                co[j] = cs[static_cast<long long>(8 * k + j) * e.T];
+                si[j] = sn[static_cast<long long>(8 * k + j) * e.T];
               }
             }
-          }
-          float ss = 0.f;
 #pragma unroll
-          for (int c = 0; c < 128; ++c) ss = fmaf(r[c], r[c], ss);
-          const float rstd = rsqrtf(ss / 128.f + e.eps);
+            for (int j = 0; j < 8; ++j) {
+              const int c = 8 * k + j;
+              const float x = (c & 1) ? hi(pk[c / 2]) : lo(pk[c / 2]);
+              const float y = (c & 1) ? hi(pk[32 + c / 2]) : lo(pk[32 + c / 2]);
+              xr[j] = rope ? fmaf(x, co[j], y * si[j]) : x;
+              yr[j] = rope ? fmaf(y, co[j], -x * si[j]) : y;
+            }
+          };
+          float ssp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            float xr[8], yr[8];
+            rotated(k, xr, yr);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ssp[j & 3] = fmaf(yr[j], yr[j], fmaf(xr[j], xr[j], ssp[j & 3]));
+          }
+          const float rstd = rsqrtf(((ssp[0] + ssp[1]) + (ssp[2] + ssp[3])) / 128.f + e.eps);
           if (valid) (sg == 0 ? e.rstd_q : e.rstd_k)[(static_cast<long long>(bb) * H + head) * e.T + t] = rstd;
           const int yrow = (bb * H + head) * e.T + t0;
+          // both halves of the normed row (channels 0..63, 64..127) at once,
+          // 8 channels of each at a time, into the warp's two buffers
+          if (lane == 0) bulk_wait_group_read<0>();
+          __syncwarp();
+          const uint32_t stg0 = sbase + S::oStg + static_cast<uint32_t>((ew * 2 + (cnt & 1)) * S::kStg);
+          const uint32_t stg1 = sbase + S::oStg + static_cast<uint32_t>((ew * 2 + ((cnt + 1) & 1)) * S::kStg);
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t o[32];   // channels 64 half .. 64 half + 63 of the normed row
+          for (int k = 0; k < 8; ++k) {
+            float xr[8], yr[8];
+            rotated(k, xr, yr);
+            uint32_t o0[4], o1[4];
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
-              const float2 gg = g ? *reinterpret_cast<const float2*>(g + 64 * half + c) : make_float2(1.f, 1.f);
-              o[c / 2] = pack_bf16x2(r[64 * half + c] * rstd * gg.x, r[64 * half + c + 1] * rstd * gg.y);
+            for (int j = 0; j < 8; j += 2) {
+              const float2 g0 = *reinterpret_cast<const float2*>(gsm + 8 * k + j);
+              const float2 g1 = *reinterpret_cast<const float2*>(gsm + 64 + 8 * k + j);
+              o0[j / 2] = pack_bf16x2(xr[j] * rstd * g0.x, xr[j + 1] * rstd * g0.y);
+              o1[j / 2] = pack_bf16x2(yr[j] * rstd * g1.x, yr[j + 1] * rstd * g1.y);
             }
-            stage_store(o, mE[sg], 64 * half, yrow);
+            stage_put(stg0, k, o0[0], o0[1], o0[2], o0[3]);
+            stage_put(stg1, k, o1[0], o1[1], o1[2], o1[3]);
           }
+          stage_close(stg0, mE[sg], 0, yrow);
+          stage_close(stg1, mE[sg], 64, yrow);
         } else if (e.ve != nullptr) {
+          uint4 er[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) er[j] = tok_ok ? ld16(vrow + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
           if (valid && !tok_ok) atomicOr(prm.status, DEV_ERR_TOKEN);   // contributes nothing, reported
           const float sc = tok_ok ? e.ve_scale * (e.gate ? e.gate[static_cast<long long>(m) * e.Hkv + head] : 1.f) : 0.f;
           const int yrow = (bb * e.Hkv + head) * e.T + t0;
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
-            uint32_t o[32];
+            const uint32_t stg = stage_open();
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               float ev[8];
-              unpack16(er[8 * half + j], ev);
+              unpack16(er[j], ev);
+              // the register takes the second half's piece once read
+              if (half == 0) er[j] = tok_ok ? ld16(vrow + 64 + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
+              uint32_t o[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const uint32_t w = pk[32 * half + 4 * j + i];
-                o[4 * j + i] = pack_bf16x2(fmaf(sc, ev[2 * i], lo(w)), fmaf(sc, ev[2 * i + 1], hi(w)));
+                o[i] = pack_bf16x2(fmaf(sc, ev[2 * i], lo(w)), fmaf(sc, ev[2 * i + 1], hi(w)));
               }
+              stage_put(stg, j, o[0], o[1], o[2], o[3]);
             }
-            stage_store(o, mE[2], 64 * half, yrow);
+            stage_close(stg, mE[2], 64 * half, yrow);
           }
         }
       }
@@ -539,7 +597,6 @@ inline bool map_2d(CUtensorMap* m, const void* base, long long inner, long long 
 }
 
 inline swa_status launch_gemm(const GemmCall& g, cudaStream_t st) {
-  using S = GmSmem;
   if (g.M == 0) return SWA_OK;
   if (g.n_kseg < 1 || g.n_kseg > 3 || g.n_nseg < 1 || g.n_nseg > 3 || (g.n_kseg > 1 && g.n_nseg > 1))
     return SWA_ERR_INVALID_ARG;
@@ -622,23 +679,24 @@ inline swa_status launch_gemm(const GemmCall& g, cudaStream_t st) {
     const long long rq = static_cast<long long>(g.M) * e.Hq, rk = static_cast<long long>(g.M) * e.Hkv;
     if (!map_2d(&me[0], e.qn, 128, rq, 128, 32) || !map_2d(&me[1], e.kn, 128, rk, 128, 32)) return SWA_ERR_CUDA;
     if (e.ve != nullptr && !map_2d(&me[2], e.veff, 128, rk, 128, 32)) return SWA_ERR_CUDA;
-    p.qkv = GmQkv{e.T, e.Hq, e.Hkv, e.vocab, e.eps, e.ve_scale, e.gq, e.gk, e.rcos, e.rsin, e.rstd_q, e.rstd_k,
+    p.qkv = GmQkv{e.T, e.Hq, e.Hkv, e.vocab, e.eps, e.ve_scale, e.gq, e.gk, e.rope_t, e.rstd_q, e.rstd_k,
                   static_cast<const elem_t*>(e.ve), e.tok, e.gate};
   }
   const int items = p.n_mt * p.n_nt * p.n_split;
   const int grid = items < num_sms() ? items : num_sms();
-  auto launch = [&](auto kern) {
+  auto launch = [&](auto kern, auto shape) {
+    using S = decltype(shape);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes) != cudaSuccess)
       return SWA_ERR_CUDA;
-    kern<<<grid, kGmThreads, S::kBytes, st>>>(ma[0], ma[1], ma[2], mb[0], mb[1], mb[2], md[0], md[1], md[2],
-                                              mc, me[0], me[1], me[2], p);
+    kern<<<grid, S::kThreads, S::kBytes, st>>>(ma[0], ma[1], ma[2], mb[0], mb[1], mb[2], md[0], md[1], md[2],
+                                               mc, me[0], me[1], me[2], p);
     return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
   };
-  if (e.on) return launch(gemm_tc_kernel<false, false, true>);
-  if (!g.a_mn && !g.b_mn) return launch(gemm_tc_kernel<false, false, false>);
-  if (!g.a_mn && g.b_mn) return launch(gemm_tc_kernel<false, true, false>);
-  if (g.a_mn && g.b_mn) return launch(gemm_tc_kernel<true, true, false>);
-  return launch(gemm_tc_kernel<true, false, false>);
+  if (e.on) return launch(gemm_tc_kernel<false, false, true>, GmShape<true>{});
+  if (!g.a_mn && !g.b_mn) return launch(gemm_tc_kernel<false, false, false>, GmShape<false>{});
+  if (!g.a_mn && g.b_mn) return launch(gemm_tc_kernel<false, true, false>, GmShape<false>{});
+  if (g.a_mn && g.b_mn) return launch(gemm_tc_kernel<true, true, false>, GmShape<false>{});
+  return launch(gemm_tc_kernel<true, false, false>, GmShape<false>{});
 }
 
 }  // namespace tc

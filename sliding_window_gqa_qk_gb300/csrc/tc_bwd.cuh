@@ -129,12 +129,17 @@ __device__ __forceinline__ float transpose_sum32(float (&v)[32], int lane) {
 // Developer Guide §8.2.1 blocks, differentiated). `have` is false when the
 // CTA visited no query tile (dK = dV = 0). The two warpgroups exchange their
 // half-row dot products through `sdot` and named barrier 3; `sgain` holds the
-// per-warp column sums. Every thread of both warpgroups must call this.
+// per-warp column sums. The raw k rows come from global memory, or (sk != 0)
+// from the key tile in shared memory as the TMA loaded it (128-byte swizzled
+// 64-column regions of kBK rows). dv goes out first (staged in sdv, TMA
+// store), so that the store reads it while dk is computed, then dk (sdk).
+// Every thread of both warpgroups must call this.
 template <int D>
 __device__ __forceinline__ void kv_epilogue(const BwdParams& prm, uint32_t tDK, uint32_t tDV,
                                             bool have, int wg, int t, int b, int hk, int kt,
                                             float* sdot, float* sgain, uint32_t sdk, uint32_t sdv,
-                                            const CUtensorMap* tmDK, const CUtensorMap* tmDV) {
+                                            const CUtensorMap* tmDK, const CUtensorMap* tmDV,
+                                            uint32_t sk = 0) {
   constexpr int HD = D / 2, NCH = HD / 32;
   float* sg = sdot + 256;                    // gains of this warpgroup's columns
   sgain += HD * 2;                           // per-warp column sums follow the gains
@@ -174,6 +179,52 @@ __device__ __forceinline__ void kv_epilogue(const BwdParams& prm, uint32_t tDK, 
     }
   }
   if (!rope && t < HD) sg[wg * HD + t] = prm.gk ? prm.gk[wg * HD + t] : 1.f;
+  // dv and the VE-table gradient
+  const int tok = (prm.dve != nullptr && valid) ? prm.tok[bt] : -1;
+  const bool ve_ok = tok >= 0 && tok < prm.vocab;
+  const float vs =
+      ve_ok ? prm.dv_mul * prm.ve_scale * (prm.gate ? prm.gate[bt * prm.Hkv + hk] : 1.f) : 0.f;
+  const float dvm = prm.dv_mul;
+  uint32_t dvr[NCH][32];
+  if (have) {
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) tmem_ld32(tDV + ch * 32, dvr[ch]);
+    tmem_wait_ld(dvr[0]);
+#pragma unroll
+    for (int ch = 1; ch < NCH; ++ch) reg_fence(dvr[ch]);
+  } else {
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+      for (int e = 0; e < 32; ++e) dvr[ch][e] = 0u;
+  }
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    const uint32_t* a = dvr[ch];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = make_uint4(pack_bf16x2(__uint_as_float(a[8 * q]) * dvm, __uint_as_float(a[8 * q + 1]) * dvm),
+                                 pack_bf16x2(__uint_as_float(a[8 * q + 2]) * dvm, __uint_as_float(a[8 * q + 3]) * dvm),
+                                 pack_bf16x2(__uint_as_float(a[8 * q + 4]) * dvm, __uint_as_float(a[8 * q + 5]) * dvm),
+                                 pack_bf16x2(__uint_as_float(a[8 * q + 6]) * dvm, __uint_as_float(a[8 * q + 7]) * dvm));
+      st_shared_v4(sw128_addr(sdv, kBK, t, (wg * HD + ch * 32) / 8 + q), w.x, w.y, w.z, w.w);
+    }
+    if (ve_ok) {
+      float* dst = prm.dve + static_cast<long long>(tok) * prm.Hkv * D + hk * D + wg * HD + ch * 32;
+#pragma unroll
+      for (int e = 0; e < 32; e += 4)
+        red_add_v4_f32(dst + e, vs * __uint_as_float(a[e]), vs * __uint_as_float(a[e + 1]),
+                       vs * __uint_as_float(a[e + 2]), vs * __uint_as_float(a[e + 3]));
+    }
+  }
+  // dv out while dk is computed
+  fence_async_smem();
+  named_bar_sync(3, 256);
+  if (wg == 0 && t == 0) {
+    // rows past T fall outside the tensor and are not written
+    for (int c = 0; c < D / 64; ++c) tma_store_4d(tmDV, sdv + c * kBK * 128, 64 * c, kt * kBK, hk, b);
+    bulk_commit_group();
+  }
   if (!rope) {
     // All loads first: dK (TMEM) and the k row (global).
     uint32_t dkr[NCH][32];
@@ -182,7 +233,10 @@ __device__ __forceinline__ void kv_epilogue(const BwdParams& prm, uint32_t tDK, 
       for (int ch = 0; ch < NCH; ++ch) tmem_ld32(tDK + ch * 32, dkr[ch]);
     }
     uint4 xr[NCH * 4];
-    if (valid) {
+    if (valid && sk != 0) {
+#pragma unroll
+      for (int q = 0; q < NCH * 4; ++q) xr[q] = ld_shared_v4u(sw128_addr(sk, kBK, t, wg * (HD / 8) + q));
+    } else if (valid) {
       const uint4* src = reinterpret_cast<const uint4*>(prm.k + rowoff);
 #pragma unroll
       for (int q = 0; q < NCH * 4; ++q) xr[q] = src[q];
@@ -240,52 +294,13 @@ __device__ __forceinline__ void kv_epilogue(const BwdParams& prm, uint32_t tDK, 
       sgain[(wg * 4 + warp4) * HD + ch * 32 + lane] = transpose_sum32(gt, lane);
     }
   }
-  // dv and the VE-table gradient
-  const int tok = (prm.dve != nullptr && valid) ? prm.tok[bt] : -1;
-  const bool ve_ok = tok >= 0 && tok < prm.vocab;
-  const float vs =
-      ve_ok ? prm.dv_mul * prm.ve_scale * (prm.gate ? prm.gate[bt * prm.Hkv + hk] : 1.f) : 0.f;
-  const float dvm = prm.dv_mul;
-  uint32_t dvr[NCH][32];
-  if (have) {
-#pragma unroll
-    for (int ch = 0; ch < NCH; ++ch) tmem_ld32(tDV + ch * 32, dvr[ch]);
-    tmem_wait_ld(dvr[0]);
-#pragma unroll
-    for (int ch = 1; ch < NCH; ++ch) reg_fence(dvr[ch]);
-  } else {
-#pragma unroll
-    for (int ch = 0; ch < NCH; ++ch)
-#pragma unroll
-      for (int e = 0; e < 32; ++e) dvr[ch][e] = 0u;
-  }
-#pragma unroll
-  for (int ch = 0; ch < NCH; ++ch) {
-    const uint32_t* a = dvr[ch];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      st_shared_v4(sw128_addr(sdv, kBK, t, (wg * HD + ch * 32) / 8 + q),
-                   pack_bf16x2(__uint_as_float(a[8 * q]) * dvm, __uint_as_float(a[8 * q + 1]) * dvm),
-                   pack_bf16x2(__uint_as_float(a[8 * q + 2]) * dvm, __uint_as_float(a[8 * q + 3]) * dvm),
-                   pack_bf16x2(__uint_as_float(a[8 * q + 4]) * dvm, __uint_as_float(a[8 * q + 5]) * dvm),
-                   pack_bf16x2(__uint_as_float(a[8 * q + 6]) * dvm, __uint_as_float(a[8 * q + 7]) * dvm));
-    if (ve_ok) {
-      float* dst = prm.dve + static_cast<long long>(tok) * prm.Hkv * D + hk * D + wg * HD + ch * 32;
-#pragma unroll
-      for (int e = 0; e < 32; e += 4)
-        red_add_v4_f32(dst + e, vs * __uint_as_float(a[e]), vs * __uint_as_float(a[e + 1]),
-                       vs * __uint_as_float(a[e + 2]), vs * __uint_as_float(a[e + 3]));
-    }
-  }
   fence_async_smem();
-  named_bar_sync(3, 256);
+  named_bar_sync(3, 256);   // (also orders the column sums in sgain before their reads)
   if (wg == 0 && t == 0) {
-    // rows past T fall outside the tensors and are not written
-    for (int c = 0; c < D / 64; ++c) {
-      if (!rope) tma_store_4d(tmDK, sdk + c * kBK * 128, 64 * c, kt * kBK, hk, b);
-      tma_store_4d(tmDV, sdv + c * kBK * 128, 64 * c, kt * kBK, hk, b);
+    if (!rope) {
+      for (int c = 0; c < D / 64; ++c) tma_store_4d(tmDK, sdk + c * kBK * 128, 64 * c, kt * kBK, hk, b);
+      bulk_commit_group();
     }
-    bulk_commit_group();
     bulk_wait_group_read<0>();   // the tiles are read out of shared memory
   }
   if (!rope && t < HD) {

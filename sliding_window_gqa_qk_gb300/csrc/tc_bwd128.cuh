@@ -88,7 +88,8 @@ enum {
   B2_XFREE = 16,     // the dQ boxes in the staging buffer were read
   B2_DSFREE = 17,    // the dQ boxes staged in the dS^T buffer were read
   B2_FINAL = 18,
-  B2_COUNT = 19
+  B2_KRAW = 19,      // the raw k rows of the key tile landed (for the epilogue)
+  B2_COUNT = 20
 };
 
 // Visible query columns [clo, chi] of key row j among the 64 queries
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(kB2Threads, 1)
     mbar_init(bar(B2_XFREE), 1);
     mbar_init(bar(B2_DSFREE), 1);
     mbar_init(bar(B2_FINAL), 1);
+    mbar_init(bar(B2_KRAW), 1);
     fence_mbar_init();
   }
   if (warp == kB2MmaWarp) {
@@ -229,9 +231,7 @@ __global__ void __launch_bounds__(kB2Threads, 1)
         bulk_load(sbase + C::oL + s * BQ * 4, prm.lse2 + row, BQ * 4, bar(B2_QFULL + s));
         bulk_load(sbase + C::oD + s * BQ * 4, prm.dvec + row, BQ * 4, bar(B2_QFULL + s));
         if (it == n_it - 1 && prm.dkn_out == nullptr) {
-          // the epilogue's raw k rows and their inverse RMS into L2, a couple
-          // of steps ahead of their use
-          for (int c = 0; c < 2; ++c) tma_prefetch_l2_4d(&tmKr, 64 * c, k0, hk, b);
+          // the epilogue's inverse RMS of the k rows into L2, a step ahead
           const float* rs = prm.rstd_k + (static_cast<long long>(b) * prm.Hkv + hk) * prm.T + k0;
           const uint32_t nrs = static_cast<uint32_t>(prm.T - k0 < kBK ? prm.T - k0 : kBK) * 4;
           // whole 16-byte units inside the row only (a bulk prefetch needs
@@ -241,9 +241,22 @@ __global__ void __launch_bounds__(kB2Threads, 1)
           if (a1 > a0) bulk_prefetch_l2(reinterpret_cast<const void*>(a0), static_cast<uint32_t>(a1 - a0));
         }
       }
+      // The epilogue's raw k rows into the Q stage that the last step does
+      // not use, once the dK product of the step before it has completed.
+      bool kraw = false;
+      if (prm.dkn_out == nullptr && !*reinterpret_cast<volatile uint32_t*>(abort_flag)) {
+        const int s = n_it & 1;
+        if (n_it < 2 || mbar_wait(bar(B2_QEMPTY + s), ((n_it >> 1) - 1) & 1, ctl)) {
+          mbar_arrive_expect_tx(bar(B2_KRAW), C::kTile);
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d(sbase + C::oQ + s * C::kTile + c * C::kHalf, &tmKr, bar(B2_KRAW), 64 * c, k0, hk, b);
+          kraw = true;
+        }
+      }
       mbar_wait_drain(bar(B2_KV), 0, kDrainLimitNs);
       for (int s = 0; s < 2; ++s)
         if (last[s] >= 0) mbar_wait_drain(bar(B2_QFULL + s), (last[s] >> 1) & 1, kDrainLimitNs);
+      if (kraw) mbar_wait_drain(bar(B2_KRAW), 0, kDrainLimitNs);
     } else if (warp == kB2GWarp && lane == 0 && n_it > 0) {
       // ---------------- TMA producer of dO (one stage) ----------------
       tma_prefetch_desc(&tmG);
@@ -527,12 +540,17 @@ __global__ void __launch_bounds__(kB2Threads, 1)
     // epilogue stages dk and dv in K and V and keeps its scratch in a Q
     // stage, while the reducer may still be reading the last dQ boxes out of
     // the dS^T buffer and the staging buffer.
-    const bool final_ok = ok && n_it > 0 && mbar_wait_warp(bar(B2_FINAL), 0, ctl);
+    const bool raw_k = prm.dkn_out == nullptr;
+    const bool final_ok = ok && n_it > 0 && mbar_wait_warp(bar(B2_FINAL), 0, ctl) &&
+                          (!raw_k || mbar_wait_warp(bar(B2_KRAW), 0, ctl));
     tc_fence_after();
-    float* scratch = reinterpret_cast<float*>(smem + C::oQ);
+    // the raw k rows in the Q stage the last step did not use, the scratch
+    // in the other
+    const uint32_t sk = final_ok && raw_k ? sbase + C::oQ + (n_it & 1) * C::kTile : 0u;
+    float* scratch = reinterpret_cast<float*>(smem + C::oQ + ((n_it - 1) & 1) * C::kTile);
     const uint32_t sdk = sbase + C::oK, sdv = sbase + C::oV;
     kv_epilogue<D>(prm, tmem + cDK + lane_off + X * 64, tmem + cDV + lane_off + X * 64, final_ok, X,
-                   t, b, hk, kt, scratch, scratch + 256, sdk, sdv, &tmDK, &tmDV);
+                   t, b, hk, kt, scratch, scratch + 256, sdk, sdv, &tmDK, &tmDV, sk);
   }
   tc_fence_before();
   __syncthreads();

@@ -133,13 +133,16 @@ __device__ __forceinline__ float transpose_sum32(float (&v)[32], int lane) {
 // from the key tile in shared memory as the TMA loaded it (128-byte swizzled
 // 64-column regions of kBK rows). dv goes out first (staged in sdv, TMA
 // store), so that the store reads it while dk is computed, then dk (sdk).
+// `have` says that dV is final (the caller may call this before the last
+// products of dK have completed); dk_ready() is called once dv is out and
+// returns whether dK is final too (waiting for it, and for the raw k rows).
 // Every thread of both warpgroups must call this.
-template <int D>
+template <int D, class DkReady>
 __device__ __forceinline__ void kv_epilogue(const BwdParams& prm, uint32_t tDK, uint32_t tDV,
                                             bool have, int wg, int t, int b, int hk, int kt,
                                             float* sdot, float* sgain, uint32_t sdk, uint32_t sdv,
                                             const CUtensorMap* tmDK, const CUtensorMap* tmDV,
-                                            uint32_t sk = 0) {
+                                            uint32_t sk, DkReady&& dk_ready) {
   constexpr int HD = D / 2, NCH = HD / 32;
   float* sg = sdot + 256;                    // gains of this warpgroup's columns
   sgain += HD * 2;                           // per-warp column sums follow the gains
@@ -150,35 +153,6 @@ __device__ __forceinline__ void kv_epilogue(const BwdParams& prm, uint32_t tDK, 
   const long long rowoff = (bt * prm.Hkv + hk) * D + wg * HD;   // into k / dk / dv
   const float r = valid ? prm.rstd_k[(static_cast<long long>(b) * prm.Hkv + hk) * prm.T + j] : 0.f;
   const bool rope = prm.dkn_out != nullptr;
-  if (rope) {
-    // dkn rows (fp32) for the post kernel, this warpgroup's half of the row
-    uint32_t dkr[NCH][32];
-    if (have) {
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) tmem_ld32(tDK + ch * 32, dkr[ch]);
-      tmem_wait_ld(dkr[0]);
-#pragma unroll
-      for (int ch = 1; ch < NCH; ++ch) reg_fence(dkr[ch]);
-    } else {
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) dkr[ch][e] = 0u;
-    }
-    if (valid) {
-      float4* dst = reinterpret_cast<float4*>(
-          prm.dkn_out + ((static_cast<long long>(b) * prm.Hkv + hk) * prm.T + j) * D + wg * HD);
-      const float m = prm.dk_mul;
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch)
-#pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          dst[(ch * 32 + e) / 4] =
-              make_float4(__uint_as_float(dkr[ch][e]) * m, __uint_as_float(dkr[ch][e + 1]) * m,
-                          __uint_as_float(dkr[ch][e + 2]) * m, __uint_as_float(dkr[ch][e + 3]) * m);
-    }
-  }
-  if (!rope && t < HD) sg[wg * HD + t] = prm.gk ? prm.gk[wg * HD + t] : 1.f;
   // dv and the VE-table gradient
   const int tok = (prm.dve != nullptr && valid) ? prm.tok[bt] : -1;
   const bool ve_ok = tok >= 0 && tok < prm.vocab;
@@ -225,10 +199,42 @@ __device__ __forceinline__ void kv_epilogue(const BwdParams& prm, uint32_t tDK, 
     for (int c = 0; c < D / 64; ++c) tma_store_4d(tmDV, sdv + c * kBK * 128, 64 * c, kt * kBK, hk, b);
     bulk_commit_group();
   }
+  const bool have_dk = dk_ready() && have;
+  if (rope) {
+    // dkn rows (fp32) for the post kernel, this warpgroup's half of the row
+    uint32_t dkr[NCH][32];
+    if (have_dk) {
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) tmem_ld32(tDK + ch * 32, dkr[ch]);
+      tmem_wait_ld(dkr[0]);
+#pragma unroll
+      for (int ch = 1; ch < NCH; ++ch) reg_fence(dkr[ch]);
+    } else {
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) dkr[ch][e] = 0u;
+    }
+    if (valid) {
+      float4* dst = reinterpret_cast<float4*>(
+          prm.dkn_out + ((static_cast<long long>(b) * prm.Hkv + hk) * prm.T + j) * D + wg * HD);
+      const float m = prm.dk_mul;
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          dst[(ch * 32 + e) / 4] =
+              make_float4(__uint_as_float(dkr[ch][e]) * m, __uint_as_float(dkr[ch][e + 1]) * m,
+                          __uint_as_float(dkr[ch][e + 2]) * m, __uint_as_float(dkr[ch][e + 3]) * m);
+    }
+  }
   if (!rope) {
+    // (the scratch may share memory with operands of the products that
+    // dk_ready() waited for)
+    if (t < HD) sg[wg * HD + t] = prm.gk ? prm.gk[wg * HD + t] : 1.f;
     // All loads first: dK (TMEM) and the k row (global).
     uint32_t dkr[NCH][32];
-    if (have) {
+    if (have_dk) {
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch) tmem_ld32(tDK + ch * 32, dkr[ch]);
     }
@@ -244,7 +250,7 @@ __device__ __forceinline__ void kv_epilogue(const BwdParams& prm, uint32_t tDK, 
 #pragma unroll
       for (int q = 0; q < NCH * 4; ++q) xr[q] = make_uint4(0u, 0u, 0u, 0u);
     }
-    if (have) {
+    if (have_dk) {
       tmem_wait_ld(dkr[0]);
 #pragma unroll
       for (int ch = 1; ch < NCH; ++ch) reg_fence(dkr[ch]);
@@ -697,7 +703,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     float* scratch = reinterpret_cast<float*>(smem + C::oQ);
     const uint32_t sdk = sbase + C::oQ + 4096, sdv = sdk + kBK * D * 2;
     kv_epilogue<D>(prm, tmem + C::cDK + lane_off + wg * (D / 2), tmem + C::cDV + lane_off + wg * (D / 2),
-                   ok && n_it > 0, wg, t, b, hk, kt, scratch, scratch + 256, sdk, sdv, &tmDK, &tmDV);
+                   ok && n_it > 0, wg, t, b, hk, kt, scratch, scratch + 256, sdk, sdv, &tmDK, &tmDV, 0u,
+                   [] { return true; });
   }
   tc_fence_before();
   __syncthreads();

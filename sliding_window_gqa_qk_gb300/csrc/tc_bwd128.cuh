@@ -535,22 +535,30 @@ __global__ void __launch_bounds__(kB2Threads, 1)
       return true;
     };
     bool ok = n_it > 0;
-    for (int i = 0; i < n_it && ok; ++i) ok = p_phase(i) && ds_phase(i);
-    // Once every product has completed, K, V and the Q stages are free: the
-    // epilogue stages dk and dv in K and V and keeps its scratch in a Q
-    // stage, while the reducer may still be reading the last dQ boxes out of
-    // the dS^T buffer and the staging buffer.
-    const bool raw_k = prm.dkn_out == nullptr;
-    const bool final_ok = ok && n_it > 0 && mbar_wait_warp(bar(B2_FINAL), 0, ctl) &&
-                          (!raw_k || mbar_wait_warp(bar(B2_KRAW), 0, ctl));
+    // After each step, wait for its dV product: after the last, dV is final
+    // and V (read by the last dP^T before it) is free.
+    for (int i = 0; i < n_it && ok; ++i)
+      ok = p_phase(i) && ds_phase(i) && mbar_wait_warp(bar(B2_GFREE), i & 1, ctl);
     tc_fence_after();
+    // The epilogue stages dv in V while the last dQ^T and dK products still
+    // run; once every product has completed (K free; dK final) it stages dk
+    // in K and keeps its scratch in a Q stage, while the reducer may still be
+    // reading the last dQ boxes out of the dS^T buffer and the staging buffer.
+    const bool raw_k = prm.dkn_out == nullptr;
+    bool final_ok = false;
+    auto dk_ready = [&] {
+      final_ok = ok && n_it > 0 && mbar_wait_warp(bar(B2_FINAL), 0, ctl) &&
+                 (!raw_k || mbar_wait_warp(bar(B2_KRAW), 0, ctl));
+      tc_fence_after();
+      return final_ok;
+    };
     // the raw k rows in the Q stage the last step did not use, the scratch
     // in the other
-    const uint32_t sk = final_ok && raw_k ? sbase + C::oQ + (n_it & 1) * C::kTile : 0u;
+    const uint32_t sk = raw_k && n_it > 0 ? sbase + C::oQ + (n_it & 1) * C::kTile : 0u;
     float* scratch = reinterpret_cast<float*>(smem + C::oQ + ((n_it - 1) & 1) * C::kTile);
     const uint32_t sdk = sbase + C::oK, sdv = sbase + C::oV;
-    kv_epilogue<D>(prm, tmem + cDK + lane_off + X * 64, tmem + cDV + lane_off + X * 64, final_ok, X,
-                   t, b, hk, kt, scratch, scratch + 256, sdk, sdv, &tmDK, &tmDV, sk);
+    kv_epilogue<D>(prm, tmem + cDK + lane_off + X * 64, tmem + cDV + lane_off + X * 64, ok && n_it > 0, X,
+                   t, b, hk, kt, scratch, scratch + 256, sdk, sdv, &tmDK, &tmDV, sk, dk_ready);
   }
   tc_fence_before();
   __syncthreads();

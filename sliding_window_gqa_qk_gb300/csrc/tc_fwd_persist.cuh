@@ -29,6 +29,9 @@
 // autoresearch Administrator & Developer Guide §8.2.1 and §6.3.
 #pragma once
 
+#include <algorithm>
+#include <vector>
+
 #include "tc_fwd.cuh"
 
 namespace swa {
@@ -88,10 +91,24 @@ struct FwdPerParams {
   unsigned long long acc_off, acc_len;
 };
 
-// The k-th item of CTA c of G: rounds of G items, even rounds dealt in CTA
-// order, odd rounds in reverse, so that the heavy rounds even out. Returns
-// -1 past the last item.
-__device__ __forceinline__ int per_item(int k, int c, int G, int n_items) {
+// Items of each CTA, chosen on the host (the items in index order, heaviest
+// first, each onto the CTA with the least work so far): CTA c takes
+// item[off[c]] .. item[off[c + 1] - 1] in that order. n = 0: no table (more
+// items or CTAs than it holds); then rounds of G items, even rounds dealt in
+// CTA order, odd rounds in reverse, so that the heavy rounds even out.
+constexpr int kPerMaxCtas = 256, kPerMaxItems = 8192;
+struct FwdSched {
+  int n;
+  uint16_t off[kPerMaxCtas + 1];
+  uint16_t item[kPerMaxItems];
+};
+
+// The k-th item of CTA c of G; -1 past its last item.
+__device__ __forceinline__ int per_item(const FwdSched& sc, int k, int c, int G, int n_items) {
+  if (sc.n > 0) {
+    const int beg = sc.off[c];
+    return k < sc.off[c + 1] - beg ? static_cast<int>(sc.item[beg + k]) : -1;
+  }
   const int idx = k * G + ((k & 1) ? (G - 1 - c) : c);
   return idx < n_items ? idx : -1;
 }
@@ -111,7 +128,7 @@ struct PerItem {
 //   query tiles 2m + 1 and 2m of one head; they share the kv head, and the K/V
 //   stream is the union of their bands (a tile outside one of them is fully
 //   masked for that tile's rows; A may lie past the end of the sequence).
-__device__ __forceinline__ PerItem per_decode(int w, const FwdPerParams& p, const Band& band) {
+__host__ __device__ __forceinline__ PerItem per_decode(int w, const FwdPerParams& p, const Band& band) {
   PerItem it;
   int lo = 0, hi = -1;
   if (p.pair_heads) {
@@ -148,7 +165,7 @@ template <int D, bool kPolled>
 __global__ void __launch_bounds__(kPerThreads, 1)
     fwd_tc_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                          const FwdPerParams prm) {
+                          const FwdPerParams prm, const __grid_constant__ FwdSched sched) {
   using L = FwdPerSmem<D>;
   constexpr int KCH = D / 64;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -210,7 +227,7 @@ __global__ void __launch_bounds__(kPerThreads, 1)
       int g = 0, it = 0;
       int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
       for (int k = 0; ok; ++k) {
-        const int w = per_item(k, cta, G, prm.n_items);
+        const int w = per_item(sched, k, cta, G, prm.n_items);
         if (w < 0) break;
         const PerItem I = per_decode(w, prm, band);
         if (I.n_tiles <= 0) continue;
@@ -305,7 +322,7 @@ __global__ void __launch_bounds__(kPerThreads, 1)
       bool ok = true;
       int g = 0, it = 0;
       for (int k = 0; ok; ++k) {
-        const int w = per_item(k, cta, G, prm.n_items);
+        const int w = per_item(sched, k, cta, G, prm.n_items);
         if (w < 0) break;
         const PerItem I = per_decode(w, prm, band);
         const int n = I.n_tiles;
@@ -376,7 +393,7 @@ __global__ void __launch_bounds__(kPerThreads, 1)
     bool ok = true;
     int g = 0, it = 0;
     for (int k = 0; ok; ++k) {
-      const int w = per_item(k, cta, G, prm.n_items);
+      const int w = per_item(sched, k, cta, G, prm.n_items);
       if (w < 0) break;
       const PerItem I = per_decode(w, prm, band);
       const int n = I.n_tiles;
@@ -551,6 +568,43 @@ __global__ void __launch_bounds__(kPerThreads, 1)
   }
 }
 
+// The item table of a launch: each item (in index order, heaviest first)
+// onto the CTA with the least work so far; work = key tiles x 5 + 7 (a key
+// tile pair against the fixed cost of an item: its first S, epilogue and
+// hand-over, measured at about 1.4 tile pairs). Kept for the next call with
+// the same shape (one per host thread).
+inline const FwdSched& fwd_schedule(const FwdPerParams& p, int grid) {
+  thread_local FwdSched s;
+  thread_local long long key[9] = {-1};
+  const long long k[9] = {p.B, p.T, p.Hq, p.Hkv, p.window, p.causal, p.pair_heads, p.n_items, grid};
+  bool same = true;
+  for (int i = 0; i < 9; ++i) same = same && key[i] == k[i];
+  if (same) return s;
+  for (int i = 0; i < 9; ++i) key[i] = k[i];
+  s.n = 0;
+  if (p.n_items > kPerMaxItems || grid > kPerMaxCtas) return s;
+  const Band band{p.T, p.window, p.causal};
+  std::vector<int> owner(p.n_items), count(grid, 0);
+  std::vector<std::pair<long long, int>> heap;   // min-heap of (work, cta)
+  for (int c = 0; c < grid; ++c) heap.push_back({0, c});
+  auto cmp = [](const std::pair<long long, int>& a, const std::pair<long long, int>& b) { return a > b; };
+  std::make_heap(heap.begin(), heap.end(), cmp);
+  for (int w = 0; w < p.n_items; ++w) {
+    const PerItem I = per_decode(w, p, band);
+    std::pop_heap(heap.begin(), heap.end(), cmp);
+    owner[w] = heap.back().second;
+    heap.back().first += I.n_tiles > 0 ? 5LL * I.n_tiles + 7 : 0;
+    ++count[owner[w]];
+    std::push_heap(heap.begin(), heap.end(), cmp);
+  }
+  s.off[0] = 0;
+  for (int c = 0; c < grid; ++c) s.off[c + 1] = static_cast<uint16_t>(s.off[c] + count[c]);
+  std::vector<int> fill(s.off, s.off + grid);
+  for (int w = 0; w < p.n_items; ++w) s.item[fill[owner[w]]++] = static_cast<uint16_t>(w);
+  s.n = p.n_items;
+  return s;
+}
+
 template <int D>
 inline swa_status launch_fwd_persist_d(const FwdLaunch& f, cudaStream_t st) {
   using L = FwdPerSmem<D>;
@@ -571,10 +625,11 @@ inline swa_status launch_fwd_persist_d(const FwdLaunch& f, cudaStream_t st) {
   p.dq_acc = f.dq_acc; p.acc_flag = f.acc_flag;
   p.acc_off = f.acc_off; p.acc_len = f.acc_len;
   const int grid = p.n_items < num_sms() ? p.n_items : num_sms();
+  const FwdSched& sched = fwd_schedule(p, grid);
   auto launch = [&](auto kern) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes) != cudaSuccess)
       return SWA_ERR_CUDA;
-    kern<<<grid, kPerThreads, L::kBytes, st>>>(mq, mk, mv, mo, p);
+    kern<<<grid, kPerThreads, L::kBytes, st>>>(mq, mk, mv, mo, p, sched);
     return cudaGetLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
   };
   return p.wait_limit_ns < kPollBelowNs ? launch(fwd_tc_persist_kernel<D, true>)

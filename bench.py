@@ -53,10 +53,10 @@ WORKLOAD = "8-layer SSSL stack (B=16, T=2048, Hq=6, Hkv=3, d=128, W=1024 on S la
 # the kernel's sources have changed since, the bench line reports these as
 # null.
 NCU_CAPTURE = {
-    "source_sha": "89e502e3067b5c27",
-    "traffic_bytes": 431_332_864,
-    "tensor_pipe_pct": 38.0,
-    "dram_gbs": 1815.1,
+    "source_sha": "d436e183b3f48910",
+    "traffic_bytes": 428_628_224,
+    "tensor_pipe_pct": 39.3,
+    "dram_gbs": 1854.7,
     "summary": "profiles/bwd_tc128_s_layer.md (S-layer launch)",
 }
 KERNEL_SOURCES = ("tc_bwd128.cuh", "tc_bwd.cuh", "tc_fwd.cuh", "ptx.cuh", "common.cuh")

@@ -22,17 +22,18 @@ namespace swa {
 
 constexpr int kRowWarps = 8;        // warps per block of the row-wise kernels
 constexpr int kPreBlocksPerSm = 4;  // persistent blocks per SM (register budget 64)
-constexpr int kProBlocksPerSm = 3;  // prologue: register budget 80
+constexpr int kProBlocksPerSm = 2;  // prologue: register budget 128
 constexpr int kPostBlocksPerSm = 2; // post: register budget 128
 constexpr int kRowSlots = 4;        // 16-byte accesses in flight per lane and tensor
+constexpr int kProSlots = 8;        // the prologue's (one tensor per row group)
 
 // Lane layout of a D-element row of elem_t.
-template <int D>
+template <int D, int SLOTS = kRowSlots>
 struct RowMap {
   static constexpr int EPL = 16 / static_cast<int>(sizeof(elem_t));  // elements per lane
   static constexpr int LPR = D / EPL;                                // lanes per row
   static constexpr int RPI = 32 / LPR;                               // rows per warp access
-  static constexpr int RG = kRowSlots * RPI;                         // rows per group
+  static constexpr int RG = SLOTS * RPI;                             // rows per group
   static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0, "row layout");
 };
 
@@ -131,9 +132,9 @@ __device__ __forceinline__ long long grid_warps() {
 // rotated (rotate_row) before the norm. GATE: the v rows' gate is the
 // learned 2 sigmoid(<w_h, x[b, t, :C]>), also written to a.gate_out.
 template <int D, bool ROPE, bool GATE>
-__global__ void __launch_bounds__(kRowWarps * 32, (ROPE || GATE) ? kProBlocksPerSm - 1 : kProBlocksPerSm)
+__global__ void __launch_bounds__(kRowWarps * 32, kProBlocksPerSm)
     prologue_kernel(ProArgs a) {
-  using M = RowMap<D>;
+  using M = RowMap<D, kProSlots>;
   constexpr int EPL = M::EPL;
   const int lane = threadIdx.x & 31;
   const int slot = lane / M::LPR, c0 = (lane % M::LPR) * EPL;
@@ -162,14 +163,14 @@ __global__ void __launch_bounds__(kRowWarps * 32, (ROPE || GATE) ? kProBlocksPer
       const elem_t* x = seg == 0 ? a.q : a.k;
       elem_t* y = seg == 0 ? a.qn : a.kn;
       float* rs = seg == 0 ? a.rstd_q : a.rstd_k;
-      uint4 xr[kRowSlots];
+      uint4 xr[kProSlots];
 #pragma unroll
-      for (int u = 0; u < kRowSlots; ++u) {
+      for (int u = 0; u < kProSlots; ++u) {
         const int t = tg + u * M::RPI;
         xr[u] = t < a.T ? ld16(x + in0 + t * in_stride) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int u = 0; u < kRowSlots; ++u) {
+      for (int u = 0; u < kProSlots; ++u) {
         const int t = tg + u * M::RPI;
         float xv[EPL];
         unpack16(xr[u], xv);
@@ -188,14 +189,14 @@ __global__ void __launch_bounds__(kRowWarps * 32, (ROPE || GATE) ? kProBlocksPer
         }
       }
     } else {
-      uint4 vr[kRowSlots], er[kRowSlots];
-      float sc[kRowSlots], lg[kRowSlots];
+      uint4 vr[kProSlots], er[kProSlots];
+      float sc[kProSlots], lg[kProSlots];
       // Learned gate 2 sigmoid(<w_h, x[b, t, :C]>) of each row (all lanes
       // of the row take part in the dot product).
       if (GATE) {
         const int cl = lane % M::LPR;
 #pragma unroll
-        for (int u = 0; u < kRowSlots; ++u) {
+        for (int u = 0; u < kProSlots; ++u) {
           const int t = tg + u * M::RPI;
           float z = 0.f;
           if (t < a.T) {
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(kRowWarps * 32, (ROPE || GATE) ? kProBlocksPer
         }
       }
 #pragma unroll
-      for (int u = 0; u < kRowSlots; ++u) {
+      for (int u = 0; u < kProSlots; ++u) {
         const int t = tg + u * M::RPI;
         er[u] = make_uint4(0u, 0u, 0u, 0u);
         sc[u] = 0.f;
@@ -226,7 +227,7 @@ __global__ void __launch_bounds__(kRowWarps * 32, (ROPE || GATE) ? kProBlocksPer
         }
       }
 #pragma unroll
-      for (int u = 0; u < kRowSlots; ++u) {
+      for (int u = 0; u < kProSlots; ++u) {
         const int t = tg + u * M::RPI;
         if (t >= a.T) continue;
         float vv[EPL], ev[EPL], o[EPL];

@@ -155,11 +155,11 @@ swa_status run_prologue(const Call& c, const elem_t* q, const elem_t* k, const e
   }
   a.status = at<uint32_t>(c, c.L.status);
   a.nseg = (ve != nullptr || copy_v) ? 3 : 2;
-  const int rg = p.d == 64 ? RowMap<64>::RG : RowMap<128>::RG;
+  const int rg = p.d == 64 ? RowMap<64, kProSlots>::RG : RowMap<128, kProSlots>::RG;
   const long long ngt = (p.T + rg - 1) / rg;
   const long long groups = ngt * p.B * (p.Hq + p.Hkv * (a.nseg - 1));
   const bool rope = a.rcos != nullptr, learned = a.gw != nullptr;
-  const int grid = row_grid(groups, (rope || learned) ? kProBlocksPerSm - 1 : kProBlocksPerSm, 0);
+  const int grid = row_grid(groups, kProBlocksPerSm, 0);
   auto launch = [&](auto kern) { kern<<<grid, kRowWarps * 32, 0, c.stream>>>(a); };
   if (p.d == 64) {
     if (rope) learned ? launch(prologue_kernel<64, true, true>) : launch(prologue_kernel<64, true, false>);

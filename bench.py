@@ -678,90 +678,76 @@ def run_ours(args, rank, world, dev):
 
 
 def run_e2e(args, stack, world):
-    """Same metric through the public API with host buffers: every step copies
-    the inputs of all layers from pinned host memory to the device, runs the
-    stack, and reads o and every gradient back. The copies run on two side
-    streams: layer i's inputs go up while earlier layers compute, and its
-    outputs come down as soon as its backward is done. Events keep each
-    layer's buffers safe across steps: the next step's upload of layer i waits
-    for this step's backward of layer i, and its forward of layer i waits for
-    this step's download of layer i."""
+    """Same metric through the library's host-buffer entry point
+    (swa_attn_step_host): per layer one C-ABI call that copies the layer's
+    inputs from pinned host memory to the device, runs its forward and
+    backward, and copies o, lse and every gradient back, all on one stream.
+    The layers alternate between two streams, each with its own device
+    buffer, so one layer's copies overlap the other stream's compute; stream
+    order keeps each buffer safe across layers and steps."""
+    swa = stack.swa
     host_in, host_out = [], []
     h2d = d2h = 0
     for L in stack.layers:
         hin = {}
         for k in ("q", "k", "v", "dO", "gq", "gk", "ve", "tok"):
             t = L["x"][k]
+            hin[k] = t.contiguous().pin_memory() if t is not None else None
             if t is not None:
-                hin[k] = t.pin_memory()
                 h2d += t.numel() * t.element_size()
         host_in.append(hin)
         hout = {}
-        for k in ("o", "dq", "dk", "dv", "dgq", "dgk", "dve"):
+        for k in ("o", "lse", "dq", "dk", "dv", "dgq", "dgk", "dve"):
             t = L[k]
+            hout[k] = torch.empty(t.shape, dtype=t.dtype).pin_memory() if t is not None else None
             if t is not None:
-                hout[k] = torch.empty(t.shape, dtype=t.dtype).pin_memory()
                 d2h += t.numel() * t.element_size()
         host_out.append(hout)
-
-    n = len(stack.layers)
-    comp = torch.cuda.current_stream()
-    up, down = torch.cuda.Stream(), torch.cuda.Stream()
-    in_ready = [torch.cuda.Event() for _ in range(n)]
-    bwd_done = [torch.cuda.Event() for _ in range(n)]
-    out_read = [torch.cuda.Event() for _ in range(n)]
-    for ev in bwd_done + out_read:
-        ev.record(comp)
-    swa = stack.swa
-    stages = (swa.SWA_BWD_STAGE_PRE, swa.SWA_BWD_STAGE_MAIN, swa.SWA_BWD_STAGE_POST)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    size = max(swa.swa_attn_step_host_size(L["prm"], "bf16") for L in stack.layers)
+    bufs = []
+    for s_ in streams:
+        b = torch.empty(size, dtype=torch.uint8, device=stack.dev)
+        if swa.swa_attn_workspace_init(b, size, s_.cuda_stream, "bf16") != swa.SWA_OK:
+            raise RuntimeError("step buffer init failed")
+        bufs.append(b)
 
     def step():
-        for i, (L, hin) in enumerate(zip(stack.layers, host_in)):
-            up.wait_event(bwd_done[i])
-            with torch.cuda.stream(up):
-                for k, t in hin.items():
-                    L["g"][k].copy_(t, non_blocking=True)
-            in_ready[i].record(up)
-        for i, L in enumerate(stack.layers):
-            comp.wait_event(in_ready[i])
-            comp.wait_event(out_read[i])
-            stack.fwd(L)
-        for i in reversed(range(n)):
-            L = stack.layers[i]
-            for stage in stages:
-                stack.bwd(L, stage)
-            bwd_done[i].record(comp)
-            down.wait_event(bwd_done[i])
-            with torch.cuda.stream(down):
-                for k, t in host_out[i].items():
-                    t.copy_(L[k], non_blocking=True)
-            out_read[i].record(down)
+        for i, (L, hin, hout) in enumerate(zip(stack.layers, host_in, host_out)):
+            st = swa.swa_attn_step_host(
+                L["prm"], L["ex"], hin["q"], hin["k"], hin["v"], hin["gq"], hin["gk"], hin["ve"],
+                hin["tok"], None, hin["dO"], hout["o"], hout["lse"], hout["dq"], hout["dk"], hout["dv"],
+                hout["dgq"], hout["dgk"], hout["dve"], bufs[i % 2], size, streams[i % 2].cuda_stream,
+                kind="bf16")
+            if st != swa.SWA_OK:
+                raise RuntimeError(f"step_host failed: {swa.swa_strerror(st)}")
 
-    def drain():
-        # the step's downloads are part of it: the compute stream waits for them
-        for ev in out_read:
-            comp.wait_event(ev)
-
+    comp = torch.cuda.current_stream()
     for _ in range(max(1, args.warmup)):
         step()
-    drain()
     torch.cuda.synchronize()
     _barrier(world)
     a, b = _ev_pair()
     a.record()
-    up.wait_stream(comp)
-    down.wait_stream(comp)
+    for s_ in streams:
+        s_.wait_stream(comp)
     for _ in range(args.steps):
         step()
-    drain()
+    for s_ in streams:
+        comp.wait_stream(s_)
     b.record()
     torch.cuda.synchronize()
+    for s_, buf in zip(streams, bufs):
+        st = swa.swa_attn_check_status(buf, s_.cuda_stream, "bf16")
+        if st != swa.SWA_OK:
+            raise RuntimeError(f"device check: {swa.swa_strerror(st)}")
     ms = _max_over_ranks(a.elapsed_time(b), world) / args.steps
     value = _aggregate(stack.flops_fwd + stack.flops_bwd, world, ms)
     return {"value": round(value, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "copies": "pinned host buffers; uploads and downloads on two side streams, "
-                      "overlapping the compute of other layers"}
+            "copies": "pinned host buffers through swa_attn_step_host (one C-ABI call per layer: "
+                      "upload, forward, backward, download on one stream); layers alternate "
+                      "between two streams"}
 
 
 def run_reference(args, rank, world):

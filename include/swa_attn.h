@@ -271,6 +271,46 @@ swa_status swa_attn_fwd_noalloc(const swa_params* p, const void* q, const void* 
                                 void* stream);
 
 /*
+ * One training step of one attention call with every tensor in HOST memory:
+ * the inputs are copied host -> device, the forward and the backward run
+ * (the backward reusing the forward's QK-norm / VE-mix outputs), and o, lse
+ * and the gradients are copied device -> host, all enqueued on `stream` in
+ * that order; the call returns without waiting (synchronize the stream, or
+ * record an event after it, before reading the outputs). The pages have no
+ * counterpart of this call: it is the library's end-to-end path for callers
+ * whose data lives on the host.
+ *   q, k, v, dO, gq, gk, ve, tok, ve_gate   host inputs, the layouts and
+ *                  meanings of swa_attn_fwd / swa_attn_bwd (gq, gk, ve, tok,
+ *                  ve_gate may be NULL as there)
+ *   o, lse, dq, dk, dv, dgq, dgk, dve        host outputs, as there
+ *                  (dgq, dgk, dve may be NULL: not computed, not copied)
+ *   ex             as for the _ex calls; its rotary tables and gate weights
+ *                  are DEVICE pointers (not copied)
+ *   device_buffer  device memory of at least swa_attn_step_host_size(p)
+ *                  bytes, 256-byte aligned, passed to swa_attn_workspace_init
+ *                  once before its first use; it holds the attention's
+ *                  workspace (so swa_attn_check_status reads it) and the
+ *                  device copies of every input and output. Reusing it on the
+ *                  same stream is safe (stream order); on several streams at
+ *                  once, give each its own buffer.
+ * Copies from and to pageable host memory make the CUDA runtime stage them
+ * and block the calling thread; page-locked (pinned) host buffers let them
+ * run asynchronously and overlap work on other streams. Each copy is one
+ * cudaMemcpyAsync. Errors: SWA_ERR_INVALID_ARG for a NULL required pointer
+ * or a misaligned device buffer, SWA_ERR_WORKSPACE for a buffer too small,
+ * both before anything is enqueued; then those of swa_attn_fwd and
+ * swa_attn_bwd, and SWA_ERR_CUDA when a copy cannot be enqueued (the outputs
+ * are then undefined).
+ */
+size_t swa_attn_step_host_size(const swa_params* p);
+swa_status swa_attn_step_host(const swa_params* p, const swa_extras* ex, const void* q,
+                              const void* k, const void* v, const float* gq, const float* gk,
+                              const void* ve, const int32_t* tok, const float* ve_gate,
+                              const void* dO, void* o, float* lse, void* dq, void* dk, void* dv,
+                              float* dgq, float* dgk, float* dve, void* device_buffer,
+                              size_t device_bytes, void* stream);
+
+/*
  * The whole attention block around the core: the block's pre-norm, the four
  * bias-free projections c_q, c_k, c_v, c_proj and the residual
  * (autoresearch Administrator & Developer Guide §8.2.1 model table,

@@ -111,6 +111,10 @@ def load(kind: str = "bf16") -> ctypes.CDLL:
     lib.swa_attn_bwd_ex.restype = ctypes.c_int
     lib.swa_attn_fwd_noalloc.argtypes = [P] + [_vp] * 10 + [_vp]
     lib.swa_attn_fwd_noalloc.restype = ctypes.c_int
+    lib.swa_attn_step_host_size.argtypes = [P]
+    lib.swa_attn_step_host_size.restype = ctypes.c_size_t
+    lib.swa_attn_step_host.argtypes = [P, R] + [_vp] * 18 + [ctypes.c_size_t, _vp]
+    lib.swa_attn_step_host.restype = ctypes.c_int
     W = ctypes.POINTER(swa_block_weights)
     lib.swa_block_workspace_size.argtypes = [P, ctypes.c_int, ctypes.c_int]
     lib.swa_block_workspace_size.restype = ctypes.c_size_t
@@ -236,6 +240,34 @@ def swa_attn_bwd_ex(p, ex, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, dO, dq, dk
         ctypes.byref(p), ep, _ptr(q), _ptr(k), _ptr(v), _ptr(gq), _ptr(gk), _ptr(ve), _ptr(tok),
         _ptr(ve_gate), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgq),
         _ptr(dgk), _ptr(dve), _ptr(ws), n, int(flags), _stream(stream)))
+
+
+def swa_attn_step_host_size(p: swa_params, kind: str = "bf16") -> int:
+    return int(load(kind).swa_attn_step_host_size(ctypes.byref(p)))
+
+
+def swa_attn_step_host(p, ex, q, k, v, gq, gk, ve, tok, ve_gate, dO, o, lse, dq, dk, dv, dgq, dgk,
+                       dve, buf, buf_bytes=None, stream=None, kind=None) -> int:
+    """One forward + backward with host tensors (inputs and outputs on the
+    CPU, ideally pinned) and a device buffer of swa_attn_step_host_size
+    bytes; enqueued on `stream`, returns without waiting."""
+    kind = kind or _kind_of(q)
+    n = buf.numel() if buf_bytes is None else buf_bytes
+    ep = None if ex is None else ctypes.byref(ex)
+    return int(load(kind).swa_attn_step_host(
+        ctypes.byref(p), ep, _ptr(q), _ptr(k), _ptr(v), _ptr(gq), _ptr(gk), _ptr(ve), _ptr(tok),
+        _ptr(ve_gate), _ptr(dO), _ptr(o), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgq),
+        _ptr(dgk), _ptr(dve), _ptr(buf), n, _stream(stream)))
+
+
+def new_step_host_buffer(p: swa_params, device, kind: str, stream=None):
+    """A device buffer for swa_attn_step_host, initialised."""
+    n = swa_attn_step_host_size(p, kind)
+    if n == 0:
+        raise SwaError(SWA_ERR_INVALID_ARG, "step buffer size")
+    buf = torch.empty(n, dtype=torch.uint8, device=device)
+    _check(swa_attn_workspace_init(buf, n, stream, kind), "step buffer init")
+    return buf
 
 
 def swa_attn_fwd_noalloc(p, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, stream=None,

@@ -737,6 +737,44 @@ swa_status block_bwd_impl(const swa_params* p, const swa_extras* ex, const swa_b
 
 }  // namespace
 
+namespace {
+
+// Device buffer of swa_attn_step_host: the attention's backward workspace,
+// then device copies of the inputs and outputs (256-byte aligned each).
+struct StepHostLayout {
+  size_t ws_bytes;
+  size_t q, k, v, gq, gk, ve, tok, gate, dO, o, lse, dq, dk, dv, dgq, dgk, dve, end;
+  size_t q_bytes, kv_bytes, gain_bytes, ve_bytes, tok_bytes, gate_bytes, lse_bytes, dve_bytes;
+};
+
+StepHostLayout step_host_layout(const swa_params& p) {
+  StepHostLayout L;
+  const size_t bt = static_cast<size_t>(p.B) * static_cast<size_t>(p.T);
+  const size_t es = sizeof(elem_t);
+  const size_t vocab = p.vocab > 0 ? static_cast<size_t>(p.vocab) : 0;
+  L.q_bytes = bt * p.Hq * p.d * es;
+  L.kv_bytes = bt * p.Hkv * p.d * es;
+  L.gain_bytes = static_cast<size_t>(p.d) * sizeof(float);
+  L.ve_bytes = vocab * p.Hkv * p.d * es;
+  L.tok_bytes = bt * sizeof(int32_t);
+  L.gate_bytes = bt * p.Hkv * sizeof(float);
+  L.lse_bytes = bt * p.Hq * sizeof(float);
+  L.dve_bytes = vocab * p.Hkv * p.d * sizeof(float);
+  L.ws_bytes = align256(ws_layout(p.B, p.T, p.Hq, p.Hkv, p.d).bwd_end);
+  size_t o = L.ws_bytes;
+  auto take = [&](size_t bytes) { const size_t at = o; o = align256(o + bytes); return at; };
+  L.q = take(L.q_bytes); L.k = take(L.kv_bytes); L.v = take(L.kv_bytes);
+  L.gq = take(L.gain_bytes); L.gk = take(L.gain_bytes); L.ve = take(L.ve_bytes);
+  L.tok = take(L.tok_bytes); L.gate = take(L.gate_bytes); L.dO = take(L.q_bytes);
+  L.o = take(L.q_bytes); L.lse = take(L.lse_bytes); L.dq = take(L.q_bytes);
+  L.dk = take(L.kv_bytes); L.dv = take(L.kv_bytes); L.dgq = take(L.gain_bytes);
+  L.dgk = take(L.gain_bytes); L.dve = take(L.dve_bytes);
+  L.end = o;
+  return L;
+}
+
+}  // namespace
+
 // ---------------------------------------------------------------------------
 // Exported C ABI
 // ---------------------------------------------------------------------------
@@ -824,6 +862,63 @@ swa_status swa_attn_fwd_noalloc(const swa_params* p, const void* q, const void* 
   if (ss != SWA_OK) return ss;
   return fwd_impl(p, nullptr, q, k, v, gq, gk, ve, tok, ve_gate, o, lse, scratch,
                   SWA_NOALLOC_SCRATCH_BYTES, 0, stream, false);
+}
+
+size_t swa_attn_step_host_size(const swa_params* p) {
+  if (check_params(p) != SWA_OK) return 0;
+  return step_host_layout(*p).end;
+}
+
+swa_status swa_attn_step_host(const swa_params* p, const swa_extras* ex, const void* q,
+                              const void* k, const void* v, const float* gq, const float* gk,
+                              const void* ve, const int32_t* tok, const float* ve_gate,
+                              const void* dO, void* o, float* lse, void* dq, void* dk, void* dv,
+                              float* dgq, float* dgk, float* dve, void* device_buffer,
+                              size_t device_bytes, void* stream) {
+  swa_status s = check_params(p);
+  if (s != SWA_OK) return s;
+  if (q == nullptr || k == nullptr || v == nullptr || dO == nullptr || o == nullptr || lse == nullptr ||
+      dq == nullptr || dk == nullptr || dv == nullptr || device_buffer == nullptr ||
+      !aligned(device_buffer, 256))
+    return SWA_ERR_INVALID_ARG;
+  if ((ve == nullptr) != (tok == nullptr) || (ve != nullptr && p->vocab <= 0)) return SWA_ERR_INVALID_ARG;
+  const StepHostLayout L = step_host_layout(*p);
+  if (device_bytes < L.end) return SWA_ERR_WORKSPACE;
+  if (p->B == 0 || p->T == 0) return SWA_OK;
+  uint8_t* base = static_cast<uint8_t*>(device_buffer);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto dev = [&](size_t off, const void* host) -> void* { return host ? base + off : nullptr; };
+  auto up = [&](size_t off, const void* host, size_t bytes) {
+    return host == nullptr || bytes == 0 ||
+           cudaMemcpyAsync(base + off, host, bytes, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  };
+  auto down = [&](void* host, size_t off, size_t bytes) {
+    return host == nullptr || bytes == 0 ||
+           cudaMemcpyAsync(host, base + off, bytes, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+  };
+  if (!(up(L.q, q, L.q_bytes) && up(L.k, k, L.kv_bytes) && up(L.v, v, L.kv_bytes) &&
+        up(L.gq, gq, L.gain_bytes) && up(L.gk, gk, L.gain_bytes) && up(L.ve, ve, L.ve_bytes) &&
+        up(L.tok, tok, L.tok_bytes) && up(L.gate, ve_gate, L.gate_bytes) && up(L.dO, dO, L.q_bytes)))
+    return SWA_ERR_CUDA;
+  const float* gq_d = static_cast<const float*>(dev(L.gq, gq));
+  const float* gk_d = static_cast<const float*>(dev(L.gk, gk));
+  const void* ve_d = dev(L.ve, ve);
+  const int32_t* tok_d = static_cast<const int32_t*>(dev(L.tok, tok));
+  const float* gate_d = static_cast<const float*>(dev(L.gate, ve_gate));
+  float* lse_d = reinterpret_cast<float*>(base + L.lse);
+  s = fwd_impl(p, ex, base + L.q, base + L.k, base + L.v, gq_d, gk_d, ve_d, tok_d, gate_d, base + L.o, lse_d,
+               base, L.ws_bytes, 0, stream, true);
+  if (s != SWA_OK) return s;
+  s = bwd_impl(p, ex, base + L.q, base + L.k, base + L.v, gq_d, gk_d, ve_d, tok_d, gate_d, base + L.o, lse_d,
+               base + L.dO, base + L.dq, base + L.dk, base + L.dv, static_cast<float*>(dev(L.dgq, dgq)),
+               static_cast<float*>(dev(L.dgk, dgk)), static_cast<float*>(dev(L.dve, ve ? dve : nullptr)),
+               base, L.ws_bytes, SWA_REUSE_PROLOGUE, stream);
+  if (s != SWA_OK) return s;
+  if (!(down(o, L.o, L.q_bytes) && down(lse, L.lse, L.lse_bytes) && down(dq, L.dq, L.q_bytes) &&
+        down(dk, L.dk, L.kv_bytes) && down(dv, L.dv, L.kv_bytes) && down(dgq, L.dgq, L.gain_bytes) &&
+        down(dgk, L.dgk, L.gain_bytes) && down(ve ? dve : nullptr, L.dve, L.dve_bytes)))
+    return SWA_ERR_CUDA;
+  return SWA_OK;
 }
 
 size_t swa_block_workspace_size(const swa_params* p, int C, int for_backward) {

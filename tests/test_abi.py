@@ -351,3 +351,34 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     k = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)
     with pytest.raises(RuntimeError, match="not built"):
         swa.attention_forward(q, k, k, window=4)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_step_host_size_and_argument_checks(kind):
+    """The host-buffer training step: its device buffer holds the backward
+    workspace plus device copies of every input and output; bad arguments are
+    refused before anything is enqueued (no GPU is touched here)."""
+    p = params()
+    es = 2 if kind == "bf16" else 4
+    B, T, Hq, Hkv, d = 2, 300, 4, 2, 128
+    ws = swa.swa_attn_workspace_size(p, 1, kind)
+    need = swa.swa_attn_step_host_size(p, kind)
+    tensors = B * T * d * es * (4 * Hq + 4 * Hkv) + B * T * Hq * 4 + 4 * d * 4 + B * T * (4 + 4 * Hkv)
+    assert ws + tensors <= need <= ws + tensors + 20 * 256
+    assert swa.swa_attn_step_host_size(params(d=96), kind) == 0
+    lib = swa.load(kind)
+
+    def call(buf=A, nbytes=1 << 40, **over):
+        a = dict(q=A, k=A, v=A, gq=None, gk=None, ve=None, tok=None, gate=None, dO=A, o=A, lse=A,
+                 dq=A, dk=A, dv=A, dgq=None, dgk=None, dve=None)
+        a.update(over)
+        return lib.swa_attn_step_host(ctypes.byref(p), None, a["q"], a["k"], a["v"], a["gq"], a["gk"],
+                                      a["ve"], a["tok"], a["gate"], a["dO"], a["o"], a["lse"], a["dq"],
+                                      a["dk"], a["dv"], a["dgq"], a["dgk"], a["dve"], buf, nbytes, None)
+
+    for name in ("q", "k", "v", "dO", "o", "lse", "dq", "dk", "dv"):
+        assert call(**{name: None}) == swa.SWA_ERR_INVALID_ARG, name
+    assert call(buf=None) == swa.SWA_ERR_INVALID_ARG
+    assert call(buf=A + 16) == swa.SWA_ERR_INVALID_ARG          # not 256-byte aligned
+    assert call(ve=A) == swa.SWA_ERR_INVALID_ARG                # a VE table needs token ids
+    assert call(nbytes=need - 1) == swa.SWA_ERR_WORKSPACE

@@ -476,12 +476,16 @@ __global__ void __launch_bounds__(kB2Threads, 1)
       if (!tile_full(band, q0, BQ, k0, kBK)) {
         int clo, chi;
         key_row_span(band, j, qb, clo, chi);
+        // visible iff clo <= col <= chi: one unsigned compare per column
+        // (an empty span masks every column)
+        const unsigned lo = chi < clo ? 64u : static_cast<unsigned>(clo);
+        const unsigned span = chi < clo ? 0u : static_cast<unsigned>(chi - clo);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const int col = cc * 32 + e;
-            if (col < clo || col > chi) sr[cc][e] = 0u;
+            const unsigned col = static_cast<unsigned>(cc * 32 + e);
+            if (col - lo > span) sr[cc][e] = 0u;
           }
       }
       uint32_t pk[32];

@@ -433,12 +433,16 @@ __global__ void __launch_bounds__(kPerThreads, 1)
         reg_fence(sr[2]);
         reg_fence(sr[3]);
         if (!full) {
+          // visible iff clo <= col <= chi: one unsigned compare per column
+          // (an empty span masks every column)
+          const unsigned lo = chi < clo ? static_cast<unsigned>(kBN) : static_cast<unsigned>(clo);
+          const unsigned span = chi < clo ? 0u : static_cast<unsigned>(chi - clo);
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              const int col = cc * 32 + e;
-              if (col < clo || col > chi) sr[cc][e] = __float_as_uint(-INFINITY);
+              const unsigned col = static_cast<unsigned>(cc * 32 + e);
+              if (col - lo > span) sr[cc][e] = __float_as_uint(-INFINITY);
             }
         }
         // Row maximum: eight independent three-input chains, then a short tree.

@@ -53,10 +53,10 @@ WORKLOAD = "8-layer SSSL stack (B=16, T=2048, Hq=6, Hkv=3, d=128, W=1024 on S la
 # the kernel's sources have changed since, the bench line reports these as
 # null.
 NCU_CAPTURE = {
-    "source_sha": "d436e183b3f48910",
-    "traffic_bytes": 428_628_224,
-    "tensor_pipe_pct": 39.3,
-    "dram_gbs": 1854.7,
+    "source_sha": "ebd410cd4fe49928",
+    "traffic_bytes": 429_616_896,
+    "tensor_pipe_pct": 39.9,
+    "dram_gbs": 1909.5,
     "summary": "profiles/bwd_tc128_s_layer.md (S-layer launch)",
 }
 KERNEL_SOURCES = ("tc_bwd128.cuh", "tc_bwd.cuh", "tc_fwd.cuh", "ptx.cuh", "common.cuh")

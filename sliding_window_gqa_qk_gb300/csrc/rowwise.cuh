@@ -267,13 +267,16 @@ __global__ void __launch_bounds__(kRowWarps * 32, kPreBlocksPerSm) bwd_pre_kerne
     const int b = bh / a.Hq, h = bh - b * a.Hq;
     const long long in0 = (static_cast<long long>(b) * a.T * a.Hq + h) * D + c0;
     uint4 orw[kRowSlots], grw[kRowSlots];
+    float lv[kRowSlots];   // the rows' LSE (read by the lanes that write D), with the rows
 #pragma unroll
     for (int u = 0; u < kRowSlots; ++u) {
       const int t = tg + u * M::RPI;
       orw[u] = grw[u] = make_uint4(0u, 0u, 0u, 0u);
+      lv[u] = 0.f;
       if (t < a.T) {
         orw[u] = ld16(a.o + in0 + t * in_stride);
         grw[u] = ld16(a.dO + in0 + t * in_stride);
+        if (c0 == 0) lv[u] = a.lse[static_cast<long long>(bh) * a.T + t];
       }
     }
 #pragma unroll
@@ -290,7 +293,7 @@ __global__ void __launch_bounds__(kRowWarps * 32, kPreBlocksPerSm) bwd_pre_kerne
       const long long prow = static_cast<long long>(bh) * a.Tpad + t;
       if (c0 == 0) {
         a.dvec[prow] = s * a.d_mul;
-        a.lse2[prow] = fmaf(a.lse[static_cast<long long>(bh) * a.T + t], a.lse2_mul, a.lse2_add);
+        a.lse2[prow] = fmaf(lv[u], a.lse2_mul, a.lse2_add);
       }
       if (clear) {
         float z[EPL];

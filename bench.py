@@ -682,9 +682,10 @@ def run_e2e(args, stack, world):
     (swa_attn_step_host): per layer one C-ABI call that copies the layer's
     inputs from pinned host memory to the device, runs its forward and
     backward, and copies o, lse and every gradient back, all on one stream.
-    The layers alternate between two streams, each with its own device
-    buffer, so one layer's copies overlap the other stream's compute; stream
-    order keeps each buffer safe across layers and steps."""
+    The layers go round args.e2e_streams streams, each with its own device
+    buffer, so that one layer's uploads, another's kernels and a third's
+    downloads run at once; stream order keeps each buffer safe across layers
+    and steps."""
     swa = stack.swa
     host_in, host_out = [], []
     h2d = d2h = 0
@@ -703,7 +704,8 @@ def run_e2e(args, stack, world):
             if t is not None:
                 d2h += t.numel() * t.element_size()
         host_out.append(hout)
-    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    n_st = max(1, args.e2e_streams)
+    streams = [torch.cuda.Stream() for _ in range(n_st)]
     size = max(swa.swa_attn_step_host_size(L["prm"], "bf16") for L in stack.layers)
     bufs = []
     for s_ in streams:
@@ -717,7 +719,7 @@ def run_e2e(args, stack, world):
             st = swa.swa_attn_step_host(
                 L["prm"], L["ex"], hin["q"], hin["k"], hin["v"], hin["gq"], hin["gk"], hin["ve"],
                 hin["tok"], None, hin["dO"], hout["o"], hout["lse"], hout["dq"], hout["dk"], hout["dv"],
-                hout["dgq"], hout["dgk"], hout["dve"], bufs[i % 2], size, streams[i % 2].cuda_stream,
+                hout["dgq"], hout["dgk"], hout["dve"], bufs[i % n_st], size, streams[i % n_st].cuda_stream,
                 kind="bf16")
             if st != swa.SWA_OK:
                 raise RuntimeError(f"step_host failed: {swa.swa_strerror(st)}")
@@ -746,8 +748,8 @@ def run_e2e(args, stack, world):
     return {"value": round(value, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "copies": "pinned host buffers through swa_attn_step_host (one C-ABI call per layer: "
-                      "upload, forward, backward, download on one stream); layers alternate "
-                      "between two streams"}
+                      "upload, forward, backward, download on one stream); layers go round "
+                      f"{n_st} streams"}
 
 
 def run_reference(args, rank, world):
@@ -824,6 +826,8 @@ def main():
                          "rotary, learned gate or Hkv = Hq; long context; the stack of whole "
                          "blocks (projections included)")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--e2e-streams", type=int, default=4,
+                    help="streams (each with its own device buffer) the e2e layers go round")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches instead of replaying a CUDA graph of one step")
     ap.add_argument("--skip-cpu", action="store_true")
